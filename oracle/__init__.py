@@ -1,0 +1,227 @@
+"""CPU oracle for one MoE FFN layer forward -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the package's smoke entry and the benchmark's CPU-baseline leg
+may import this package.  The product path (the CUDA library and its binding)
+never touches it; the two share no code.  The arithmetic lives in
+``moe_oracle.c`` (plain loops, float accumulation, or double in the
+``fp64=True`` build); this file only compiles it and marshals numpy arrays.
+
+Parity pins: every function here is pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle_pins.py`` against library routines, closed forms,
+invariants and brute force (see that file's docstring for the list).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIBS = {}
+_LOCK = threading.Lock()
+
+_C = ctypes
+_i64, _i32, _vp = _C.c_int64, _C.c_int32, _C.c_void_p
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [
+        ("hidden", _i32), ("num_experts", _i32), ("top_k", _i32), ("inter", _i32),
+        ("shared_inter", _i32), ("fp8", _i32),
+        ("w1", _vp), ("w3", _vp), ("w2", _vp),
+        ("s1", _vp), ("s3", _vp), ("s2", _vp),
+        ("ws1", _vp), ("ws3", _vp), ("ws2", _vp),
+        ("ss1", _vp), ("ss3", _vp), ("ss2", _vp),
+    ]
+
+
+def lib_path(fp64: bool = False) -> str:
+    return os.path.join(_BUILD, "libmoe_oracle_f64.so" if fp64 else "libmoe_oracle_f32.so")
+
+
+def build(force: bool = False) -> None:
+    """Compile both oracle builds (float and double accumulation) with gcc."""
+    os.makedirs(_BUILD, exist_ok=True)
+    for fp64 in (False, True):
+        out = lib_path(fp64)
+        if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+            continue
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11",
+               "-fvisibility=hidden", _SRC, "-o", tmp, "-lm"]
+        if fp64:
+            cmd.insert(1, "-DORACLE_FP64")
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+
+
+def _lib(fp64: bool = False):
+    with _LOCK:
+        if fp64 not in _LIBS:
+            build()
+            lib = ctypes.CDLL(lib_path(fp64))
+            lib.oracle_e4m3_decode.argtypes = [_vp, _vp, _i64]
+            lib.oracle_e4m3_encode.argtypes = [_vp, _vp, _i64]
+            lib.oracle_act_quant.argtypes = [_vp, _i64, _vp, _vp, _vp]
+            lib.oracle_router_logits.argtypes = [_vp, _i64, _C.c_int, _vp, _vp, _C.c_int, _vp]
+            lib.oracle_topk_softmax.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _vp, _vp]
+            lib.oracle_permute.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _vp, _vp]
+            lib.oracle_moe_forward.argtypes = [ctypes.POINTER(_Layer), _vp, _i64, _vp, _i64, _vp, _vp, _vp]
+            lib.oracle_moe_forward.restype = _C.c_int
+            lib.oracle_set_threads.argtypes = [_C.c_int]
+            lib.oracle_set_threads.restype = _C.c_int
+            lib.oracle_acc_bits.restype = _C.c_int
+            _LIBS[fp64] = lib
+        return _LIBS[fp64]
+
+
+def _np(a, dtype=None):
+    """torch tensor (any device) or array -> contiguous numpy array on the host."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            t = a.detach().cpu().contiguous()
+            if t.dtype == torch.bfloat16:
+                t = t.view(torch.int16)
+                return t.numpy().view(np.uint16)
+            a = t.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(a)
+    if dtype is not None and a.dtype != dtype:
+        a = a.astype(dtype)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def set_threads(n: int = 0, fp64: bool = False) -> int:
+    """Set the OpenMP thread count (0 keeps the default); returns the count in use."""
+    return _lib(fp64).oracle_set_threads(int(n))
+
+
+def acc_bits(fp64: bool = False) -> int:
+    return _lib(fp64).oracle_acc_bits()
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = _np(codes, np.uint8)
+    out = np.empty(c.shape, np.float32)
+    _lib().oracle_e4m3_decode(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def e4m3_encode(values) -> np.ndarray:
+    v = _np(values, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _lib().oracle_e4m3_encode(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def act_quant(values):
+    """1x128 block quantisation of a 1-D vector -> (codes, scales, dequantised)."""
+    v = _np(values, np.float32).reshape(-1)
+    n = v.size
+    q = np.empty(n, np.uint8)
+    s = np.empty((n + 127) // 128, np.float32)
+    d = np.empty(n, np.float32)
+    _lib().oracle_act_quant(_ptr(v), n, _ptr(q), _ptr(s), _ptr(d))
+    return q, s, d
+
+
+def router_logits(x, router_w, router_bias=None, fp64: bool = False) -> np.ndarray:
+    xb = _np(x)
+    assert xb.dtype == np.uint16, "x must be bf16"
+    m, H = xb.shape
+    wr = _np(router_w, np.float32)
+    E = wr.shape[0]
+    b = None if router_bias is None else _np(router_bias, np.float32)
+    L = np.empty((m, E), np.float32)
+    _lib(fp64).oracle_router_logits(_ptr(xb), m, H, _ptr(wr), _ptr(b), E, _ptr(L))
+    return L
+
+
+def topk_softmax(logits, k: int):
+    """-> ids int32 [m,k], weights float32 [m,k], margin float32 [m]."""
+    L = _np(logits, np.float32)
+    m, E = L.shape
+    ids = np.empty((m, k), np.int32)
+    w = np.empty((m, k), np.float32)
+    margin = np.empty(m, np.float32)
+    _lib().oracle_topk_softmax(_ptr(L), m, E, k, _ptr(ids), _ptr(w), _ptr(margin))
+    return ids, w, margin
+
+
+def permute(ids, num_experts: int):
+    """-> expert_offsets int32 [E+1], sorted_pair int32 [P], slot_of_pair int32 [P]."""
+    a = _np(ids, np.int32)
+    m, k = a.shape
+    P = m * k
+    off = np.empty(num_experts + 1, np.int32)
+    sp = np.empty(P, np.int32)
+    sl = np.empty(P, np.int32)
+    _lib().oracle_permute(_ptr(a), m, k, num_experts, _ptr(off), _ptr(sp), _ptr(sl))
+    return off, sp, sl
+
+
+def _layer_struct(shape, layer, keep):
+    def arr(name, dtype):
+        t = layer.get(name)
+        if t is None:
+            return None
+        a = _np(t, dtype) if dtype is not None else _np(t)
+        keep.append(a)
+        return a
+
+    wdt = np.uint8 if shape.fp8 else None
+    s = _Layer()
+    s.hidden, s.num_experts, s.top_k = shape.hidden, shape.num_experts, shape.top_k
+    s.inter, s.shared_inter, s.fp8 = shape.inter, shape.shared_inter, int(shape.fp8)
+    for name in ("w1", "w3", "w2", "ws1", "ws3", "ws2"):
+        a = arr(name, wdt)
+        setattr(s, name, _ptr(a))
+    for name in ("s1", "s3", "s2", "ss1", "ss3", "ss2"):
+        a = arr(name, np.float32)
+        setattr(s, name, _ptr(a))
+    return s
+
+
+def moe_forward(shape, layer, x, ids, w, rows=None, fp64: bool = False) -> np.ndarray:
+    """Layer output (float32 [len(rows) or m, H]) for a given routing (ids, w)."""
+    keep = []
+    st = _layer_struct(shape, layer, keep)
+    xb = _np(x)
+    assert xb.dtype == np.uint16, "x must be bf16"
+    m = xb.shape[0]
+    ids_a = _np(ids, np.int32)
+    w_a = _np(w, np.float32)
+    assert ids_a.shape == (m, shape.top_k) and w_a.shape == (m, shape.top_k)
+    r = None if rows is None else _np(rows, np.int64).reshape(-1)
+    n = m if r is None else r.size
+    out = np.empty((n, shape.hidden), np.float32)
+    rc = _lib(fp64).oracle_moe_forward(ctypes.byref(st), _ptr(xb), m, _ptr(r), n,
+                                       _ptr(ids_a), _ptr(w_a), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_moe_forward: token row or expert id out of range")
+    return out
+
+
+def route(shape, layer, x, fp64: bool = False):
+    """Router logits + softmax top-k for all tokens -> (logits, ids, w, margin)."""
+    L = router_logits(x, layer["router_w"], layer.get("router_bias"), fp64=fp64)
+    ids, w, margin = topk_softmax(L, shape.top_k)
+    return L, ids, w, margin
+
+
+def reference(shape, layer, x, rows=None, fp64: bool = False):
+    """The whole layer: route every token, then the expert sum for `rows`."""
+    L, ids, w, margin = route(shape, layer, x, fp64=fp64)
+    out = moe_forward(shape, layer, x, ids, w, rows=rows, fp64=fp64)
+    return {"logits": L, "ids": ids, "w": w, "margin": margin, "out": out}

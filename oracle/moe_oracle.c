@@ -1,0 +1,365 @@
+/*
+ * CPU oracle for one mixture-of-experts FFN layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the package's smoke entry and the
+ * benchmark's CPU-baseline leg may load this library. The product path (the
+ * CUDA library and its Python binding) never calls it and shares no code with
+ * it.
+ *
+ * What it computes is the plain definition of the layer, one token at a time,
+ * one selected expert at a time, with no blocking, fusion or reordering:
+ *
+ *   spark_model/layers/moe/forward_prefill.rs, MoeLayer::forward_prefill, the
+ *   pipeline in its doc comment: gate -> topK -> sort -> grouped gate/up GEMM
+ *   -> SiLU -> grouped down GEMM -> unpermute + weighted reduce -> shared
+ *   expert blend.  Grouping and sorting only reorder work, so per token:
+ *
+ *     L[e]   = sum_h x[h] * Wr[e,h] (+ bias[e])                  (step 1)
+ *     ids    = the k largest L, descending, ties to the lower index
+ *     w[j]   = softmax over the k selected logits (renormalised)  (step 2)
+ *     g[i]   = sum_h x[h] W1[e,i,h];  u[i] = sum_h x[h] W3[e,i,h]
+ *     a[i]   = silu(g[i]) * u[i],  silu(g) = g / (1 + exp(-g))   (steps 4-5)
+ *     y[o]   = sum_i a[i] W2[e,o,i]                               (step 6)
+ *     out    = sum_j w[j] y_j  (+ shared expert, weight 1)        (steps 7-8)
+ *
+ * The accumulation type is float (the default build) or double (the build
+ * with ORACLE_FP64 defined, used to bound the float build's own rounding).
+ * Every sum runs in ascending index order.  Routing weights are formed in
+ * double and rounded to float in both builds.
+ *
+ * fp8 weights (e4m3, 128x128 fp32 block scales) and fp8 activations (e4m3,
+ * one fp32 scale per token per 128 contiguous elements) follow the block-scaled
+ * fp8 layer shape: activation scale s = amax / 448 in float, code =
+ * e4m3(round-to-nearest-even, saturating to +-448)(x / s), value = decode(code)
+ * * s; an all-zero block takes s = 1 and codes 0.  The e4m3 codec here is
+ * written from the format's definition (1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities, S.1111.111 is NaN, largest finite 448).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifdef ORACLE_FP64
+typedef double acc_t;
+#define ACC_EXP(v) exp(v)
+#else
+typedef float acc_t;
+#define ACC_EXP(v) expf(v)
+#endif
+
+#define EXPORT __attribute__((visibility("default")))
+
+/* ---------------------------------------------------------------- codecs */
+
+/* bf16 bit pattern -> float: the bf16 value is the top half of an IEEE float. */
+static float bf16_to_float(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* e4m3 code -> float, from the format definition. */
+static float e4m3_decode_one(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int expo = (c >> 3) & 0xF;
+    int mant = c & 0x7;
+    float v;
+    if (expo == 0xF && mant == 0x7) {
+        v = NAN;
+    } else if (expo == 0) {
+        v = ldexpf((float)mant, -9); /* subnormal: mant/8 * 2^(1-7) */
+    } else {
+        v = ldexpf(1.0f + (float)mant / 8.0f, expo - 7);
+    }
+    return sign ? -v : v;
+}
+
+/*
+ * float -> e4m3 code, round to nearest, ties to even, saturating to +-448.
+ * Exhaustive: the code whose value is nearest; on an exact tie the code with
+ * an even mantissa (lowest bit 0).  Searching the 127 non-negative finite codes
+ * keeps this obviously correct; speed does not matter here.
+ */
+static uint8_t e4m3_encode_one(float x) {
+    if (isnan(x)) return 0x7F;
+    int neg = signbit(x) ? 1 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)((neg << 7) | 0x7E);
+    int best = 0;
+    double best_err = a; /* code 0 has value 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        double v = (double)e4m3_decode_one((uint8_t)c);
+        double err = fabs(v - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    if (best == 0) return (uint8_t)(neg << 7); /* keep the sign of zero */
+    return (uint8_t)((neg << 7) | best);
+}
+
+/* decode table, filled from e4m3_decode_one before any parallel region */
+static float g_e4m3[256];
+static int g_e4m3_ready = 0;
+static void e4m3_table_init(void) {
+    if (g_e4m3_ready) return;
+    for (int c = 0; c < 256; ++c) g_e4m3[c] = e4m3_decode_one((uint8_t)c);
+    g_e4m3_ready = 1;
+}
+
+EXPORT void oracle_e4m3_decode(const uint8_t* in, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_decode_one(in[i]);
+}
+
+EXPORT void oracle_e4m3_encode(const float* in, uint8_t* out, int64_t n) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_encode_one(in[i]);
+}
+
+/*
+ * Per-block activation quantisation, one block = 128 contiguous elements (the
+ * last block of a row may be shorter).  v: [n] floats; q: [n] codes;
+ * s: [ceil(n/128)] scales.  deq (optional): decode(q) * s.
+ */
+EXPORT void oracle_act_quant(const float* v, int64_t n, uint8_t* q, float* s, float* deq) {
+    for (int64_t b0 = 0; b0 < n; b0 += 128) {
+        int64_t b1 = b0 + 128 < n ? b0 + 128 : n;
+        float amax = 0.0f;
+        for (int64_t i = b0; i < b1; ++i) {
+            float a = fabsf(v[i]);
+            if (a > amax) amax = a;
+        }
+        float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        s[b0 / 128] = sc;
+        for (int64_t i = b0; i < b1; ++i) {
+            q[i] = amax > 0.0f ? e4m3_encode_one(v[i] / sc) : 0;
+            if (deq) deq[i] = e4m3_decode_one(q[i]) * sc;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- routing */
+
+/*
+ * Step "1. Gate GEMM" of forward_prefill (and "10. Router gemv" of
+ * qwen3_moe/forward_layer.rs): logits[t,e] = sum_h x[t,h] * Wr[e,h] + bias[e].
+ * x: [m,H] bf16 bits; Wr: [E,H] float; bias: [E] or NULL; L: [m,E].
+ */
+EXPORT void oracle_router_logits(const uint16_t* x, int64_t m, int H, const float* Wr,
+                                 const float* bias, int E, float* L) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < m; ++t) {
+        const uint16_t* xt = x + t * (int64_t)H;
+        for (int e = 0; e < E; ++e) {
+            const float* we = Wr + (int64_t)e * H;
+            acc_t acc = 0;
+            for (int h = 0; h < H; ++h) acc += (acc_t)bf16_to_float(xt[h]) * (acc_t)we[h];
+            float l = (float)acc;
+            if (bias) l = l + bias[e];
+            L[t * (int64_t)E + e] = l;
+        }
+    }
+}
+
+/*
+ * Step "2. Batched topK dispatch", the softmax branch with norm_topk_prob set:
+ * ids = the k largest logits in descending order, equal logits ordered by the
+ * lower expert index; w[j] = exp(L[ids[j]] - L[ids[0]]) / sum over the k
+ * selected of exp(L[ids[i]] - L[ids[0]]), in double, rounded to float.
+ * margin[t] (optional) = L of the k-th pick minus the best unpicked logit
+ * (+inf when k == E).
+ */
+EXPORT void oracle_topk_softmax(const float* L, int64_t m, int E, int k, int32_t* ids, float* w,
+                                float* margin) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < m; ++t) {
+        const float* lt = L + t * (int64_t)E;
+        unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+        int32_t* it = ids + t * (int64_t)k;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || lt[e] > lt[best]) best = e; /* strict: ties keep the lower index */
+            }
+            taken[best] = 1;
+            it[j] = best;
+        }
+        double l0 = (double)lt[it[0]];
+        double den = 0.0;
+        for (int j = 0; j < k; ++j) den += exp((double)lt[it[j]] - l0);
+        for (int j = 0; j < k; ++j) w[t * (int64_t)k + j] = (float)(exp((double)lt[it[j]] - l0) / den);
+        if (margin) {
+            if (k >= E) {
+                margin[t] = INFINITY;
+            } else {
+                int best = -1;
+                for (int e = 0; e < E; ++e)
+                    if (!taken[e] && (best < 0 || lt[e] > lt[best])) best = e;
+                margin[t] = lt[it[k - 1]] - lt[best];
+            }
+        }
+        free(taken);
+    }
+}
+
+/*
+ * Step "3. Sort tokens by expert": a stable counting sort of the pairs
+ * p = t*k + j by their expert ids[p].  offsets[E+1] is the exclusive prefix
+ * sum of the per-expert counts; sorted_pair[s] is the pair at sorted slot s
+ * (pairs ascending within an expert); slot_of_pair[p] is its inverse.
+ */
+EXPORT void oracle_permute(const int32_t* ids, int64_t m, int k, int E, int32_t* offsets,
+                           int32_t* sorted_pair, int32_t* slot_of_pair) {
+    int64_t P = m * (int64_t)k;
+    int32_t* cursor = (int32_t*)calloc((size_t)E + 1, sizeof(int32_t));
+    for (int e = 0; e <= E; ++e) offsets[e] = 0;
+    for (int64_t p = 0; p < P; ++p) offsets[ids[p] + 1] += 1;
+    for (int e = 0; e < E; ++e) offsets[e + 1] += offsets[e];
+    for (int64_t p = 0; p < P; ++p) {
+        int e = ids[p];
+        int32_t s = offsets[e] + cursor[e]++;
+        sorted_pair[s] = (int32_t)p;
+        slot_of_pair[p] = s;
+    }
+    free(cursor);
+}
+
+/* ---------------------------------------------------------------- experts */
+
+typedef struct {
+    int32_t hidden, num_experts, top_k, inter, shared_inter, fp8;
+    const void *w1, *w3, *w2;  /* [E,I,H], [E,I,H], [E,H,I]: bf16 bits or e4m3 codes */
+    const float *s1, *s3, *s2; /* fp8 only: [E,I/128,H/128], [E,I/128,H/128], [E,H/128,I/128] */
+    const void *ws1, *ws3, *ws2; /* shared expert, [Is,H], [Is,H], [H,Is] */
+    const float *ss1, *ss3, *ss2;
+} oracle_layer;
+
+/* Element (r, c) of one expert's [R, C] weight matrix, dequantised. */
+static acc_t weight_at(const void* w, const float* sc, int fp8, int64_t base, int C, int r, int c) {
+    if (!fp8) return (acc_t)bf16_to_float(((const uint16_t*)w)[base + (int64_t)r * C + c]);
+    int cb = (C + 127) / 128;
+    float code = g_e4m3[((const uint8_t*)w)[base + (int64_t)r * C + c]];
+    return (acc_t)(code * sc[(int64_t)(r / 128) * cb + (c / 128)]);
+}
+
+/*
+ * One expert's SwiGLU FFN on one input row (metrale moe_v41 forward.rs, the
+ * swiglu launch, without its clamp; the routing weight is applied by the
+ * caller after the down projection, as in forward_prefill step 7).
+ *   xin: [H] (already fp8-emulated when fp8); y: [H] out.
+ * w1/w3 base offsets are in elements; sc1/sc3/sc2 point at this expert's scales.
+ */
+static void expert_ffn(const oracle_layer* Lr, int I, const void* w1, const float* sc1,
+                       const void* w3, const float* sc3, const void* w2, const float* sc2,
+                       int64_t b13, int64_t b2, const acc_t* xin, acc_t* a, acc_t* y) {
+    int H = Lr->hidden;
+    int fp8 = Lr->fp8;
+    if (I <= 0 || H <= 0) return;
+    for (int i = 0; i < I; ++i) {
+        acc_t g = 0, u = 0;
+        for (int h = 0; h < H; ++h) {
+            g += xin[h] * weight_at(w1, sc1, fp8, b13, H, i, h);
+            u += xin[h] * weight_at(w3, sc3, fp8, b13, H, i, h);
+        }
+        acc_t silu = g / ((acc_t)1 + ACC_EXP(-g));
+        a[i] = silu * u;
+    }
+    if (fp8) {
+        /* the down projection's input is quantised per 128 elements along I */
+        float* af = (float*)malloc(sizeof(float) * (size_t)I);
+        float* ad = (float*)malloc(sizeof(float) * (size_t)I);
+        uint8_t* q = (uint8_t*)malloc((size_t)I);
+        float* s = (float*)malloc(sizeof(float) * (size_t)((I + 127) / 128));
+        for (int i = 0; i < I; ++i) af[i] = (float)a[i];
+        oracle_act_quant(af, I, q, s, ad);
+        for (int i = 0; i < I; ++i) a[i] = (acc_t)ad[i];
+        free(af); free(ad); free(q); free(s);
+    }
+    for (int o = 0; o < H; ++o) {
+        acc_t acc = 0;
+        for (int i = 0; i < I; ++i) acc += a[i] * weight_at(w2, sc2, fp8, b2, I, o, i);
+        y[o] = acc;
+    }
+}
+
+/*
+ * The layer output for the token rows listed in `rows` (all m tokens when
+ * rows is NULL), given the routing (ids, w: [m,k]).  out: [nrows, H] float.
+ * Per token: acc = sum_j w[j] * FFN_{ids[j]}(xin) (j ascending), then
+ * acc += FFN_shared(xin) when a shared expert exists (metrale moe_v41
+ * forward.rs, shared_expert_tail: acc += sd).  Returns 0, or -1 on a bad id.
+ */
+EXPORT int oracle_moe_forward(const oracle_layer* Lr, const uint16_t* x, int64_t m,
+                              const int64_t* rows, int64_t nrows, const int32_t* ids,
+                              const float* w, float* out) {
+    int H = Lr->hidden, E = Lr->num_experts, k = Lr->top_k, I = Lr->inter;
+    int Is = Lr->shared_inter;
+    int64_t n = rows ? nrows : m;
+    int bad = 0;
+    e4m3_table_init();
+    int Imax = I > Is ? I : Is;
+    int hb = (H + 127) / 128, ib = (I + 127) / 128;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t t = rows ? rows[r] : r;
+        if (t < 0 || t >= m) { bad |= 1; continue; }
+        acc_t* xin = (acc_t*)malloc(sizeof(acc_t) * (size_t)H);
+        acc_t* a = (acc_t*)malloc(sizeof(acc_t) * (size_t)Imax);
+        acc_t* y = (acc_t*)malloc(sizeof(acc_t) * (size_t)H);
+        acc_t* acc = (acc_t*)calloc((size_t)H, sizeof(acc_t));
+        const uint16_t* xt = x + t * (int64_t)H;
+        if (Lr->fp8) {
+            float* xf = (float*)malloc(sizeof(float) * (size_t)H);
+            float* xd = (float*)malloc(sizeof(float) * (size_t)H);
+            uint8_t* q = (uint8_t*)malloc((size_t)H);
+            float* s = (float*)malloc(sizeof(float) * (size_t)hb);
+            for (int h = 0; h < H; ++h) xf[h] = bf16_to_float(xt[h]);
+            oracle_act_quant(xf, H, q, s, xd);
+            for (int h = 0; h < H; ++h) xin[h] = (acc_t)xd[h];
+            free(xf); free(xd); free(q); free(s);
+        } else {
+            for (int h = 0; h < H; ++h) xin[h] = (acc_t)bf16_to_float(xt[h]);
+        }
+        for (int j = 0; j < k; ++j) {
+            int e = ids[t * (int64_t)k + j];
+            if (e < 0 || e >= E) { bad |= 1; break; }
+            int64_t b13 = (int64_t)e * I * H, b2 = (int64_t)e * H * I;
+            const float *c1 = 0, *c3 = 0, *c2 = 0;
+            if (Lr->fp8) {
+                c1 = Lr->s1 + (int64_t)e * ib * hb;
+                c3 = Lr->s3 + (int64_t)e * ib * hb;
+                c2 = Lr->s2 + (int64_t)e * hb * ib;
+            }
+            expert_ffn(Lr, I, Lr->w1, c1, Lr->w3, c3, Lr->w2, c2, b13, b2, xin, a, y);
+            acc_t wj = (acc_t)w[t * (int64_t)k + j];
+            for (int h = 0; h < H; ++h) acc[h] += wj * y[h];
+        }
+        if (Is > 0) {
+            expert_ffn(Lr, Is, Lr->ws1, Lr->ss1, Lr->ws3, Lr->ss3, Lr->ws2, Lr->ss2, 0, 0, xin, a, y);
+            for (int h = 0; h < H; ++h) acc[h] += y[h];
+        }
+        for (int h = 0; h < H; ++h) out[r * (int64_t)H + h] = (float)acc[h];
+        free(xin); free(a); free(y); free(acc);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Threads the OpenMP loops use (0 leaves the runtime default). */
+EXPORT int oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
+EXPORT int oracle_acc_bits(void) { return (int)(8 * sizeof(acc_t)); }
