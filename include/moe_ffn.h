@@ -1,0 +1,185 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) MoE FFN layer forward.
+ *
+ * One mixture-of-experts FFN layer for m tokens: router logits, softmax top-k
+ * with renormalised weights, a stable permute of (token, expert) pairs by
+ * expert, grouped SwiGLU experts (gate/up projection fused with
+ * SiLU(gate) * up, then the down projection), and a routing-weighted
+ * unpermute-reduce plus an optional shared-expert add.  The pipeline is the
+ * one spelled out in spark_model/layers/moe/forward_prefill.rs
+ * (MoeLayer::forward_prefill, doc comment and numbered steps 1-8); the
+ * small-m GEMV arm follows the decode chain of span-02
+ * engine/crates/model/src/gpu_model/forward.rs (forward_rows, "MoE" block:
+ * router, glu, down for r <= 16 rows).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *     row-major and densely packed; the caller owns every buffer (weights,
+ *     activations, outputs, workspace).  The library never allocates device
+ *     memory and never synchronises the stream, so a call can be captured in
+ *     a CUDA graph.  `stream` is a cudaStream_t (NULL = legacy default).
+ *   - bf16 tensors are passed as `const void*` holding IEEE bfloat16 bits.
+ *   - Calls return MOE_OK or an error status; on error nothing was launched
+ *     unless the status is MOE_ERR_CUDA (a launch failed part-way).
+ *   - m == 0 returns MOE_OK and launches nothing (metrale moe_v41 forward.rs,
+ *     launch_n: early return at n == 0; forward_prefill: no grid.x = 0).
+ *   - Results are deterministic: fixed reduction orders, no float atomics.
+ *   - The workspace must be at least moe_workspace_size(layer, m) bytes and
+ *     256-byte aligned; it carries no state between calls except the device
+ *     error word read by moe_device_status.  Calls that share a workspace
+ *     must be ordered on one stream.
+ */
+#ifndef MOE_FFN_GB300_H
+#define MOE_FFN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols the shared library exports (everything else is hidden). */
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* ---- status codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1 /* null/misaligned pointer, bad size, id out of range */
+#define MOE_ERR_UNSUPPORTED 2 /* shape the kernels do not cover (see moe_layer_create) */
+#define MOE_ERR_WORKSPACE 3   /* workspace smaller than moe_workspace_size() */
+#define MOE_ERR_CUDA 4        /* a CUDA runtime/driver call or launch failed */
+#define MOE_ERR_DEVICE 5      /* a kernel flagged an error (bounded wait expired, bad id) */
+
+/* ---- weight formats */
+#define MOE_WEIGHTS_BF16 0
+/* e4m3 codes (uint8) with one fp32 scale per 128x128 block of each weight
+ * matrix (blocks aligned at (0,0) over (out, in)); activations are quantised
+ * to e4m3 with one fp32 scale per token per 128 contiguous inputs,
+ * s = amax / 448, round-to-nearest-even, saturating. */
+#define MOE_WEIGHTS_FP8_E4M3_B128 1
+
+/* ---- expert arms for moe_experts / moe_forward */
+#define MOE_ARM_AUTO 0 /* pick by rows per expert (moe_select_arm) */
+#define MOE_ARM_GEMV 1 /* small-m arm: each selected expert's weights streamed once */
+#define MOE_ARM_GEMM 2 /* tcgen05/TMEM grouped GEMM arm fed by TMA */
+
+typedef struct moe_config {
+    int32_t hidden;       /* H: multiple of 128 */
+    int32_t num_experts;  /* E: 1..1024 */
+    int32_t top_k;        /* k: 1..min(E, 32) */
+    int32_t inter;        /* I: expert intermediate size, multiple of 128 */
+    int32_t shared_inter; /* 0 = no shared expert; otherwise must equal inter */
+    int32_t weights;      /* MOE_WEIGHTS_BF16 or MOE_WEIGHTS_FP8_E4M3_B128 */
+} moe_config;
+
+/* Stacked expert weights in nn.Linear (out, in) layout.
+ *   routed:  w1, w3 [E, I, H]   w2 [E, H, I]
+ *   shared:  w1, w3 [I, H]      w2 [H, I]        (E = 1 of the same layout)
+ *   fp8 only: s1, s3 [E, I/128, H/128]  s2 [E, H/128, I/128]  (fp32)
+ * Element type: bf16 or e4m3 codes (uint8) per moe_config.weights.
+ * Pointers must be 16-byte aligned.  The weights must outlive the layer. */
+typedef struct moe_expert_weights {
+    const void* w1;
+    const void* w3;
+    const void* w2;
+    const float* s1;
+    const float* s3;
+    const float* s2;
+} moe_expert_weights;
+
+typedef struct moe_layer moe_layer;
+
+/* Create a layer handle on the current CUDA device.  The handle keeps a copy
+ * of the config, the weight pointers and host-side TMA descriptors of the
+ * weights; it owns no device memory.  `shared` may be NULL (and must be when
+ * cfg->shared_inter == 0).  Returns MOE_ERR_UNSUPPORTED for shapes outside
+ * the documented ranges. */
+MOE_API int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed,
+                     const moe_expert_weights* shared, moe_layer** out);
+MOE_API int moe_layer_destroy(moe_layer* layer);
+
+/* Workspace bytes a call with m tokens needs (any entry point). */
+MOE_API int moe_workspace_size(const moe_layer* layer, int64_t m, size_t* bytes);
+
+/* Which arm MOE_ARM_AUTO takes for m tokens (MOE_ARM_GEMV or MOE_ARM_GEMM). */
+MOE_API int moe_select_arm(const moe_layer* layer, int64_t m);
+
+/* Steps 1-2 of forward_prefill ("Gate GEMM", "Batched topK dispatch", softmax
+ * with norm_topk_prob): logits[t,e] = sum_h x[t,h] Wr[e,h] (+ bias[e]) in
+ * fp32; topk_ids[t,:] = the k largest logits in descending order (equal
+ * logits: lower expert index first); topk_w[t,j] = exp(L_j - L_0) / sum over
+ * the k selected of exp(L_i - L_0).
+ *   x        bf16 [m, H]           router_w fp32 [E, H]
+ *   router_bias fp32 [E] or NULL   logits_out fp32 [m, E] or NULL
+ *   topk_ids int32 [m, k]          topk_w fp32 [m, k]                       */
+MOE_API int moe_route(const moe_layer* layer, const void* x, int64_t m, const float* router_w,
+              const float* router_bias, float* logits_out, int32_t* topk_ids, float* topk_w,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Step 3 of forward_prefill ("Sort tokens by expert"), as a stable counting
+ * sort of the pairs p = t*k + j by expert topk_ids[p]:
+ *   expert_offsets int32 [E+1]: exclusive prefix sum of per-expert counts
+ *   sorted_pair    int32 [m*k]: pair at sorted slot s (ascending p within an expert)
+ *   slot_of_pair   int32 [m*k]: inverse of sorted_pair
+ * Ids outside [0, E) set the device error word (MOE_ERR_DEVICE).            */
+MOE_API int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t m,
+                int32_t* expert_offsets, int32_t* sorted_pair, int32_t* slot_of_pair,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Steps 3-8 for a given routing: permute, grouped gate/up + SiLU(gate)*up,
+ * grouped down, then out[t] = sum_j topk_w[t,j] * y_{t,j} (+ shared expert
+ * output, weight 1), accumulated in fp32 in j order and stored as bf16.
+ *   x bf16 [m, H]; topk_ids int32 [m, k]; topk_w fp32 [m, k]; out bf16 [m, H]
+ * out is fully overwritten (metrale moe_v41 forward.rs: acc is cleared before
+ * any routed or shared row is added).  arm: MOE_ARM_*.                      */
+MOE_API int moe_experts(const moe_layer* layer, const void* x, int64_t m, const int32_t* topk_ids,
+                const float* topk_w, void* out, int arm, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* The whole layer: moe_route then moe_experts on one stream, no host sync.
+ * topk_ids_out / topk_w_out may be NULL (the routing then stays in the
+ * workspace).                                                               */
+MOE_API int moe_forward(const moe_layer* layer, const void* x, int64_t m, const float* router_w,
+                const float* router_bias, void* out, int32_t* topk_ids_out, float* topk_w_out,
+                int arm, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Activation quantisation of the fp8 layers (the expert input and the down
+ * projection's input): per row, per block of 128 contiguous elements,
+ * s = amax / 448 (IEEE fp32 divide), code = e4m3(x / s) rounded to nearest
+ * even and saturated to +-448; an all-zero block gets s = 1 and zero codes.
+ *   x bf16 [rows, n]; codes uint8 [rows, n]; scales fp32 [rows, n/128];
+ *   n a multiple of 128.  Needs no layer and no workspace.                  */
+MOE_API int moe_act_quant_fp8(const void* x, int64_t rows, int64_t n, uint8_t* codes, float* scales,
+                              void* stream);
+
+/* Synchronises `stream` and reads the device error word a previous call left
+ * in `workspace` (0 = none).  Returns MOE_OK, MOE_ERR_DEVICE when the word is
+ * set, or MOE_ERR_CUDA.                                                     */
+MOE_API int moe_device_status(const void* workspace, void* stream, int32_t* device_code);
+
+/* Kernels the last successful call on `layer` launched (for launch counting). */
+MOE_API int moe_last_launch_count(const moe_layer* layer);
+
+/* Optional per-kernel timing for profiling: while enabled, each kernel
+ * launch of a call on `layer` is bracketed by two CUDA events on the call's
+ * stream (so calls are then not capturable in a CUDA graph).  Enabling or
+ * disabling resets the totals.  moe_kernel_timing_read synchronises on the
+ * recorded events and returns the summed device time (ms) and launch count of
+ * kernel `kernel` (0 .. moe_kernel_count()-1, named by moe_kernel_name). */
+MOE_API int moe_kernel_timing_enable(moe_layer* layer, int enable);
+MOE_API int moe_kernel_timing_read(moe_layer* layer, int kernel, double* total_ms, int64_t* launches);
+MOE_API int moe_kernel_count(void);
+MOE_API const char* moe_kernel_name(int kernel);
+
+/* Human-readable name of a status code (static storage). */
+MOE_API const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_GB300_H */

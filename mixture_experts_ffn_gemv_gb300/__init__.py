@@ -14,7 +14,8 @@ __all__ = ["LayerShape", "Workload", "WORKLOADS", "TINY", "QWEN3_30B_A3B", "DEEP
 def __getattr__(name):
     # the binding (and with it the CUDA library) loads only when asked for
     if name in ("binding", "MoeLayer", "build_library"):
-        from . import binding
+        import importlib
+        binding = importlib.import_module(__name__ + ".binding")
         if name == "binding":
             return binding
         return getattr(binding, name)

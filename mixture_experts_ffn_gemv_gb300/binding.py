@@ -1,0 +1,245 @@
+"""ctypes binding of libmoe_ffn_gb300.so (argument marshalling only).
+
+Every entry point keeps the C-ABI's name (moe_route, moe_permute,
+moe_experts, moe_forward); the tensors' data pointers and the current torch
+CUDA stream are passed straight through.  No computation happens here, and a
+missing library is an error: there is no CPU or torch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB, build_library, up_to_date
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
+MOE_WEIGHTS_BF16, MOE_WEIGHTS_FP8_E4M3_B128 = 0, 1
+MOE_ARM_AUTO, MOE_ARM_GEMV, MOE_ARM_GEMM = 0, 1, 2
+ARMS = {"auto": MOE_ARM_AUTO, "gemv": MOE_ARM_GEMV, "gemm": MOE_ARM_GEMM}
+
+EXPORTED = (
+    "moe_layer_create", "moe_layer_destroy", "moe_workspace_size", "moe_select_arm", "moe_route",
+    "moe_permute", "moe_experts", "moe_forward", "moe_act_quant_fp8", "moe_device_status",
+    "moe_last_launch_count", "moe_kernel_timing_enable", "moe_kernel_timing_read", "moe_kernel_count",
+    "moe_kernel_name", "moe_status_string",
+)
+
+_vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("hidden", _i32), ("num_experts", _i32), ("top_k", _i32), ("inter", _i32),
+                ("shared_inter", _i32), ("weights", _i32)]
+
+
+class MoeExpertWeights(ctypes.Structure):
+    _fields_ = [("w1", _vp), ("w3", _vp), ("w2", _vp), ("s1", _vp), ("s3", _vp), ("s2", _vp)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str | None = None, build: bool = True):
+    """Load (building first if stale) the CUDA library; raises if unavailable."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB
+        if build and path is None and not up_to_date():
+            build_library()
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library {p} is missing; build it with build_library()")
+        lib = ctypes.CDLL(p)
+        lib.moe_layer_create.argtypes = [ctypes.POINTER(MoeConfig), ctypes.POINTER(MoeExpertWeights),
+                                         ctypes.POINTER(MoeExpertWeights), ctypes.POINTER(_vp)]
+        lib.moe_layer_destroy.argtypes = [_vp]
+        lib.moe_workspace_size.argtypes = [_vp, _i64, ctypes.POINTER(ctypes.c_size_t)]
+        lib.moe_select_arm.argtypes = [_vp, _i64]
+        lib.moe_route.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        lib.moe_permute.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        lib.moe_experts.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+        lib.moe_forward.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+        lib.moe_act_quant_fp8.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp]
+        lib.moe_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
+        lib.moe_last_launch_count.argtypes = [_vp]
+        lib.moe_kernel_timing_enable.argtypes = [_vp, ctypes.c_int]
+        lib.moe_kernel_timing_read.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                               ctypes.POINTER(_i64)]
+        lib.moe_kernel_count.argtypes = []
+        lib.moe_kernel_name.argtypes = [ctypes.c_int]
+        lib.moe_kernel_name.restype = ctypes.c_char_p
+        lib.moe_status_string.argtypes = [ctypes.c_int]
+        lib.moe_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library(build=False).moe_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover - library absent
+        return "status"
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def moe_act_quant_fp8(x, stream=None):
+    """x bf16 [rows, n] (device) -> (codes uint8 [rows, n], scales fp32 [rows, n/128])."""
+    lib = load_library()
+    rows, n = x.shape
+    codes = torch.empty(rows, n, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(rows, n // 128, dtype=torch.float32, device=x.device)
+    _check(lib.moe_act_quant_fp8(_p(x), rows, n, _p(codes), _p(scales), _stream(stream)), "moe_act_quant_fp8")
+    return codes, scales
+
+
+class MoeLayer:
+    """A layer handle over caller-owned device weights (see include/moe_ffn.h).
+
+    tensors: dict with w1, w3, w2 (and s1, s3, s2 for fp8), optionally ws1,
+    ws3, ws2 (+ ss1, ss3, ss2) for the shared expert, as produced by
+    ``inputs.make_experts`` and moved to the device.
+    """
+
+    def __init__(self, shape, tensors: dict):
+        self.lib = load_library()
+        self.shape = shape
+        self._keep = dict(tensors)
+        cfg = MoeConfig(shape.hidden, shape.num_experts, shape.top_k, shape.inter, shape.shared_inter,
+                        MOE_WEIGHTS_FP8_E4M3_B128 if shape.fp8 else MOE_WEIGHTS_BF16)
+        routed = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("w1", "w3", "w2", "s1", "s3", "s2")])
+        shared = None
+        if shape.shared_inter:
+            shared = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2")])
+        handle = _vp()
+        _check(self.lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(routed),
+                                         ctypes.byref(shared) if shared is not None else None,
+                                         ctypes.byref(handle)), "moe_layer_create")
+        self.handle = handle
+        self._ws = None
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.moe_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- workspace
+    def workspace_size(self, m: int) -> int:
+        n = ctypes.c_size_t()
+        _check(self.lib.moe_workspace_size(self.handle, int(m), ctypes.byref(n)), "moe_workspace_size")
+        return n.value
+
+    def workspace(self, m: int, device=None) -> torch.Tensor:
+        need = self.workspace_size(m)
+        if self._ws is None or self._ws.numel() < need:
+            dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        return self._ws
+
+    def select_arm(self, m: int) -> int:
+        return self.lib.moe_select_arm(self.handle, int(m))
+
+    def last_launch_count(self) -> int:
+        return self.lib.moe_last_launch_count(self.handle)
+
+    def kernel_timing(self, enable: bool):
+        """Turn per-kernel event timing on or off (resets the totals)."""
+        _check(self.lib.moe_kernel_timing_enable(self.handle, int(bool(enable))), "moe_kernel_timing_enable")
+
+    def kernel_times(self) -> dict:
+        """{kernel name: (total ms, launches)} for kernels launched while timing was on."""
+        out = {}
+        for k in range(self.lib.moe_kernel_count()):
+            ms = ctypes.c_double()
+            n = _i64()
+            _check(self.lib.moe_kernel_timing_read(self.handle, k, ctypes.byref(ms), ctypes.byref(n)),
+                   "moe_kernel_timing_read")
+            if n.value:
+                out[self.lib.moe_kernel_name(k).decode()] = (ms.value, n.value)
+        return out
+
+    def device_status(self, stream=None) -> int:
+        code = _i32()
+        ws = self._ws
+        if ws is None:
+            return 0
+        rc = self.lib.moe_device_status(_p(ws), _stream(stream), ctypes.byref(code))
+        if rc not in (MOE_OK, MOE_ERR_DEVICE):
+            raise MoeError(rc, "moe_device_status")
+        return code.value
+
+    # ---- entry points
+    def moe_route(self, x, router_w, router_bias=None, logits=False, stream=None):
+        m = x.shape[0]
+        dev = x.device
+        ids = torch.empty(m, self.shape.top_k, dtype=torch.int32, device=dev)
+        w = torch.empty(m, self.shape.top_k, dtype=torch.float32, device=dev)
+        lg = torch.empty(m, self.shape.num_experts, dtype=torch.float32, device=dev) if logits else None
+        ws = self.workspace(m)
+        _check(self.lib.moe_route(self.handle, _p(x), m, _p(router_w), _p(router_bias), _p(lg), _p(ids), _p(w),
+                                  _p(ws), ws.numel(), _stream(stream)), "moe_route")
+        return (ids, w, lg) if logits else (ids, w)
+
+    def moe_permute(self, topk_ids, stream=None):
+        m = topk_ids.shape[0]
+        dev = topk_ids.device
+        P = m * self.shape.top_k
+        off = torch.empty(self.shape.num_experts + 1, dtype=torch.int32, device=dev)
+        sp = torch.empty(P, dtype=torch.int32, device=dev)
+        sl = torch.empty(P, dtype=torch.int32, device=dev)
+        ws = self.workspace(m)
+        _check(self.lib.moe_permute(self.handle, _p(topk_ids), m, _p(off), _p(sp), _p(sl), _p(ws), ws.numel(),
+                                    _stream(stream)), "moe_permute")
+        return off, sp, sl
+
+    def moe_experts(self, x, topk_ids, topk_w, arm="auto", out=None, stream=None):
+        m = x.shape[0]
+        if out is None:
+            out = torch.empty(m, self.shape.hidden, dtype=torch.bfloat16, device=x.device)
+        ws = self.workspace(m)
+        _check(self.lib.moe_experts(self.handle, _p(x), m, _p(topk_ids), _p(topk_w), _p(out), ARMS[arm], _p(ws),
+                                    ws.numel(), _stream(stream)), "moe_experts")
+        return out
+
+    def moe_forward(self, x, router_w, router_bias=None, arm="auto", out=None, return_routing=False, stream=None):
+        m = x.shape[0]
+        dev = x.device
+        if out is None:
+            out = torch.empty(m, self.shape.hidden, dtype=torch.bfloat16, device=dev)
+        ids = w = None
+        if return_routing:
+            ids = torch.empty(m, self.shape.top_k, dtype=torch.int32, device=dev)
+            w = torch.empty(m, self.shape.top_k, dtype=torch.float32, device=dev)
+        ws = self.workspace(m)
+        _check(self.lib.moe_forward(self.handle, _p(x), m, _p(router_w), _p(router_bias), _p(out), _p(ids), _p(w),
+                                    ARMS[arm], _p(ws), ws.numel(), _stream(stream)), "moe_forward")
+        return (out, ids, w) if return_routing else out

@@ -1,0 +1,498 @@
+// C-ABI of the MoE FFN layer: argument checks, workspace layout, arm
+// selection and the launch sequence.  Declarations and the contract of every
+// entry point: include/moe_ffn.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "kernels.h"
+#include "moe_ffn.h"
+
+using namespace moe;
+
+namespace {
+
+// Optional per-kernel timing: every launch bracketed by two CUDA events on its
+// stream, resolved when the totals are read.
+enum KernelId : int {
+    K_ROUTER = 0, K_TOPK, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
+    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_COUNT
+};
+const char* const kKernelNames[K_COUNT] = {
+    "router", "topk_softmax", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
+    "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine",
+};
+
+struct Pending {
+    int kid;
+    cudaEvent_t a, b;
+};
+
+struct KernelTimer {
+    bool on = false;
+    std::vector<cudaEvent_t> pool;
+    std::vector<Pending> pending;
+    double ms[K_COUNT] = {};
+    int64_t launches[K_COUNT] = {};
+
+    cudaEvent_t get() {
+        if (!pool.empty()) {
+            cudaEvent_t e = pool.back();
+            pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        return e;
+    }
+    int resolve() {
+        int rc = 0;
+        for (const Pending& p : pending) {
+            float t = 0.f;
+            if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&t, p.a, p.b) != cudaSuccess)
+                rc = 1;
+            ms[p.kid] += t;
+            launches[p.kid] += 1;
+            pool.push_back(p.a);
+            pool.push_back(p.b);
+        }
+        pending.clear();
+        return rc;
+    }
+    ~KernelTimer() {
+        for (const Pending& p : pending) {
+            cudaEventDestroy(p.a);
+            cudaEventDestroy(p.b);
+        }
+        for (cudaEvent_t e : pool) cudaEventDestroy(e);
+    }
+};
+
+}  // namespace
+
+struct moe_layer {
+    moe_config cfg;
+    moe_expert_weights routed;
+    moe_expert_weights shared;
+    bool has_shared;
+    bool fp8;
+    int device;
+    mutable int last_launches;
+    mutable KernelTimer timer;
+    GemmWeights gemm;  // host-side TMA descriptors of the weights
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+    size_t hdr, part, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile, sorted_pair, slot_of_pair;
+    size_t xq, xsc, xs, xs_sc, h, hsc, y, total;
+    int S, P, rows, nchunk;
+};
+
+Layout layout(const moe_layer* L, int64_t m) {
+    Layout o{};
+    const int E = L->cfg.num_experts, k = L->cfg.top_k, H = L->cfg.hidden, I = L->cfg.inter;
+    o.P = (int)(m * k);
+    o.rows = o.P + (L->has_shared ? (int)m : 0);
+    o.S = router_slices(H, (int)m);
+    o.nchunk = ceil_div(std::max(o.P, 1), kPermChunk);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, kAlign);
+        return at;
+    };
+    const size_t ab = L->fp8 ? 1 : 2;  // activation element bytes
+    o.hdr = take(sizeof(WsHeader));
+    o.part = take((size_t)o.S * m * E * 4);
+    o.ids = take((size_t)o.P * 4);
+    o.w = take((size_t)o.P * 4);
+    o.chunk_base = take((size_t)o.nchunk * E * 4);
+    o.grp_off = take((size_t)(E + 1) * 4);
+    o.grp_cnt = take((size_t)(E + 1) * 4);
+    o.act_group = take((size_t)(E + 1) * 4);
+    o.act_tile = take((size_t)(E + 2) * 4);
+    o.sorted_pair = take((size_t)o.P * 4);
+    o.slot_of_pair = take((size_t)o.P * 4);
+    if (L->fp8) {
+        o.xq = take((size_t)m * H);
+        o.xsc = take((size_t)m * (H / 128) * 4);
+    }
+    o.xs = take((size_t)o.rows * H * ab);
+    if (L->fp8) o.xs_sc = take((size_t)o.rows * (H / 128) * 4);
+    o.h = take((size_t)o.rows * I * ab);
+    if (L->fp8) o.hsc = take((size_t)o.rows * (I / 128) * 4);
+    o.y = take((size_t)o.rows * H * 4);
+    o.total = off;
+    return o;
+}
+
+template <typename T>
+inline T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_call(const moe_layer* L, int64_t m, void* ws, size_t ws_bytes, Layout* lo) {
+    if (!L || m < 0) return MOE_ERR_INVALID_ARG;
+    if (m > (int64_t)(INT32_MAX / 64) / std::max(1, L->cfg.top_k)) return MOE_ERR_UNSUPPORTED;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev != L->device) return MOE_ERR_INVALID_ARG;
+    *lo = layout(L, m);
+    if (m == 0) return MOE_OK;
+    if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < lo->total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+// Launches one kernel (f returns its cudaError_t), counting it and, when the
+// layer's kernel timing is on, bracketing it with events.
+struct Launcher {
+    const moe_layer* L;
+    cudaStream_t st;
+    int n = 0;
+    template <class F>
+    bool run(int kid, F&& f) {
+        KernelTimer& T = L->timer;
+        cudaEvent_t a = nullptr, b = nullptr;
+        if (T.on) {
+            a = T.get();
+            b = T.get();
+            if (!a || !b || cudaEventRecord(a, st) != cudaSuccess) return false;
+        }
+        if (f() != cudaSuccess) return false;
+        if (T.on) {
+            if (cudaEventRecord(b, st) != cudaSuccess) return false;
+            T.pending.push_back({kid, a, b});
+        }
+        ++n;
+        return true;
+    }
+};
+
+#define MOE_LAUNCH(kid, expr)                                    \
+    do {                                                         \
+        if (!ln.run((kid), [&]() { return (expr); })) return MOE_ERR_CUDA; \
+    } while (0)
+
+int run_route(const moe_layer* L, const Layout& lo, const void* x, int m, const float* wr, const float* bias,
+              float* logits_out, int32_t* ids, float* w, void* ws, Launcher& ln) {
+    const moe_config& c = L->cfg;
+    const cudaStream_t st = ln.st;
+    float* part = at<float>(ws, lo.part);
+    MOE_LAUNCH(K_ROUTER, launch_router(static_cast<const uint16_t*>(x), m, c.hidden, wr, c.num_experts, part, lo.S, st));
+    MOE_LAUNCH(K_TOPK, launch_topk(part, lo.S, m, c.num_experts, c.top_k, bias, logits_out, ids, w, st));
+    return MOE_OK;
+}
+
+PermuteOut permute_out(const Layout& lo, void* ws, int32_t* sorted_pair, int32_t* slot_of_pair,
+                       int32_t* expert_offsets) {
+    PermuteOut o;
+    o.chunk_base = at<int>(ws, lo.chunk_base);
+    o.grp_off = at<int>(ws, lo.grp_off);
+    o.grp_cnt = at<int>(ws, lo.grp_cnt);
+    o.act_group = at<int>(ws, lo.act_group);
+    o.act_tile = at<int>(ws, lo.act_tile);
+    o.sorted_pair = sorted_pair ? sorted_pair : at<int32_t>(ws, lo.sorted_pair);
+    o.slot_of_pair = slot_of_pair ? slot_of_pair : at<int32_t>(ws, lo.slot_of_pair);
+    o.expert_offsets = expert_offsets;
+    return o;
+}
+
+int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, const int32_t* ids, const float* w,
+                void* out, int arm, void* ws, Launcher& ln) {
+    const moe_config& c = L->cfg;
+    const cudaStream_t st = ln.st;
+    const int E = c.num_experts, k = c.top_k, H = c.hidden, I = c.inter;
+    WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
+    const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
+    MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->has_shared ? 1 : 0, po, hdr, st));
+    MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(ids, m, k, E, po, st));
+    if (arm == MOE_ARM_AUTO) arm = moe_select_arm(L, m);
+    const int has_shared = L->has_shared ? 1 : 0;
+    if (arm == MOE_ARM_GEMV) {
+        GemvArgs a;
+        a.hdr = hdr;
+        a.grp_off = po.grp_off;
+        a.grp_cnt = po.grp_cnt;
+        a.act_group = po.act_group;
+        a.sorted_pair = po.sorted_pair;
+        a.P = lo.P;
+        a.k = k;
+        a.E = E;
+        a.H = H;
+        a.I = I;
+        a.max_groups = std::min(E, lo.P) + has_shared;
+        a.w1 = L->routed.w1; a.w3 = L->routed.w3; a.w2 = L->routed.w2;
+        a.s1 = L->routed.s1; a.s3 = L->routed.s3; a.s2 = L->routed.s2;
+        a.sw1 = L->shared.w1; a.sw3 = L->shared.w3; a.sw2 = L->shared.w2;
+        a.ss1 = L->shared.s1; a.ss3 = L->shared.s3; a.ss2 = L->shared.s2;
+        float* y = at<float>(ws, lo.y);
+        if (L->fp8) {
+            uint8_t* xq = at<uint8_t>(ws, lo.xq);
+            float* xsc = at<float>(ws, lo.xsc);
+            uint8_t* hq = at<uint8_t>(ws, lo.h);
+            float* hsc = at<float>(ws, lo.hsc);
+            MOE_LAUNCH(K_ACT_QUANT, launch_act_quant_fp8(static_cast<const uint16_t*>(x), m, H, xq, xsc, st));
+            MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_fp8(a, xq, xsc, hq, hsc, st));
+            MOE_LAUNCH(K_GEMV_DOWN, launch_gemv_down_fp8(a, hq, hsc, y, st));
+        } else {
+            uint16_t* h = at<uint16_t>(ws, lo.h);
+            MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_bf16(a, static_cast<const uint16_t*>(x), h, st));
+            MOE_LAUNCH(K_GEMV_DOWN, launch_gemv_down_bf16(a, h, y, st));
+        }
+        MOE_LAUNCH(K_COMBINE, launch_combine_f32(y, po.slot_of_pair, w, m, k, H, lo.P, has_shared, static_cast<uint16_t*>(out),
+                                      st));
+        return MOE_OK;
+    }
+    if (arm != MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
+    if (!gemm_supported(L->cfg)) return MOE_ERR_UNSUPPORTED;
+    GemmCall g{};
+    g.hdr = hdr;
+    g.grp_off = po.grp_off;
+    g.grp_cnt = po.grp_cnt;
+    g.act_group = po.act_group;
+    g.act_tile = po.act_tile;
+    g.rows = lo.rows;
+    g.E = E;
+    g.H = H;
+    g.I = I;
+    g.max_tiles = gemm_max_tiles(lo.P, E, has_shared, m);
+    uint16_t* ybf = at<uint16_t>(ws, lo.y);
+    if (L->fp8) {
+        uint8_t* xq = at<uint8_t>(ws, lo.xq);
+        float* xsc = at<float>(ws, lo.xsc);
+        MOE_LAUNCH(K_ACT_QUANT, launch_act_quant_fp8(static_cast<const uint16_t*>(x), m, H, xq, xsc, st));
+        MOE_LAUNCH(K_GATHER, launch_gather_fp8(xq, xsc, po.sorted_pair, k, lo.P, lo.rows, H, at<uint8_t>(ws, lo.xs),
+                                     at<float>(ws, lo.xs_sc), st));
+        g.xs = at<void>(ws, lo.xs);
+        g.xs_sc = at<float>(ws, lo.xs_sc);
+        g.h = at<void>(ws, lo.h);
+        g.hsc = at<float>(ws, lo.hsc);
+    } else {
+        MOE_LAUNCH(K_GATHER, launch_gather_bf16(static_cast<const uint16_t*>(x), po.sorted_pair, k, lo.P, lo.rows, H,
+                                      at<uint16_t>(ws, lo.xs), st));
+        g.xs = at<void>(ws, lo.xs);
+        g.h = at<void>(ws, lo.h);
+    }
+    g.y = ybf;
+    GemmLaunch gl;
+    int rc = gemm_plan(L->gemm, g, &gl);
+    if (rc != MOE_OK) return rc;
+    MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(gl, st));
+    MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(gl, st));
+    MOE_LAUNCH(K_COMBINE, launch_combine_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, static_cast<uint16_t*>(out),
+                                   st));
+    return MOE_OK;
+}
+
+bool weights_ok(const moe_expert_weights* w, bool fp8) {
+    if (!w || !w->w1 || !w->w3 || !w->w2) return false;
+    if (!aligned(w->w1, 16) || !aligned(w->w3, 16) || !aligned(w->w2, 16)) return false;
+    if (fp8 && (!w->s1 || !w->s3 || !w->s2)) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, const moe_expert_weights* shared,
+                     moe_layer** out) {
+    if (!cfg || !out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    const moe_config& c = *cfg;
+    if (c.weights != MOE_WEIGHTS_BF16 && c.weights != MOE_WEIGHTS_FP8_E4M3_B128) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = c.weights == MOE_WEIGHTS_FP8_E4M3_B128;
+    if (c.hidden <= 0 || c.inter <= 0 || c.num_experts <= 0 || c.top_k <= 0 || c.shared_inter < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (c.top_k > c.num_experts) return MOE_ERR_INVALID_ARG;
+    if (c.num_experts > kMaxExperts || c.top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+    if (c.hidden % 128 != 0 || c.inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (fp8 && c.inter % 512 != 0) return MOE_ERR_UNSUPPORTED;
+    if (c.shared_inter != 0 && c.shared_inter != c.inter) return MOE_ERR_UNSUPPORTED;
+    if (!weights_ok(routed, fp8)) return MOE_ERR_INVALID_ARG;
+    const bool has_shared = c.shared_inter > 0;
+    if (has_shared != (shared != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (has_shared && !weights_ok(shared, fp8)) return MOE_ERR_INVALID_ARG;
+    moe_layer* L = new (std::nothrow) moe_layer();
+    if (!L) return MOE_ERR_INVALID_ARG;
+    L->cfg = c;
+    L->routed = *routed;
+    if (has_shared) L->shared = *shared;
+    L->has_shared = has_shared;
+    L->fp8 = fp8;
+    L->last_launches = 0;
+    if (cudaGetDevice(&L->device) != cudaSuccess) {
+        delete L;
+        return MOE_ERR_CUDA;
+    }
+    const int rc = gemm_prepare_weights(c, routed, has_shared ? shared : nullptr, &L->gemm);
+    if (rc != MOE_OK) {
+        delete L;
+        return rc;
+    }
+    *out = L;
+    return MOE_OK;
+}
+
+int moe_layer_destroy(moe_layer* layer) {
+    delete layer;
+    return MOE_OK;
+}
+
+int moe_workspace_size(const moe_layer* layer, int64_t m, size_t* bytes) {
+    if (!layer || !bytes || m < 0) return MOE_ERR_INVALID_ARG;
+    *bytes = layout(layer, m).total;
+    return MOE_OK;
+}
+
+int moe_select_arm(const moe_layer* layer, int64_t m) {
+    if (!layer) return MOE_ERR_INVALID_ARG;
+    // rows per selected expert: the GEMV arm while they stay few (span-02
+    // forward_rows takes its GEMV path for r <= 16 rows; metrale moe_v41 for
+    // groups of at most eight rows)
+    const int64_t P = m * layer->cfg.top_k;
+    if (!gemm_supported(layer->cfg)) return MOE_ARM_GEMV;
+    return P <= (int64_t)8 * layer->cfg.num_experts ? MOE_ARM_GEMV : MOE_ARM_GEMM;
+}
+
+int moe_route(const moe_layer* layer, const void* x, int64_t m, const float* router_w, const float* router_bias,
+              float* logits_out, int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
+              void* stream) {
+    Layout lo;
+    int rc = check_call(layer, m, workspace, workspace_bytes, &lo);
+    if (rc != MOE_OK || m == 0) return rc;
+    if (!x || !router_w || !topk_ids || !topk_w || !aligned(x, 16) || !aligned(router_w, 16))
+        return MOE_ERR_INVALID_ARG;
+    Launcher ln{layer, static_cast<cudaStream_t>(stream)};
+    rc = run_route(layer, lo, x, (int)m, router_w, router_bias, logits_out, topk_ids, topk_w, workspace, ln);
+    layer->last_launches = ln.n;
+    return rc;
+}
+
+int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t m, int32_t* expert_offsets,
+                int32_t* sorted_pair, int32_t* slot_of_pair, void* workspace, size_t workspace_bytes, void* stream) {
+    Layout lo;
+    int rc = check_call(layer, m, workspace, workspace_bytes, &lo);
+    if (rc != MOE_OK || m == 0) return rc;
+    if (!topk_ids || !expert_offsets || !sorted_pair || !slot_of_pair) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WsHeader* hdr = at<WsHeader>(workspace, lo.hdr);
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
+    Launcher ln{layer, st};
+    const PermuteOut po = permute_out(lo, workspace, sorted_pair, slot_of_pair, expert_offsets);
+    const int k = layer->cfg.top_k, E = layer->cfg.num_experts;
+    MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(topk_ids, (int)m, k, E, 0, po, hdr, st));
+    MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(topk_ids, (int)m, k, E, po, st));
+    layer->last_launches = ln.n;
+    return MOE_OK;
+}
+
+int moe_experts(const moe_layer* layer, const void* x, int64_t m, const int32_t* topk_ids, const float* topk_w,
+                void* out, int arm, void* workspace, size_t workspace_bytes, void* stream) {
+    Layout lo;
+    int rc = check_call(layer, m, workspace, workspace_bytes, &lo);
+    if (rc != MOE_OK || m == 0) return rc;
+    if (!x || !topk_ids || !topk_w || !out || !aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    if (arm < MOE_ARM_AUTO || arm > MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
+    Launcher ln{layer, static_cast<cudaStream_t>(stream)};
+    rc = run_experts(layer, lo, x, (int)m, topk_ids, topk_w, out, arm, workspace, ln);
+    layer->last_launches = ln.n;
+    return rc;
+}
+
+int moe_forward(const moe_layer* layer, const void* x, int64_t m, const float* router_w, const float* router_bias,
+                void* out, int32_t* topk_ids_out, float* topk_w_out, int arm, void* workspace, size_t workspace_bytes,
+                void* stream) {
+    Layout lo;
+    int rc = check_call(layer, m, workspace, workspace_bytes, &lo);
+    if (rc != MOE_OK || m == 0) return rc;
+    if (!x || !router_w || !out || !aligned(x, 16) || !aligned(out, 16) || !aligned(router_w, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (arm < MOE_ARM_AUTO || arm > MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, lo.ids);
+    float* w = topk_w_out ? topk_w_out : at<float>(workspace, lo.w);
+    Launcher ln{layer, st};
+    rc = run_route(layer, lo, x, (int)m, router_w, router_bias, nullptr, ids, w, workspace, ln);
+    if (rc == MOE_OK) rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln);
+    layer->last_launches = ln.n;
+    return rc;
+}
+
+int moe_act_quant_fp8(const void* x, int64_t rows, int64_t n, uint8_t* codes, float* scales, void* stream) {
+    if (rows < 0 || n <= 0 || n % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (rows * (n / 128) > INT32_MAX / 8) return MOE_ERR_UNSUPPORTED;
+    if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16)) return MOE_ERR_INVALID_ARG;
+    if (launch_act_quant_fp8(static_cast<const uint16_t*>(x), (int)rows, (int)n, codes, scales,
+                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_device_status(const void* workspace, void* stream, int32_t* device_code) {
+    if (!workspace || !device_code) return MOE_ERR_INVALID_ARG;
+    WsHeader h;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    *device_code = h.err;
+    return h.err ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+int moe_last_launch_count(const moe_layer* layer) { return layer ? layer->last_launches : -1; }
+
+int moe_kernel_timing_enable(moe_layer* layer, int enable) {
+    if (!layer) return MOE_ERR_INVALID_ARG;
+    if (layer->timer.resolve() != 0) return MOE_ERR_CUDA;
+    layer->timer.on = enable != 0;
+    for (int i = 0; i < K_COUNT; ++i) {
+        layer->timer.ms[i] = 0.0;
+        layer->timer.launches[i] = 0;
+    }
+    return MOE_OK;
+}
+
+int moe_kernel_timing_read(moe_layer* layer, int kernel, double* total_ms, int64_t* launches) {
+    if (!layer || kernel < 0 || kernel >= K_COUNT || !total_ms || !launches) return MOE_ERR_INVALID_ARG;
+    if (layer->timer.resolve() != 0) return MOE_ERR_CUDA;
+    *total_ms = layer->timer.ms[kernel];
+    *launches = layer->timer.launches[kernel];
+    return MOE_OK;
+}
+
+int moe_kernel_count(void) { return K_COUNT; }
+
+const char* moe_kernel_name(int kernel) {
+    return (kernel >= 0 && kernel < K_COUNT) ? kKernelNames[kernel] : "unknown";
+}
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE: return "device-side error flag set";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

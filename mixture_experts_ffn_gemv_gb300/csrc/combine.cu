@@ -1,0 +1,72 @@
+// Unpermute + routing-weighted reduce + shared-expert add: step "7. Unpermute
+// + weighted reduce" of spark_model/layers/moe/forward_prefill.rs
+// (moe_unpermute_reduce_indexed) and shared_expert_tail of metrale
+// moe_v41/forward.rs (acc += sd, then out = bf16(acc)).
+//
+// out[t, :] = sum_{j < k} w[t, j] * Y[slot_of_pair[t*k + j], :]  (+ Y[P + t, :])
+// accumulated in fp32 in ascending j, a gather (no atomics), so the result is
+// deterministic and out is fully overwritten.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    v[0] = bf16lo(a.x); v[1] = bf16hi(a.x); v[2] = bf16lo(a.y); v[3] = bf16hi(a.y);
+    v[4] = bf16lo(a.z); v[5] = bf16hi(a.z); v[6] = bf16lo(a.w); v[7] = bf16hi(a.w);
+}
+
+// grid (ceil(H / 1024), m), 128 threads x 8 columns
+template <typename YT>
+__global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
+                                               const float* __restrict__ w, int k, int H, int P, int has_shared,
+                                               uint16_t* __restrict__ out) {
+    const int t = blockIdx.y;
+    const int h0 = (blockIdx.x * 128 + threadIdx.x) * 8;
+    if (h0 >= H) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+        const int s = slot[(size_t)t * k + j];
+        if (s < 0 || s >= P) continue;  // pair with an invalid expert id
+        const float wj = w[(size_t)t * k + j];
+        float v[8];
+        load8(y + (size_t)s * H + h0, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+    }
+    if (has_shared) {
+        float v[8];
+        load8(y + (size_t)(P + t) * H + h0, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(out + (size_t)t * H + h0) = o;
+}
+
+cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
+                               int P, int has_shared, uint16_t* out, cudaStream_t st) {
+    const dim3 grid(ceil_div(H, 1024), m);
+    combine<float><<<grid, 128, 0, st>>>(y, slot_of_pair, w, k, H, P, has_shared, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
+                                int H, int P, int has_shared, uint16_t* out, cudaStream_t st) {
+    const dim3 grid(ceil_div(H, 1024), m);
+    combine<uint16_t><<<grid, 128, 0, st>>>(y, slot_of_pair, w, k, H, P, has_shared, out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,97 @@
+// Shared device helpers of the MoE FFN kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Workspace header (first 256 bytes of every workspace), zeroed at the start
+// of each entry-point call.
+struct WsHeader {
+    int err;          // first device error code (0 = none)
+    int err_info;     // detail (e.g. offending index)
+    int done;         // permute: chunks finished (last chunk does the scan)
+    int n_active;     // groups with at least one row
+    int total_tiles;  // grouped GEMM: m-tiles over all active groups
+    int pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// device error codes (the header's err word)
+enum : int {
+    DEV_ERR_NONE = 0,
+    DEV_ERR_BAD_ID = 1,      // expert id outside [0, E)
+    DEV_ERR_TIMEOUT = 2,     // a bounded mbarrier wait ran out
+    DEV_ERR_CAPACITY = 3,    // a size the launch was not set up for
+};
+
+__device__ __forceinline__ void set_error(WsHeader* h, int code, int info) {
+    if (atomicCAS(&h->err, 0, code) == 0) h->err_info = info;
+}
+
+// ---- bf16 / fp32
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs)
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)((u >> 16) | ((u & 0xffff) ? 0x40 : 0));
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
+}
+
+// ---- loads
+// Streaming 16-byte load that bypasses L1 allocation (weights are read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// ---- e4m3
+// Two e4m3 codes (low byte = element 0) -> two floats.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
+    uint32_t h2;
+    uint16_t c = (uint16_t)two_codes;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    float2 r;
+    asm("{ .reg .f16 a, b;\n\t mov.b32 {a, b}, %2;\n\t cvt.f32.f16 %0, a;\n\t cvt.f32.f16 %1, b; }"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(h2));
+    return r;
+}
+
+// Two floats -> two e4m3 codes (element 0 in the low byte), round to nearest
+// even, saturating to +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float e0, float e1) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(e1), "f"(e0));
+    return (uint32_t)r;
+}
+
+// ---- warp reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// SiLU(g) * u with silu(g) = g / (1 + exp(-g)).
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace moe

@@ -1,0 +1,54 @@
+// Grouped-GEMM arm (tcgen05 / TMEM / TMA, sm_103a): host interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_ffn.h"
+
+namespace moe {
+
+struct WsHeader;
+
+// TMA descriptors of the stacked weights, built once per layer on the host.
+struct GemmWeights {
+    bool ready;
+    CUtensorMap w13;   // routed gate/up weights, [E][2][I][H] view: W1 and W3 tiles
+    CUtensorMap w1, w3, w2;
+    CUtensorMap sw1, sw3, sw2;
+};
+
+struct GemmCall {
+    WsHeader* hdr;
+    const int* grp_off;
+    const int* grp_cnt;
+    const int* act_group;
+    const int* act_tile;
+    int rows, E, H, I, max_tiles;
+    void* xs;      // gathered activations [rows, H] (bf16 or e4m3)
+    float* xs_sc;  // fp8: [rows, H/128]
+    void* h;       // [rows, I] (bf16 or e4m3)
+    float* hsc;    // fp8: [rows, I/128]
+    uint16_t* y;   // [rows, H] bf16
+};
+
+// Everything the two grouped-GEMM launches of one call need (tensor maps of
+// the call's activation buffers included).
+struct GemmLaunch {
+    const GemmWeights* w;
+    GemmCall call;
+    CUtensorMap a_xs;  // gate/up A operand: gathered activations
+    CUtensorMap a_h;   // down A operand: h
+    int grid;
+};
+
+bool gemm_supported(const moe_config& c);
+int gemm_max_tiles(int P, int E, int has_shared, int m);
+int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, const moe_expert_weights* shared,
+                         GemmWeights* out);
+int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out);  // MOE_OK or an error status
+cudaError_t launch_gemm_gateup(const GemmLaunch& p, cudaStream_t st);
+cudaError_t launch_gemm_down(const GemmLaunch& p, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,449 @@
+// Small-m expert arm: for each non-empty expert, stream its weights exactly
+// once and apply them to the (few) token rows routed to it.
+//
+// Follows the decode chain of span-02 gpu_model/forward.rs (forward_rows,
+// "small = r <= 16": moe_glu_decode = gate/up fused with SiLU(gate)*up, then
+// moe_down_decode) and the one-launch-over-all-selected-experts idea of
+// metrale moe_v41 forward.rs (routed_m1 over a pointer table): one launch
+// covers every active expert, indexed from the permute's compact group list.
+//
+// Inner product: the weights are the 16-row A operand and the tokens the
+// 8-column B operand of mma.sync (bf16 m16n8k16 / e4m3 m16n8k32, fp32
+// accumulate).  A 16-byte streaming load of one weight row feeds two MMAs:
+// the K order inside the load is permuted identically for the weight and the
+// token fragment, which leaves the dot product unchanged.  The kernel stays
+// HBM-bound with almost no ALU work per weight byte.
+//
+// fp8 weights carry one fp32 scale per 128x128 block and activations one per
+// 128 inputs: each 128-wide K block is accumulated into a fresh partial that
+// is then scaled by s_w * s_x and added (the two-level fp32 block-scale
+// accumulation of spark_model forward_prefill's fp8 grouped GEMM).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two MMAs from one 16-byte chunk of weight rows g and g+8 and one 16-byte
+// chunk of the token column's activations.
+__device__ __forceinline__ void mma2_bf16(float (&c)[4], const uint4& ag, const uint4& ag8, const uint4& xb) {
+    mma_bf16(c, ag.x, ag8.x, ag.y, ag8.y, xb.x, xb.y);
+    mma_bf16(c, ag.z, ag8.z, ag.w, ag8.w, xb.z, xb.w);
+}
+__device__ __forceinline__ void mma2_e4m3(float (&c)[4], const uint4& ag, const uint4& ag8, const uint4& xb) {
+    mma_e4m3(c, ag.x, ag8.x, ag.y, ag8.y, xb.x, xb.y);
+    mma_e4m3(c, ag.z, ag8.z, ag.w, ag8.w, xb.z, xb.w);
+}
+
+struct Group {
+    int g, off, cnt;
+};
+
+__device__ __forceinline__ bool load_group(const GemvArgs& a, int ga, Group& gr) {
+    if (ga >= a.hdr->n_active) return false;
+    gr.g = a.act_group[ga];
+    gr.off = a.grp_off[gr.g];
+    gr.cnt = a.grp_cnt[gr.g];
+    return true;
+}
+
+__device__ __forceinline__ int row_token(const GemvArgs& a, int s) {
+    return s < a.P ? a.sorted_pair[s] / a.k : s - a.P;
+}
+
+}  // namespace
+
+// ============================================================ gate/up, bf16
+// CTA: 8 warps = 2 row tiles (16 rows of I each) x 4 K-slices of H.  The four
+// K-slice partials are summed in fixed order through shared memory, then
+// h = silu(g) * u is stored as bf16 [rows, I].
+template <int NT>
+__global__ __launch_bounds__(256) void gemv_gateup_bf16(const GemvArgs a, const uint16_t* __restrict__ x,
+                                                        uint16_t* __restrict__ h, int n_slices) {
+    constexpr int KS = 4, RT = 2;
+    __shared__ float red[KS][RT][32][NT * 8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int rt = warp % RT, kq = warp / RT;
+    Group gr;
+    if (!load_group(a, blockIdx.x / n_slices, gr)) return;
+    const int H = a.H, I = a.I;
+    const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
+    const uint16_t* W1 = gr.g < a.E ? (const uint16_t*)a.w1 + (size_t)gr.g * I * H : (const uint16_t*)a.sw1;
+    const uint16_t* W3 = gr.g < a.E ? (const uint16_t*)a.w3 + (size_t)gr.g * I * H : (const uint16_t*)a.sw3;
+    const uint4* w1g = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8) * H);
+    const uint4* w1g8 = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8 + 8) * H);
+    const uint4* w3g = reinterpret_cast<const uint4*>(W3 + (size_t)(row0 + g8) * H);
+    const uint4* w3g8 = reinterpret_cast<const uint4*>(W3 + (size_t)(row0 + g8 + 8) * H);
+    const int kc0 = kq * (H / KS) / 8, kc1 = (kq + 1) * (H / KS) / 8;  // 16-byte chunk range
+    for (int r0 = 0; r0 < gr.cnt; r0 += 8 * NT) {
+        const int R = min(8 * NT, gr.cnt - r0);
+        const uint4* xr[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g8;
+            const int s = gr.off + r0 + (col < R ? col : 0);
+            xr[nt] = reinterpret_cast<const uint4*>(x + (size_t)row_token(a, s) * H);
+        }
+        float c1[NT][4], c3[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c1[nt][i] = c3[nt][i] = 0.f;
+#pragma unroll 4
+        for (int kc = kc0 + tig; kc < kc1; kc += 4) {
+            const uint4 a1 = ld_stream_v4(w1g + kc), a18 = ld_stream_v4(w1g8 + kc);
+            const uint4 a3 = ld_stream_v4(w3g + kc), a38 = ld_stream_v4(w3g8 + kc);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint4 xb = __ldg(xr[nt] + kc);
+                mma2_bf16(c1[nt], a1, a18, xb);
+                mma2_bf16(c3[nt], a3, a38, xb);
+            }
+        }
+        // fixed-order K-slice reduction
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                red[kq][rt][lane][nt * 8 + i] = c1[nt][i];
+                red[kq][rt][lane][nt * 8 + 4 + i] = c3[nt][i];
+            }
+        __syncthreads();
+        if (kq == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float gs[4], us[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    gs[i] = red[0][rt][lane][nt * 8 + i];
+                    us[i] = red[0][rt][lane][nt * 8 + 4 + i];
+                }
+#pragma unroll
+                for (int q = 1; q < KS; ++q)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        gs[i] += red[q][rt][lane][nt * 8 + i];
+                        us[i] += red[q][rt][lane][nt * 8 + 4 + i];
+                    }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int col = nt * 8 + tig * 2 + (i & 1);
+                    const int row = row0 + g8 + (i >> 1) * 8;
+                    if (col < R) h[(size_t)(gr.off + r0 + col) * I + row] = f32_to_bf16(swiglu(gs[i], us[i]));
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ============================================================ down, bf16
+// CTA: 2 row tiles (16 rows of H) x 4 K-slices of I; y fp32 [rows, H].
+template <int NT>
+__global__ __launch_bounds__(256) void gemv_down_bf16(const GemvArgs a, const uint16_t* __restrict__ h,
+                                                      float* __restrict__ y, int n_slices) {
+    constexpr int KS = 4, RT = 2;
+    __shared__ float red[KS][RT][32][NT * 4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int rt = warp % RT, kq = warp / RT;
+    Group gr;
+    if (!load_group(a, blockIdx.x / n_slices, gr)) return;
+    const int H = a.H, I = a.I;
+    const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
+    const uint16_t* W2 = gr.g < a.E ? (const uint16_t*)a.w2 + (size_t)gr.g * H * I : (const uint16_t*)a.sw2;
+    const uint4* wg = reinterpret_cast<const uint4*>(W2 + (size_t)(row0 + g8) * I);
+    const uint4* wg8 = reinterpret_cast<const uint4*>(W2 + (size_t)(row0 + g8 + 8) * I);
+    const int kc0 = kq * (I / KS) / 8, kc1 = (kq + 1) * (I / KS) / 8;
+    for (int r0 = 0; r0 < gr.cnt; r0 += 8 * NT) {
+        const int R = min(8 * NT, gr.cnt - r0);
+        const uint4* hr[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g8;
+            hr[nt] = reinterpret_cast<const uint4*>(h + (size_t)(gr.off + r0 + (col < R ? col : 0)) * I);
+        }
+        float c[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
+#pragma unroll 4
+        for (int kc = kc0 + tig; kc < kc1; kc += 4) {
+            const uint4 w0 = ld_stream_v4(wg + kc), w8 = ld_stream_v4(wg8 + kc);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma2_bf16(c[nt], w0, w8, __ldg(hr[nt] + kc));
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[kq][rt][lane][nt * 4 + i] = c[nt][i];
+        __syncthreads();
+        if (kq == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float v = red[0][rt][lane][nt * 4 + i];
+#pragma unroll
+                    for (int q = 1; q < KS; ++q) v += red[q][rt][lane][nt * 4 + i];
+                    const int col = nt * 8 + tig * 2 + (i & 1);
+                    const int row = row0 + g8 + (i >> 1) * 8;
+                    if (col < R) y[(size_t)(gr.off + r0 + col) * H + row] = v;
+                }
+        }
+        __syncthreads();
+    }
+}
+
+// ============================================================ gate/up, fp8
+// CTA: 8 row tiles = 128 rows of I (one scale block), whole H per warp, so the
+// CTA can quantise its h block (1x128 along I) itself: hq e4m3 [rows, I] and
+// hsc fp32 [rows, I/128].
+template <int NT>
+__global__ __launch_bounds__(256) void gemv_gateup_fp8(const GemvArgs a, const uint8_t* __restrict__ xq,
+                                                       const float* __restrict__ xsc, uint8_t* __restrict__ hq,
+                                                       float* __restrict__ hsc, int n_slices) {
+    __shared__ float hs[NT * 8][128 + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, tig = lane & 3;
+    Group gr;
+    if (!load_group(a, blockIdx.x / n_slices, gr)) return;
+    const int H = a.H, I = a.I, hb = H / 128;
+    const int blk0 = (blockIdx.x % n_slices) * 128;  // first row of this CTA's I block
+    const int row0 = blk0 + warp * 16;
+    const bool routed = gr.g < a.E;
+    const uint8_t* W1 = routed ? (const uint8_t*)a.w1 + (size_t)gr.g * I * H : (const uint8_t*)a.sw1;
+    const uint8_t* W3 = routed ? (const uint8_t*)a.w3 + (size_t)gr.g * I * H : (const uint8_t*)a.sw3;
+    const float* S1 = (routed ? a.s1 + (size_t)gr.g * (I / 128) * hb : a.ss1) + (size_t)(blk0 / 128) * hb;
+    const float* S3 = (routed ? a.s3 + (size_t)gr.g * (I / 128) * hb : a.ss3) + (size_t)(blk0 / 128) * hb;
+    const uint4* w1g = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8) * H);
+    const uint4* w1g8 = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8 + 8) * H);
+    const uint4* w3g = reinterpret_cast<const uint4*>(W3 + (size_t)(row0 + g8) * H);
+    const uint4* w3g8 = reinterpret_cast<const uint4*>(W3 + (size_t)(row0 + g8 + 8) * H);
+    for (int r0 = 0; r0 < gr.cnt; r0 += 8 * NT) {
+        const int R = min(8 * NT, gr.cnt - r0);
+        const uint4* xr[NT];
+        const float* sa[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g8;
+            xr[nt] = reinterpret_cast<const uint4*>(xq + (size_t)row_token(a, gr.off + r0 + (col < R ? col : 0)) * H);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int cc = nt * 8 + tig * 2 + j;
+                sa[nt][j] = xsc + (size_t)row_token(a, gr.off + r0 + (cc < R ? cc : 0)) * hb;
+            }
+        }
+        float c1[NT][4], c3[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c1[nt][i] = c3[nt][i] = 0.f;
+        for (int b = 0; b < hb; ++b) {  // one 128-wide K block per pass: 8 chunks of 16 codes
+            float p1[NT][4], p3[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) p1[nt][i] = p3[nt][i] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int kc = b * 8 + q * 4 + tig;
+                const uint4 a1 = ld_stream_v4(w1g + kc), a18 = ld_stream_v4(w1g8 + kc);
+                const uint4 a3 = ld_stream_v4(w3g + kc), a38 = ld_stream_v4(w3g8 + kc);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint4 xb = __ldg(xr[nt] + kc);
+                    mma2_e4m3(p1[nt], a1, a18, xb);
+                    mma2_e4m3(p3[nt], a3, a38, xb);
+                }
+            }
+            const float sb1 = __ldg(S1 + b), sb3 = __ldg(S3 + b);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float sx0 = __ldg(sa[nt][0] + b), sx1 = __ldg(sa[nt][1] + b);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float sx = (i & 1) ? sx1 : sx0;
+                    c1[nt][i] = fmaf(p1[nt][i], sb1 * sx, c1[nt][i]);
+                    c3[nt][i] = fmaf(p3[nt][i], sb3 * sx, c3[nt][i]);
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int col = nt * 8 + tig * 2 + (i & 1);
+                const int rr = warp * 16 + g8 + (i >> 1) * 8;
+                hs[col][rr] = swiglu(c1[nt][i], c3[nt][i]);
+            }
+        __syncthreads();
+        // quantise each column's 128 values: one warp per column
+        for (int col = warp; col < R; col += 8) {
+            float v[4];
+            float amax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[j] = hs[col][lane * 4 + j];
+                amax = fmaxf(amax, fabsf(v[j]));
+            }
+            amax = warp_max(amax);
+            uint32_t codes = 0;
+            float s = 1.0f;
+            if (amax > 0.f) {
+                s = __fdiv_rn(amax, 448.0f);
+                codes = f32x2_to_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
+                        (f32x2_to_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
+            }
+            const size_t srow = (size_t)(gr.off + r0 + col);
+            *reinterpret_cast<uint32_t*>(hq + srow * I + blk0 + lane * 4) = codes;
+            if (lane == 0) hsc[srow * (I / 128) + blk0 / 128] = s;
+        }
+        __syncthreads();
+    }
+}
+
+// ============================================================ down, fp8
+// CTA: 2 row tiles (16 rows of H) x 4 K-slices of I (each a whole number of
+// 128-blocks); y fp32 [rows, H].
+template <int NT>
+__global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uint8_t* __restrict__ hq,
+                                                     const float* __restrict__ hsc, float* __restrict__ y,
+                                                     int n_slices) {
+    constexpr int KS = 4, RT = 2;
+    __shared__ float red[KS][RT][32][NT * 4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int rt = warp % RT, kq = warp / RT;
+    Group gr;
+    if (!load_group(a, blockIdx.x / n_slices, gr)) return;
+    const int H = a.H, I = a.I, ib = I / 128;
+    const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
+    const bool routed = gr.g < a.E;
+    const uint8_t* W2 = routed ? (const uint8_t*)a.w2 + (size_t)gr.g * H * I : (const uint8_t*)a.sw2;
+    const float* S2 = (routed ? a.s2 + (size_t)gr.g * (H / 128) * ib : a.ss2) + (size_t)(row0 / 128) * ib;
+    const uint4* wg = reinterpret_cast<const uint4*>(W2 + (size_t)(row0 + g8) * I);
+    const uint4* wg8 = reinterpret_cast<const uint4*>(W2 + (size_t)(row0 + g8 + 8) * I);
+    const int b0 = kq * (ib / KS), b1 = (kq + 1) * (ib / KS);
+    for (int r0 = 0; r0 < gr.cnt; r0 += 8 * NT) {
+        const int R = min(8 * NT, gr.cnt - r0);
+        const uint4* hr[NT];
+        const float* sa[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g8;
+            hr[nt] = reinterpret_cast<const uint4*>(hq + (size_t)(gr.off + r0 + (col < R ? col : 0)) * I);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int cc = nt * 8 + tig * 2 + j;
+                sa[nt][j] = hsc + (size_t)(gr.off + r0 + (cc < R ? cc : 0)) * ib;
+            }
+        }
+        float c[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
+        for (int b = b0; b < b1; ++b) {
+            float p[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) p[nt][i] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int kc = b * 8 + q * 4 + tig;
+                const uint4 w0 = ld_stream_v4(wg + kc), w8 = ld_stream_v4(wg8 + kc);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma2_e4m3(p[nt], w0, w8, __ldg(hr[nt] + kc));
+            }
+            const float sb = __ldg(S2 + b);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float sx0 = __ldg(sa[nt][0] + b), sx1 = __ldg(sa[nt][1] + b);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) c[nt][i] = fmaf(p[nt][i], sb * ((i & 1) ? sx1 : sx0), c[nt][i]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[kq][rt][lane][nt * 4 + i] = c[nt][i];
+        __syncthreads();
+        if (kq == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float v = red[0][rt][lane][nt * 4 + i];
+#pragma unroll
+                    for (int q = 1; q < KS; ++q) v += red[q][rt][lane][nt * 4 + i];
+                    const int col = nt * 8 + tig * 2 + (i & 1);
+                    const int row = row0 + g8 + (i >> 1) * 8;
+                    if (col < R) y[(size_t)(gr.off + r0 + col) * H + row] = v;
+                }
+        }
+        __syncthreads();
+    }
+}
+
+// ============================================================ launchers
+// Token columns per pass: 16 when a group can have more than 8 rows.
+static inline bool wide(const GemvArgs& a) { return a.P > 8 * a.max_groups || a.P >= 64; }
+
+cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st) {
+    const int n_slices = a.I / 32;
+    const dim3 grid(n_slices * a.max_groups);
+    if (wide(a)) gemv_gateup_bf16<2><<<grid, 256, 0, st>>>(a, x, h, n_slices);
+    else gemv_gateup_bf16<1><<<grid, 256, 0, st>>>(a, x, h, n_slices);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_down_bf16(const GemvArgs& a, const uint16_t* h, float* y, cudaStream_t st) {
+    const int n_slices = a.H / 32;
+    const dim3 grid(n_slices * a.max_groups);
+    if (wide(a)) gemv_down_bf16<2><<<grid, 256, 0, st>>>(a, h, y, n_slices);
+    else gemv_down_bf16<1><<<grid, 256, 0, st>>>(a, h, y, n_slices);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const float* xsc, uint8_t* hq,
+                                   float* hsc, cudaStream_t st) {
+    const int n_slices = a.I / 128;
+    const dim3 grid(n_slices * a.max_groups);
+    if (wide(a)) gemv_gateup_fp8<2><<<grid, 256, 0, st>>>(a, xq, xsc, hq, hsc, n_slices);
+    else gemv_gateup_fp8<1><<<grid, 256, 0, st>>>(a, xq, xsc, hq, hsc, n_slices);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
+                                 cudaStream_t st) {
+    const int n_slices = a.H / 32;
+    const dim3 grid(n_slices * a.max_groups);
+    if (wide(a)) gemv_down_fp8<2><<<grid, 256, 0, st>>>(a, hq, hsc, y, n_slices);
+    else gemv_down_fp8<1><<<grid, 256, 0, st>>>(a, hq, hsc, y, n_slices);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

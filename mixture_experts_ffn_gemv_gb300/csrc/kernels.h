@@ -1,0 +1,74 @@
+// Internal launch interface between the C-ABI host code and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct WsHeader;
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kRouterSmallMaxM = 64;  // up to this m the router is a split-H GEMV
+constexpr int kPermChunk = 2048;      // pairs per permute block (8 warps x 256)
+constexpr int kGemvRows = 8;          // token rows a GEMV block holds at once
+constexpr int kGemmBM = 128;          // grouped-GEMM m-tile (rows per tile)
+
+// routing
+int router_slices(int H, int m);
+cudaError_t launch_router(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
+                          cudaStream_t st);
+cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const float* bias, float* logits_out,
+                        int32_t* ids, float* w, cudaStream_t st);
+
+// permute: groups g < E are the routed experts, g == E the shared expert
+// (rows P .. P+m-1, token t at row P+t) when has_shared.
+struct PermuteOut {
+    int* chunk_base;         // [nchunk, E]
+    int* grp_off;            // [E+1] first sorted row of each group
+    int* grp_cnt;            // [E+1] rows of each group
+    int* act_group;          // [E+1] active (non-empty) groups, ascending
+    int* act_tile;           // [E+2] first m-tile of each active group; [n_active] = total
+    int32_t* sorted_pair;    // [P]
+    int32_t* slot_of_pair;   // [P]
+    int32_t* expert_offsets; // [E+1] optional copy for the caller (may be null)
+};
+cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int has_shared, const PermuteOut& o,
+                                 WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, const PermuteOut& o, cudaStream_t st);
+
+// activations
+cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st);
+cudaError_t launch_gather_bf16(const uint16_t* x, const int32_t* sorted_pair, int k, int P, int rows, int H,
+                               uint16_t* xs, cudaStream_t st);
+cudaError_t launch_gather_fp8(const uint8_t* xq, const float* xsc, const int32_t* sorted_pair, int k, int P,
+                              int rows, int H, uint8_t* xs, float* xs_sc, cudaStream_t st);
+
+// GEMV arm: h is bf16 (bf16 weights) or e4m3 + 1x128 scales (fp8 weights);
+// y is fp32; rows in sorted order
+struct GemvArgs {
+    const WsHeader* hdr;
+    const int* grp_off;
+    const int* grp_cnt;
+    const int* act_group;
+    const int32_t* sorted_pair;
+    int P, k, E, H, I, max_groups;
+    // routed weights (stacked) and the shared expert's (g == E)
+    const void *w1, *w3, *w2, *sw1, *sw3, *sw2;
+    const float *s1, *s3, *s2, *ss1, *ss3, *ss2;
+};
+cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st);
+cudaError_t launch_gemv_down_bf16(const GemvArgs& a, const uint16_t* h, float* y, cudaStream_t st);
+cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const float* xsc, uint8_t* hq,
+                                   float* hsc, cudaStream_t st);
+cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
+                                 cudaStream_t st);
+
+// combine: out[t] = sum_j w[t,j] * Y[slot(t,j)] (+ Y[P+t] when has_shared)
+cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
+                               int P, int has_shared, uint16_t* out, cudaStream_t st);
+cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
+                                int H, int P, int has_shared, uint16_t* out, cudaStream_t st);
+
+}  // namespace moe

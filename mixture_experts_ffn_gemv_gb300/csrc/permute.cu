@@ -1,0 +1,273 @@
+// Permute of (token, expert) pairs by expert: step "3. Sort tokens by expert"
+// of spark_model/layers/moe/forward_prefill.rs (moe_sort_by_expert), the
+// prefix-sum route of span-02 gpu_model/forward.rs (moe_route: counts,
+// offsets, pair_of_slot, slot_of_pair), and the device route scratch of
+// ferrum qwen3_moe/forward_layer.rs (expert offsets + per-block tile list).
+//
+// A stable counting sort in two launches:
+//   permute_count   per-chunk histograms; the last chunk to finish (an atomic
+//                   ticket, no waiting) scans them into per-(chunk, expert)
+//                   bases, expert offsets, the list of non-empty groups and
+//                   the grouped GEMM's m-tile starts;
+//   permute_scatter per chunk, warp-level ranks (match_any) give each pair
+//                   its slot: pairs keep ascending order within an expert.
+// Plus the activation gathers for the grouped GEMM and the fp8 activation
+// quantiser (one e4m3 code + fp32 scale per 128 inputs).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// Exclusive scan of a[0, n) in shared memory by a 256-thread block; returns
+// the total.  Every thread of the block must call it.
+__device__ int block_exclusive_scan(int* a, int n, int* warp_sums) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + 255) / 256;
+    const int b = tid * per, e = min(n, b + per);
+    int local = 0;
+    for (int i = b; i < e; ++i) local += a[i];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < 8; ++w) {
+            const int v = warp_sums[w];
+            warp_sums[w] = run;
+            run += v;
+        }
+        warp_sums[8] = run;
+    }
+    __syncthreads();
+    int run = warp_sums[warp] + incl - local;
+    for (int i = b; i < e; ++i) {
+        const int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    __syncthreads();
+    return warp_sums[8];
+}
+
+__global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__ ids, int P, int m, int E,
+                                                     int has_shared, int nchunk, PermuteOut o, WsHeader* hdr) {
+    __shared__ int hist[kMaxExperts + 2];
+    __shared__ int off[kMaxExperts + 2];
+    __shared__ int wsum[9];
+    __shared__ int is_last;
+    const int tid = threadIdx.x;
+    const int c = blockIdx.x;
+    const int p0 = c * kPermChunk, p1 = min(P, p0 + kPermChunk);
+    for (int e = tid; e < E; e += 256) hist[e] = 0;
+    __syncthreads();
+    for (int p = p0 + tid; p < p1; p += 256) {
+        const int e = ids[p];
+        if (e < 0 || e >= E) {
+            set_error(hdr, DEV_ERR_BAD_ID, p);
+            continue;
+        }
+        atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += 256) o.chunk_base[(size_t)c * E + e] = hist[e];
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) is_last = (atomicAdd(&hdr->done, 1) == nchunk - 1);
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+
+    // per-expert totals; chunk bases relative to the expert's first row
+    for (int e = tid; e < E; e += 256) {
+        int run = 0;
+        for (int cc = 0; cc < nchunk; ++cc) {
+            const int v = __ldcg(&o.chunk_base[(size_t)cc * E + e]);
+            o.chunk_base[(size_t)cc * E + e] = run;
+            run += v;
+        }
+        hist[e] = run;
+        off[e] = run;
+    }
+    if (tid == 0) hist[E] = has_shared ? m : 0;
+    __syncthreads();
+    block_exclusive_scan(off, E, wsum);
+    for (int e = tid; e < E; e += 256) {
+        o.grp_off[e] = off[e];
+        o.grp_cnt[e] = hist[e];
+        if (o.expert_offsets) o.expert_offsets[e] = off[e];
+        for (int cc = 0; cc < nchunk; ++cc) o.chunk_base[(size_t)cc * E + e] += off[e];
+    }
+    if (tid == 0) {
+        o.grp_off[E] = P;
+        o.grp_cnt[E] = hist[E];
+        if (o.expert_offsets) o.expert_offsets[E] = P;
+    }
+    __syncthreads();
+    // non-empty groups (routed experts, then the shared expert), ascending
+    for (int g = tid; g <= E; g += 256) off[g] = hist[g] > 0 ? 1 : 0;
+    __syncthreads();
+    const int n_active = block_exclusive_scan(off, E + 1, wsum);
+    for (int g = tid; g <= E; g += 256)
+        if (hist[g] > 0) o.act_group[off[g]] = g;
+    __syncthreads();
+    // m-tiles of kGemmBM rows per active group, as a prefix over groups
+    for (int g = tid; g <= E; g += 256) {
+        const int flagpos = off[g];
+        off[g] = hist[g] > 0 ? (hist[g] + kGemmBM - 1) / kGemmBM : 0;
+        hist[g] = hist[g] > 0 ? flagpos : -1;  // reuse: position in the active list
+    }
+    __syncthreads();
+    const int total_tiles = block_exclusive_scan(off, E + 1, wsum);
+    for (int g = tid; g <= E; g += 256)
+        if (hist[g] >= 0) o.act_tile[hist[g]] = off[g];
+    if (tid == 0) {
+        o.act_tile[n_active] = total_tiles;
+        hdr->n_active = n_active;
+        hdr->total_tiles = total_tiles;
+        hdr->done = 0;
+    }
+}
+
+__global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict__ ids, int P, int E, PermuteOut o) {
+    extern __shared__ int wbase[];  // [8][E]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x;
+    const int p0 = c * kPermChunk + warp * (kPermChunk / 8);
+    const int p1 = min(P, p0 + kPermChunk / 8);
+    for (int i = tid; i < 8 * E; i += 256) wbase[i] = 0;
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    int* mine = wbase + warp * E;
+    for (int pb = p0; pb < p0 + kPermChunk / 8; pb += 32) {
+        const int p = pb + lane;
+        int e = -1;
+        if (p < p1) {
+            e = ids[p];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += 256) {
+        int run = o.chunk_base[(size_t)c * E + e];
+        for (int w = 0; w < 8; ++w) {
+            const int v = wbase[w * E + e];
+            wbase[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int pb = p0; pb < p0 + kPermChunk / 8; pb += 32) {
+        const int p = pb + lane;
+        int e = -1;
+        if (p < p1) {
+            e = ids[p];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0) {
+            const int slot = mine[e] + __popc(peers & lt);
+            o.sorted_pair[slot] = p;
+            o.slot_of_pair[p] = slot;
+        } else if (p < p1) {
+            o.slot_of_pair[p] = -1;  // invalid id (flagged by permute_count): the pair is dropped
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int has_shared, const PermuteOut& o,
+                                 WsHeader* hdr, cudaStream_t st) {
+    const int P = m * k;
+    const int nchunk = ceil_div(P, kPermChunk);
+    permute_count<<<nchunk, 256, 0, st>>>(ids, P, m, E, has_shared, nchunk, o, hdr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, const PermuteOut& o, cudaStream_t st) {
+    const int P = m * k;
+    const int nchunk = ceil_div(P, kPermChunk);
+    const size_t smem = sizeof(int) * 8 * (size_t)E;
+    permute_scatter<<<nchunk, 256, smem, st>>>(ids, P, E, o);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- gathers
+// Row s of the grouped-GEMM input: token sorted_pair[s] / k for s < P (routed
+// pairs), token s - P for the shared expert's rows.  One warp per row.
+__global__ __launch_bounds__(256) void gather_bf16(const uint16_t* __restrict__ x,
+                                                   const int32_t* __restrict__ sorted_pair, int k, int P,
+                                                   int rows, int H, uint16_t* __restrict__ xs) {
+    const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (s >= rows) return;
+    const int t = s < P ? sorted_pair[s] / k : s - P;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
+    for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+}
+
+__global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq, const float* __restrict__ xsc,
+                                                  const int32_t* __restrict__ sorted_pair, int k, int P, int rows,
+                                                  int H, uint8_t* __restrict__ xs, float* __restrict__ xs_sc) {
+    const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (s >= rows) return;
+    const int t = s < P ? sorted_pair[s] / k : s - P;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
+    for (int c = lane; c < H / 16; c += 32) dst[c] = __ldg(src + c);
+    const int nb = H / 128;
+    for (int b = lane; b < nb; b += 32) xs_sc[(size_t)s * nb + b] = xsc[(size_t)t * nb + b];
+}
+
+cudaError_t launch_gather_bf16(const uint16_t* x, const int32_t* sorted_pair, int k, int P, int rows, int H,
+                               uint16_t* xs, cudaStream_t st) {
+    gather_bf16<<<ceil_div(rows, 8), 256, 0, st>>>(x, sorted_pair, k, P, rows, H, xs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_fp8(const uint8_t* xq, const float* xsc, const int32_t* sorted_pair, int k, int P,
+                              int rows, int H, uint8_t* xs, float* xs_sc, cudaStream_t st) {
+    gather_fp8<<<ceil_div(rows, 8), 256, 0, st>>>(xq, xsc, sorted_pair, k, P, rows, H, xs, xs_sc);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- fp8 activations
+// One warp per (token, 128-block): s = amax / 448 (IEEE divide), code =
+// e4m3_rn_satfinite(x / s); an all-zero block gets s = 1 and zero codes.
+__global__ __launch_bounds__(256) void act_quant_fp8(const uint16_t* __restrict__ x, int m, int H,
+                                                     uint8_t* __restrict__ xq, float* __restrict__ xsc) {
+    const int nb = H / 128;
+    const int blk = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (blk >= m * nb) return;
+    const int t = blk / nb, b = blk % nb;
+    const size_t base = (size_t)t * H + (size_t)b * 128 + lane * 4;
+    const uint2 v = *reinterpret_cast<const uint2*>(x + base);
+    const float f0 = bf16lo(v.x), f1 = bf16hi(v.x), f2 = bf16lo(v.y), f3 = bf16hi(v.y);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+    uint32_t codes = 0;
+    float s = 1.0f;
+    if (amax > 0.f) {
+        s = __fdiv_rn(amax, 448.0f);
+        codes = f32x2_to_e4m3x2(__fdiv_rn(f0, s), __fdiv_rn(f1, s)) |
+                (f32x2_to_e4m3x2(__fdiv_rn(f2, s), __fdiv_rn(f3, s)) << 16);
+    }
+    *reinterpret_cast<uint32_t*>(xq + base) = codes;
+    if (lane == 0) xsc[(size_t)t * nb + b] = s;
+}
+
+cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st) {
+    const int blocks = m * (H / 128);
+    act_quant_fp8<<<ceil_div(blocks, 8), 256, 0, st>>>(x, m, H, xq, xs);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

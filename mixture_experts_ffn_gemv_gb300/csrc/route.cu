@@ -1,0 +1,209 @@
+// Router logits and softmax top-k (steps "1. Gate GEMM" and "2. Batched topK
+// dispatch" of spark_model/layers/moe/forward_prefill.rs; the fused decode
+// router of span-02 gpu_model/forward.rs, moe_router_decode).
+//
+// The logits are produced as S partial sums over disjoint slices of H
+// ([S, m, E] fp32); the top-k kernel adds the partials in slice order, so the
+// result is deterministic and the decode case can spread a 1-token GEMV over
+// many SMs without atomics.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- small m
+// grid (ceil(E/8), S); 8 warps, warp w owns expert blockIdx.x*8+w over the
+// H-slice [s*HS, (s+1)*HS).  HS is a multiple of 128 (32 lanes x float4).
+template <int MT>
+__global__ __launch_bounds__(256) void router_partial_small(const uint16_t* __restrict__ x, int m, int H,
+                                                            const float* __restrict__ wr, int E, int HS,
+                                                            float* __restrict__ part) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + warp;
+    if (e >= E) return;
+    const int s = blockIdx.y;
+    const int h0 = s * HS, h1 = h0 + HS;
+    const float* we = wr + (size_t)e * H;
+    for (int t0 = 0; t0 < m; t0 += MT) {
+        float acc[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+        for (int h = h0 + lane * 4; h < h1; h += 128) {
+            const float4 w = __ldg(reinterpret_cast<const float4*>(we + h));
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                if (t0 + t < m) {
+                    const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * H + h));
+                    acc[t] = fmaf(w.x, bf16lo(xv.x), acc[t]);
+                    acc[t] = fmaf(w.y, bf16hi(xv.x), acc[t]);
+                    acc[t] = fmaf(w.z, bf16lo(xv.y), acc[t]);
+                    acc[t] = fmaf(w.w, bf16hi(xv.y), acc[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const float v = warp_sum(acc[t]);
+            if (lane == 0 && t0 + t < m) part[((size_t)s * m + t0 + t) * E + e] = v;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- large m
+// Tiled fp32 SIMT GEMM: L[m, E] = X[m, H] * Wr[E, H]^T.  Tile 64 tokens x 64
+// experts x 32 of H; 256 threads, 4x4 outputs each.  H % 32 == 0.
+constexpr int RT_BM = 64, RT_BN = 64, RT_BK = 32;
+__global__ __launch_bounds__(256) void router_logits_tiled(const uint16_t* __restrict__ x, int m, int H,
+                                                           const float* __restrict__ wr, int E,
+                                                           float* __restrict__ L) {
+    __shared__ float xs[RT_BK][RT_BM + 4];
+    __shared__ float ws[RT_BK][RT_BN + 4];
+    const int tid = threadIdx.x;
+    const int tx = tid & 15, ty = tid >> 4;
+    const int m0 = blockIdx.x * RT_BM, e0 = blockIdx.y * RT_BN;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < H; k0 += RT_BK) {
+        // x tile: 64 rows x 32 bf16 = 256 x 16 B -> one uint4 (8 bf16) per thread
+        {
+            const int r = tid >> 2, c = (tid & 3) * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (m0 + r < m) v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(m0 + r) * H + k0 + c));
+            xs[c + 0][r] = bf16lo(v.x); xs[c + 1][r] = bf16hi(v.x);
+            xs[c + 2][r] = bf16lo(v.y); xs[c + 3][r] = bf16hi(v.y);
+            xs[c + 4][r] = bf16lo(v.z); xs[c + 5][r] = bf16hi(v.z);
+            xs[c + 6][r] = bf16lo(v.w); xs[c + 7][r] = bf16hi(v.w);
+        }
+        // w tile: 64 experts x 32 fp32 = 512 float4 -> two per thread
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int idx = tid + q * 256;
+            const int r = idx >> 3, c = (idx & 7) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e0 + r < E) v = __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + r) * H + k0 + c));
+            ws[c + 0][r] = v.x; ws[c + 1][r] = v.y; ws[c + 2][r] = v.z; ws[c + 3][r] = v.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < RT_BK; ++kk) {
+            const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+            const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = m0 + ty * 4 + i;
+        if (t >= m) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx * 4 + j;
+            if (e < E) L[(size_t)t * E + e] = acc[i][j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- top-k
+// One warp per token; lane l holds logits e = l + 32 v.  k picks of a warp
+// arg-max ordered by (logit desc, index asc); weights = softmax over the k
+// picks (norm_topk_prob).
+template <int VPL>
+__global__ __launch_bounds__(256) void topk_softmax(const float* __restrict__ part, int S, int m, int E, int k,
+                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
+                                                    int32_t* __restrict__ ids, float* __restrict__ wts) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= m) return;
+    float v[VPL];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+            float a = 0.f;
+            for (int s = 0; s < S; ++s) a += part[((size_t)s * m + t) * E + e];
+            if (bias) a += bias[e];
+            v[i] = a;
+            if (logits_out) logits_out[(size_t)t * E + e] = a;
+        } else {
+            v[i] = -INFINITY;
+            taken |= 1u << i;
+        }
+    }
+    float my_l = 0.f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            my_l = bv;
+            my_id = bi;
+        }
+    }
+    const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+    const float ex = lane < k ? expf(my_l - l0) : 0.f;
+    float den = ex;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = my_id;
+        wts[(size_t)t * k + lane] = ex / den;
+    }
+}
+
+// ---------------------------------------------------------------- launchers
+int router_slices(int H, int m) {
+    if (m > kRouterSmallMaxM) return 1;
+    int S = H / 512;
+    while (S > 1 && (H % (S * 128) != 0)) --S;
+    return S < 1 ? 1 : S;
+}
+
+cudaError_t launch_router(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
+                          cudaStream_t st) {
+    if (m <= kRouterSmallMaxM) {
+        dim3 grid(ceil_div(E, 8), S);
+        router_partial_small<8><<<grid, 256, 0, st>>>(x, m, H, wr, E, H / S, part);
+    } else {
+        dim3 grid(ceil_div(m, RT_BM), ceil_div(E, RT_BN));
+        router_logits_tiled<<<grid, 256, 0, st>>>(x, m, H, wr, E, part);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const float* bias, float* logits_out,
+                        int32_t* ids, float* w, cudaStream_t st) {
+    const int vpl = ceil_div(E, 32);
+    dim3 grid(ceil_div(m, 8));
+    if (vpl <= 1) topk_softmax<1><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
+    else if (vpl <= 2) topk_softmax<2><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
+    else if (vpl <= 4) topk_softmax<4><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
+    else if (vpl <= 8) topk_softmax<8><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
+    else if (vpl <= 16) topk_softmax<16><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
+    else topk_softmax<32><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

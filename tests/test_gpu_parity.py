@@ -1,0 +1,301 @@
+"""GPU parity: the CUDA path (through the C-ABI) against the CPU oracle.
+
+Integer work (permute, e4m3 activation codes) is compared bit-exactly;
+expert ids exactly except at oracle near-ties (margin 1e-4); routing weights
+to 2e-5; layer outputs by relative L2 over [rows, H]: 1e-2 for bf16 weights,
+2e-2 for fp8 block-scaled weights.  Full-size workloads run in the launch
+configuration the benchmark times, with the oracle evaluated on sampled rows.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_ffn_gemv_gb300 import inputs as I
+from _parity import TOL, check_ids, oracle_rows, rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixture_experts_ffn_gemv_gb300 import binding
+    binding.load_library()
+    return torch.device("cuda", 0)
+
+
+_CACHE = {}
+
+
+def layer_for(workload, device, seed=0):
+    """Device tensors of a workload's layer (one big layer cached at a time)."""
+    key = (workload.name, workload.shape, seed)
+    if key not in _CACHE:
+        _CACHE.clear()
+        torch.cuda.empty_cache()
+        from mixture_experts_ffn_gemv_gb300 import binding
+        tensors = I.make_layer(workload, seed=seed, device=device)
+        _CACHE[key] = (tensors, binding.MoeLayer(workload.shape, tensors))
+    return _CACHE[key]
+
+
+def oracle_route(oracle_mod, shape, tensors, x):
+    host = {"router_w": tensors["router_w"].cpu(),
+            "router_bias": None if tensors["router_bias"] is None else tensors["router_bias"].cpu()}
+    return oracle_mod.route(shape, host, x.cpu())
+
+
+def sample_rows(m, n=48, seed=0):
+    if m <= n:
+        return np.arange(m)
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(np.arange(1, m - 1), size=n - 2, replace=False)
+    return np.sort(np.concatenate([[0, m - 1], pick]))
+
+
+SMALL_FP8 = I.LayerShape(hidden=512, num_experts=8, top_k=2, inter=512, shared_inter=512, fp8=True)
+MEDIUM_BF16 = I.LayerShape(hidden=512, num_experts=16, top_k=4, inter=256)
+ODD_E = I.LayerShape(hidden=256, num_experts=40, top_k=3, inter=128)
+
+
+# ------------------------------------------------------------------ activations
+
+def test_act_quant_fp8_bitwise(cuda, oracle_mod):
+    from mixture_experts_ffn_gemv_gb300 import binding
+    x = I.make_x(SMALL_FP8, 37, seed=21, device=cuda)
+    x[3, 128:256] = 0            # an all-zero block
+    x[5, :128] *= 1e-3           # small magnitudes (subnormal codes)
+    x[6, 7] = -0.0
+    x[7, 0] = 3e4                # one large value dominating its block
+    codes, scales = binding.moe_act_quant_fp8(x)
+    torch.cuda.synchronize()
+    xc = x.cpu()
+    for r in range(x.shape[0]):
+        q, s, _ = oracle_mod.act_quant(xc[r].float().numpy())
+        assert np.array_equal(codes[r].cpu().numpy(), q), f"row {r}"
+        assert np.array_equal(scales[r].cpu().numpy(), s), f"row {r}"
+
+
+# ------------------------------------------------------------------ permute
+
+@pytest.mark.parametrize("m,k,E,kind", [
+    (1, 8, 128, "random"), (16, 2, 8, "random"), (700, 8, 128, "random"),   # 2 chunks + ragged tail
+    (600, 8, 40, "random"), (300, 4, 256, "one_expert"), (4096, 8, 256, "random"),
+    (16384, 8, 128, "skewed"),
+])
+def test_permute_exact(cuda, oracle_mod, m, k, E, kind):
+    from mixture_experts_ffn_gemv_gb300 import binding
+    rng = np.random.default_rng(m * 7 + E)
+    if kind == "random":
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(m)])
+    elif kind == "one_expert":  # expert 3 in every token's slot 0
+        ids = np.stack([np.concatenate([[3], rng.permutation([e for e in range(E) if e != 3])[:k - 1]])
+                        for _ in range(m)])
+    else:  # Zipf-like popularity
+        p = 1.0 / np.arange(1, E + 1) ** 1.2
+        p /= p.sum()
+        ids = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(m)])
+    ids = ids.astype(np.int32)
+    shape = I.LayerShape(hidden=256, num_experts=E, top_k=k, inter=128)
+    # a layer handle of the right E / k over zero weights (only the permute runs)
+    dummy = {n: torch.zeros(E, 128, 256, dtype=torch.bfloat16, device=cuda) for n in ("w1", "w3")}
+    dummy["w2"] = torch.zeros(E, 256, 128, dtype=torch.bfloat16, device=cuda)
+    layer = binding.MoeLayer(shape, dummy)
+    off, sp, sl = layer.moe_permute(torch.from_numpy(ids).to(cuda))
+    torch.cuda.synchronize()
+    r_off, r_sp, r_sl = oracle_mod.permute(ids, E)
+    assert np.array_equal(off.cpu().numpy(), r_off)
+    assert np.array_equal(sp.cpu().numpy(), r_sp)
+    assert np.array_equal(sl.cpu().numpy(), r_sl)
+    assert layer.device_status() == 0
+
+
+# ------------------------------------------------------------------ routing
+
+ROUTE_CASES = [("tiny", 16), ("qwen3_decode", 1), ("qwen3_decode", 64), ("qwen3_prefill", 4096),
+               ("deepseek_v3_fp8", 16), ("qwen3_zipf", 8192)]
+
+
+@pytest.mark.parametrize("wl_name,m", ROUTE_CASES)
+def test_route_parity(cuda, oracle_mod, wl_name, m):
+    wl = I.WORKLOADS[wl_name]
+    tensors, layer = layer_for(wl, cuda)
+    x = I.make_x(wl.shape, m, device=cuda)
+    ids, w, logits = layer.moe_route(x, tensors["router_w"], tensors["router_bias"], logits=True)
+    torch.cuda.synchronize()
+    L, r_ids, r_w, margin = oracle_route(oracle_mod, wl.shape, tensors, x)
+    scale = np.abs(L).max()
+    assert np.abs(to_np(logits) - L).max() <= 1e-5 * max(scale, 1.0)
+    swapped, bad = check_ids(to_np(ids), r_ids, L)
+    assert not bad, bad[:5]
+    same = np.ones(m, bool)
+    same[swapped] = False
+    assert np.abs(to_np(w)[same] - r_w[same]).max() < 2e-5
+    assert np.abs(to_np(w).astype(np.float64).sum(1) - 1).max() < 1e-5
+    assert len(swapped) <= max(2, m // 200)
+
+
+# ------------------------------------------------------------------ experts (given routing)
+
+def _small_case(shape, m, seed, device):
+    wl = I.Workload("t", shape, (m,))
+    tensors = I.make_layer(wl, seed=seed, device=device)
+    x = I.make_x(shape, m, seed=seed, device=device)
+    return tensors, x
+
+
+@pytest.mark.parametrize("arm", ["gemv", "gemm"])
+@pytest.mark.parametrize("shape,m", [(I.TINY, 16), (I.TINY, 1), (MEDIUM_BF16, 300), (ODD_E, 77),
+                                     (SMALL_FP8, 24), (SMALL_FP8, 1), (SMALL_FP8, 200)])
+def test_experts_given_oracle_routing(cuda, oracle_mod, arm, shape, m):
+    from mixture_experts_ffn_gemv_gb300 import binding
+    tensors, x = _small_case(shape, m, seed=31, device=cuda)
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
+    ref = oracle_mod.reference(shape, host, x.cpu())
+    layer = binding.MoeLayer(shape, tensors)
+    try:
+        out = layer.moe_experts(x, torch.from_numpy(ref["ids"]).to(cuda), torch.from_numpy(ref["w"]).to(cuda),
+                                arm=arm)
+    except binding.MoeError as e:
+        if e.status == binding.MOE_ERR_UNSUPPORTED and arm == "gemm":
+            pytest.skip("grouped GEMM arm not available for this shape")
+        raise
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    err = rel_l2(to_np(out), ref["out"])
+    assert err < TOL[shape.fp8], err
+
+
+# ------------------------------------------------------------------ whole layer, full sizes
+
+FULL_CASES = [("tiny", 16)] + [("qwen3_decode", m) for m in (1, 4, 16, 64)] + \
+             [("qwen3_prefill", m) for m in (512, 4096, 16384)] + \
+             [("deepseek_v3_fp8", m) for m in (1, 16, 4096)] + [("qwen3_zipf", 8192)]
+
+
+@pytest.mark.parametrize("wl_name,m", FULL_CASES)
+def test_forward_full_size(cuda, oracle_mod, wl_name, m):
+    from mixture_experts_ffn_gemv_gb300 import binding
+    wl = I.WORKLOADS[wl_name]
+    tensors, layer = layer_for(wl, cuda)
+    x = I.make_x(wl.shape, m, device=cuda)
+    try:
+        out, ids, w = layer.moe_forward(x, tensors["router_w"], tensors["router_bias"], return_routing=True)
+    except binding.MoeError as e:
+        if e.status == binding.MOE_ERR_UNSUPPORTED:
+            pytest.skip("grouped GEMM arm not available")
+        raise
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    L, r_ids, r_w, margin = oracle_route(oracle_mod, wl.shape, tensors, x)
+    swapped, bad = check_ids(to_np(ids), r_ids, L)
+    assert not bad, bad[:5]
+    rows = np.array([r for r in sample_rows(m) if r not in set(swapped)])
+    ref = oracle_rows(oracle_mod, wl.shape, tensors, x, r_ids, r_w, rows)
+    err = rel_l2(to_np(out)[rows], ref)
+    assert err < TOL[wl.shape.fp8], err
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_zero_tokens_launch_nothing(cuda):
+    wl = I.WORKLOADS["tiny"]
+    tensors, layer = layer_for(wl, cuda)
+    x = torch.empty(0, wl.shape.hidden, dtype=torch.bfloat16, device=cuda)
+    out = layer.moe_forward(x, tensors["router_w"])
+    assert out.shape == (0, wl.shape.hidden)
+    assert layer.last_launch_count() == 0
+
+
+def test_zero_router_ties_pick_lowest_indices(cuda, oracle_mod):
+    wl = I.WORKLOADS["tiny"]
+    tensors, layer = layer_for(wl, cuda)
+    x = I.make_x(wl.shape, 9, seed=5, device=cuda)
+    zero = torch.zeros_like(tensors["router_w"])
+    out, ids, w = layer.moe_forward(x, zero, return_routing=True)
+    torch.cuda.synchronize()
+    k = wl.shape.top_k
+    assert np.array_equal(to_np(ids), np.tile(np.arange(k), (9, 1)))
+    assert np.all(to_np(w) == np.float32(1.0 / k))
+    host = {n: tensors[n].cpu() for n in ("w1", "w3", "w2")}
+    ref = oracle_mod.moe_forward(wl.shape, host, x.cpu(), to_np(ids).astype(np.int32),
+                                 np.full((9, k), 1.0 / k, np.float32))
+    assert rel_l2(to_np(out), ref) < TOL[False]
+
+
+@pytest.mark.parametrize("arm", ["gemv", "gemm"])
+def test_all_tokens_on_one_expert(cuda, oracle_mod, arm):
+    from mixture_experts_ffn_gemv_gb300 import binding
+    shape = MEDIUM_BF16
+    tensors, x = _small_case(shape, 260, seed=41, device=cuda)
+    bias = torch.zeros(shape.num_experts, device=cuda)
+    bias[5] = 100.0  # expert 5 is every token's first choice: 260 rows, 3 m-tiles with a ragged end
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
+    host["router_bias"] = bias.cpu()
+    ref = oracle_mod.reference(shape, host, x.cpu())
+    assert np.all(ref["ids"][:, 0] == 5)
+    layer = binding.MoeLayer(shape, tensors)
+    try:
+        out, ids, w = layer.moe_forward(x, tensors["router_w"], bias, arm=arm, return_routing=True)
+    except binding.MoeError as e:
+        if e.status == binding.MOE_ERR_UNSUPPORTED and arm == "gemm":
+            pytest.skip("grouped GEMM arm not available")
+        raise
+    torch.cuda.synchronize()
+    swapped, bad = check_ids(to_np(ids), ref["ids"], ref["logits"])
+    assert not bad
+    keep = np.array([r for r in range(260) if r not in set(swapped)])
+    assert rel_l2(to_np(out)[keep], ref["out"][keep]) < TOL[False]
+
+
+def test_single_expert_top1_is_dense_mlp(cuda, oracle_mod):
+    from mixture_experts_ffn_gemv_gb300 import binding
+    shape = I.LayerShape(hidden=256, num_experts=1, top_k=1, inter=256)
+    tensors, x = _small_case(shape, 33, seed=51, device=cuda)
+    layer = binding.MoeLayer(shape, tensors)
+    out, ids, w = layer.moe_forward(x, tensors["router_w"], return_routing=True)
+    torch.cuda.synchronize()
+    assert np.all(to_np(ids) == 0) and np.all(to_np(w) == 1.0)
+    x64 = x.double()
+    g = x64 @ tensors["w1"][0].double().T
+    u = x64 @ tensors["w3"][0].double().T
+    dense = (torch.nn.functional.silu(g) * u) @ tensors["w2"][0].double().T
+    assert rel_l2(to_np(out), dense.cpu().numpy()) < TOL[False]
+
+
+def test_bad_expert_id_sets_device_flag(cuda):
+    from mixture_experts_ffn_gemv_gb300 import binding
+    wl = I.WORKLOADS["tiny"]
+    tensors, layer = layer_for(wl, cuda)
+    x = I.make_x(wl.shape, 4, device=cuda)
+    ids = torch.tensor([[0, 1], [2, 8], [3, 4], [5, -1]], dtype=torch.int32, device=cuda)
+    w = torch.full((4, 2), 0.5, device=cuda)
+    layer.moe_experts(x, ids, w, arm="gemv")
+    assert layer.device_status() == 1  # DEV_ERR_BAD_ID
+    layer.moe_experts(x, ids.clamp(0, 7), w, arm="gemv")
+    assert layer.device_status() == 0  # the next call starts clean
+
+
+@pytest.mark.parametrize("wl_name,m", [("tiny", 16), ("qwen3_decode", 16), ("deepseek_v3_fp8", 1)])
+def test_deterministic_and_graph_capturable(cuda, wl_name, m):
+    wl = I.WORKLOADS[wl_name]
+    tensors, layer = layer_for(wl, cuda)
+    x = I.make_x(wl.shape, m, device=cuda)
+    a = layer.moe_forward(x, tensors["router_w"], tensors["router_bias"])
+    b = layer.moe_forward(x, tensors["router_w"], tensors["router_bias"])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    layer.workspace(m)
+    out = torch.empty_like(a)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer.moe_forward(x, tensors["router_w"], tensors["router_bias"], out=out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, a)
