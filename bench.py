@@ -2,7 +2,7 @@
 """Benchmark of the MoE FFN layer forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload qwen3_decode] [--m 16] [--no-sweep]
+                    [--workload qwen3_decode] [--tokens 16] [--no-sweep]
 
 One step = one forward of the whole layer (router, top-k, permute, experts,
 combine) over one batch of m synthetic tokens.  Steps rotate over R layer
@@ -505,7 +505,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_decode", choices=sorted(I.WORKLOADS))
-    ap.add_argument("--m", type=int, default=16)
+    ap.add_argument("--tokens", dest="m", type=int, default=16, help="tokens per step (m)")
     ap.add_argument("--no-sweep", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
