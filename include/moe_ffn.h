@@ -130,6 +130,30 @@ MOE_API int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t
                 int32_t* expert_offsets, int32_t* sorted_pair, int32_t* slot_of_pair,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* moe_permute for callers that cannot allocate device memory at all: code
+ * running while a CUDA graph is being captured, real-time serving loops that
+ * forbid allocator calls after start-up, and host runtimes that own no device
+ * allocator and only hold the tensors handed to them.  The pages have no
+ * counterpart of this entry point; it computes exactly what moe_permute does
+ * (same outputs, same kernels) but takes no workspace.
+ *   topk_ids int32 [m, top_k]; expert_offsets int32 [num_experts + 1];
+ *   sorted_pair, slot_of_pair int32 [m * top_k] -- as for moe_permute.
+ * Its scratch is a fixed 320 KiB array inside this library's device memory
+ * (each GPU that loads the library holds it until the process exits).  A
+ * call whose scratch would not fit -- more than 320 KiB of per-chunk
+ * histograms, about E * m * top_k / 512 bytes -- returns MOE_ERR_UNSUPPORTED
+ * and launches nothing.  It calls no allocator (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ * All calls on a device share that one array and it keeps the last call's
+ * contents: each call clears the part that must start at zero itself, but two
+ * calls that overlap on the GPU (different streams without ordering between
+ * them) race on it; order them on one stream.  The first call on a device
+ * looks up the array's device address (with that device current), so make it
+ * before any stream capture begins.                                        */
+MOE_API int moe_permute_noalloc(const int32_t* topk_ids, int64_t m, int32_t top_k, int32_t num_experts,
+                                int32_t* expert_offsets, int32_t* sorted_pair, int32_t* slot_of_pair,
+                                void* stream);
+
 /* Steps 3-8 for a given routing: permute, grouped gate/up + SiLU(gate)*up,
  * grouped down, then out[t] = sum_j topk_w[t,j] * y_{t,j} (+ shared expert
  * output, weight 1), accumulated in fp32 in j order and stored as bf16.

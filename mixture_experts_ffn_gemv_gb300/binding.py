@@ -22,7 +22,7 @@ ARMS = {"auto": MOE_ARM_AUTO, "gemv": MOE_ARM_GEMV, "gemm": MOE_ARM_GEMM}
 
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_workspace_size", "moe_select_arm", "moe_route",
-    "moe_permute", "moe_experts", "moe_forward", "moe_act_quant_fp8", "moe_device_status",
+    "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_forward", "moe_act_quant_fp8", "moe_device_status",
     "moe_last_launch_count", "moe_kernel_timing_enable", "moe_kernel_timing_read", "moe_kernel_count",
     "moe_kernel_name", "moe_status_string",
 )
@@ -68,6 +68,7 @@ def load_library(path: str | None = None, build: bool = True):
         lib.moe_select_arm.argtypes = [_vp, _i64]
         lib.moe_route.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
         lib.moe_permute.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        lib.moe_permute_noalloc.argtypes = [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp]
         lib.moe_experts.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         lib.moe_forward.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         lib.moe_act_quant_fp8.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp]
