@@ -1,17 +1,395 @@
-// Grouped-GEMM arm: not built yet.
+// Grouped-GEMM expert arm for large m: "grouped gate/up GEMM -> SiLU ->
+// grouped down GEMM" of spark_model/layers/moe/forward_prefill.rs
+// (run_routed_grouped_gemm: every expert's weights loaded once for all of
+// its rows) and moe_glu_prefill / moe_down_prefill of span-02
+// gpu_model/forward.rs (grouped via offsets and counts).
+//
+// One persistent kernel per projection, one CTA per SM, warp-specialised:
+//   warp 0      TMA producer: A tile (128 sorted rows x 64 of K) and B tile
+//               (256 weight rows x 64 of K) into a 4-stage smem ring;
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16, fp32
+//               accumulators in TMEM, double-buffered (2 x 256 columns);
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, then
+//               gate/up: h = silu(G) * U (B tile = 128 rows of W1 followed by
+//               the same 128 rows of W3, so one MMA chain yields G and U),
+//               down: y = D; stored as bf16 in sorted-row order.
+// The work list is (m-tile, n-tile) over the non-empty groups the permute
+// left in the workspace (group m-tile starts in act_tile); every tile costs
+// the same K work, so CTAs take tiles round-robin.  Every mbarrier wait is
+// bounded: on expiry the CTA records DEV_ERR_TIMEOUT, stops issuing, drains
+// its tensor-core work and frees TMEM before returning.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "gemm.h"
+#include "kernels.h"
+#include "sm100.cuh"
 
 namespace moe {
 
-bool gemm_supported(const moe_config&) { return false; }
-int gemm_max_tiles(int, int, int, int) { return 0; }
-int gemm_prepare_weights(const moe_config&, const moe_expert_weights*, const moe_expert_weights*, GemmWeights* out) {
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128, BN = 256, BK = 64;  // BK bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int THREADS = 192;
+constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
+constexpr int TABLE_INTS = 2 * kMaxExperts + 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + TABLE_INTS * 4;
+
+struct GemmParams {
+    WsHeader* hdr;
+    const int* grp_off;
+    const int* grp_cnt;
+    const int* act_group;
+    const int* act_tile;
+    int E;         // routed experts; group E is the shared expert
+    int n_tiles;   // n-tiles per m-tile
+    int kblocks;   // K / BK
+    int ldo;       // output row stride (elements)
+    int n_rows_b;  // weight rows per B load box (128 gate/up, 256 down)
+    uint16_t* out;
+};
+
+__device__ __forceinline__ int find_group(const int* tile_start, int n_active, int mt) {
+    int lo = 0, hi = n_active - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= mt) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                      const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
+                      const __grid_constant__ CUtensorMap tmS1, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_tile = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+    int* s_group = s_tile + kMaxExperts + 2;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_active = p.hdr->n_active;
+    const int total = p.hdr->total_tiles * p.n_tiles;
+    for (int i = threadIdx.x; i <= n_active; i += THREADS) s_tile[i] = p.act_tile[i];
+    for (int i = threadIdx.x; i < n_active; i += THREADS) s_group[i] = p.act_group[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB0);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (*abort_flag) break;
+                const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+                const int a = find_group(s_tile, n_active, mt);
+                const int g = s_group[a];
+                const int row0 = p.grp_off[g] + (mt - s_tile[a]) * BM;
+                const bool routed = g < p.E;
+                const CUtensorMap* b0 = routed ? &tmB0 : &tmS0;
+                const CUtensorMap* b1 = routed ? &tmB1 : &tmS1;
+                const int gz = routed ? g : 0;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+                    mbar_arrive_expect_tx(full0 + 8 * s, STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, kb * BK, row0, full0 + 8 * s);
+                    if (GATEUP) {
+                        tma_load_3d(sb, b0, kb * BK, nt * p.n_rows_b, gz, full0 + 8 * s);
+                        tma_load_3d(sb + B_BYTES / 2, b1, kb * BK, nt * p.n_rows_b, gz, full0 + 8 * s);
+                    } else {
+                        tma_load_3d(sb, b0, kb * BK, nt * p.n_rows_b, gz, full0 + 8 * s);
+                    }
+                }
+            }
+            if (!ok) {
+                set_error(p.hdr, DEV_ERR_TIMEOUT, 1);
+                *abort_flag = 1;
+            }
+            // every issued load has landed before the CTA can exit
+            for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
+                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, WAIT_NS);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(BM, BN);
+            uint32_t it = 0, tc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+                if (*abort_flag) break;
+                const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+                if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(sbase + s * STAGE_BYTES);
+                    const uint64_t bd = desc_sw128(sbase + s * STAGE_BYTES + A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per MMA
+                        mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    mma_commit(empty0 + 8 * s);
+                }
+                if (!ok) break;
+                mma_commit(tfull0 + 8 * acc);
+            }
+            if (!ok) {
+                set_error(p.hdr, DEV_ERR_TIMEOUT, 2);
+                *abort_flag = 1;
+            }
+            mma_commit(drain);
+            mbar_wait(drain, 0, WAIT_NS);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;  // the TMEM lane quarter this warp may read
+        const int r = q * 32 + lane;
+        uint32_t tc = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            if (*abort_flag) break;
+            const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+            if (!mbar_wait(tfull0 + 8 * acc, aph, WAIT_NS)) {
+                set_error(p.hdr, DEV_ERR_TIMEOUT, 3);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+            const int a = find_group(s_tile, n_active, mt);
+            const int g = s_group[a];
+            const int j = mt - s_tile[a];
+            const int valid = p.grp_cnt[g] - j * BM;
+            const bool ok = r < valid;
+            uint16_t* orow = p.out + (size_t)(p.grp_off[g] + j * BM + r) * p.ldo;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            if (GATEUP) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t gv[32], uv[32];
+                    tmem_ld32(taddr + c * 32, gv);
+                    tmem_ld32(taddr + 128 + c * 32, uv);
+                    tmem_wait_ld();
+                    if (ok) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + nt * 128 + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack_bf16x2(swiglu(__uint_as_float(gv[8 * v + 0]), __uint_as_float(uv[8 * v + 0])),
+                                              swiglu(__uint_as_float(gv[8 * v + 1]), __uint_as_float(uv[8 * v + 1])));
+                            o.y = pack_bf16x2(swiglu(__uint_as_float(gv[8 * v + 2]), __uint_as_float(uv[8 * v + 2])),
+                                              swiglu(__uint_as_float(gv[8 * v + 3]), __uint_as_float(uv[8 * v + 3])));
+                            o.z = pack_bf16x2(swiglu(__uint_as_float(gv[8 * v + 4]), __uint_as_float(uv[8 * v + 4])),
+                                              swiglu(__uint_as_float(gv[8 * v + 5]), __uint_as_float(uv[8 * v + 5])));
+                            o.w = pack_bf16x2(swiglu(__uint_as_float(gv[8 * v + 6]), __uint_as_float(uv[8 * v + 6])),
+                                              swiglu(__uint_as_float(gv[8 * v + 7]), __uint_as_float(uv[8 * v + 7])));
+                            dst[v] = o;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t dv[32];
+                    tmem_ld32(taddr + c * 32, dv);
+                    tmem_wait_ld();
+                    if (ok) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + nt * BN + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(dv[8 * v + 0]), __uint_as_float(dv[8 * v + 1]));
+                            o.y = pack_bf16x2(__uint_as_float(dv[8 * v + 2]), __uint_as_float(dv[8 * v + 3]));
+                            o.z = pack_bf16x2(__uint_as_float(dv[8 * v + 4]), __uint_as_float(dv[8 * v + 5]));
+                            o.w = pack_bf16x2(__uint_as_float(dv[8 * v + 6]), __uint_as_float(dv[8 * v + 7]));
+                            dst[v] = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// Row-major [outer..., rows, cols] tensor of `esize`-byte elements; box of
+// box_rows x box_cols (x 1), 128-byte swizzle.
+bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, int esize, uint32_t box_cols,
+            uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[3], gstride[2];
+    cuuint32_t box[3] = {box_cols, box_rows, 1}, estr[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
+    gstride[0] = dims[0] * esize;
+    if (rank == 3) gstride[1] = dims[0] * dims[1] * esize;
+    const CUresult r = fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                          (cuuint32_t)rank, const_cast<void*>(base), gdim, gstride, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    return sms;
+}
+
+template <bool GATEUP>
+cudaError_t set_smem_attr() {
+    static cudaError_t e = cudaFuncSetAttribute(grouped_gemm_bf16<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                SMEM_BYTES);
+    return e;
+}
+
+}  // namespace
+
+bool gemm_supported(const moe_config& c) {
+    return c.weights == MOE_WEIGHTS_BF16 && c.hidden % 256 == 0 && c.inter % 128 == 0 &&
+           c.num_experts <= kMaxExperts;
+}
+
+int gemm_max_tiles(int P, int E, int has_shared, int m) {
+    return ceil_div(P, BM) + std::min(E, P) + (has_shared ? ceil_div(m, BM) : 0);
+}
+
+int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, const moe_expert_weights* shared,
+                         GemmWeights* out) {
     out->ready = false;
+    if (!gemm_supported(c)) return MOE_OK;
+    const uint64_t H = c.hidden, I = c.inter, E = c.num_experts;
+    const uint64_t d13[3] = {H, I, E}, d2[3] = {I, H, E};
+    const uint64_t s13[3] = {H, I, 1}, s2[3] = {I, H, 1};
+    if (!encode(&out->w1, routed->w1, 3, d13, 2, BK, 128) || !encode(&out->w3, routed->w3, 3, d13, 2, BK, 128) ||
+        !encode(&out->w2, routed->w2, 3, d2, 2, BK, BN))
+        return MOE_ERR_CUDA;
+    if (shared) {
+        if (!encode(&out->sw1, shared->w1, 3, s13, 2, BK, 128) || !encode(&out->sw3, shared->w3, 3, s13, 2, BK, 128) ||
+            !encode(&out->sw2, shared->w2, 3, s2, 2, BK, BN))
+            return MOE_ERR_CUDA;
+    } else {
+        out->sw1 = out->w1;
+        out->sw3 = out->w3;
+        out->sw2 = out->w2;
+    }
+    out->ready = true;
     return MOE_OK;
 }
-int gemm_plan(const GemmWeights&, const GemmCall&, GemmLaunch*) { return MOE_ERR_UNSUPPORTED; }
-cudaError_t launch_gemm_gateup(const GemmLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_gemm_down(const GemmLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
+
+int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out) {
+    if (!w.ready) return MOE_ERR_UNSUPPORTED;
+    out->w = &w;
+    out->call = g;
+    const uint64_t da[2] = {(uint64_t)g.H, (uint64_t)g.rows}, dh[2] = {(uint64_t)g.I, (uint64_t)g.rows};
+    if (!encode(&out->a_xs, g.xs, 2, da, 2, BK, BM) || !encode(&out->a_h, g.h, 2, dh, 2, BK, BM))
+        return MOE_ERR_CUDA;
+    out->grid = std::max(1, std::min(num_sms(), g.max_tiles * std::max(g.I / 128, g.H / BN)));
+    return MOE_OK;
+}
+
+cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
+    cudaError_t e = set_smem_attr<true>();
+    if (e != cudaSuccess) return e;
+    const GemmCall& g = L.call;
+    GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.I / 128, g.H / BK, g.I, 128,
+                 static_cast<uint16_t*>(g.h)};
+    const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
+    grouped_gemm_bf16<true><<<grid, THREADS, SMEM_BYTES, st>>>(L.a_xs, L.w->w1, L.w->w3, L.w->sw1, L.w->sw3, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_down(const GemmLaunch& L, cudaStream_t st) {
+    cudaError_t e = set_smem_attr<false>();
+    if (e != cudaSuccess) return e;
+    const GemmCall& g = L.call;
+    GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.H / BN, g.I / BK, g.H, BN, g.y};
+    const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
+    grouped_gemm_bf16<false><<<grid, THREADS, SMEM_BYTES, st>>>(L.a_h, L.w->w2, L.w->w2, L.w->sw2, L.w->sw2, p);
+    return cudaGetLastError();
+}
 
 }  // namespace moe
