@@ -21,11 +21,11 @@ namespace {
 // Optional per-kernel timing: every launch bracketed by two CUDA events on its
 // stream, resolved when the totals are read.
 enum KernelId : int {
-    K_ROUTER = 0, K_TOPK, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
+    K_ROUTER_SPLIT = 0, K_ROUTER, K_TOPK, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
     K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
-    "router", "topk_softmax", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
+    "router_split", "router", "topk_softmax", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
     "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine",
 };
 
@@ -95,9 +95,10 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-    size_t hdr, part, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile, sorted_pair, slot_of_pair;
+    size_t hdr, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile, sorted_pair, slot_of_pair;
     size_t xq, xsc, xs, xs_sc, h, hsc, y, total;
     int S, P, rows, nchunk;
+    bool router_tc;
 };
 
 Layout layout(const moe_layer* L, int64_t m) {
@@ -105,7 +106,8 @@ Layout layout(const moe_layer* L, int64_t m) {
     const int E = L->cfg.num_experts, k = L->cfg.top_k, H = L->cfg.hidden, I = L->cfg.inter;
     o.P = (int)(m * k);
     o.rows = o.P + (L->has_shared ? (int)m : 0);
-    o.S = router_slices(H, (int)m);
+    o.router_tc = router_tc_usable((int)m, H, E);
+    o.S = o.router_tc ? router_tc_slices((int)m, H) : router_slices(H, (int)m);
     o.nchunk = ceil_div(std::max(o.P, 1), kPermChunk);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -116,6 +118,7 @@ Layout layout(const moe_layer* L, int64_t m) {
     const size_t ab = L->fp8 ? 1 : 2;  // activation element bytes
     o.hdr = take(sizeof(WsHeader));
     o.part = take((size_t)o.S * m * E * 4);
+    o.planes = o.router_tc ? take(router_tc_split_bytes(E, H)) : 0;
     o.ids = take((size_t)o.P * 4);
     o.w = take((size_t)o.P * 4);
     o.chunk_base = take((size_t)o.nchunk * E * 4);
@@ -193,7 +196,15 @@ int run_route(const moe_layer* L, const Layout& lo, const void* x, int m, const 
     const moe_config& c = L->cfg;
     const cudaStream_t st = ln.st;
     float* part = at<float>(ws, lo.part);
-    MOE_LAUNCH(K_ROUTER, launch_router(static_cast<const uint16_t*>(x), m, c.hidden, wr, c.num_experts, part, lo.S, st));
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    if (lo.router_tc) {
+        uint16_t* planes = at<uint16_t>(ws, lo.planes);
+        WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
+        MOE_LAUNCH(K_ROUTER_SPLIT, launch_router_split(wr, c.num_experts, c.hidden, planes, st));
+        MOE_LAUNCH(K_ROUTER, launch_router_tc(xb, m, c.hidden, planes, c.num_experts, part, lo.S, hdr, st));
+    } else {
+        MOE_LAUNCH(K_ROUTER, launch_router(xb, m, c.hidden, wr, c.num_experts, part, lo.S, st));
+    }
     MOE_LAUNCH(K_TOPK, launch_topk(part, lo.S, m, c.num_experts, c.top_k, bias, logits_out, ids, w, st));
     return MOE_OK;
 }
@@ -218,7 +229,6 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     const cudaStream_t st = ln.st;
     const int E = c.num_experts, k = c.top_k, H = c.hidden, I = c.inter;
     WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
-    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
     const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
     MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->has_shared ? 1 : 0, po, hdr, st));
     MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(ids, m, k, E, po, st));
@@ -380,6 +390,7 @@ int moe_route(const moe_layer* layer, const void* x, int64_t m, const float* rou
     if (!x || !router_w || !topk_ids || !topk_w || !aligned(x, 16) || !aligned(router_w, 16))
         return MOE_ERR_INVALID_ARG;
     Launcher ln{layer, static_cast<cudaStream_t>(stream)};
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), ln.st) != cudaSuccess) return MOE_ERR_CUDA;
     rc = run_route(layer, lo, x, (int)m, router_w, router_bias, logits_out, topk_ids, topk_w, workspace, ln);
     layer->last_launches = ln.n;
     return rc;
@@ -411,6 +422,7 @@ int moe_experts(const moe_layer* layer, const void* x, int64_t m, const int32_t*
     if (!x || !topk_ids || !topk_w || !out || !aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
     if (arm < MOE_ARM_AUTO || arm > MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
     Launcher ln{layer, static_cast<cudaStream_t>(stream)};
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), ln.st) != cudaSuccess) return MOE_ERR_CUDA;
     rc = run_experts(layer, lo, x, (int)m, topk_ids, topk_w, out, arm, workspace, ln);
     layer->last_launches = ln.n;
     return rc;
@@ -429,6 +441,7 @@ int moe_forward(const moe_layer* layer, const void* x, int64_t m, const float* r
     int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, lo.ids);
     float* w = topk_w_out ? topk_w_out : at<float>(workspace, lo.w);
     Launcher ln{layer, st};
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
     rc = run_route(layer, lo, x, (int)m, router_w, router_bias, nullptr, ids, w, workspace, ln);
     if (rc == MOE_OK) rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln);
     layer->last_launches = ln.n;

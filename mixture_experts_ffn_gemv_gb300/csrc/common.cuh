@@ -89,8 +89,11 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// SiLU(g) * u with silu(g) = g / (1 + exp(-g)).
-__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// SiLU(g) * u with silu(g) = g / (1 + exp(-g)).  The approximate divide is
+// within a few ulp of fp32 -- far below the bf16/e4m3 rounding of its result --
+// and keeps the right limit for very negative g (divisor inf or above 2^126:
+// the quotient is 0).
+__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 

@@ -26,6 +26,7 @@
 #include "gemm.h"
 #include "kernels.h"
 #include "sm100.cuh"
+#include "tmap.h"
 
 namespace moe {
 
@@ -272,50 +273,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-// Row-major [outer..., rows, cols] tensor of `esize`-byte elements; box of
-// box_rows x box_cols (x 1), 128-byte swizzle.
-bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, int esize, uint32_t box_cols,
-            uint32_t box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t gdim[3], gstride[2];
-    cuuint32_t box[3] = {box_cols, box_rows, 1}, estr[3] = {1, 1, 1};
-    for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
-    gstride[0] = dims[0] * esize;
-    if (rank == 3) gstride[1] = dims[0] * dims[1] * esize;
-    const CUresult r = fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                          (cuuint32_t)rank, const_cast<void*>(base), gdim, gstride, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 int num_sms() {
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 1;
-    }
+    static int sms = device_sm_count();
     return sms;
 }
 
@@ -329,8 +288,8 @@ cudaError_t set_smem_attr() {
 }  // namespace
 
 bool gemm_supported(const moe_config& c) {
-    return c.weights == MOE_WEIGHTS_BF16 && c.hidden % 256 == 0 && c.inter % 128 == 0 &&
-           c.num_experts <= kMaxExperts;
+    return (c.weights == MOE_WEIGHTS_BF16 || c.weights == MOE_WEIGHTS_FP8_E4M3_B128) && c.hidden % 256 == 0 &&
+           c.inter % 128 == 0 && c.num_experts <= kMaxExperts;
 }
 
 int gemm_max_tiles(int P, int E, int has_shared, int m) {
@@ -341,20 +300,34 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
                          GemmWeights* out) {
     out->ready = false;
     if (!gemm_supported(c)) return MOE_OK;
+    out->fp8 = c.weights == MOE_WEIGHTS_FP8_E4M3_B128;
+    const int es = out->fp8 ? 1 : 2;
+    const uint32_t bc = 128 / es;  // one 128-byte swizzle row of K per box
     const uint64_t H = c.hidden, I = c.inter, E = c.num_experts;
     const uint64_t d13[3] = {H, I, E}, d2[3] = {I, H, E};
     const uint64_t s13[3] = {H, I, 1}, s2[3] = {I, H, 1};
-    if (!encode(&out->w1, routed->w1, 3, d13, 2, BK, 128) || !encode(&out->w3, routed->w3, 3, d13, 2, BK, 128) ||
-        !encode(&out->w2, routed->w2, 3, d2, 2, BK, BN))
+    if (!tmap_encode(&out->w1, routed->w1, 3, d13, es, bc, 128) ||
+        !tmap_encode(&out->w3, routed->w3, 3, d13, es, bc, 128) ||
+        !tmap_encode(&out->w2, routed->w2, 3, d2, es, bc, BN))
         return MOE_ERR_CUDA;
+    out->s1 = routed->s1;
+    out->s3 = routed->s3;
+    out->s2 = routed->s2;
     if (shared) {
-        if (!encode(&out->sw1, shared->w1, 3, s13, 2, BK, 128) || !encode(&out->sw3, shared->w3, 3, s13, 2, BK, 128) ||
-            !encode(&out->sw2, shared->w2, 3, s2, 2, BK, BN))
+        if (!tmap_encode(&out->sw1, shared->w1, 3, s13, es, bc, 128) ||
+            !tmap_encode(&out->sw3, shared->w3, 3, s13, es, bc, 128) ||
+            !tmap_encode(&out->sw2, shared->w2, 3, s2, es, bc, BN))
             return MOE_ERR_CUDA;
+        out->ss1 = shared->s1;
+        out->ss3 = shared->s3;
+        out->ss2 = shared->s2;
     } else {
         out->sw1 = out->w1;
         out->sw3 = out->w3;
         out->sw2 = out->w2;
+        out->ss1 = out->s1;
+        out->ss3 = out->s3;
+        out->ss2 = out->s2;
     }
     out->ready = true;
     return MOE_OK;
@@ -364,14 +337,16 @@ int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out) {
     if (!w.ready) return MOE_ERR_UNSUPPORTED;
     out->w = &w;
     out->call = g;
+    const int es = w.fp8 ? 1 : 2;
     const uint64_t da[2] = {(uint64_t)g.H, (uint64_t)g.rows}, dh[2] = {(uint64_t)g.I, (uint64_t)g.rows};
-    if (!encode(&out->a_xs, g.xs, 2, da, 2, BK, BM) || !encode(&out->a_h, g.h, 2, dh, 2, BK, BM))
+    if (!tmap_encode(&out->a_xs, g.xs, 2, da, es, 128 / es, BM) || !tmap_encode(&out->a_h, g.h, 2, dh, es, 128 / es, BM))
         return MOE_ERR_CUDA;
     out->grid = std::max(1, std::min(num_sms(), g.max_tiles * std::max(g.I / 128, g.H / BN)));
     return MOE_OK;
 }
 
 cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
+    if (L.w->fp8) return launch_gemm_fp8_gateup(L, st);
     cudaError_t e = set_smem_attr<true>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;
@@ -383,6 +358,7 @@ cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
 }
 
 cudaError_t launch_gemm_down(const GemmLaunch& L, cudaStream_t st) {
+    if (L.w->fp8) return launch_gemm_fp8_down(L, st);
     cudaError_t e = set_smem_attr<false>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;

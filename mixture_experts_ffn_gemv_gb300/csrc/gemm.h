@@ -14,9 +14,10 @@ struct WsHeader;
 // TMA descriptors of the stacked weights, built once per layer on the host.
 struct GemmWeights {
     bool ready;
-    CUtensorMap w13;   // routed gate/up weights, [E][2][I][H] view: W1 and W3 tiles
+    bool fp8;  // e4m3 codes with 128x128 fp32 block scales
     CUtensorMap w1, w3, w2;
     CUtensorMap sw1, sw3, sw2;
+    const float *s1, *s3, *s2, *ss1, *ss3, *ss2;  // fp8 block scales (routed, shared)
 };
 
 struct GemmCall {
@@ -50,5 +51,7 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
 int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out);  // MOE_OK or an error status
 cudaError_t launch_gemm_gateup(const GemmLaunch& p, cudaStream_t st);
 cudaError_t launch_gemm_down(const GemmLaunch& p, cudaStream_t st);
+cudaError_t launch_gemm_fp8_gateup(const GemmLaunch& p, cudaStream_t st);
+cudaError_t launch_gemm_fp8_down(const GemmLaunch& p, cudaStream_t st);
 
 }  // namespace moe

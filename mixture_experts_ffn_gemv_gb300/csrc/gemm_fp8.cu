@@ -1,0 +1,339 @@
+// fp8 (e4m3, 128x128 fp32 block scales) grouped GEMM arm for large m:
+// "grouped gate/up GEMM -> SiLU -> grouped down GEMM" of
+// spark_model/layers/moe/forward_prefill.rs, fp8 body, with the two-level
+// fp32 block-scale accumulation that page describes for its fp8 grouped GEMM
+// (exact fp32 scales, not power-of-two block exponents).
+//
+// Persistent, one CTA per SM, 10 warps:
+//   warp 0      TMA producer: A (128 rows x 128 codes) and B (256 weight rows
+//               x 128 codes) per stage -- one stage is exactly one 128-wide
+//               scale block of K;
+//   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M128 N256 K32) per
+//               stage into one of two TMEM partial buffers (2 x 256 columns),
+//               a fresh partial for every K block;
+//   warps 2..9  promotion + epilogue: two warps per TMEM lane quarter, each
+//               owning half of the 256 columns; per K block they read the
+//               partial, multiply by s_x[row, kb] * s_w[block, kb] and add it
+//               into fp32 register accumulators, then release the buffer.
+// Gate/up epilogue: h = silu(G) * U for the tile's 128 I columns, quantised
+// as one 1x128 block per row (s = amax/448, e4m3 RNE satfinite); the two
+// warps sharing a row exchange their halves' amax through shared memory with
+// an mbarrier (bounded wait).  Down epilogue: y as bf16.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace moe {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128, BN = 256, BK = 128;  // BK e4m3 codes = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int THREADS = 320;
+constexpr int EPI_THREADS = 256;
+constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr int TABLE_INTS = 2 * kMaxExperts + 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + TABLE_INTS * 4 + 2 * BM * 2 * 4;
+
+struct Fp8Params {
+    WsHeader* hdr;
+    const int* grp_off;
+    const int* grp_cnt;
+    const int* act_group;
+    const int* act_tile;
+    const float* a_sc;   // [rows, kb_total]
+    const float* b_sc0;  // routed scales: gate/up s1, down s2
+    const float* b_sc1;  // gate/up s3
+    const float* s_sc0;  // shared expert: ss1 / ss2
+    const float* s_sc1;  // ss3
+    int E, rows, n_tiles, kblocks, ldo;
+    int b_row_blocks;  // 128-row blocks of one expert's weight (I/128 gate/up, H/128 down)
+    uint8_t* out_q;    // gate/up: h codes [rows, I]
+    float* out_sc;     // gate/up: h scales [rows, I/128]
+    uint16_t* out_y;   // down: y [rows, H]
+};
+
+__device__ __forceinline__ int find_group(const int* tile_start, int n_active, int mt) {
+    int lo = 0, hi = n_active - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= mt) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_fp8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
+                     const __grid_constant__ CUtensorMap tmS1, const Fp8Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t pfull0 = smem_u32(bars + 2 * STAGES), pempty0 = smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t xbar0 = smem_u32(bars + 2 * STAGES + 4), drain = smem_u32(bars + 2 * STAGES + 6);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 7);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_tile = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+    int* s_group = s_tile + kMaxExperts + 2;
+    float* xchg = reinterpret_cast<float*>(s_tile + TABLE_INTS);  // [2 parities][BM rows][2 halves]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_active = p.hdr->n_active;
+    const int total = p.hdr->total_tiles * p.n_tiles;
+    for (int i = threadIdx.x; i <= n_active; i += THREADS) s_tile[i] = p.act_tile[i];
+    for (int i = threadIdx.x; i < n_active; i += THREADS) s_group[i] = p.act_group[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(pfull0 + 8 * b, 1);
+            mbar_init(pempty0 + 8 * b, EPI_THREADS / 32);
+            mbar_init(xbar0 + 8 * b, EPI_THREADS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB0);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (*abort_flag) break;
+                const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+                const int a = find_group(s_tile, n_active, mt);
+                const int g = s_group[a];
+                const int row0 = p.grp_off[g] + (mt - s_tile[a]) * BM;
+                const bool routed = g < p.E;
+                const CUtensorMap* b0 = routed ? &tmB0 : &tmS0;
+                const CUtensorMap* b1 = routed ? &tmB1 : &tmS1;
+                const int gz = routed ? g : 0;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+                    mbar_arrive_expect_tx(full0 + 8 * s, STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, kb * BK, row0, full0 + 8 * s);
+                    if (GATEUP) {
+                        tma_load_3d(sb, b0, kb * BK, nt * 128, gz, full0 + 8 * s);
+                        tma_load_3d(sb + B_BYTES / 2, b1, kb * BK, nt * 128, gz, full0 + 8 * s);
+                    } else {
+                        tma_load_3d(sb, b0, kb * BK, nt * BN, gz, full0 + 8 * s);
+                    }
+                }
+            }
+            if (!ok) {
+                set_error(p.hdr, DEV_ERR_TIMEOUT, 21);
+                *abort_flag = 1;
+            }
+            for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
+                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, WAIT_NS);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_e4m3(BM, BN);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                if (*abort_flag) break;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    const uint32_t b = it & 1u, pph = (it >> 1) & 1u;
+                    if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS) || !mbar_wait(pempty0 + 8 * b, pph ^ 1u, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(sbase + s * STAGE_BYTES);
+                    const uint64_t bd = desc_sw128(sbase + s * STAGE_BYTES + A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; ++kk)  // +32 bytes of K per MMA
+                        mma_e4m3(tmem_base + b * BN, ad + 2 * kk, bd + 2 * kk, idesc, kk != 0);
+                    mma_commit(empty0 + 8 * s);
+                    mma_commit(pfull0 + 8 * b);
+                }
+            }
+            if (!ok) {
+                set_error(p.hdr, DEV_ERR_TIMEOUT, 22);
+                *abort_flag = 1;
+            }
+            mma_commit(drain);
+            mbar_wait(drain, 0, WAIT_NS);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;            // TMEM lane quarter
+        const int half = (warp - 2) >> 2;  // which 128 of the 256 columns
+        const int r = q * 32 + lane;       // tile row
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        uint32_t it = 0, tc = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+            const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+            const int a = find_group(s_tile, n_active, mt);
+            const int g = s_group[a];
+            const int j = mt - s_tile[a];
+            const int valid = p.grp_cnt[g] - j * BM;
+            const int row = p.grp_off[g] + j * BM + r;
+            const float* asc = p.a_sc + (size_t)min(row, p.rows - 1) * p.kblocks;
+            const bool routed = g < p.E;
+            const float* bsc0 = routed ? p.b_sc0 + (size_t)g * p.b_row_blocks * p.kblocks : p.s_sc0;
+            const float* bsc1 = routed ? p.b_sc1 + (size_t)g * p.b_row_blocks * p.kblocks : p.s_sc1;
+            // gate/up: this half owns G cols [64h, 64h+64) and U cols [128+64h, ...);
+            // down: cols [128h, 128h+128) of one 128-row block of W2
+            const float* sc_lo = GATEUP ? bsc0 + (size_t)nt * p.kblocks : bsc0 + (size_t)(nt * 2 + half) * p.kblocks;
+            const float* sc_hi = GATEUP ? bsc1 + (size_t)nt * p.kblocks : sc_lo;
+            const uint32_t c_lo = GATEUP ? 64 * half : 128 * half;
+            const uint32_t c_hi = GATEUP ? 128 + 64 * half : 128 * half + 64;
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+            for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                const uint32_t b = it & 1u, pph = (it >> 1) & 1u;
+                const float sx = __ldg(asc + kb);
+                const float f_lo = sx * __ldg(sc_lo + kb), f_hi = sx * __ldg(sc_hi + kb);
+                if (!mbar_wait(pfull0 + 8 * b, pph, WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = tmem_base + lane_off + b * BN;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t v[16];
+                    tmem_ld16(base + (c < 4 ? c_lo + 16 * c : c_hi + 16 * (c - 4)), v);
+                    tmem_wait_ld();
+                    const float f = c < 4 ? f_lo : f_hi;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(__uint_as_float(v[i]), f, acc[16 * c + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pempty0 + 8 * b);
+            }
+            if (!ok) break;
+            if (GATEUP) {
+                // acc[0..63] = G, acc[64..127] = U for I columns nt*128 + 64*half + [0, 64)
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    acc[i] = swiglu(acc[i], acc[64 + i]);
+                    amax = fmaxf(amax, fabsf(acc[i]));
+                }
+                const uint32_t par = tc & 1u;
+                float* slot = xchg + (par * BM + r) * 2;
+                slot[half] = amax;
+                mbar_arrive(xbar0 + 8 * par);
+                if (!mbar_wait(xbar0 + 8 * par, (tc >> 1) & 1u, WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                amax = fmaxf(slot[0], slot[1]);
+                if (r < valid) {
+                    float s = 1.0f;
+                    uint32_t w[16];
+                    if (amax > 0.f) {
+                        s = __fdiv_rn(amax, 448.0f);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            w[i] = f32x2_to_e4m3x2(__fdiv_rn(acc[4 * i], s), __fdiv_rn(acc[4 * i + 1], s)) |
+                                   (f32x2_to_e4m3x2(__fdiv_rn(acc[4 * i + 2], s), __fdiv_rn(acc[4 * i + 3], s)) << 16);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = 0;
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(p.out_q + (size_t)row * p.ldo + nt * 128 + 64 * half);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    if (half == 0) p.out_sc[(size_t)row * (p.ldo / 128) + nt] = s;
+                }
+            } else if (r < valid) {
+                uint4* dst = reinterpret_cast<uint4*>(p.out_y + (size_t)row * p.ldo + nt * BN + 128 * half);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    dst[i] = make_uint4(pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]), pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
+                                        pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]), pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
+            }
+        }
+        if (!ok) {
+            set_error(p.hdr, DEV_ERR_TIMEOUT, 23);
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+int num_sms() {
+    static int sms = device_sm_count();
+    return sms;
+}
+
+template <bool GATEUP>
+cudaError_t set_smem_attr() {
+    static cudaError_t e =
+        cudaFuncSetAttribute(grouped_gemm_fp8<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_fp8_gateup(const GemmLaunch& L, cudaStream_t st) {
+    cudaError_t e = set_smem_attr<true>();
+    if (e != cudaSuccess) return e;
+    const GemmCall& g = L.call;
+    const GemmWeights& w = *L.w;
+    Fp8Params p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.xs_sc, w.s1, w.s3, w.ss1, w.ss3,
+                g.E, g.rows, g.I / 128, g.H / BK, g.I, g.I / 128, static_cast<uint8_t*>(g.h), g.hsc, nullptr};
+    const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
+    grouped_gemm_fp8<true><<<grid, THREADS, SMEM_BYTES, st>>>(L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_fp8_down(const GemmLaunch& L, cudaStream_t st) {
+    cudaError_t e = set_smem_attr<false>();
+    if (e != cudaSuccess) return e;
+    const GemmCall& g = L.call;
+    const GemmWeights& w = *L.w;
+    Fp8Params p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.hsc, w.s2, w.s2, w.ss2, w.ss2,
+                g.E, g.rows, g.H / BN, g.I / BK, g.H, g.H / 128, nullptr, nullptr, g.y};
+    const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
+    grouped_gemm_fp8<false><<<grid, THREADS, SMEM_BYTES, st>>>(L.a_h, w.w2, w.w2, w.sw2, w.sw2, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

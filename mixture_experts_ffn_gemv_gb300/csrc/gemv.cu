@@ -77,7 +77,7 @@ __device__ __forceinline__ int row_token(const GemvArgs& a, int s) {
 // K-slice partials are summed in fixed order through shared memory, then
 // h = silu(g) * u is stored as bf16 [rows, I].
 template <int NT>
-__global__ __launch_bounds__(256) void gemv_gateup_bf16(const GemvArgs a, const uint16_t* __restrict__ x,
+__global__ __launch_bounds__(256, (NT == 1 ? 4 : 3)) void gemv_gateup_bf16(const GemvArgs a, const uint16_t* __restrict__ x,
                                                         uint16_t* __restrict__ h, int n_slices) {
     constexpr int KS = 4, RT = 2;
     __shared__ float red[KS][RT][32][NT * 8];
@@ -109,7 +109,7 @@ __global__ __launch_bounds__(256) void gemv_gateup_bf16(const GemvArgs a, const 
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) c1[nt][i] = c3[nt][i] = 0.f;
-#pragma unroll 4
+#pragma unroll 2
         for (int kc = kc0 + tig; kc < kc1; kc += 4) {
             const uint4 a1 = ld_stream_v4(w1g + kc), a18 = ld_stream_v4(w1g8 + kc);
             const uint4 a3 = ld_stream_v4(w3g + kc), a38 = ld_stream_v4(w3g8 + kc);
@@ -160,7 +160,7 @@ __global__ __launch_bounds__(256) void gemv_gateup_bf16(const GemvArgs a, const 
 // ============================================================ down, bf16
 // CTA: 2 row tiles (16 rows of H) x 4 K-slices of I; y fp32 [rows, H].
 template <int NT>
-__global__ __launch_bounds__(256) void gemv_down_bf16(const GemvArgs a, const uint16_t* __restrict__ h,
+__global__ __launch_bounds__(256, 4) void gemv_down_bf16(const GemvArgs a, const uint16_t* __restrict__ h,
                                                       float* __restrict__ y, int n_slices) {
     constexpr int KS = 4, RT = 2;
     __shared__ float red[KS][RT][32][NT * 4];
@@ -188,7 +188,7 @@ __global__ __launch_bounds__(256) void gemv_down_bf16(const GemvArgs a, const ui
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
-#pragma unroll 4
+#pragma unroll 2
         for (int kc = kc0 + tig; kc < kc1; kc += 4) {
             const uint4 w0 = ld_stream_v4(wg + kc), w8 = ld_stream_v4(wg8 + kc);
 #pragma unroll

@@ -138,6 +138,22 @@ def test_route_parity(cuda, oracle_mod, wl_name, m):
     assert len(swapped) <= max(2, m // 200)
 
 
+@pytest.mark.parametrize("shape,m", [(I.TINY, 300), (ODD_E, 500), (MEDIUM_BF16, 129)])
+def test_route_tensor_core_path_odd_shapes(cuda, oracle_mod, shape, m):
+    """m > 64 takes the tensor-core router (bf16 x3 split of the fp32 weight);
+    E of 8, 40 and 16 exercise the padded N of its MMA."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    tensors, x = _small_case(shape, m, seed=61, device=cuda)
+    layer = binding.MoeLayer(shape, tensors)
+    ids, w, logits = layer.moe_route(x, tensors["router_w"], logits=True)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    L, r_ids, r_w, _ = oracle_route(oracle_mod, shape, tensors, x)
+    assert np.abs(to_np(logits) - L).max() <= 1e-5 * max(np.abs(L).max(), 1.0)
+    swapped, bad = check_ids(to_np(ids), r_ids, L)
+    assert not bad, bad[:5]
+
+
 # ------------------------------------------------------------------ experts (given routing)
 
 def _small_case(shape, m, seed, device):
