@@ -387,10 +387,22 @@ def sweep(device, steps, warmup):
                 tc_peak = tc * (2.0 if wl.shape.fp8 else 1.0)
                 t_roof = max(byt / bw, flops / tc_peak)
                 arm = reps[0]["layer"].select_arm(m)
+                totals, _ = kernel_profile(reps, n, wl, m)
+                kern = {}
+                for kname, (kms, kcnt) in sorted(totals.items(), key=lambda kv: -kv[1][0]):
+                    avg = kms / kcnt / 1e3
+                    ent = {"avg_us": avg * 1e6}
+                    kb = kernel_alg_bytes(kname, wl.shape, m, U)
+                    kf = kernel_flops(kname, wl.shape, m)
+                    if kb:
+                        ent["hbm_frac"] = kb / avg / bw
+                    if kf and kname.startswith("gemm"):
+                        ent["tensor_frac"] = kf / avg / tc_peak
+                    kern[kname] = ent
                 res.append({"workload": name, "m": m, "arm": {1: "gemv", 2: "gemm"}.get(arm, arm),
                             "tokens_per_s": m / per, "ms_per_step": per * 1e3, "alg_bytes": byt,
                             "alg_flops": flops, "active_groups": U, "bound": "hbm" if byt / bw >= flops / tc_peak else "tensor",
-                            "layer_roofline_frac": t_roof / per})
+                            "layer_roofline_frac": t_roof / per, "kernels": kern})
             except Exception as e:  # keep the headline line even if one size fails
                 res.append({"workload": name, "m": m, "error": str(e)[:200]})
             finally:

@@ -68,10 +68,10 @@ extern "C" {
 #define MOE_ARM_GEMM 2 /* tcgen05/TMEM grouped GEMM arm fed by TMA */
 
 typedef struct moe_config {
-    int32_t hidden;       /* H: multiple of 128 */
+    int32_t hidden;       /* H: multiple of 128 (of 512 for fp8 weights) */
     int32_t num_experts;  /* E: 1..1024 */
     int32_t top_k;        /* k: 1..min(E, 32) */
-    int32_t inter;        /* I: expert intermediate size, multiple of 128 */
+    int32_t inter;        /* I: expert intermediate size, multiple of 128 (of 512 for fp8) */
     int32_t shared_inter; /* 0 = no shared expert; otherwise must equal inter */
     int32_t weights;      /* MOE_WEIGHTS_BF16 or MOE_WEIGHTS_FP8_E4M3_B128 */
 } moe_config;

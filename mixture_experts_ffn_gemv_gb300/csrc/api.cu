@@ -21,12 +21,12 @@ namespace {
 // Optional per-kernel timing: every launch bracketed by two CUDA events on its
 // stream, resolved when the totals are read.
 enum KernelId : int {
-    K_ROUTER_SPLIT = 0, K_ROUTER, K_TOPK, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
-    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_COUNT
+    K_ROUTER_SPLIT = 0, K_ROUTER, K_TOPK, K_ROUTE_PERMUTE, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
+    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_H_QUANT, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
-    "router_split", "router", "topk_softmax", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
-    "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine",
+    "router_split", "router", "topk_softmax", "route_permute", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
+    "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine", "h_quant_fp8",
 };
 
 struct Pending {
@@ -96,7 +96,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
     size_t hdr, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile, sorted_pair, slot_of_pair;
-    size_t xq, xsc, xs, xs_sc, h, hsc, y, total;
+    size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, total;
     int S, P, rows, nchunk;
     bool router_tc;
 };
@@ -135,7 +135,10 @@ Layout layout(const moe_layer* L, int64_t m) {
     o.xs = take((size_t)o.rows * H * ab);
     if (L->fp8) o.xs_sc = take((size_t)o.rows * (H / 128) * 4);
     o.h = take((size_t)o.rows * I * ab);
-    if (L->fp8) o.hsc = take((size_t)o.rows * (I / 128) * 4);
+    if (L->fp8) {
+        o.hsc = take((size_t)o.rows * (I / 128) * 4);
+        o.hf = take((size_t)o.rows * I * 4);  // GEMV arm: fp32 h before quantisation
+    }
     o.y = take((size_t)o.rows * H * 4);
     o.total = off;
     return o;
@@ -224,14 +227,16 @@ PermuteOut permute_out(const Layout& lo, void* ws, int32_t* sorted_pair, int32_t
 }
 
 int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, const int32_t* ids, const float* w,
-                void* out, int arm, void* ws, Launcher& ln) {
+                void* out, int arm, void* ws, Launcher& ln, bool permuted = false) {
     const moe_config& c = L->cfg;
     const cudaStream_t st = ln.st;
     const int E = c.num_experts, k = c.top_k, H = c.hidden, I = c.inter;
     WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
     const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
-    MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->has_shared ? 1 : 0, po, hdr, st));
-    MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(ids, m, k, E, po, st));
+    if (!permuted) {
+        MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->has_shared ? 1 : 0, po, hdr, st));
+        MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(ids, m, k, E, po, st));
+    }
     if (arm == MOE_ARM_AUTO) arm = moe_select_arm(L, m);
     const int has_shared = L->has_shared ? 1 : 0;
     if (arm == MOE_ARM_GEMV) {
@@ -258,7 +263,9 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
             uint8_t* hq = at<uint8_t>(ws, lo.h);
             float* hsc = at<float>(ws, lo.hsc);
             MOE_LAUNCH(K_ACT_QUANT, launch_act_quant_fp8(static_cast<const uint16_t*>(x), m, H, xq, xsc, st));
-            MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_fp8(a, xq, xsc, hq, hsc, st));
+            float* hf = at<float>(ws, lo.hf);
+            MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_fp8(a, xq, xsc, hf, st));
+            MOE_LAUNCH(K_H_QUANT, launch_quant_rows_fp8(hf, lo.rows, I, hq, hsc, st));
             MOE_LAUNCH(K_GEMV_DOWN, launch_gemv_down_fp8(a, hq, hsc, y, st));
         } else {
             uint16_t* h = at<uint16_t>(ws, lo.h);
@@ -333,7 +340,7 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
     if (c.top_k > c.num_experts) return MOE_ERR_INVALID_ARG;
     if (c.num_experts > kMaxExperts || c.top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
     if (c.hidden % 128 != 0 || c.inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
-    if (fp8 && c.inter % 512 != 0) return MOE_ERR_UNSUPPORTED;
+    if (fp8 && (c.inter % 512 != 0 || c.hidden % 512 != 0)) return MOE_ERR_UNSUPPORTED;
     if (c.shared_inter != 0 && c.shared_inter != c.inter) return MOE_ERR_UNSUPPORTED;
     if (!weights_ok(routed, fp8)) return MOE_ERR_INVALID_ARG;
     const bool has_shared = c.shared_inter > 0;
@@ -442,8 +449,20 @@ int moe_forward(const moe_layer* layer, const void* x, int64_t m, const float* r
     float* w = topk_w_out ? topk_w_out : at<float>(workspace, lo.w);
     Launcher ln{layer, st};
     if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
-    rc = run_route(layer, lo, x, (int)m, router_w, router_bias, nullptr, ids, w, workspace, ln);
-    if (rc == MOE_OK) rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln);
+    const moe_config& c = layer->cfg;
+    if (!lo.router_tc && route_permute_fusable((int)m, c.top_k, c.num_experts)) {
+        // decode: router, top-k and the permute in one launch
+        const PermuteOut po = permute_out(lo, workspace, nullptr, nullptr, nullptr);
+        MOE_LAUNCH(K_ROUTE_PERMUTE,
+                   launch_route_permute_small(static_cast<const uint16_t*>(x), (int)m, c.hidden, router_w,
+                                              c.num_experts, at<float>(workspace, lo.part), lo.S, c.top_k, router_bias,
+                                              ids, w, layer->has_shared ? 1 : 0, po, at<WsHeader>(workspace, lo.hdr),
+                                              st));
+        rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln, true);
+    } else {
+        rc = run_route(layer, lo, x, (int)m, router_w, router_bias, nullptr, ids, w, workspace, ln);
+        if (rc == MOE_OK) rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln);
+    }
     layer->last_launches = ln.n;
     return rc;
 }

@@ -8,6 +8,7 @@
 // deterministic and out is fully overwritten.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -28,18 +29,38 @@ template <typename YT>
 __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
                                                const float* __restrict__ w, int k, int H, int P, int has_shared,
                                                uint16_t* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.y;
     const int h0 = (blockIdx.x * 128 + threadIdx.x) * 8;
     if (h0 >= H) return;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-        const int s = slot[(size_t)t * k + j];
-        if (s < 0 || s >= P) continue;  // pair with an invalid expert id
-        const float wj = w[(size_t)t * k + j];
-        float v[8];
-        load8(y + (size_t)s * H + h0, v);
+    // slots and weights of 8 pairs first, then their 8 rows, then the sums in
+    // ascending j: the loads overlap instead of forming a dependent chain
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        int sl[8];
+        float wj[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+        for (int u = 0; u < 8; ++u) {
+            const bool in = j0 + u < k;
+            sl[u] = in ? slot[(size_t)t * k + j0 + u] : -1;
+            wj[u] = in ? w[(size_t)t * k + j0 + u] : 0.f;
+        }
+        float v[8][8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (sl[u] >= 0 && sl[u] < P) {  // slot -1: a pair with an invalid expert id
+                load8(y + (size_t)sl[u] * H + h0, v[u]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
+                wj[u] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], v[u][i], acc[i]);
     }
     if (has_shared) {
         float v[8];
@@ -58,14 +79,14 @@ __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const i
 cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
                                int P, int has_shared, uint16_t* out, cudaStream_t st) {
     const dim3 grid(ceil_div(H, 1024), m);
-    combine<float><<<grid, 128, 0, st>>>(y, slot_of_pair, w, k, H, P, has_shared, out);
+    launch_pdl(combine<float>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, out);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
                                 int H, int P, int has_shared, uint16_t* out, cudaStream_t st) {
     const dim3 grid(ceil_div(H, 1024), m);
-    combine<uint16_t><<<grid, 128, 0, st>>>(y, slot_of_pair, w, k, H, P, has_shared, out);
+    launch_pdl(combine<uint16_t>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, out);
     return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "kernels.h"
+#include "launch.cuh"
 #include "sm100.cuh"
 #include "tmap.h"
 
@@ -74,6 +75,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
                       const __grid_constant__ CUtensorMap tmS1, const GemmParams p) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -353,7 +356,7 @@ cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
     GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.I / 128, g.H / BK, g.I, 128,
                  static_cast<uint16_t*>(g.h)};
     const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
-    grouped_gemm_bf16<true><<<grid, THREADS, SMEM_BYTES, st>>>(L.a_xs, L.w->w1, L.w->w3, L.w->sw1, L.w->sw3, p);
+    launch_pdl(grouped_gemm_bf16<true>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_xs, L.w->w1, L.w->w3, L.w->sw1, L.w->sw3, p);
     return cudaGetLastError();
 }
 
@@ -364,7 +367,7 @@ cudaError_t launch_gemm_down(const GemmLaunch& L, cudaStream_t st) {
     const GemmCall& g = L.call;
     GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.H / BN, g.I / BK, g.H, BN, g.y};
     const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
-    grouped_gemm_bf16<false><<<grid, THREADS, SMEM_BYTES, st>>>(L.a_h, L.w->w2, L.w->w2, L.w->sw2, L.w->sw2, p);
+    launch_pdl(grouped_gemm_bf16<false>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_h, L.w->w2, L.w->w2, L.w->sw2, L.w->sw2, p);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "kernels.h"
+#include "launch.cuh"
 #include "sm100.cuh"
 #include "tmap.h"
 
@@ -78,6 +79,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_fp8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                      const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
                      const __grid_constant__ CUtensorMap tmS1, const Fp8Params p) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -320,7 +323,7 @@ cudaError_t launch_gemm_fp8_gateup(const GemmLaunch& L, cudaStream_t st) {
     Fp8Params p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.xs_sc, w.s1, w.s3, w.ss1, w.ss3,
                 g.E, g.rows, g.I / 128, g.H / BK, g.I, g.I / 128, static_cast<uint8_t*>(g.h), g.hsc, nullptr};
     const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
-    grouped_gemm_fp8<true><<<grid, THREADS, SMEM_BYTES, st>>>(L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
+    launch_pdl(grouped_gemm_fp8<true>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
     return cudaGetLastError();
 }
 
@@ -332,7 +335,7 @@ cudaError_t launch_gemm_fp8_down(const GemmLaunch& L, cudaStream_t st) {
     Fp8Params p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.hsc, w.s2, w.s2, w.ss2, w.ss2,
                 g.E, g.rows, g.H / BN, g.I / BK, g.H, g.H / 128, nullptr, nullptr, g.y};
     const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
-    grouped_gemm_fp8<false><<<grid, THREADS, SMEM_BYTES, st>>>(L.a_h, w.w2, w.w2, w.sw2, w.sw2, p);
+    launch_pdl(grouped_gemm_fp8<false>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_h, w.w2, w.w2, w.sw2, w.sw2, p);
     return cudaGetLastError();
 }
 

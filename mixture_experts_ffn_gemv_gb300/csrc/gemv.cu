@@ -20,6 +20,7 @@
 // accumulation of spark_model forward_prefill's fp8 grouped GEMM).
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace moe {
 
@@ -77,8 +78,10 @@ __device__ __forceinline__ int row_token(const GemvArgs& a, int s) {
 // K-slice partials are summed in fixed order through shared memory, then
 // h = silu(g) * u is stored as bf16 [rows, I].
 template <int NT>
-__global__ __launch_bounds__(256, (NT == 1 ? 4 : 3)) void gemv_gateup_bf16(const GemvArgs a, const uint16_t* __restrict__ x,
+__global__ __launch_bounds__(256, (NT == 1 ? 4 : 2)) void gemv_gateup_bf16(const GemvArgs a, const uint16_t* __restrict__ x,
                                                         uint16_t* __restrict__ h, int n_slices) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int KS = 4, RT = 2;
     __shared__ float red[KS][RT][32][NT * 8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,6 +165,8 @@ __global__ __launch_bounds__(256, (NT == 1 ? 4 : 3)) void gemv_gateup_bf16(const
 template <int NT>
 __global__ __launch_bounds__(256, 4) void gemv_down_bf16(const GemvArgs a, const uint16_t* __restrict__ h,
                                                       float* __restrict__ y, int n_slices) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int KS = 4, RT = 2;
     __shared__ float red[KS][RT][32][NT * 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -217,30 +222,35 @@ __global__ __launch_bounds__(256, 4) void gemv_down_bf16(const GemvArgs a, const
 }
 
 // ============================================================ gate/up, fp8
-// CTA: 8 row tiles = 128 rows of I (one scale block), whole H per warp, so the
-// CTA can quantise its h block (1x128 along I) itself: hq e4m3 [rows, I] and
-// hsc fp32 [rows, I/128].
+// CTA: 8 warps = 2 row tiles (16 rows of I) x 4 K-slices of H, each slice a
+// whole number of 128-wide scale blocks.  The K-slice partials are summed in
+// fixed order through shared memory and h = silu(g) * u is stored as fp32
+// [rows, I]; quant_rows_fp8 then quantises each row per 1x128 block.
 template <int NT>
-__global__ __launch_bounds__(256) void gemv_gateup_fp8(const GemvArgs a, const uint8_t* __restrict__ xq,
-                                                       const float* __restrict__ xsc, uint8_t* __restrict__ hq,
-                                                       float* __restrict__ hsc, int n_slices) {
-    __shared__ float hs[NT * 8][128 + 1];
+__global__ __launch_bounds__(256, (NT == 1 ? 2 : 1)) void gemv_gateup_fp8(const GemvArgs a, const uint8_t* __restrict__ xq,
+                                                          const float* __restrict__ xsc, float* __restrict__ hf,
+                                                          int n_slices) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int KS = 4, RT = 2;
+    __shared__ float red[KS][RT][32][NT * 8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, tig = lane & 3;
+    const int rt = warp % RT, kq = warp / RT;
     Group gr;
     if (!load_group(a, blockIdx.x / n_slices, gr)) return;
     const int H = a.H, I = a.I, hb = H / 128;
-    const int blk0 = (blockIdx.x % n_slices) * 128;  // first row of this CTA's I block
-    const int row0 = blk0 + warp * 16;
+    const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
     const bool routed = gr.g < a.E;
     const uint8_t* W1 = routed ? (const uint8_t*)a.w1 + (size_t)gr.g * I * H : (const uint8_t*)a.sw1;
     const uint8_t* W3 = routed ? (const uint8_t*)a.w3 + (size_t)gr.g * I * H : (const uint8_t*)a.sw3;
-    const float* S1 = (routed ? a.s1 + (size_t)gr.g * (I / 128) * hb : a.ss1) + (size_t)(blk0 / 128) * hb;
-    const float* S3 = (routed ? a.s3 + (size_t)gr.g * (I / 128) * hb : a.ss3) + (size_t)(blk0 / 128) * hb;
+    const float* S1 = (routed ? a.s1 + (size_t)gr.g * (I / 128) * hb : a.ss1) + (size_t)(row0 / 128) * hb;
+    const float* S3 = (routed ? a.s3 + (size_t)gr.g * (I / 128) * hb : a.ss3) + (size_t)(row0 / 128) * hb;
     const uint4* w1g = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8) * H);
     const uint4* w1g8 = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8 + 8) * H);
     const uint4* w3g = reinterpret_cast<const uint4*>(W3 + (size_t)(row0 + g8) * H);
     const uint4* w3g8 = reinterpret_cast<const uint4*>(W3 + (size_t)(row0 + g8 + 8) * H);
+    const int b0 = kq * (hb / KS), b1 = (kq + 1) * (hb / KS);
     for (int r0 = 0; r0 < gr.cnt; r0 += 8 * NT) {
         const int R = min(8 * NT, gr.cnt - r0);
         const uint4* xr[NT];
@@ -260,7 +270,7 @@ __global__ __launch_bounds__(256) void gemv_gateup_fp8(const GemvArgs a, const u
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) c1[nt][i] = c3[nt][i] = 0.f;
-        for (int b = 0; b < hb; ++b) {  // one 128-wide K block per pass: 8 chunks of 16 codes
+        for (int b = b0; b < b1; ++b) {  // one 128-wide K block: 8 chunks of 16 codes
             float p1[NT][4], p3[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -294,31 +304,25 @@ __global__ __launch_bounds__(256) void gemv_gateup_fp8(const GemvArgs a, const u
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int col = nt * 8 + tig * 2 + (i & 1);
-                const int rr = warp * 16 + g8 + (i >> 1) * 8;
-                hs[col][rr] = swiglu(c1[nt][i], c3[nt][i]);
+                red[kq][rt][lane][nt * 8 + i] = c1[nt][i];
+                red[kq][rt][lane][nt * 8 + 4 + i] = c3[nt][i];
             }
         __syncthreads();
-        // quantise each column's 128 values: one warp per column
-        for (int col = warp; col < R; col += 8) {
-            float v[4];
-            float amax = 0.f;
+        if (kq == 0) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[j] = hs[col][lane * 4 + j];
-                amax = fmaxf(amax, fabsf(v[j]));
-            }
-            amax = warp_max(amax);
-            uint32_t codes = 0;
-            float s = 1.0f;
-            if (amax > 0.f) {
-                s = __fdiv_rn(amax, 448.0f);
-                codes = f32x2_to_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
-                        (f32x2_to_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
-            }
-            const size_t srow = (size_t)(gr.off + r0 + col);
-            *reinterpret_cast<uint32_t*>(hq + srow * I + blk0 + lane * 4) = codes;
-            if (lane == 0) hsc[srow * (I / 128) + blk0 / 128] = s;
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float gs = red[0][rt][lane][nt * 8 + i], us = red[0][rt][lane][nt * 8 + 4 + i];
+#pragma unroll
+                    for (int q = 1; q < KS; ++q) {
+                        gs += red[q][rt][lane][nt * 8 + i];
+                        us += red[q][rt][lane][nt * 8 + 4 + i];
+                    }
+                    const int col = nt * 8 + tig * 2 + (i & 1);
+                    const int row = row0 + g8 + (i >> 1) * 8;
+                    if (col < R) hf[(size_t)(gr.off + r0 + col) * I + row] = swiglu(gs, us);
+                }
         }
         __syncthreads();
     }
@@ -331,6 +335,8 @@ template <int NT>
 __global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uint8_t* __restrict__ hq,
                                                      const float* __restrict__ hsc, float* __restrict__ y,
                                                      int n_slices) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int KS = 4, RT = 2;
     __shared__ float red[KS][RT][32][NT * 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -409,31 +415,33 @@ __global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uin
 }
 
 // ============================================================ launchers
-// Token columns per pass: 16 when a group can have more than 8 rows.
-static inline bool wide(const GemvArgs& a) { return a.P > 8 * a.max_groups || a.P >= 64; }
+// Token columns per pass: 16 when the groups average more than 4 rows (a
+// group with more rows than one pass covers takes further passes, re-reading
+// its weight slice from L2).
+static inline bool wide(const GemvArgs& a) { return a.P > 4 * a.max_groups; }
 
 cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st) {
     const int n_slices = a.I / 32;
     const dim3 grid(n_slices * a.max_groups);
-    if (wide(a)) gemv_gateup_bf16<2><<<grid, 256, 0, st>>>(a, x, h, n_slices);
-    else gemv_gateup_bf16<1><<<grid, 256, 0, st>>>(a, x, h, n_slices);
+    if (wide(a)) launch_pdl(gemv_gateup_bf16<2>, dim3(grid), dim3(256), 0, st, a, x, h, n_slices);
+    else launch_pdl(gemv_gateup_bf16<1>, dim3(grid), dim3(256), 0, st, a, x, h, n_slices);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_down_bf16(const GemvArgs& a, const uint16_t* h, float* y, cudaStream_t st) {
     const int n_slices = a.H / 32;
     const dim3 grid(n_slices * a.max_groups);
-    if (wide(a)) gemv_down_bf16<2><<<grid, 256, 0, st>>>(a, h, y, n_slices);
-    else gemv_down_bf16<1><<<grid, 256, 0, st>>>(a, h, y, n_slices);
+    if (wide(a)) launch_pdl(gemv_down_bf16<2>, dim3(grid), dim3(256), 0, st, a, h, y, n_slices);
+    else launch_pdl(gemv_down_bf16<1>, dim3(grid), dim3(256), 0, st, a, h, y, n_slices);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const float* xsc, uint8_t* hq,
-                                   float* hsc, cudaStream_t st) {
-    const int n_slices = a.I / 128;
+cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const float* xsc, float* hf,
+                                   cudaStream_t st) {
+    const int n_slices = a.I / 32;
     const dim3 grid(n_slices * a.max_groups);
-    if (wide(a)) gemv_gateup_fp8<2><<<grid, 256, 0, st>>>(a, xq, xsc, hq, hsc, n_slices);
-    else gemv_gateup_fp8<1><<<grid, 256, 0, st>>>(a, xq, xsc, hq, hsc, n_slices);
+    if (wide(a)) launch_pdl(gemv_gateup_fp8<2>, dim3(grid), dim3(256), 0, st, a, xq, xsc, hf, n_slices);
+    else launch_pdl(gemv_gateup_fp8<1>, dim3(grid), dim3(256), 0, st, a, xq, xsc, hf, n_slices);
     return cudaGetLastError();
 }
 
@@ -441,8 +449,8 @@ cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const flo
                                  cudaStream_t st) {
     const int n_slices = a.H / 32;
     const dim3 grid(n_slices * a.max_groups);
-    if (wide(a)) gemv_down_fp8<2><<<grid, 256, 0, st>>>(a, hq, hsc, y, n_slices);
-    else gemv_down_fp8<1><<<grid, 256, 0, st>>>(a, hq, hsc, y, n_slices);
+    if (wide(a)) launch_pdl(gemv_down_fp8<2>, dim3(grid), dim3(256), 0, st, a, hq, hsc, y, n_slices);
+    else launch_pdl(gemv_down_fp8<1>, dim3(grid), dim3(256), 0, st, a, hq, hsc, y, n_slices);
     return cudaGetLastError();
 }
 

@@ -46,8 +46,16 @@ cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int ha
                                  WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, const PermuteOut& o, cudaStream_t st);
 
+// decode fusion: router partials + top-k + single-block permute in one launch
+bool route_permute_fusable(int m, int k, int E);
+cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
+                                       int k, const float* bias, int32_t* ids, float* w, int has_shared,
+                                       const PermuteOut& o, WsHeader* hdr, cudaStream_t st);
+
 // activations
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st);
+// the same 1x128 quantisation of fp32 rows (the GEMV arm's h)
+cudaError_t launch_quant_rows_fp8(const float* v, int rows, int n, uint8_t* q, float* s, cudaStream_t st);
 cudaError_t launch_gather_bf16(const uint16_t* x, const int32_t* sorted_pair, int k, int P, int rows, int H,
                                uint16_t* xs, cudaStream_t st);
 cudaError_t launch_gather_fp8(const uint8_t* xq, const float* xsc, const int32_t* sorted_pair, int k, int P,
@@ -68,8 +76,8 @@ struct GemvArgs {
 };
 cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st);
 cudaError_t launch_gemv_down_bf16(const GemvArgs& a, const uint16_t* h, float* y, cudaStream_t st);
-cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const float* xsc, uint8_t* hq,
-                                   float* hsc, cudaStream_t st);
+cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const float* xsc, float* hf,
+                                   cudaStream_t st);
 cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
                                  cudaStream_t st);
 

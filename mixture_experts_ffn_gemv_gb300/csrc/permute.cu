@@ -15,47 +15,15 @@
 // quantiser (one e4m3 code + fp32 scale per 128 inputs).
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
+#include "route_permute.cuh"
 
 namespace moe {
 
-// Exclusive scan of a[0, n) in shared memory by a 256-thread block; returns
-// the total.  Every thread of the block must call it.
-__device__ int block_exclusive_scan(int* a, int n, int* warp_sums) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (n + 255) / 256;
-    const int b = tid * per, e = min(n, b + per);
-    int local = 0;
-    for (int i = b; i < e; ++i) local += a[i];
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int w = 0; w < 8; ++w) {
-            const int v = warp_sums[w];
-            warp_sums[w] = run;
-            run += v;
-        }
-        warp_sums[8] = run;
-    }
-    __syncthreads();
-    int run = warp_sums[warp] + incl - local;
-    for (int i = b; i < e; ++i) {
-        const int v = a[i];
-        a[i] = run;
-        run += v;
-    }
-    __syncthreads();
-    return warp_sums[8];
-}
-
 __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__ ids, int P, int m, int E,
                                                      int has_shared, int nchunk, PermuteOut o, WsHeader* hdr) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int hist[kMaxExperts + 2];
     __shared__ int off[kMaxExperts + 2];
     __shared__ int wsum[9];
@@ -134,6 +102,8 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
 }
 
 __global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict__ ids, int P, int E, PermuteOut o) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int wbase[];  // [8][E]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x;
@@ -189,7 +159,7 @@ cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int ha
                                  WsHeader* hdr, cudaStream_t st) {
     const int P = m * k;
     const int nchunk = ceil_div(P, kPermChunk);
-    permute_count<<<nchunk, 256, 0, st>>>(ids, P, m, E, has_shared, nchunk, o, hdr);
+    launch_pdl(permute_count, dim3(nchunk), dim3(256), 0, st, ids, P, m, E, has_shared, nchunk, o, hdr);
     return cudaGetLastError();
 }
 
@@ -197,7 +167,7 @@ cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, cons
     const int P = m * k;
     const int nchunk = ceil_div(P, kPermChunk);
     const size_t smem = sizeof(int) * 8 * (size_t)E;
-    permute_scatter<<<nchunk, 256, smem, st>>>(ids, P, E, o);
+    launch_pdl(permute_scatter, dim3(nchunk), dim3(256), smem, st, ids, P, E, o);
     return cudaGetLastError();
 }
 
@@ -207,6 +177,8 @@ cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, cons
 __global__ __launch_bounds__(256) void gather_bf16(const uint16_t* __restrict__ x,
                                                    const int32_t* __restrict__ sorted_pair, int k, int P,
                                                    int rows, int H, uint16_t* __restrict__ xs) {
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (s >= rows) return;
     const int t = s < P ? sorted_pair[s] / k : s - P;
@@ -218,6 +190,8 @@ __global__ __launch_bounds__(256) void gather_bf16(const uint16_t* __restrict__ 
 __global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq, const float* __restrict__ xsc,
                                                   const int32_t* __restrict__ sorted_pair, int k, int P, int rows,
                                                   int H, uint8_t* __restrict__ xs, float* __restrict__ xs_sc) {
+    pdl_wait();
+    pdl_trigger();
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (s >= rows) return;
     const int t = s < P ? sorted_pair[s] / k : s - P;
@@ -230,35 +204,48 @@ __global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq
 
 cudaError_t launch_gather_bf16(const uint16_t* x, const int32_t* sorted_pair, int k, int P, int rows, int H,
                                uint16_t* xs, cudaStream_t st) {
-    gather_bf16<<<ceil_div(rows, 8), 256, 0, st>>>(x, sorted_pair, k, P, rows, H, xs);
+    launch_pdl(gather_bf16, dim3(ceil_div(rows, 8)), dim3(256), 0, st, x, sorted_pair, k, P, rows, H, xs);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather_fp8(const uint8_t* xq, const float* xsc, const int32_t* sorted_pair, int k, int P,
                               int rows, int H, uint8_t* xs, float* xs_sc, cudaStream_t st) {
-    gather_fp8<<<ceil_div(rows, 8), 256, 0, st>>>(xq, xsc, sorted_pair, k, P, rows, H, xs, xs_sc);
+    launch_pdl(gather_fp8, dim3(ceil_div(rows, 8)), dim3(256), 0, st, xq, xsc, sorted_pair, k, P, rows, H, xs, xs_sc);
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- fp8 activations
-// One warp per (token, 128-block): s = amax / 448 (IEEE divide), code =
-// e4m3_rn_satfinite(x / s); an all-zero block gets s = 1 and zero codes.
-__global__ __launch_bounds__(256) void act_quant_fp8(const uint16_t* __restrict__ x, int m, int H,
-                                                     uint8_t* __restrict__ xq, float* __restrict__ xsc) {
+// One warp per (row, 128-block): s = amax / 448 (IEEE divide), code =
+// e4m3_rn_satfinite(v / s); an all-zero block gets s = 1 and zero codes.
+// Input bf16 (x) or fp32 (the GEMV arm's h).
+__device__ __forceinline__ void load4(const uint16_t* p, float (&f)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+}
+__device__ __forceinline__ void load4(const float* p, float (&f)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+
+template <typename T>
+__global__ __launch_bounds__(256) void act_quant_fp8(const T* __restrict__ x, int m, int H, uint8_t* __restrict__ xq,
+                                                     float* __restrict__ xsc) {
+    pdl_wait();
+    pdl_trigger();
     const int nb = H / 128;
     const int blk = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (blk >= m * nb) return;
     const int t = blk / nb, b = blk % nb;
     const size_t base = (size_t)t * H + (size_t)b * 128 + lane * 4;
-    const uint2 v = *reinterpret_cast<const uint2*>(x + base);
-    const float f0 = bf16lo(v.x), f1 = bf16hi(v.x), f2 = bf16lo(v.y), f3 = bf16hi(v.y);
-    const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+    float f[4];
+    load4(x + base, f);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
     uint32_t codes = 0;
     float s = 1.0f;
     if (amax > 0.f) {
         s = __fdiv_rn(amax, 448.0f);
-        codes = f32x2_to_e4m3x2(__fdiv_rn(f0, s), __fdiv_rn(f1, s)) |
-                (f32x2_to_e4m3x2(__fdiv_rn(f2, s), __fdiv_rn(f3, s)) << 16);
+        codes = f32x2_to_e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
+                (f32x2_to_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
     }
     *reinterpret_cast<uint32_t*>(xq + base) = codes;
     if (lane == 0) xsc[(size_t)t * nb + b] = s;
@@ -266,7 +253,13 @@ __global__ __launch_bounds__(256) void act_quant_fp8(const uint16_t* __restrict_
 
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st) {
     const int blocks = m * (H / 128);
-    act_quant_fp8<<<ceil_div(blocks, 8), 256, 0, st>>>(x, m, H, xq, xs);
+    launch_pdl(act_quant_fp8<uint16_t>, dim3(ceil_div(blocks, 8)), dim3(256), 0, st, x, m, H, xq, xs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows_fp8(const float* v, int rows, int n, uint8_t* q, float* s, cudaStream_t st) {
+    const int blocks = rows * (n / 128);
+    launch_pdl(act_quant_fp8<float>, dim3(ceil_div(blocks, 8)), dim3(256), 0, st, v, rows, n, q, s);
     return cudaGetLastError();
 }
 

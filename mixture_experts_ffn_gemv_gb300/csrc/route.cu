@@ -8,6 +8,8 @@
 // many SMs without atomics.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
+#include "route_permute.cuh"
 
 namespace moe {
 
@@ -18,6 +20,8 @@ template <int MT>
 __global__ __launch_bounds__(256) void router_partial_small(const uint16_t* __restrict__ x, int m, int H,
                                                             const float* __restrict__ wr, int E, int HS,
                                                             float* __restrict__ part) {
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * 8 + warp;
     if (e >= E) return;
@@ -28,6 +32,7 @@ __global__ __launch_bounds__(256) void router_partial_small(const uint16_t* __re
         float acc[MT];
 #pragma unroll
         for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+#pragma unroll 4
         for (int h = h0 + lane * 4; h < h1; h += 128) {
             const float4 w = __ldg(reinterpret_cast<const float4*>(we + h));
 #pragma unroll
@@ -56,6 +61,8 @@ constexpr int RT_BM = 64, RT_BN = 64, RT_BK = 32;
 __global__ __launch_bounds__(256) void router_logits_tiled(const uint16_t* __restrict__ x, int m, int H,
                                                            const float* __restrict__ wr, int E,
                                                            float* __restrict__ L) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float xs[RT_BK][RT_BM + 4];
     __shared__ float ws[RT_BK][RT_BN + 4];
     const int tid = threadIdx.x;
@@ -108,69 +115,97 @@ __global__ __launch_bounds__(256) void router_logits_tiled(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------- top-k
-// One warp per token; lane l holds logits e = l + 32 v.  k picks of a warp
-// arg-max ordered by (logit desc, index asc); weights = softmax over the k
-// picks (norm_topk_prob).
+// One warp per token; lane l holds logits e = l + 32 v.
 template <int VPL>
 __global__ __launch_bounds__(256) void topk_softmax(const float* __restrict__ part, int S, int m, int E, int k,
                                                     const float* __restrict__ bias, float* __restrict__ logits_out,
                                                     int32_t* __restrict__ ids, float* __restrict__ wts) {
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= m) return;
-    float v[VPL];
-    uint32_t taken = 0;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            float a = 0.f;
-            for (int s = 0; s < S; ++s) a += part[((size_t)s * m + t) * E + e];
-            if (bias) a += bias[e];
-            v[i] = a;
-            if (logits_out) logits_out[(size_t)t * E + e] = a;
-        } else {
-            v[i] = -INFINITY;
-            taken |= 1u << i;
-        }
-    }
-    float my_l = 0.f;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-                bv = v[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) {
-            my_l = bv;
-            my_id = bi;
-        }
-    }
-    const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
-    const float ex = lane < k ? expf(my_l - l0) : 0.f;
-    float den = ex;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    int id;
+    float wt;
+    warp_topk_softmax<VPL, false>(part, S, m, E, k, bias, logits_out, t, lane, &id, &wt);
     if (lane < k) {
-        ids[(size_t)t * k + lane] = my_id;
-        wts[(size_t)t * k + lane] = ex / den;
+        ids[(size_t)t * k + lane] = id;
+        wts[(size_t)t * k + lane] = wt;
     }
+}
+
+// ---------------------------------------------------------------- fused decode route + permute
+// m <= kRouterSmallMaxM, m*k <= kPermChunk, E <= 256: every block computes
+// split-H router partials exactly as router_partial_small; the last block to
+// finish (an atomic ticket, nothing waits) runs the top-k of every token and
+// the single-block stable permute.  One launch instead of four.
+template <int VPL>
+__global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __restrict__ x, int m, int H,
+                                                           const float* __restrict__ wr, int E, int HS,
+                                                           float* __restrict__ part, int k,
+                                                           const float* __restrict__ bias, int32_t* __restrict__ ids,
+                                                           float* __restrict__ wts, int has_shared, PermuteOut o,
+                                                           WsHeader* hdr) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int MT = 8;
+    __shared__ int ids_s[kPermChunk];
+    __shared__ int hist[256 + 2];
+    __shared__ int off[256 + 2];
+    __shared__ int wbase[8 * 256];
+    __shared__ int wsum[9];
+    __shared__ int is_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + warp;
+    const int s = blockIdx.y;
+    if (e < E) {
+        const int h0 = s * HS, h1 = h0 + HS;
+        const float* we = wr + (size_t)e * H;
+        for (int t0 = 0; t0 < m; t0 += MT) {
+            float acc[MT];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+#pragma unroll 4
+            for (int h = h0 + lane * 4; h < h1; h += 128) {
+                const float4 w = __ldg(reinterpret_cast<const float4*>(we + h));
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    if (t0 + t < m) {
+                        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * H + h));
+                        acc[t] = fmaf(w.x, bf16lo(xv.x), acc[t]);
+                        acc[t] = fmaf(w.y, bf16hi(xv.x), acc[t]);
+                        acc[t] = fmaf(w.z, bf16lo(xv.y), acc[t]);
+                        acc[t] = fmaf(w.w, bf16hi(xv.y), acc[t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const float v = warp_sum(acc[t]);
+                if (lane == 0 && t0 + t < m) part[((size_t)s * m + t0 + t) * E + e] = v;
+            }
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(&hdr->done, 1) == (int)(gridDim.x * gridDim.y) - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const int S = gridDim.y;
+    for (int t = warp; t < m; t += 8) {
+        int id;
+        float wt;
+        warp_topk_softmax<VPL, true>(part, S, m, E, k, bias, nullptr, t, lane, &id, &wt);
+        if (lane < k) {
+            ids[(size_t)t * k + lane] = id;
+            wts[(size_t)t * k + lane] = wt;
+            ids_s[t * k + lane] = id;
+        }
+    }
+    __syncthreads();
+    block_permute_small(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, wbase, wsum);
+    if (threadIdx.x == 0) hdr->done = 0;
 }
 
 // ---------------------------------------------------------------- launchers
@@ -185,11 +220,31 @@ cudaError_t launch_router(const uint16_t* x, int m, int H, const float* wr, int 
                           cudaStream_t st) {
     if (m <= kRouterSmallMaxM) {
         dim3 grid(ceil_div(E, 8), S);
-        router_partial_small<8><<<grid, 256, 0, st>>>(x, m, H, wr, E, H / S, part);
+        launch_pdl(router_partial_small<8>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part);
     } else {
         dim3 grid(ceil_div(m, RT_BM), ceil_div(E, RT_BN));
-        router_logits_tiled<<<grid, 256, 0, st>>>(x, m, H, wr, E, part);
+        launch_pdl(router_logits_tiled, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, part);
     }
+    return cudaGetLastError();
+}
+
+bool route_permute_fusable(int m, int k, int E) {
+    return m <= kRouterSmallMaxM && m * k <= kPermChunk && E <= 256;
+}
+
+cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
+                                       int k, const float* bias, int32_t* ids, float* w, int has_shared,
+                                       const PermuteOut& o, WsHeader* hdr, cudaStream_t st) {
+    const dim3 grid(ceil_div(E, 8), S);
+    const int vpl = ceil_div(E, 32);
+    if (vpl <= 1)
+        launch_pdl(route_permute_small<1>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
+    else if (vpl <= 2)
+        launch_pdl(route_permute_small<2>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
+    else if (vpl <= 4)
+        launch_pdl(route_permute_small<4>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
+    else
+        launch_pdl(route_permute_small<8>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
     return cudaGetLastError();
 }
 
@@ -197,12 +252,12 @@ cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const flo
                         int32_t* ids, float* w, cudaStream_t st) {
     const int vpl = ceil_div(E, 32);
     dim3 grid(ceil_div(m, 8));
-    if (vpl <= 1) topk_softmax<1><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
-    else if (vpl <= 2) topk_softmax<2><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
-    else if (vpl <= 4) topk_softmax<4><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
-    else if (vpl <= 8) topk_softmax<8><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
-    else if (vpl <= 16) topk_softmax<16><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
-    else topk_softmax<32><<<grid, 256, 0, st>>>(part, S, m, E, k, bias, logits_out, ids, w);
+    if (vpl <= 1) launch_pdl(topk_softmax<1>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
+    else if (vpl <= 2) launch_pdl(topk_softmax<2>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
+    else if (vpl <= 4) launch_pdl(topk_softmax<4>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
+    else if (vpl <= 8) launch_pdl(topk_softmax<8>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
+    else if (vpl <= 16) launch_pdl(topk_softmax<16>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
+    else launch_pdl(topk_softmax<32>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
     return cudaGetLastError();
 }
 

@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "sm100.cuh"
 #include "tmap.h"
 
@@ -33,6 +34,8 @@ constexpr int R_SMEM_MAX = 220 * 1024;
 
 __global__ void __launch_bounds__(256) router_split(const float* __restrict__ wr, int E, int H, int Epad,
                                                     uint16_t* __restrict__ planes) {
+    pdl_wait();
+    pdl_trigger();
     const size_t n = (size_t)Epad * H;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int e = (int)(i / H);
@@ -56,6 +59,8 @@ struct RouterParams {
 __global__ void __launch_bounds__(R_THREADS, 1)
     router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const RouterParams p, uint32_t tmem_cols) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -196,7 +201,7 @@ cudaError_t launch_router_split(const float* wr, int E, int H, uint16_t* planes,
     const int Epad = router_tc_epad(E);
     const size_t n = (size_t)Epad * H;
     const int grid = (int)std::min<size_t>((n + 255) / 256, 4096);
-    router_split<<<grid, 256, 0, st>>>(wr, E, H, Epad, planes);
+    launch_pdl(router_split, dim3(grid), dim3(256), 0, st, wr, E, H, Epad, planes);
     return cudaGetLastError();
 }
 
@@ -224,7 +229,7 @@ cudaError_t launch_router_tc(const uint16_t* x, int m, int H, const uint16_t* pl
                                                    R_SMEM_MAX);
     if (attr != cudaSuccess) return attr;
     const dim3 grid(ceil_div(m, RBM), S);
-    router_logits_tc<<<grid, R_THREADS, smem, st>>>(tx, tw, p, cols);
+    launch_pdl(router_logits_tc, dim3(grid), dim3(R_THREADS), smem, st, tx, tw, p, cols);
     return cudaGetLastError();
 }
 

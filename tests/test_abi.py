@@ -67,6 +67,7 @@ def _weights(fp8=False):
     (dict(weights=7), 1),
     (dict(shared_inter=256), 2),        # shared expert of another width
     (dict(weights=1, inter=384), 2),    # fp8 needs I % 512 == 0
+    (dict(weights=1, inter=512, hidden=384), 2),  # ... and H % 512 == 0
 ])
 def test_create_rejects_unsupported_shapes(lib, kw, want):
     from mixture_experts_ffn_gemv_gb300.binding import MoeExpertWeights
@@ -88,7 +89,7 @@ def test_create_rejects_null_and_misaligned(lib):
     bad = MoeExpertWeights(0x10001, 0x10000, 0x10000)
     assert lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(bad), None, ctypes.byref(out)) == 1
     missing_scales = _weights(fp8=False)
-    cfg8 = _cfg(weights=1, inter=512)
+    cfg8 = _cfg(weights=1, inter=512, hidden=512)
     assert lib.moe_layer_create(ctypes.byref(cfg8), ctypes.byref(missing_scales), None, ctypes.byref(out)) == 1
 
 
