@@ -247,7 +247,7 @@ def recorded_traffic(kernel, workload, m):
 # ----------------------------------------------------------------- our arm
 
 
-def build_replicas(wl, m, device, seed_base, max_bytes=48e9):
+def build_replicas(wl, m, device, seed_base, max_bytes=48e9, replicas=0):
     from mixture_experts_ffn_gemv_gb300 import binding
     shape = wl.shape
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -257,6 +257,8 @@ def build_replicas(wl, m, device, seed_base, max_bytes=48e9):
     touched = max(exp_u * expert_bytes(shape), 1)
     R = max(2, math.ceil(4 * l2 / touched))
     R = int(max(1, min(R, 16, max_bytes // max(full, 1))))
+    if replicas > 0:
+        R = replicas
     reps = []
     ws = None
     for r in range(R):
@@ -418,9 +420,12 @@ def run_ours(args):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     wl = I.WORKLOADS[args.workload]
+    if args.experts > 0:
+        import dataclasses
+        wl = dataclasses.replace(wl, shape=dataclasses.replace(wl.shape, num_experts=args.experts))
     m = args.m
     shape = wl.shape
-    reps, R, rep_bytes = build_replicas(wl, m, device, seed_base=1000 * rank)
+    reps, R, rep_bytes = build_replicas(wl, m, device, seed_base=1000 * rank, replicas=args.replicas)
     run_steps(reps, args.warmup)
     torch.cuda.synchronize(device)
     with ClockSampler(device.index) as clk:
@@ -461,7 +466,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3" if shape.fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "m": m, "hidden": shape.hidden, "experts": shape.num_experts,
+        "config": {"workload": args.workload + (f" (experts overridden: {args.experts})" if args.experts else ""), "m": m, "hidden": shape.hidden, "experts": shape.num_experts,
                    "top_k": shape.top_k, "inter": shape.inter, "shared_inter": shape.shared_inter,
                    "global_batch": ws * m, "parallelism": f"token-parallel x{ws} (replicas, no collective)",
                    "l2": f"inputs larger than L2: {R} rotating layer replicas, {rep_bytes / 1e9:.1f} GB of weights"},
@@ -495,6 +500,9 @@ def run_reference(args):
         return
     import oracle
     wl = I.WORKLOADS[args.workload]
+    if args.experts > 0:
+        import dataclasses
+        wl = dataclasses.replace(wl, shape=dataclasses.replace(wl.shape, num_experts=args.experts))
     m = args.m
     tensors = I.make_layer(wl, seed=0, device="cpu")
     x = I.make_x(wl.shape, m, seed=0, device="cpu")
@@ -511,7 +519,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3" if wl.shape.fp8 else "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "m": m, "hidden": wl.shape.hidden, "experts": wl.shape.num_experts,
+        "config": {"workload": args.workload + (f" (experts overridden: {args.experts})" if args.experts else ""), "m": m, "hidden": wl.shape.hidden, "experts": wl.shape.num_experts,
                    "top_k": wl.shape.top_k, "inter": wl.shape.inter, "global_batch": m},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} whole-layer forwards of the {m}-token batch on the host cores"},
@@ -529,6 +537,9 @@ def main():
     ap.add_argument("--workload", default="qwen3_decode", choices=sorted(I.WORKLOADS))
     ap.add_argument("--tokens", dest="m", type=int, default=16, help="tokens per step (m)")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the workload's expert count (small cases for profiling captures)")
+    ap.add_argument("--replicas", type=int, default=0, help="override the number of rotating layer replicas")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

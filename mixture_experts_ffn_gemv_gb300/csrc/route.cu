@@ -148,7 +148,7 @@ __global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __res
                                                            WsHeader* hdr) {
     pdl_wait();
     pdl_trigger();
-    constexpr int MT = 8;
+    constexpr int MT = 16;
     __shared__ int ids_s[kPermChunk];
     __shared__ int hist[256 + 2];
     __shared__ int off[256 + 2];
@@ -209,10 +209,14 @@ __global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------- launchers
+// Slices of H for the small-m router: as many as 16 slices of whole
+// 128-float chunks, so that many short warps (one or a few load round trips
+// each) cover the GPU instead of a few long ones.
 int router_slices(int H, int m) {
     if (m > kRouterSmallMaxM) return 1;
-    int S = H / 512;
-    while (S > 1 && (H % (S * 128) != 0)) --S;
+    const int chunks = H / 128;
+    int S = chunks < 16 ? chunks : 16;
+    while (S > 1 && chunks % S != 0) --S;
     return S < 1 ? 1 : S;
 }
 
@@ -220,7 +224,7 @@ cudaError_t launch_router(const uint16_t* x, int m, int H, const float* wr, int 
                           cudaStream_t st) {
     if (m <= kRouterSmallMaxM) {
         dim3 grid(ceil_div(E, 8), S);
-        launch_pdl(router_partial_small<8>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part);
+        launch_pdl(router_partial_small<16>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part);
     } else {
         dim3 grid(ceil_div(m, RT_BM), ceil_div(E, RT_BN));
         launch_pdl(router_logits_tiled, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, part);

@@ -60,6 +60,7 @@ __device__ __forceinline__ void warp_topk_softmax(const float* part, int S, int 
         const int e = lane + 32 * i;
         if (e < E) {
             float a = 0.f;
+#pragma unroll 8
             for (int s = 0; s < S; ++s) {
                 const float* src = part + ((size_t)s * m + t) * E + e;
                 a += LDCG ? __ldcg(src) : *src;
