@@ -9,7 +9,8 @@
 //               (256 weight rows x 64 of K) into a 4-stage smem ring;
 //   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16, fp32
 //               accumulators in TMEM, double-buffered (2 x 256 columns);
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, then
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (each half of the
+//               columns): tcgen05.ld of the accumulator, then
 //               gate/up: h = silu(G) * U (B tile = 128 rows of W1 followed by
 //               the same 128 rows of W3, so one MMA chain yields G and U),
 //               down: y = D; stored as bf16 in sorted-row order.
@@ -41,7 +42,8 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half the columns
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 constexpr int TABLE_INTS = 2 * kMaxExperts + 4;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + TABLE_INTS * 4;
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull0 + 8 * a, 1);
-            mbar_init(tempty0 + 8 * a, 4);
+            mbar_init(tempty0 + 8 * a, EPI_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -197,7 +199,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int q = warp & 3;  // the TMEM lane quarter this warp may read
+        const int q = warp & 3;           // the TMEM lane quarter this warp may read
+        const int half = (warp - 2) >> 2;  // which half of the tile's output columns
         const int r = q * 32 + lane;
         uint32_t tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
             if (GATEUP) {
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 2 * half; c < 2 * half + 2; ++c) {
                     uint32_t gv[32], uv[32];
                     tmem_ld32(taddr + c * 32, gv);
                     tmem_ld32(taddr + 128 + c * 32, uv);
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             } else {
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
                     uint32_t dv[32];
                     tmem_ld32(taddr + c * 32, dv);
                     tmem_wait_ld();

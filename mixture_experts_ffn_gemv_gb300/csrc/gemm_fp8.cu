@@ -4,20 +4,22 @@
 // fp32 block-scale accumulation that page describes for its fp8 grouped GEMM
 // (exact fp32 scales, not power-of-two block exponents).
 //
-// Persistent, one CTA per SM, 10 warps:
+// Persistent, one CTA per SM, 18 warps:
 //   warp 0      TMA producer: A (128 rows x 128 codes) and B (256 weight rows
 //               x 128 codes) per stage -- one stage is exactly one 128-wide
 //               scale block of K;
 //   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M128 N256 K32) per
 //               stage into one of two TMEM partial buffers (2 x 256 columns),
 //               a fresh partial for every K block;
-//   warps 2..9  promotion + epilogue: two warps per TMEM lane quarter, each
-//               owning half of the 256 columns; per K block they read the
+//   warps 2..17 promotion + epilogue: four warps per TMEM lane quarter, each
+//               owning a quarter of the 256 columns; per K block they read the
 //               partial, multiply by s_x[row, kb] * s_w[block, kb] and add it
-//               into fp32 register accumulators, then release the buffer.
+//               into fp32 register accumulators, then release the buffer (the
+//               promotion, not the MMA, bounds this kernel, so it gets many
+//               warps).
 // Gate/up epilogue: h = silu(G) * U for the tile's 128 I columns, quantised
-// as one 1x128 block per row (s = amax/448, e4m3 RNE satfinite); the two
-// warps sharing a row exchange their halves' amax through shared memory with
+// as one 1x128 block per row (s = amax/448, e4m3 RNE satfinite); the four
+// warps sharing a row exchange their parts' amax through shared memory with
 // an mbarrier (bounded wait).  Down epilogue: y as bf16.
 #include <cuda_runtime.h>
 
@@ -40,11 +42,14 @@ constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int THREADS = 320;
-constexpr int EPI_THREADS = 256;
+constexpr int EPI_WARPS = 16;               // four per TMEM lane quarter
+constexpr int QC = EPI_WARPS / 4;           // column groups per row
+constexpr int NC = BN / QC;                 // accumulator columns per epilogue thread
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int THREADS = 64 + EPI_THREADS;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int TABLE_INTS = 2 * kMaxExperts + 4;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + TABLE_INTS * 4 + 2 * BM * 2 * 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + TABLE_INTS * 4 + 2 * BM * QC * 4;
 
 struct Fp8Params {
     WsHeader* hdr;
@@ -92,7 +97,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_tile = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
     int* s_group = s_tile + kMaxExperts + 2;
-    float* xchg = reinterpret_cast<float*>(s_tile + TABLE_INTS);  // [2 parities][BM rows][2 halves]
+    float* xchg = reinterpret_cast<float*>(s_tile + TABLE_INTS);  // [2 parities][BM rows][QC groups]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_active = p.hdr->n_active;
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(pfull0 + 8 * b, 1);
-            mbar_init(pempty0 + 8 * b, EPI_THREADS / 32);
+            mbar_init(pempty0 + 8 * b, EPI_WARPS);
             mbar_init(xbar0 + 8 * b, EPI_THREADS);
         }
         mbar_init(drain, 1);
@@ -195,9 +200,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int q = warp & 3;            // TMEM lane quarter
-        const int half = (warp - 2) >> 2;  // which 128 of the 256 columns
-        const int r = q * 32 + lane;       // tile row
+        const int q = warp & 3;         // TMEM lane quarter
+        const int cg = (warp - 2) >> 2;  // column group 0..QC-1
+        const int r = q * 32 + lane;     // tile row
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         uint32_t it = 0, tc = 0;
         bool ok = true;
@@ -212,15 +217,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool routed = g < p.E;
             const float* bsc0 = routed ? p.b_sc0 + (size_t)g * p.b_row_blocks * p.kblocks : p.s_sc0;
             const float* bsc1 = routed ? p.b_sc1 + (size_t)g * p.b_row_blocks * p.kblocks : p.s_sc1;
-            // gate/up: this half owns G cols [64h, 64h+64) and U cols [128+64h, ...);
-            // down: cols [128h, 128h+128) of one 128-row block of W2
-            const float* sc_lo = GATEUP ? bsc0 + (size_t)nt * p.kblocks : bsc0 + (size_t)(nt * 2 + half) * p.kblocks;
+            // gate/up: this thread owns G cols [NC/2*cg, +NC/2) and the same U cols
+            // (128 further); down: cols [NC*cg, +NC), inside one 128-row block of W2
+            const float* sc_lo =
+                GATEUP ? bsc0 + (size_t)nt * p.kblocks : bsc0 + (size_t)(nt * 2 + (NC * cg) / 128) * p.kblocks;
             const float* sc_hi = GATEUP ? bsc1 + (size_t)nt * p.kblocks : sc_lo;
-            const uint32_t c_lo = GATEUP ? 64 * half : 128 * half;
-            const uint32_t c_hi = GATEUP ? 128 + 64 * half : 128 * half + 64;
-            float acc[128];
+            const uint32_t c_lo = GATEUP ? (NC / 2) * cg : NC * cg;
+            const uint32_t c_hi = GATEUP ? 128 + (NC / 2) * cg : NC * cg + NC / 2;
+            float acc[NC];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+            for (int i = 0; i < NC; ++i) acc[i] = 0.f;
             for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                 const uint32_t b = it & 1u, pph = (it >> 1) & 1u;
                 const float sx = __ldg(asc + kb);
@@ -231,12 +237,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t base = tmem_base + lane_off + b * BN;
+                constexpr int NCH = NC / 16;  // 16-column loads per thread
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < NCH; ++c) {
                     uint32_t v[16];
-                    tmem_ld16(base + (c < 4 ? c_lo + 16 * c : c_hi + 16 * (c - 4)), v);
+                    tmem_ld16(base + (c < NCH / 2 ? c_lo + 16 * c : c_hi + 16 * (c - NCH / 2)), v);
                     tmem_wait_ld();
-                    const float f = c < 4 ? f_lo : f_hi;
+                    const float f = c < NCH / 2 ? f_lo : f_hi;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(__uint_as_float(v[i]), f, acc[16 * c + i]);
                 }
@@ -246,44 +253,46 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) break;
             if (GATEUP) {
-                // acc[0..63] = G, acc[64..127] = U for I columns nt*128 + 64*half + [0, 64)
+                // acc[0, NC/2) = G and acc[NC/2, NC) = U for I columns nt*128 + (NC/2)*cg + [0, NC/2)
+                constexpr int NH = NC / 2;
                 float amax = 0.f;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    acc[i] = swiglu(acc[i], acc[64 + i]);
+                for (int i = 0; i < NH; ++i) {
+                    acc[i] = swiglu(acc[i], acc[NH + i]);
                     amax = fmaxf(amax, fabsf(acc[i]));
                 }
                 const uint32_t par = tc & 1u;
-                float* slot = xchg + (par * BM + r) * 2;
-                slot[half] = amax;
+                float* slot = xchg + (par * BM + r) * QC;
+                slot[cg] = amax;
                 mbar_arrive(xbar0 + 8 * par);
                 if (!mbar_wait(xbar0 + 8 * par, (tc >> 1) & 1u, WAIT_NS)) {
                     ok = false;
                     break;
                 }
-                amax = fmaxf(slot[0], slot[1]);
+#pragma unroll
+                for (int i = 0; i < QC; ++i) amax = fmaxf(amax, slot[i]);
                 if (r < valid) {
                     float s = 1.0f;
-                    uint32_t w[16];
+                    uint32_t w[NH / 4];
                     if (amax > 0.f) {
                         s = __fdiv_rn(amax, 448.0f);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
+                        for (int i = 0; i < NH / 4; ++i)
                             w[i] = f32x2_to_e4m3x2(__fdiv_rn(acc[4 * i], s), __fdiv_rn(acc[4 * i + 1], s)) |
                                    (f32x2_to_e4m3x2(__fdiv_rn(acc[4 * i + 2], s), __fdiv_rn(acc[4 * i + 3], s)) << 16);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) w[i] = 0;
+                        for (int i = 0; i < NH / 4; ++i) w[i] = 0;
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(p.out_q + (size_t)row * p.ldo + nt * 128 + 64 * half);
+                    uint4* dst = reinterpret_cast<uint4*>(p.out_q + (size_t)row * p.ldo + nt * 128 + NH * cg);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                    if (half == 0) p.out_sc[(size_t)row * (p.ldo / 128) + nt] = s;
+                    for (int i = 0; i < NH / 16; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    if (cg == 0) p.out_sc[(size_t)row * (p.ldo / 128) + nt] = s;
                 }
             } else if (r < valid) {
-                uint4* dst = reinterpret_cast<uint4*>(p.out_y + (size_t)row * p.ldo + nt * BN + 128 * half);
+                uint4* dst = reinterpret_cast<uint4*>(p.out_y + (size_t)row * p.ldo + nt * BN + NC * cg);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
+                for (int i = 0; i < NC / 8; ++i)
                     dst[i] = make_uint4(pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]), pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
                                         pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]), pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
             }

@@ -14,6 +14,8 @@ constexpr int kRouterSmallMaxM = 64;  // up to this m the router is a split-H GE
 constexpr int kPermChunk = 2048;      // pairs per permute block (8 warps x 256)
 constexpr int kGemvRows = 8;          // token rows a GEMV block holds at once
 constexpr int kGemmBM = 128;          // grouped-GEMM m-tile (rows per tile)
+constexpr int kRouteFuseLogits = 8192; // fused decode routing keeps m*E logits in shared memory
+constexpr int kRouteFuseMaxM = 32;     // above this the top-k runs as its own (token-parallel) kernel
 
 // routing
 int router_slices(int H, int m);

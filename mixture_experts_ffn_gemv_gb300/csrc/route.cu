@@ -150,9 +150,14 @@ __global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __res
     pdl_trigger();
     constexpr int MT = 16;
     __shared__ int ids_s[kPermChunk];
-    __shared__ int hist[256 + 2];
-    __shared__ int off[256 + 2];
-    __shared__ int wbase[8 * 256];
+    // the logits live only until the top-k is done, the permute's tables only
+    // after it: one buffer holds either
+    __shared__ __align__(16) int tail_buf[kRouteFuseLogits];
+    static_assert(kRouteFuseLogits >= 8 * 256 + 2 * (256 + 2), "permute tables fit the logits buffer");
+    float* logits_s = reinterpret_cast<float*>(tail_buf);
+    int* wbase = tail_buf;
+    int* hist = tail_buf + 8 * 256;
+    int* off = hist + 256 + 2;
     __shared__ int wsum[9];
     __shared__ int is_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -192,30 +197,46 @@ __global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __res
     __syncthreads();
     if (!is_last) return;
     __threadfence();
+    // all 256 threads reduce the slice partials (coalesced over e, many loads
+    // in flight) into shared-memory logits; the warps then pick from those
     const int S = gridDim.y;
+    const int n = m * E;
+    for (int i0 = threadIdx.x; i0 < n; i0 += 4 * 256) {
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int q = 0; q < S; ++q)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i0 + u * 256 < n) a[u] += __ldcg(part + (size_t)q * n + i0 + u * 256);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i0 + u * 256 < n) logits_s[i0 + u * 256] = a[u];
+    }
+    __syncthreads();
     for (int t = warp; t < m; t += 8) {
         int id;
         float wt;
-        warp_topk_softmax<VPL, true>(part, S, m, E, k, bias, nullptr, t, lane, &id, &wt);
+        warp_topk_softmax<VPL, false>(logits_s, 1, m, E, k, bias, nullptr, t, lane, &id, &wt);
         if (lane < k) {
             ids[(size_t)t * k + lane] = id;
             wts[(size_t)t * k + lane] = wt;
             ids_s[t * k + lane] = id;
         }
     }
-    __syncthreads();
+    __syncthreads();  // logits no longer needed: the buffer becomes the permute's tables
     block_permute_small(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, wbase, wsum);
     if (threadIdx.x == 0) hdr->done = 0;
 }
 
 // ---------------------------------------------------------------- launchers
-// Slices of H for the small-m router: as many as 16 slices of whole
-// 128-float chunks, so that many short warps (one or a few load round trips
-// each) cover the GPU instead of a few long ones.
+// Slices of H for the small-m router: whole 128-float chunks, as many as 16
+// for m <= 16 (many short warps, one or a few load round trips each, cover
+// the GPU), fewer as m grows (each slice adds m*E partials to reduce).
 int router_slices(int H, int m) {
     if (m > kRouterSmallMaxM) return 1;
     const int chunks = H / 128;
-    int S = chunks < 16 ? chunks : 16;
+    const int cap = m <= 16 ? 16 : (m <= 32 ? 8 : 4);
+    int S = chunks < cap ? chunks : cap;
     while (S > 1 && chunks % S != 0) --S;
     return S < 1 ? 1 : S;
 }
@@ -233,7 +254,7 @@ cudaError_t launch_router(const uint16_t* x, int m, int H, const float* wr, int 
 }
 
 bool route_permute_fusable(int m, int k, int E) {
-    return m <= kRouterSmallMaxM && m * k <= kPermChunk && E <= 256;
+    return m <= kRouteFuseMaxM && m * k <= kPermChunk && E <= 256 && m * E <= kRouteFuseLogits;
 }
 
 cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,

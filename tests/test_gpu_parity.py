@@ -185,6 +185,53 @@ def test_experts_given_oracle_routing(cuda, oracle_mod, arm, shape, m):
     assert err < TOL[shape.fp8], err
 
 
+SHARED_BF16 = I.LayerShape(hidden=512, num_experts=16, top_k=4, inter=256, shared_inter=256)
+TOP1 = I.LayerShape(hidden=256, num_experts=12, top_k=1, inter=128)
+
+
+@pytest.mark.parametrize("arm", ["gemv", "gemm"])
+@pytest.mark.parametrize("shape,m", [(SHARED_BF16, 5), (SHARED_BF16, 260), (TOP1, 37), (TOP1, 400)])
+def test_whole_layer_shared_bf16_and_top1(cuda, oracle_mod, arm, shape, m):
+    """A bf16 layer with a shared expert (group E of every kernel) and a top-1
+    layer, through moe_forward on both arms, against the oracle."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    tensors, x = _small_case(shape, m, seed=71, device=cuda)
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
+    ref = oracle_mod.reference(shape, host, x.cpu())
+    layer = binding.MoeLayer(shape, tensors)
+    out, ids, w = layer.moe_forward(x, tensors["router_w"], arm=arm, return_routing=True)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    swapped, bad = check_ids(to_np(ids), ref["ids"], ref["logits"])
+    assert not bad, bad[:5]
+    keep = np.array([r for r in range(m) if r not in set(swapped)])
+    assert rel_l2(to_np(out)[keep], ref["out"][keep]) < TOL[False]
+
+
+@pytest.mark.parametrize("m", [1, 50, 200])
+def test_route_and_permute_at_the_largest_expert_count(cuda, oracle_mod, m):
+    """E = 1024 experts and top_k = 32: the widest top-k lanes (32 logits per
+    lane) and the permute's largest per-warp tables."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    shape = I.LayerShape(hidden=256, num_experts=1024, top_k=32, inter=128)
+    x = I.make_x(shape, m, seed=81, device=cuda)
+    wr, _ = I.make_router(shape, seed=81, device=cuda)
+    zeros = {n: torch.zeros(1024, 128, 256, dtype=torch.bfloat16, device=cuda) for n in ("w1", "w3")}
+    zeros["w2"] = torch.zeros(1024, 256, 128, dtype=torch.bfloat16, device=cuda)
+    layer = binding.MoeLayer(shape, zeros)
+    ids, w, logits = layer.moe_route(x, wr, logits=True)
+    L, r_ids, r_w, _ = oracle_mod.route(shape, {"router_w": wr.cpu(), "router_bias": None}, x.cpu())
+    off, sp, sl = layer.moe_permute(torch.from_numpy(r_ids).to(cuda))  # both sides permute the oracle's ids
+    torch.cuda.synchronize()
+    swapped, bad = check_ids(to_np(ids), r_ids, L)
+    assert not bad, bad[:5]
+    r_off, r_sp, r_sl = oracle_mod.permute(r_ids, 1024)
+    assert np.array_equal(off.cpu().numpy(), r_off)
+    assert np.array_equal(sp.cpu().numpy(), r_sp)
+    assert np.array_equal(sl.cpu().numpy(), r_sl)
+    assert np.abs(to_np(w).astype(np.float64).sum(1) - 1).max() < 1e-5
+
+
 # ------------------------------------------------------------------ whole layer, full sizes
 
 FULL_CASES = [("tiny", 16)] + [("qwen3_decode", m) for m in (1, 4, 16, 64)] + \
