@@ -107,7 +107,7 @@ Layout layout(const moe_layer* L, int64_t m) {
     o.P = (int)(m * k);
     o.rows = o.P + (L->has_shared ? (int)m : 0);
     o.router_tc = router_tc_usable((int)m, H, E);
-    o.S = o.router_tc ? router_tc_slices((int)m, H) : router_slices(H, (int)m);
+    o.S = o.router_tc ? router_tc_slices((int)m, H, E) : router_slices(H, (int)m);
     o.nchunk = ceil_div(std::max(o.P, 1), kPermChunk);
     size_t off = 0;
     auto take = [&](size_t bytes) {

@@ -24,7 +24,7 @@ cudaError_t launch_router(const uint16_t* x, int m, int H, const float* wr, int 
 // tensor-core router (m > kRouterSmallMaxM, E <= 256): fp32 weights split into
 // three bf16 planes, then tcgen05 MMAs; partial logits [S, m, E]
 bool router_tc_usable(int m, int H, int E);
-int router_tc_slices(int m, int H);
+int router_tc_slices(int m, int H, int E);
 size_t router_tc_split_bytes(int E, int H);
 cudaError_t launch_router_split(const float* wr, int E, int H, uint16_t* planes, cudaStream_t st);
 cudaError_t launch_router_tc(const uint16_t* x, int m, int H, const uint16_t* planes, int E, float* part, int S,

@@ -14,8 +14,10 @@
 namespace moe {
 
 // ---------------------------------------------------------------- small m
-// grid (ceil(E/8), S); 8 warps, warp w owns expert blockIdx.x*8+w over the
-// H-slice [s*HS, (s+1)*HS).  HS is a multiple of 128 (32 lanes x float4).
+// grid (ceil(E/8), S, ceil(m/MT)); 8 warps, warp w owns expert blockIdx.x*8+w
+// over the H-slice [s*HS, (s+1)*HS) for the MT tokens of blockIdx.z.  HS is a
+// multiple of 128 (32 lanes x float4).  Many short warps: each is one or a few
+// load round trips.
 template <int MT>
 __global__ __launch_bounds__(256) void router_partial_small(const uint16_t* __restrict__ x, int m, int H,
                                                             const float* __restrict__ wr, int E, int HS,
@@ -25,32 +27,30 @@ __global__ __launch_bounds__(256) void router_partial_small(const uint16_t* __re
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * 8 + warp;
     if (e >= E) return;
-    const int s = blockIdx.y;
+    const int s = blockIdx.y, t0 = blockIdx.z * MT;
     const int h0 = s * HS, h1 = h0 + HS;
     const float* we = wr + (size_t)e * H;
-    for (int t0 = 0; t0 < m; t0 += MT) {
-        float acc[MT];
+    float acc[MT];
 #pragma unroll
-        for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+    for (int t = 0; t < MT; ++t) acc[t] = 0.f;
 #pragma unroll 4
-        for (int h = h0 + lane * 4; h < h1; h += 128) {
-            const float4 w = __ldg(reinterpret_cast<const float4*>(we + h));
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                if (t0 + t < m) {
-                    const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * H + h));
-                    acc[t] = fmaf(w.x, bf16lo(xv.x), acc[t]);
-                    acc[t] = fmaf(w.y, bf16hi(xv.x), acc[t]);
-                    acc[t] = fmaf(w.z, bf16lo(xv.y), acc[t]);
-                    acc[t] = fmaf(w.w, bf16hi(xv.y), acc[t]);
-                }
-            }
-        }
+    for (int h = h0 + lane * 4; h < h1; h += 128) {
+        const float4 w = __ldg(reinterpret_cast<const float4*>(we + h));
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
-            const float v = warp_sum(acc[t]);
-            if (lane == 0 && t0 + t < m) part[((size_t)s * m + t0 + t) * E + e] = v;
+            if (t0 + t < m) {
+                const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * H + h));
+                acc[t] = fmaf(w.x, bf16lo(xv.x), acc[t]);
+                acc[t] = fmaf(w.y, bf16hi(xv.x), acc[t]);
+                acc[t] = fmaf(w.z, bf16lo(xv.y), acc[t]);
+                acc[t] = fmaf(w.w, bf16hi(xv.y), acc[t]);
+            }
         }
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0 && t0 + t < m) part[((size_t)s * m + t0 + t) * E + e] = v;
     }
 }
 
@@ -244,8 +244,8 @@ int router_slices(int H, int m) {
 cudaError_t launch_router(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
                           cudaStream_t st) {
     if (m <= kRouterSmallMaxM) {
-        dim3 grid(ceil_div(E, 8), S);
-        launch_pdl(router_partial_small<16>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part);
+        const dim3 grid(ceil_div(E, 8), S, ceil_div(m, 4));
+        launch_pdl(router_partial_small<4>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part);
     } else {
         dim3 grid(ceil_div(m, RT_BM), ceil_div(E, RT_BN));
         launch_pdl(router_logits_tiled, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, part);

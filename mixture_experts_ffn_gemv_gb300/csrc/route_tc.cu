@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(256) router_split(const float* __restrict__ wr
 struct RouterParams {
     float* part;  // [S, m, E]
     int m, E, Epad, kblocks_per_slice, stages, stage_bytes, b_plane_bytes;
+    int N;  // experts per CTA (grid z splits Epad into blocks of N <= 128)
     WsHeader* hdr;
 };
 
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * RBM, s = blockIdx.y;
+    const int m0 = blockIdx.x * RBM, s = blockIdx.y, e0 = blockIdx.z * p.N;
     const int kb0 = s * p.kblocks_per_slice, nk = p.kblocks_per_slice;
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
                 const int kc = (kb0 + it) * RBK;
                 tma_load_2d(sa, &tmX, kc, m0, full0 + 8 * st);
 #pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_3d(sb + j * p.b_plane_bytes, &tmW, kc, 0, j, full0 + 8 * st);
+                for (int j = 0; j < 3; ++j) tma_load_3d(sb + j * p.b_plane_bytes, &tmW, kc, e0, j, full0 + 8 * st);
             }
             if (!ok) {
                 set_error(p.hdr, DEV_ERR_TIMEOUT, 11);
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(RBM, p.Epad);
+            const uint32_t idesc = idesc_bf16(RBM, p.N);
             bool ok = true;
             for (int it = 0; it < nk && ok; ++it) {
                 if (*abort_flag) break;
@@ -152,15 +153,15 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         if (!wait_ok) set_error(p.hdr, DEV_ERR_TIMEOUT, 13);
         tc_fence_after();
         if (wait_ok && !*abort_flag) {
-            float* dst = p.part + ((size_t)s * p.m + row) * p.E;
-            for (int c = 0; c < p.Epad; c += 32) {
+            float* dst = p.part + ((size_t)s * p.m + row) * p.E + e0;
+            for (int c = 0; c < p.N; c += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + c, v);
                 tmem_wait_ld();
                 if (row < p.m) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (c + j < p.E) dst[c + j] = __uint_as_float(v[j]);
+                        if (c + j < p.N && e0 + c + j < p.E) dst[c + j] = __uint_as_float(v[j]);
                 }
             }
         }
@@ -186,9 +187,14 @@ bool router_tc_usable(int m, int H, int E) {
     return m > kRouterSmallMaxM && E <= 256 && H % RBK == 0;
 }
 
-// Slices of H so that (m-tiles x slices) covers the SMs; H/S a multiple of 64.
-int router_tc_slices(int m, int H) {
-    const int mt = ceil_div(m, RBM);
+// Experts per CTA: at most 128, so that a stage (x tile + three weight
+// planes) stays small enough for a multi-stage ring.
+int router_tc_n(int E) { return std::min(router_tc_epad(E), 128); }
+
+// Slices of H so that (m-tiles x slices x expert blocks) covers the SMs; H/S a
+// multiple of 64.
+int router_tc_slices(int m, int H, int E) {
+    const int mt = ceil_div(m, RBM) * ceil_div(router_tc_epad(E), router_tc_n(E));
     const int kb = H / RBK;
     int S = std::max(1, std::min(kb, sm_count() / std::max(mt, 1)));
     while (S > 1 && kb % S != 0) --S;
@@ -209,26 +215,28 @@ cudaError_t launch_router_tc(const uint16_t* x, int m, int H, const uint16_t* pl
                              WsHeader* hdr, cudaStream_t st) {
     const int Epad = router_tc_epad(E);
     CUtensorMap tx, tw;
+    const int N = router_tc_n(E);
     const uint64_t dx[2] = {(uint64_t)H, (uint64_t)m}, dw[3] = {(uint64_t)H, (uint64_t)Epad, 3};
-    if (!tmap_encode(&tx, x, 2, dx, 2, RBK, RBM) || !tmap_encode(&tw, planes, 3, dw, 2, RBK, (uint32_t)Epad))
+    if (!tmap_encode(&tx, x, 2, dx, 2, RBK, RBM) || !tmap_encode(&tw, planes, 3, dw, 2, RBK, (uint32_t)N))
         return cudaErrorInvalidValue;
     RouterParams p;
     p.part = part;
     p.m = m;
     p.E = E;
     p.Epad = Epad;
+    p.N = N;
     p.kblocks_per_slice = (H / RBK) / S;
-    p.b_plane_bytes = Epad * RBK * 2;
+    p.b_plane_bytes = N * RBK * 2;
     p.stage_bytes = RBM * RBK * 2 + 3 * p.b_plane_bytes;
     p.stages = std::max(1, std::min(8, (R_SMEM_MAX - 2048) / p.stage_bytes));
     p.hdr = hdr;
     uint32_t cols = 32;
-    while ((int)cols < Epad) cols <<= 1;
+    while ((int)cols < N) cols <<= 1;
     const int smem = 1024 + p.stages * p.stage_bytes + 256;
     static cudaError_t attr = cudaFuncSetAttribute(router_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    R_SMEM_MAX);
     if (attr != cudaSuccess) return attr;
-    const dim3 grid(ceil_div(m, RBM), S);
+    const dim3 grid(ceil_div(m, RBM), S, ceil_div(Epad, N));
     launch_pdl(router_logits_tc, dim3(grid), dim3(R_THREADS), smem, st, tx, tw, p, cols);
     return cudaGetLastError();
 }
