@@ -74,15 +74,15 @@ __device__ __forceinline__ int row_token(const GemvArgs& a, int s) {
 }  // namespace
 
 // ============================================================ gate/up, bf16
-// CTA: 8 warps = 2 row tiles (16 rows of I each) x 4 K-slices of H.  The four
+// CTA: 8 warps = RT row tiles (16 rows of I each) x 8/RT K-slices of H.  The
 // K-slice partials are summed in fixed order through shared memory, then
 // h = silu(g) * u is stored as bf16 [rows, I].
-template <int NT>
+template <int NT, int RT>
 __global__ __launch_bounds__(256, (NT == 1 ? 4 : 2)) void gemv_gateup_bf16(const GemvArgs a, const uint16_t* __restrict__ x,
                                                         uint16_t* __restrict__ h, int n_slices) {
     pdl_wait();
     pdl_trigger();
-    constexpr int KS = 4, RT = 2;
+    constexpr int KS = 8 / RT;
     __shared__ float red[KS][RT][32][NT * 8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, tig = lane & 3;
@@ -161,13 +161,13 @@ __global__ __launch_bounds__(256, (NT == 1 ? 4 : 2)) void gemv_gateup_bf16(const
 }
 
 // ============================================================ down, bf16
-// CTA: 2 row tiles (16 rows of H) x 4 K-slices of I; y fp32 [rows, H].
-template <int NT>
+// CTA: RT row tiles (16 rows of H) x 8/RT K-slices of I; y fp32 [rows, H].
+template <int NT, int RT>
 __global__ __launch_bounds__(256, 4) void gemv_down_bf16(const GemvArgs a, const uint16_t* __restrict__ h,
                                                       float* __restrict__ y, int n_slices) {
     pdl_wait();
     pdl_trigger();
-    constexpr int KS = 4, RT = 2;
+    constexpr int KS = 8 / RT;
     __shared__ float red[KS][RT][32][NT * 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, tig = lane & 3;
@@ -222,17 +222,17 @@ __global__ __launch_bounds__(256, 4) void gemv_down_bf16(const GemvArgs a, const
 }
 
 // ============================================================ gate/up, fp8
-// CTA: 8 warps = 2 row tiles (16 rows of I) x 4 K-slices of H, each slice a
-// whole number of 128-wide scale blocks.  The K-slice partials are summed in
+// CTA: 8 warps = RT row tiles (16 rows of I) x 8/RT K-slices of H, each slice
+// a whole number of 128-wide scale blocks.  The K-slice partials are summed in
 // fixed order through shared memory and h = silu(g) * u is stored as fp32
 // [rows, I]; quant_rows_fp8 then quantises each row per 1x128 block.
-template <int NT>
+template <int NT, int RT>
 __global__ __launch_bounds__(256, (NT == 1 ? 2 : 1)) void gemv_gateup_fp8(const GemvArgs a, const uint8_t* __restrict__ xq,
                                                           const float* __restrict__ xsc, float* __restrict__ hf,
                                                           int n_slices) {
     pdl_wait();
     pdl_trigger();
-    constexpr int KS = 4, RT = 2;
+    constexpr int KS = 8 / RT;
     __shared__ float red[KS][RT][32][NT * 8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, tig = lane & 3;
@@ -329,15 +329,15 @@ __global__ __launch_bounds__(256, (NT == 1 ? 2 : 1)) void gemv_gateup_fp8(const 
 }
 
 // ============================================================ down, fp8
-// CTA: 2 row tiles (16 rows of H) x 4 K-slices of I (each a whole number of
-// 128-blocks); y fp32 [rows, H].
-template <int NT>
+// CTA: RT row tiles (16 rows of H) x 8/RT K-slices of I (each a whole number
+// of 128-blocks); y fp32 [rows, H].
+template <int NT, int RT>
 __global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uint8_t* __restrict__ hq,
                                                      const float* __restrict__ hsc, float* __restrict__ y,
                                                      int n_slices) {
     pdl_wait();
     pdl_trigger();
-    constexpr int KS = 4, RT = 2;
+    constexpr int KS = 8 / RT;
     __shared__ float red[KS][RT][32][NT * 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, tig = lane & 3;
@@ -418,39 +418,60 @@ __global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uin
 // Token columns per pass: 16 when the groups average more than 4 rows (a
 // group with more rows than one pass covers takes further passes, re-reading
 // its weight slice from L2).
-static inline bool wide(const GemvArgs& a) { return a.P > 4 * a.max_groups; }
+static bool wide(const GemvArgs& a) { return a.P > 4 * a.max_groups; }
+
+static int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+    }
+    return n;
+}
+
+// One row tile and eight K-slices per CTA (twice the CTAs, half the rows each)
+// when two-tile CTAs would leave the GPU short of resident warps.  Only for
+// the gate/up projection: its K (= hidden) is long enough that eight slices
+// still stream for a while; the K-slices must hold whole 4-chunk steps
+// (kslice_align elements).
+static bool narrow(const GemvArgs& a, int n_out, int k, int kslice_align, bool gateup) {
+    return gateup && (n_out / 32) * a.max_groups < 8 * sm_count() && k % (8 * kslice_align) == 0;
+}
+
+#define MOE_GEMV_LAUNCH(KERNEL, GATEUP, N_OUT, K, ALIGN, ...)                                                      \
+    do {                                                                                                  \
+        const bool nw = narrow(a, N_OUT, K, ALIGN, GATEUP);                                                         \
+        const int n_slices = (N_OUT) / (nw ? 16 : 32);                                                    \
+        const dim3 grid(n_slices * a.max_groups);                                                         \
+        if (wide(a)) {                                                                                    \
+            if (nw) launch_pdl(KERNEL<2, 1>, grid, dim3(256), 0, st, a, __VA_ARGS__, n_slices);           \
+            else launch_pdl(KERNEL<2, 2>, grid, dim3(256), 0, st, a, __VA_ARGS__, n_slices);              \
+        } else {                                                                                          \
+            if (nw) launch_pdl(KERNEL<1, 1>, grid, dim3(256), 0, st, a, __VA_ARGS__, n_slices);           \
+            else launch_pdl(KERNEL<1, 2>, grid, dim3(256), 0, st, a, __VA_ARGS__, n_slices);              \
+        }                                                                                                 \
+    } while (0)
 
 cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st) {
-    const int n_slices = a.I / 32;
-    const dim3 grid(n_slices * a.max_groups);
-    if (wide(a)) launch_pdl(gemv_gateup_bf16<2>, dim3(grid), dim3(256), 0, st, a, x, h, n_slices);
-    else launch_pdl(gemv_gateup_bf16<1>, dim3(grid), dim3(256), 0, st, a, x, h, n_slices);
+    MOE_GEMV_LAUNCH(gemv_gateup_bf16, true, a.I, a.H, 32, x, h);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_down_bf16(const GemvArgs& a, const uint16_t* h, float* y, cudaStream_t st) {
-    const int n_slices = a.H / 32;
-    const dim3 grid(n_slices * a.max_groups);
-    if (wide(a)) launch_pdl(gemv_down_bf16<2>, dim3(grid), dim3(256), 0, st, a, h, y, n_slices);
-    else launch_pdl(gemv_down_bf16<1>, dim3(grid), dim3(256), 0, st, a, h, y, n_slices);
+    MOE_GEMV_LAUNCH(gemv_down_bf16, false, a.H, a.I, 32, h, y);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const float* xsc, float* hf,
                                    cudaStream_t st) {
-    const int n_slices = a.I / 32;
-    const dim3 grid(n_slices * a.max_groups);
-    if (wide(a)) launch_pdl(gemv_gateup_fp8<2>, dim3(grid), dim3(256), 0, st, a, xq, xsc, hf, n_slices);
-    else launch_pdl(gemv_gateup_fp8<1>, dim3(grid), dim3(256), 0, st, a, xq, xsc, hf, n_slices);
+    MOE_GEMV_LAUNCH(gemv_gateup_fp8, true, a.I, a.H, 128, xq, xsc, hf);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
                                  cudaStream_t st) {
-    const int n_slices = a.H / 32;
-    const dim3 grid(n_slices * a.max_groups);
-    if (wide(a)) launch_pdl(gemv_down_fp8<2>, dim3(grid), dim3(256), 0, st, a, hq, hsc, y, n_slices);
-    else launch_pdl(gemv_down_fp8<1>, dim3(grid), dim3(256), 0, st, a, hq, hsc, y, n_slices);
+    MOE_GEMV_LAUNCH(gemv_down_fp8, false, a.H, a.I, 128, hq, hsc, y);
     return cudaGetLastError();
 }
 

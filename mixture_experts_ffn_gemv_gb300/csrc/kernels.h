@@ -12,6 +12,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kRouterSmallMaxM = 64;  // up to this m the router is a split-H GEMV
 constexpr int kPermChunk = 2048;      // pairs per permute block (8 warps x 256)
+constexpr int kPermTiny = 256;        // the fused decode routing's rank-loop permute takes up to this many pairs
 constexpr int kGemvRows = 8;          // token rows a GEMV block holds at once
 constexpr int kGemmBM = 128;          // grouped-GEMM m-tile (rows per tile)
 constexpr int kRouteFuseLogits = 8192; // fused decode routing keeps m*E logits in shared memory

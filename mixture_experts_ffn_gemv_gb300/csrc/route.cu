@@ -153,7 +153,7 @@ __global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __res
     // the logits live only until the top-k is done, the permute's tables only
     // after it: one buffer holds either
     __shared__ __align__(16) int tail_buf[kRouteFuseLogits];
-    static_assert(kRouteFuseLogits >= 8 * 256 + 2 * (256 + 2), "permute tables fit the logits buffer");
+    static_assert(kRouteFuseLogits >= 8 * 256 + 2 * (256 + 2) + 27, "permute tables fit the logits buffer");
     float* logits_s = reinterpret_cast<float*>(tail_buf);
     int* wbase = tail_buf;
     int* hist = tail_buf + 8 * 256;
@@ -224,7 +224,8 @@ __global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __res
         }
     }
     __syncthreads();  // logits no longer needed: the buffer becomes the permute's tables
-    block_permute_small(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, wbase, wsum);
+    if (m * k <= kPermTiny) block_permute_tiny(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, tail_buf + 8 * 256 + 2 * (256 + 2));
+    else block_permute_small(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, wbase, wsum);
     if (threadIdx.x == 0) hdr->done = 0;
 }
 

@@ -1,6 +1,6 @@
 // Device routines shared by the routing and permute kernels: warp top-k
 // softmax of one token, block-wide exclusive scan, and the single-block
-// stable permute used when all pairs fit in one block.
+// stable permutes used when all pairs fit in one block.
 #pragma once
 
 #include "common.cuh"
@@ -44,20 +44,31 @@ __device__ __forceinline__ int block_exclusive_scan(int* a, int n, int* warp_sum
     return warp_sums[8];
 }
 
+// Order-preserving unsigned key of a float (a > b  <=>  key(a) > key(b)), with
+// -0 folded into +0 so that equal values compare equal; from_key inverts it.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_key(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // Top-k softmax of token t by one warp ("2. Batched topK dispatch", softmax
 // with norm_topk_prob): logits = sum of the S partial slices in slice order
-// (+ bias); k picks of a warp arg-max ordered by (logit desc, index asc);
-// weights = softmax over the k picks.  Lane j < k returns pick j in
-// (*id, *wt).  LDCG: read the partials through L2 (they were written by
-// other blocks of the same launch).
+// (+ bias); k picks, each the largest remaining logit with ties to the lowest
+// expert index -- one warp-wide max of the order keys and one min of the
+// indices holding it per pick (redux.sync); weights = softmax over the k
+// picks.  Lane j < k returns pick j in (*id, *wt).  LDCG: read the partials
+// through L2 (they were written by other blocks of the same launch).
 template <int VPL, bool LDCG>
 __device__ __forceinline__ void warp_topk_softmax(const float* part, int S, int m, int E, int k, const float* bias,
                                                   float* logits_out, int t, int lane, int* id, float* wt) {
-    float v[VPL];
-    uint32_t taken = 0;
+    uint32_t key[VPL];  // 0 = not a candidate (outside [0, E), or already picked)
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
+        key[i] = 0u;
         if (e < E) {
             float a = 0.f;
 #pragma unroll 8
@@ -66,39 +77,31 @@ __device__ __forceinline__ void warp_topk_softmax(const float* part, int S, int 
                 a += LDCG ? __ldcg(src) : *src;
             }
             if (bias) a += bias[e];
-            v[i] = a;
+            key[i] = order_key(a);
             if (logits_out) logits_out[(size_t)t * E + e] = a;
-        } else {
-            v[i] = -INFINITY;
-            taken |= 1u << i;
         }
     }
     float my_l = 0.f;
     int my_id = 0;
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+        uint32_t bk = 0u;  // this lane's largest key, lowest i among equals
+        int bi = 0;
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-                bv = v[i];
-                bi = e;
+        for (int i = 0; i < VPL; ++i)
+            if (key[i] > bk) {
+                bk = key[i];
+                bi = i;
             }
-        }
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t ge = __reduce_min_sync(0xffffffffu, bk == gk ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+        if ((int)(ge & 31u) == lane) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
+            for (int i = 0; i < VPL; ++i)
+                if (i == (int)(ge >> 5)) key[i] = 0u;
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
         if (lane == j) {
-            my_l = bv;
-            my_id = bi;
+            my_l = from_key(gk);
+            my_id = (int)ge;
         }
     }
     const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
@@ -193,6 +196,92 @@ __device__ __forceinline__ void block_permute_small(const int* ids_s, int P, int
         o.act_tile[n_active] = total_tiles;
         hdr->n_active = n_active;
         hdr->total_tiles = total_tiles;
+    }
+}
+
+
+// Stable counting sort of P <= kPermTiny pairs (ids in shared memory, all in
+// [0, E), E <= 256) by one 256-thread block, writing everything
+// block_permute_small writes: counts by shared-memory atomics, one block scan
+// of (rows, non-empty, m-tiles) over the E + 1 groups, and each pair's slot =
+// its group's first row + the number of earlier pairs in the group (so pairs
+// keep ascending order within an expert).  Shared scratch: cnt/off [E+1],
+// wsum [3 * 9].
+__device__ __forceinline__ void block_permute_tiny(const int* ids_s, int P, int m, int E, int has_shared,
+                                                   const PermuteOut& o, WsHeader* hdr, int* cnt, int* off,
+                                                   int* wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = E + 1;  // groups: the routed experts, then the shared expert
+    for (int g = tid; g < n; g += 256) cnt[g] = g == E ? (has_shared ? m : 0) : 0;
+    __syncthreads();
+    for (int p = tid; p < P; p += 256) atomicAdd(&cnt[ids_s[p]], 1);
+    __syncthreads();
+    // thread tid owns groups [2 tid, 2 tid + 2) (n <= 257 < 512)
+    int c[2], loc[3] = {0, 0, 0};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int g = 2 * tid + q;
+        c[q] = g < n ? cnt[g] : 0;
+        loc[0] += c[q];
+        loc[1] += c[q] > 0 ? 1 : 0;
+        loc[2] += (c[q] + kGemmBM - 1) / kGemmBM;
+    }
+    int inc[3] = {loc[0], loc[1], loc[2]};
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+        for (int v = 0; v < 3; ++v) {
+            const int y = __shfl_up_sync(0xffffffffu, inc[v], d);
+            if (lane >= d) inc[v] += y;
+        }
+    }
+    if (lane == 31)
+        for (int v = 0; v < 3; ++v) wsum[v * 9 + warp] = inc[v];
+    __syncthreads();
+    if (tid < 3) {  // exclusive scan of the 8 warp totals of value tid; [8] = grand total
+        int run = 0;
+        for (int w = 0; w < 8; ++w) {
+            const int y = wsum[tid * 9 + w];
+            wsum[tid * 9 + w] = run;
+            run += y;
+        }
+        wsum[tid * 9 + 8] = run;
+    }
+    __syncthreads();
+    int ex[3];
+#pragma unroll
+    for (int v = 0; v < 3; ++v) ex[v] = wsum[v * 9 + warp] + inc[v] - loc[v];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int g = 2 * tid + q;
+        if (g < n) {
+            off[g] = ex[0];
+            o.grp_off[g] = ex[0];
+            o.grp_cnt[g] = c[q];
+            if (o.expert_offsets) o.expert_offsets[g] = ex[0];
+            if (c[q] > 0) {
+                o.act_group[ex[1]] = g;
+                o.act_tile[ex[1]] = ex[2];
+            }
+        }
+        ex[0] += c[q];
+        ex[1] += c[q] > 0 ? 1 : 0;
+        ex[2] += (c[q] + kGemmBM - 1) / kGemmBM;
+    }
+    if (tid == 0) {
+        const int n_active = wsum[1 * 9 + 8], total_tiles = wsum[2 * 9 + 8];
+        o.act_tile[n_active] = total_tiles;
+        hdr->n_active = n_active;
+        hdr->total_tiles = total_tiles;
+    }
+    __syncthreads();
+    for (int p = tid; p < P; p += 256) {
+        const int e = ids_s[p];
+        int r = 0;
+        for (int q = 0; q < p; ++q) r += ids_s[q] == e ? 1 : 0;
+        const int slot = off[e] + r;
+        o.sorted_pair[slot] = p;
+        o.slot_of_pair[p] = slot;
     }
 }
 
