@@ -49,7 +49,8 @@ cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int ha
                                  WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, const PermuteOut& o, cudaStream_t st);
 
-// decode fusion: router partials + top-k + single-block permute in one launch
+// decode fusion: router sums + top-k + single-block permute in one launch
+// (part: [S, m, E] scratch, S = router_slices(H, m))
 bool route_permute_fusable(int m, int k, int E);
 cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
                                        int k, const float* bias, int32_t* ids, float* w, int has_shared,

@@ -5,7 +5,8 @@
 // The logits are produced as S partial sums over disjoint slices of H
 // ([S, m, E] fp32); the top-k kernel adds the partials in slice order, so the
 // result is deterministic and the decode case can spread a 1-token GEMV over
-// many SMs without atomics.
+// many SMs without atomics (the fused decode kernel for m <= 4 instead sums
+// whole logits inside each block, again in a fixed order).
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -135,29 +136,179 @@ __global__ __launch_bounds__(256) void topk_softmax(const float* __restrict__ pa
 }
 
 // ---------------------------------------------------------------- fused decode route + permute
-// m <= kRouterSmallMaxM, m*k <= kPermChunk, E <= 256: every block computes
-// split-H router partials exactly as router_partial_small; the last block to
-// finish (an atomic ticket, nothing waits) runs the top-k of every token and
-// the single-block stable permute.  One launch instead of four.
+// m <= kRouteFuseMaxM, m*k <= kPermChunk, E <= 256: one launch instead of
+// four.  Every block computes router sums; the last block to finish (an atomic
+// ticket, nothing waits) runs route_tail: the top-k of every token and the
+// single-block stable permute.  Two ways of spreading the router GEMV:
+//   m <= 4   route_permute_whole: block b computes the whole logits of
+//            experts [2b, 2b + 2); its 8 warps split H into eighths, each warp
+//            sums its values over the lanes by recursive halving (about one
+//            shuffle per value) and the eight warp partials are added in warp
+//            order.  No partial slices for the tail to add.
+//   m > 4    route_permute_sliced: split-H partials [S, m, E] exactly as
+//            router_partial_small (8 experts x one H-slice per block, 16-token
+//            passes), which re-reads x least; the tail adds the S slices in
+//            slice order.
+
+// Shared tail, run by the last block: logits = the S slices of part summed in
+// slice order (into shared memory), then the top-k of every token, then the
+// permute.  Shared scratch: ids_s [kPermChunk], tail_buf [kRouteFuseLogits]
+// (the logits, then the permute's tables), wsum [9].
 template <int VPL>
-__global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __restrict__ x, int m, int H,
-                                                           const float* __restrict__ wr, int E, int HS,
-                                                           float* __restrict__ part, int k,
-                                                           const float* __restrict__ bias, int32_t* __restrict__ ids,
-                                                           float* __restrict__ wts, int has_shared, PermuteOut o,
-                                                           WsHeader* hdr) {
-    pdl_wait();
-    pdl_trigger();
-    constexpr int MT = 16;
-    __shared__ int ids_s[kPermChunk];
-    // the logits live only until the top-k is done, the permute's tables only
-    // after it: one buffer holds either
-    __shared__ __align__(16) int tail_buf[kRouteFuseLogits];
+__device__ __forceinline__ void route_tail(const float* part, int S, int m, int E, int k, const float* bias,
+                                           int32_t* ids, float* wts, int has_shared, const PermuteOut& o,
+                                           WsHeader* hdr, int* ids_s, int* tail_buf, int* wsum) {
     static_assert(kRouteFuseLogits >= 8 * 256 + 2 * (256 + 2) + 27, "permute tables fit the logits buffer");
     float* logits_s = reinterpret_cast<float*>(tail_buf);
     int* wbase = tail_buf;
     int* hist = tail_buf + 8 * 256;
     int* off = hist + 256 + 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // all 256 threads reduce the slices (coalesced over e, many loads in
+    // flight); the warps then pick from shared memory
+    const int n = m * E;
+    for (int i0 = threadIdx.x; i0 < n; i0 += 4 * 256) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int q = 0; q < S; ++q)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i0 + u * 256 < n) v[u] += __ldcg(part + (size_t)q * n + i0 + u * 256);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i0 + u * 256 < n) logits_s[i0 + u * 256] = v[u];
+    }
+    __syncthreads();
+    for (int t = warp; t < m; t += 8) {
+        int id;
+        float wt;
+        warp_topk_softmax<VPL, false>(logits_s, 1, m, E, k, bias, nullptr, t, lane, &id, &wt);
+        if (lane < k) {
+            ids[(size_t)t * k + lane] = id;
+            wts[(size_t)t * k + lane] = wt;
+            ids_s[t * k + lane] = id;
+        }
+    }
+    __syncthreads();  // logits no longer needed: the buffer becomes the permute's tables
+    if (m * k <= kPermTiny) block_permute_tiny(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, tail_buf + 8 * 256 + 2 * (256 + 2));
+    else block_permute_small(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, wbase, wsum);
+    if (threadIdx.x == 0) hdr->done = 0;
+}
+
+// Ticket of the fused kernels: true in the last block of the grid to finish
+// its router sums (after a fence, so all blocks' sums are visible).
+__device__ __forceinline__ bool last_block(WsHeader* hdr, int* flag) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *flag = atomicAdd(&hdr->done, 1) == (int)(gridDim.x * gridDim.y) - 1;
+    __syncthreads();
+    if (!*flag) return false;
+    __threadfence();
+    return true;
+}
+
+// Recursive-halving sum over the 32 lanes of the C live values v[0, C) (C a
+// power of two), using xor offsets O, O/2, ..., 1: at each level a lane keeps
+// one half of its live values and adds the partner's copy of that half.  On
+// return lane l holds in v[0, max(C/32, 1)) the totals of values base + j
+// (lanes that differ only in bits beyond the splitting levels hold copies).
+template <int N, int C, int O>
+__device__ __forceinline__ void rhalve(float (&v)[N], int lane, int& base) {
+    if constexpr (O > 0) {
+        if constexpr (C >= 2) {
+            const bool up = (lane & O) != 0;
+#pragma unroll
+            for (int j = 0; j < C / 2; ++j) {
+                const float send = up ? v[j] : v[j + C / 2];
+                const float keep = up ? v[j + C / 2] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+            }
+            if (up) base += C / 2;
+            rhalve<N, C / 2, O / 2>(v, lane, base);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+            rhalve<N, 1, O / 2>(v, lane, base);
+        }
+    }
+}
+
+constexpr int kWholeEB = 2;  // experts per block of route_permute_whole
+
+template <int VPL, int MT>
+__global__ __launch_bounds__(256) void route_permute_whole(const uint16_t* __restrict__ x, int m, int H,
+                                                           const float* __restrict__ wr, int E,
+                                                           float* __restrict__ logits, int k,
+                                                           const float* __restrict__ bias, int32_t* __restrict__ ids,
+                                                           float* __restrict__ wts, int has_shared, PermuteOut o,
+                                                           WsHeader* hdr) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int N = kWholeEB * MT;  // values per lane: [expert][token]
+    __shared__ int ids_s[kPermChunk];
+    __shared__ __align__(16) int tail_buf[kRouteFuseLogits];
+    __shared__ int wsum[9];
+    __shared__ float red[8][N];
+    __shared__ int is_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * kWholeEB;
+    const int hs = H / 8, h0 = warp * hs, h1 = h0 + hs;  // this warp's eighth of H (a multiple of 16)
+    for (int t0 = 0; t0 < m; t0 += MT) {
+        float acc[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = 0.f;
+#pragma unroll 2
+        for (int h = h0 + lane * 4; h < h1; h += 128) {
+            float4 w[kWholeEB];
+#pragma unroll
+            for (int e = 0; e < kWholeEB; ++e)
+                w[e] = e0 + e < E ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + e) * H + h))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                if (t0 + t < m) {
+                    const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * H + h));
+                    const float x0 = bf16lo(xv.x), x1 = bf16hi(xv.x), x2 = bf16lo(xv.y), x3 = bf16hi(xv.y);
+#pragma unroll
+                    for (int e = 0; e < kWholeEB; ++e) {
+                        float& a = acc[e * MT + t];
+                        a = fmaf(w[e].x, x0, a);
+                        a = fmaf(w[e].y, x1, a);
+                        a = fmaf(w[e].z, x2, a);
+                        a = fmaf(w[e].w, x3, a);
+                    }
+                }
+            }
+        }
+        int base = 0;
+        rhalve<N, N, 16>(acc, lane, base);
+#pragma unroll
+        for (int j = 0; j < (N >= 32 ? N / 32 : 1); ++j) red[warp][base + j] = acc[j];
+        __syncthreads();
+        if (threadIdx.x < N) {
+            const int el = threadIdx.x / MT, t = threadIdx.x % MT;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) v += red[w][threadIdx.x];
+            if (t0 + t < m && e0 + el < E) logits[(size_t)(t0 + t) * E + e0 + el] = v;
+        }
+        __syncthreads();  // red is reused by the next pass
+    }
+    if (!last_block(hdr, &is_last)) return;
+    route_tail<VPL>(logits, 1, m, E, k, bias, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
+}
+
+template <int VPL>
+__global__ __launch_bounds__(256) void route_permute_sliced(const uint16_t* __restrict__ x, int m, int H,
+                                                            const float* __restrict__ wr, int E, int HS,
+                                                            float* __restrict__ part, int k,
+                                                            const float* __restrict__ bias, int32_t* __restrict__ ids,
+                                                            float* __restrict__ wts, int has_shared, PermuteOut o,
+                                                            WsHeader* hdr) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int MT = 16;
+    __shared__ int ids_s[kPermChunk];
+    __shared__ __align__(16) int tail_buf[kRouteFuseLogits];
     __shared__ int wsum[9];
     __shared__ int is_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -191,42 +342,8 @@ __global__ __launch_bounds__(256) void route_permute_small(const uint16_t* __res
             }
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) is_last = atomicAdd(&hdr->done, 1) == (int)(gridDim.x * gridDim.y) - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    // all 256 threads reduce the slice partials (coalesced over e, many loads
-    // in flight) into shared-memory logits; the warps then pick from those
-    const int S = gridDim.y;
-    const int n = m * E;
-    for (int i0 = threadIdx.x; i0 < n; i0 += 4 * 256) {
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int q = 0; q < S; ++q)
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (i0 + u * 256 < n) a[u] += __ldcg(part + (size_t)q * n + i0 + u * 256);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (i0 + u * 256 < n) logits_s[i0 + u * 256] = a[u];
-    }
-    __syncthreads();
-    for (int t = warp; t < m; t += 8) {
-        int id;
-        float wt;
-        warp_topk_softmax<VPL, false>(logits_s, 1, m, E, k, bias, nullptr, t, lane, &id, &wt);
-        if (lane < k) {
-            ids[(size_t)t * k + lane] = id;
-            wts[(size_t)t * k + lane] = wt;
-            ids_s[t * k + lane] = id;
-        }
-    }
-    __syncthreads();  // logits no longer needed: the buffer becomes the permute's tables
-    if (m * k <= kPermTiny) block_permute_tiny(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, tail_buf + 8 * 256 + 2 * (256 + 2));
-    else block_permute_small(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, wbase, wsum);
-    if (threadIdx.x == 0) hdr->done = 0;
+    if (!last_block(hdr, &is_last)) return;
+    route_tail<VPL>(part, gridDim.y, m, E, k, bias, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -258,19 +375,27 @@ bool route_permute_fusable(int m, int k, int E) {
     return m <= kRouteFuseMaxM && m * k <= kPermChunk && E <= 256 && m * E <= kRouteFuseLogits;
 }
 
+template <int VPL>
+static void launch_rps(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S, int k,
+                       const float* bias, int32_t* ids, float* w, int has_shared, const PermuteOut& o, WsHeader* hdr,
+                       cudaStream_t st) {
+    const dim3 whole(ceil_div(E, kWholeEB));
+    if (m <= 1)
+        launch_pdl(route_permute_whole<VPL, 1>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, ids, w, has_shared, o, hdr);
+    else if (m <= 4)
+        launch_pdl(route_permute_whole<VPL, 4>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, ids, w, has_shared, o, hdr);
+    else
+        launch_pdl(route_permute_sliced<VPL>, dim3(ceil_div(E, 8), S), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
+}
+
 cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
                                        int k, const float* bias, int32_t* ids, float* w, int has_shared,
                                        const PermuteOut& o, WsHeader* hdr, cudaStream_t st) {
-    const dim3 grid(ceil_div(E, 8), S);
     const int vpl = ceil_div(E, 32);
-    if (vpl <= 1)
-        launch_pdl(route_permute_small<1>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
-    else if (vpl <= 2)
-        launch_pdl(route_permute_small<2>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
-    else if (vpl <= 4)
-        launch_pdl(route_permute_small<4>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
-    else
-        launch_pdl(route_permute_small<8>, dim3(grid), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
+    if (vpl <= 1) launch_rps<1>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, st);
+    else if (vpl <= 2) launch_rps<2>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, st);
+    else if (vpl <= 4) launch_rps<4>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, st);
+    else launch_rps<8>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, st);
     return cudaGetLastError();
 }
 
