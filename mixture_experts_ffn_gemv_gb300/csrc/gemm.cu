@@ -227,20 +227,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld32(taddr + c * 32, gv);
                     tmem_ld32(taddr + 128 + c * 32, uv);
                     tmem_wait_ld();
-                    if (ok) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + nt * 128 + c * 32);
+                    if (ok) {  // 32 columns = two 32-byte stores, each a whole sector
+                        uint16_t* dst = orow + nt * 128 + c * 32;
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 o;
-                            o.x = pack_bf16x2(swiglu(__uint_as_float(gv[8 * v + 0]), __uint_as_float(uv[8 * v + 0])),
-                                              swiglu(__uint_as_float(gv[8 * v + 1]), __uint_as_float(uv[8 * v + 1])));
-                            o.y = pack_bf16x2(swiglu(__uint_as_float(gv[8 * v + 2]), __uint_as_float(uv[8 * v + 2])),
-                                              swiglu(__uint_as_float(gv[8 * v + 3]), __uint_as_float(uv[8 * v + 3])));
-                            o.z = pack_bf16x2(swiglu(__uint_as_float(gv[8 * v + 4]), __uint_as_float(uv[8 * v + 4])),
-                                              swiglu(__uint_as_float(gv[8 * v + 5]), __uint_as_float(uv[8 * v + 5])));
-                            o.w = pack_bf16x2(swiglu(__uint_as_float(gv[8 * v + 6]), __uint_as_float(uv[8 * v + 6])),
-                                              swiglu(__uint_as_float(gv[8 * v + 7]), __uint_as_float(uv[8 * v + 7])));
-                            dst[v] = o;
+                        for (int v = 0; v < 2; ++v) {
+                            uint32_t o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                o[i] = pack_bf16x2(swiglu(__uint_as_float(gv[16 * v + 2 * i]), __uint_as_float(uv[16 * v + 2 * i])),
+                                                   swiglu(__uint_as_float(gv[16 * v + 2 * i + 1]),
+                                                          __uint_as_float(uv[16 * v + 2 * i + 1])));
+                            st_global_v8(dst + 16 * v, o);
                         }
                     }
                 }
@@ -250,16 +247,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t dv[32];
                     tmem_ld32(taddr + c * 32, dv);
                     tmem_wait_ld();
-                    if (ok) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + nt * BN + c * 32);
+                    if (ok) {  // 32 columns = two 32-byte stores, each a whole sector
+                        uint16_t* dst = orow + nt * BN + c * 32;
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(dv[8 * v + 0]), __uint_as_float(dv[8 * v + 1]));
-                            o.y = pack_bf16x2(__uint_as_float(dv[8 * v + 2]), __uint_as_float(dv[8 * v + 3]));
-                            o.z = pack_bf16x2(__uint_as_float(dv[8 * v + 4]), __uint_as_float(dv[8 * v + 5]));
-                            o.w = pack_bf16x2(__uint_as_float(dv[8 * v + 6]), __uint_as_float(dv[8 * v + 7]));
-                            dst[v] = o;
+                        for (int v = 0; v < 2; ++v) {
+                            uint32_t o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                o[i] = pack_bf16x2(__uint_as_float(dv[16 * v + 2 * i]), __uint_as_float(dv[16 * v + 2 * i + 1]));
+                            st_global_v8(dst + 16 * v, o);
                         }
                     }
                 }

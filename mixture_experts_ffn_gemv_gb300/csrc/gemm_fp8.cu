@@ -284,17 +284,25 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < NH / 4; ++i) w[i] = 0;
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(p.out_q + (size_t)row * p.ldo + nt * 128 + NH * cg);
+                    uint8_t* dst = p.out_q + (size_t)row * p.ldo + nt * 128 + NH * cg;  // whole 32-byte sectors
 #pragma unroll
-                    for (int i = 0; i < NH / 16; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    for (int i = 0; i < NH / 32; ++i) {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) o[u] = w[8 * i + u];
+                        st_global_v8(dst + 32 * i, o);
+                    }
                     if (cg == 0) p.out_sc[(size_t)row * (p.ldo / 128) + nt] = s;
                 }
             } else if (r < valid) {
-                uint4* dst = reinterpret_cast<uint4*>(p.out_y + (size_t)row * p.ldo + nt * BN + NC * cg);
+                uint16_t* dst = p.out_y + (size_t)row * p.ldo + nt * BN + NC * cg;  // whole 32-byte sectors
 #pragma unroll
-                for (int i = 0; i < NC / 8; ++i)
-                    dst[i] = make_uint4(pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]), pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
-                                        pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]), pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
+                for (int i = 0; i < NC / 16; ++i) {
+                    uint32_t o[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) o[u] = pack_bf16x2(acc[16 * i + 2 * u], acc[16 * i + 2 * u + 1]);
+                    st_global_v8(dst + 16 * i, o);
+                }
             }
         }
         if (!ok) {
