@@ -62,6 +62,15 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
                  : "l"(p));
     return r;
 }
+// The same streaming load with a 256-byte L2 fetch: the lines a warp reads in
+// its next few K steps arrive with this one.
+__device__ __forceinline__ uint4 ld_stream_v4_l2pf(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
 
 // ---- e4m3
 // Two e4m3 codes (low byte = element 0) -> two floats.

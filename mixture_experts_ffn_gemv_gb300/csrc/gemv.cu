@@ -55,6 +55,14 @@ __device__ __forceinline__ void mma2_e4m3(float (&c)[4], const uint4& ag, const 
     mma_e4m3(c, ag.z, ag8.z, ag.w, ag8.w, xb.z, xb.w);
 }
 
+// Weight-row loads: with the 256-byte L2 fetch for two-row-tile blocks (each
+// warp streams a K-slice long enough to use it); plain for the one-tile blocks
+// of small m, where the hint measured slower.
+template <int RT>
+__device__ __forceinline__ uint4 ldw(const uint4* p) {
+    return RT == 2 ? ld_stream_v4_l2pf(p) : ld_stream_v4(p);
+}
+
 struct Group {
     int g, off, cnt;
 };
@@ -114,8 +122,8 @@ __global__ __launch_bounds__(256, (NT == 1 ? 4 : 2)) void gemv_gateup_bf16(const
             for (int i = 0; i < 4; ++i) c1[nt][i] = c3[nt][i] = 0.f;
 #pragma unroll 2
         for (int kc = kc0 + tig; kc < kc1; kc += 4) {
-            const uint4 a1 = ld_stream_v4(w1g + kc), a18 = ld_stream_v4(w1g8 + kc);
-            const uint4 a3 = ld_stream_v4(w3g + kc), a38 = ld_stream_v4(w3g8 + kc);
+            const uint4 a1 = ldw<RT>(w1g + kc), a18 = ldw<RT>(w1g8 + kc);
+            const uint4 a3 = ldw<RT>(w3g + kc), a38 = ldw<RT>(w3g8 + kc);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const uint4 xb = __ldg(xr[nt] + kc);
@@ -195,7 +203,7 @@ __global__ __launch_bounds__(256, 4) void gemv_down_bf16(const GemvArgs a, const
             for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
 #pragma unroll 2
         for (int kc = kc0 + tig; kc < kc1; kc += 4) {
-            const uint4 w0 = ld_stream_v4(wg + kc), w8 = ld_stream_v4(wg8 + kc);
+            const uint4 w0 = ldw<RT>(wg + kc), w8 = ldw<RT>(wg8 + kc);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma2_bf16(c[nt], w0, w8, __ldg(hr[nt] + kc));
         }
@@ -279,8 +287,8 @@ __global__ __launch_bounds__(256, (NT == 1 ? 2 : 1)) void gemv_gateup_fp8(const 
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int kc = b * 8 + q * 4 + tig;
-                const uint4 a1 = ld_stream_v4(w1g + kc), a18 = ld_stream_v4(w1g8 + kc);
-                const uint4 a3 = ld_stream_v4(w3g + kc), a38 = ld_stream_v4(w3g8 + kc);
+                const uint4 a1 = ldw<RT>(w1g + kc), a18 = ldw<RT>(w1g8 + kc);
+                const uint4 a3 = ldw<RT>(w3g + kc), a38 = ldw<RT>(w3g8 + kc);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint4 xb = __ldg(xr[nt] + kc);
@@ -380,7 +388,7 @@ __global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uin
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int kc = b * 8 + q * 4 + tig;
-                const uint4 w0 = ld_stream_v4(wg + kc), w8 = ld_stream_v4(wg8 + kc);
+                const uint4 w0 = ldw<RT>(wg + kc), w8 = ldw<RT>(wg8 + kc);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) mma2_e4m3(p[nt], w0, w8, __ldg(hr[nt] + kc));
             }
