@@ -55,9 +55,10 @@ __device__ __forceinline__ void mma2_e4m3(float (&c)[4], const uint4& ag, const 
     mma_e4m3(c, ag.z, ag8.z, ag.w, ag8.w, xb.z, xb.w);
 }
 
-// Weight-row loads: with the 256-byte L2 fetch for two-row-tile blocks (each
-// warp streams a K-slice long enough to use it); plain for the one-tile blocks
-// of small m, where the hint measured slower.
+// bf16 weight-row loads: with the 256-byte L2 fetch for two-row-tile blocks
+// (each warp streams a K-slice long enough to use it); plain for the one-tile
+// blocks of small m, where the hint measured slower.  The fp8 kernels always
+// use the hint.
 template <int RT>
 __device__ __forceinline__ uint4 ldw(const uint4* p) {
     return RT == 2 ? ld_stream_v4_l2pf(p) : ld_stream_v4(p);
@@ -287,8 +288,8 @@ __global__ __launch_bounds__(256, (NT == 1 ? 2 : 1)) void gemv_gateup_fp8(const 
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int kc = b * 8 + q * 4 + tig;
-                const uint4 a1 = ldw<RT>(w1g + kc), a18 = ldw<RT>(w1g8 + kc);
-                const uint4 a3 = ldw<RT>(w3g + kc), a38 = ldw<RT>(w3g8 + kc);
+                const uint4 a1 = ld_stream_v4_l2pf(w1g + kc), a18 = ld_stream_v4_l2pf(w1g8 + kc);
+                const uint4 a3 = ld_stream_v4_l2pf(w3g + kc), a38 = ld_stream_v4_l2pf(w3g8 + kc);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint4 xb = __ldg(xr[nt] + kc);
@@ -388,7 +389,7 @@ __global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uin
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int kc = b * 8 + q * 4 + tig;
-                const uint4 w0 = ldw<RT>(wg + kc), w8 = ldw<RT>(wg8 + kc);
+                const uint4 w0 = ld_stream_v4_l2pf(wg + kc), w8 = ld_stream_v4_l2pf(wg8 + kc);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) mma2_e4m3(p[nt], w0, w8, __ldg(hr[nt] + kc));
             }

@@ -50,11 +50,13 @@ cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int ha
 cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, const PermuteOut& o, cudaStream_t st);
 
 // decode fusion: router sums + top-k + single-block permute in one launch
-// (part: [S, m, E] scratch, S = router_slices(H, m))
+// (part: [S, m, E] scratch, S = router_slices(H, m)); with xq non-null it also
+// quantises x to e4m3 codes xq [m, H] and scales xsc [m, H/128]
 bool route_permute_fusable(int m, int k, int E);
 cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
                                        int k, const float* bias, int32_t* ids, float* w, int has_shared,
-                                       const PermuteOut& o, WsHeader* hdr, cudaStream_t st);
+                                       const PermuteOut& o, WsHeader* hdr, uint8_t* xq, float* xsc,
+                                       cudaStream_t st);
 
 // activations
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st);

@@ -215,40 +215,16 @@ cudaError_t launch_gather_fp8(const uint8_t* xq, const float* xsc, const int32_t
 }
 
 // ---------------------------------------------------------------- fp8 activations
-// One warp per (row, 128-block): s = amax / 448 (IEEE divide), code =
-// e4m3_rn_satfinite(v / s); an all-zero block gets s = 1 and zero codes.
+// One warp per (row, 128-block), quant_block_fp8 in route_permute.cuh.
 // Input bf16 (x) or fp32 (the GEMV arm's h).
-__device__ __forceinline__ void load4(const uint16_t* p, float (&f)[4]) {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
-    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-}
-__device__ __forceinline__ void load4(const float* p, float (&f)[4]) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-}
-
 template <typename T>
 __global__ __launch_bounds__(256) void act_quant_fp8(const T* __restrict__ x, int m, int H, uint8_t* __restrict__ xq,
                                                      float* __restrict__ xsc) {
     pdl_wait();
     pdl_trigger();
-    const int nb = H / 128;
-    const int blk = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (blk >= m * nb) return;
-    const int t = blk / nb, b = blk % nb;
-    const size_t base = (size_t)t * H + (size_t)b * 128 + lane * 4;
-    float f[4];
-    load4(x + base, f);
-    const float amax = warp_max(fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
-    uint32_t codes = 0;
-    float s = 1.0f;
-    if (amax > 0.f) {
-        s = __fdiv_rn(amax, 448.0f);
-        codes = f32x2_to_e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
-                (f32x2_to_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
-    }
-    *reinterpret_cast<uint32_t*>(xq + base) = codes;
-    if (lane == 0) xsc[(size_t)t * nb + b] = s;
+    const int blk = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (blk >= m * (H / 128)) return;
+    quant_block_fp8(x, H, blk, xq, xsc, threadIdx.x & 31);
 }
 
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st) {

@@ -195,6 +195,15 @@ __device__ __forceinline__ void route_tail(const float* part, int S, int m, int 
     if (threadIdx.x == 0) hdr->done = 0;
 }
 
+// fp8 layers: the fused kernels also quantise x (1x128 blocks, one warp per
+// block over all warps of the grid), which the expert kernels read next.
+__device__ __forceinline__ void quantize_x(const uint16_t* x, int m, int H, uint8_t* xq, float* xsc) {
+    if (!xq) return;
+    const int nwarps = gridDim.x * gridDim.y * 8;
+    const int w0 = (blockIdx.y * gridDim.x + blockIdx.x) * 8 + (threadIdx.x >> 5);
+    for (int blk = w0; blk < m * (H / 128); blk += nwarps) quant_block_fp8(x, H, blk, xq, xsc, threadIdx.x & 31);
+}
+
 // Ticket of the fused kernels: true in the last block of the grid to finish
 // its router sums (after a fence, so all blocks' sums are visible).
 __device__ __forceinline__ bool last_block(WsHeader* hdr, int* flag) {
@@ -240,9 +249,11 @@ __global__ __launch_bounds__(256) void route_permute_whole(const uint16_t* __res
                                                            float* __restrict__ logits, int k,
                                                            const float* __restrict__ bias, int32_t* __restrict__ ids,
                                                            float* __restrict__ wts, int has_shared, PermuteOut o,
-                                                           WsHeader* hdr) {
+                                                           WsHeader* hdr, uint8_t* __restrict__ xq,
+                                                           float* __restrict__ xsc) {
     pdl_wait();
     pdl_trigger();
+    quantize_x(x, m, H, xq, xsc);
     constexpr int N = kWholeEB * MT;  // values per lane: [expert][token]
     __shared__ int ids_s[kPermChunk];
     __shared__ __align__(16) int tail_buf[kRouteFuseLogits];
@@ -303,9 +314,11 @@ __global__ __launch_bounds__(256) void route_permute_sliced(const uint16_t* __re
                                                             float* __restrict__ part, int k,
                                                             const float* __restrict__ bias, int32_t* __restrict__ ids,
                                                             float* __restrict__ wts, int has_shared, PermuteOut o,
-                                                            WsHeader* hdr) {
+                                                            WsHeader* hdr, uint8_t* __restrict__ xq,
+                                                            float* __restrict__ xsc) {
     pdl_wait();
     pdl_trigger();
+    quantize_x(x, m, H, xq, xsc);
     constexpr int MT = 16;
     __shared__ int ids_s[kPermChunk];
     __shared__ __align__(16) int tail_buf[kRouteFuseLogits];
@@ -378,24 +391,25 @@ bool route_permute_fusable(int m, int k, int E) {
 template <int VPL>
 static void launch_rps(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S, int k,
                        const float* bias, int32_t* ids, float* w, int has_shared, const PermuteOut& o, WsHeader* hdr,
-                       cudaStream_t st) {
+                       uint8_t* xq, float* xsc, cudaStream_t st) {
     const dim3 whole(ceil_div(E, kWholeEB));
     if (m <= 1)
-        launch_pdl(route_permute_whole<VPL, 1>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, ids, w, has_shared, o, hdr);
+        launch_pdl(route_permute_whole<VPL, 1>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, ids, w, has_shared, o, hdr, xq, xsc);
     else if (m <= 4)
-        launch_pdl(route_permute_whole<VPL, 4>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, ids, w, has_shared, o, hdr);
+        launch_pdl(route_permute_whole<VPL, 4>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, ids, w, has_shared, o, hdr, xq, xsc);
     else
-        launch_pdl(route_permute_sliced<VPL>, dim3(ceil_div(E, 8), S), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr);
+        launch_pdl(route_permute_sliced<VPL>, dim3(ceil_div(E, 8), S), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr, xq, xsc);
 }
 
 cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
                                        int k, const float* bias, int32_t* ids, float* w, int has_shared,
-                                       const PermuteOut& o, WsHeader* hdr, cudaStream_t st) {
+                                       const PermuteOut& o, WsHeader* hdr, uint8_t* xq, float* xsc,
+                                       cudaStream_t st) {
     const int vpl = ceil_div(E, 32);
-    if (vpl <= 1) launch_rps<1>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, st);
-    else if (vpl <= 2) launch_rps<2>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, st);
-    else if (vpl <= 4) launch_rps<4>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, st);
-    else launch_rps<8>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, st);
+    if (vpl <= 1) launch_rps<1>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, xq, xsc, st);
+    else if (vpl <= 2) launch_rps<2>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, xq, xsc, st);
+    else if (vpl <= 4) launch_rps<4>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, xq, xsc, st);
+    else launch_rps<8>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, xq, xsc, st);
     return cudaGetLastError();
 }
 

@@ -44,6 +44,37 @@ __device__ __forceinline__ int block_exclusive_scan(int* a, int n, int* warp_sum
     return warp_sums[8];
 }
 
+// fp8 activation quantiser, one warp per (row t, 128-block b) with blk = t *
+// (H / 128) + b: s = amax / 448 (IEEE divide), code = e4m3_rn_satfinite(v / s);
+// an all-zero block gets s = 1 and zero codes ("per-token 1x128" activation
+// scales of the DeepSeek-V3-shaped layer).  Input bf16 (x) or fp32 (h).
+__device__ __forceinline__ void quant_load4(const uint16_t* p, float (&f)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+}
+__device__ __forceinline__ void quant_load4(const float* p, float (&f)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+template <typename T>
+__device__ __forceinline__ void quant_block_fp8(const T* x, int H, int blk, uint8_t* xq, float* xsc, int lane) {
+    const int nb = H / 128;
+    const int t = blk / nb, b = blk % nb;
+    const size_t base = (size_t)t * H + (size_t)b * 128 + lane * 4;
+    float f[4];
+    quant_load4(x + base, f);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3]))));
+    uint32_t codes = 0;
+    float s = 1.0f;
+    if (amax > 0.f) {
+        s = __fdiv_rn(amax, 448.0f);
+        codes = f32x2_to_e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
+                (f32x2_to_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
+    }
+    *reinterpret_cast<uint32_t*>(xq + base) = codes;
+    if (lane == 0) xsc[(size_t)t * nb + b] = s;
+}
+
 // Order-preserving unsigned key of a float (a > b  <=>  key(a) > key(b)), with
 // -0 folded into +0 so that equal values compare equal; from_key inverts it.
 __device__ __forceinline__ uint32_t order_key(float v) {
