@@ -12,6 +12,7 @@ Storage formats (the layout the C-ABI documents):
             bf16, or e4m3 codes (uint8) with fp32 scales per 128x128 block:
   s1, s3    fp32 [E, I/128, H/128]     s2 fp32 [E, H/128, I/128]
   shared expert (optional): ws1, ws3 [Is, H], ws2 [H, Is] (+ ss1, ss3, ss2)
+  shared_gate fp32 [H] (optional: the shared expert's sigmoid gate)
 
 Every tensor has its own generator seeded from (seed, name, expert), so any one
 expert can be regenerated alone and the draws do not depend on the device
@@ -37,17 +38,31 @@ class LayerShape:
     inter: int
     shared_inter: int = 0
     fp8: bool = False
+    # routing: "softmax" (renormalised over the k picks; a router bias is added
+    # to the logits) or "sigmoid" (scores sigmoid(L); the bias is a correction
+    # that only selects; weights are the picked scores, renormalised when
+    # norm_topk_prob, times routed_scaling)
+    scoring: str = "softmax"
+    norm_topk_prob: bool = True
+    routed_scaling: float = 1.0
+    shared_gate: bool = False  # shared expert scaled by sigmoid(x . gate), gate fp32 [H]
 
     @property
     def name(self) -> str:
         return (f"H{self.hidden}_E{self.num_experts}_k{self.top_k}_I{self.inter}"
                 + (f"_S{self.shared_inter}" if self.shared_inter else "")
-                + ("_fp8" if self.fp8 else "_bf16"))
+                + ("_fp8" if self.fp8 else "_bf16")
+                + ("_sigmoid" if self.scoring == "sigmoid" else "")
+                + ("_gated" if self.shared_gate else ""))
 
 
 TINY = LayerShape(hidden=256, num_experts=8, top_k=2, inter=128)
 QWEN3_30B_A3B = LayerShape(hidden=2048, num_experts=128, top_k=8, inter=768)
 DEEPSEEK_V3 = LayerShape(hidden=7168, num_experts=256, top_k=8, inter=2048, shared_inter=2048, fp8=True)
+# the same layer with its own router: sigmoid scores + correction bias, weights renormalised and scaled by 2.5
+DEEPSEEK_V3_SIGMOID = dataclasses.replace(DEEPSEEK_V3, scoring="sigmoid", routed_scaling=2.5)
+# a small layer whose shared expert is blended through a sigmoid gate
+GATED_SHARED = LayerShape(hidden=512, num_experts=16, top_k=4, inter=256, shared_inter=256, shared_gate=True)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -57,6 +72,7 @@ class Workload:
     ms: tuple
     router: str = "normal"  # "normal": N(0, 0.02); "uniform": U(-a, a) with std 0.02
     zipf_s: float = 0.0     # > 0: router bias making expert popularity Zipf(s)
+    correction_std: float = 0.0  # > 0: sigmoid routing's correction bias ~ N(0, correction_std)
 
 
 WORKLOADS = {
@@ -65,6 +81,8 @@ WORKLOADS = {
     "qwen3_prefill": Workload("qwen3_prefill", QWEN3_30B_A3B, (512, 4096, 16384), router="uniform"),
     "deepseek_v3_fp8": Workload("deepseek_v3_fp8", DEEPSEEK_V3, (1, 16, 4096)),
     "qwen3_zipf": Workload("qwen3_zipf", QWEN3_30B_A3B, (8192,), zipf_s=1.2),
+    "deepseek_v3_sigmoid": Workload("deepseek_v3_sigmoid", DEEPSEEK_V3_SIGMOID, (1, 16, 512), correction_std=0.01),
+    "gated_shared": Workload("gated_shared", GATED_SHARED, (16, 512)),
 }
 
 
@@ -91,13 +109,15 @@ def make_x(shape: LayerShape, m: int, seed: int = 0, device="cpu", stream_id: in
     return torch.randn(m, shape.hidden, generator=g, device=device).to(torch.bfloat16)
 
 
-def make_router(shape: LayerShape, seed: int = 0, device="cpu", kind: str = "normal", zipf_s: float = 0.0):
+def make_router(shape: LayerShape, seed: int = 0, device="cpu", kind: str = "normal", zipf_s: float = 0.0,
+                correction_std: float = 0.0):
     """Router weights fp32 [E, H] and an optional bias fp32 [E].
 
     kind "normal": N(0, 0.02).  kind "uniform": U(-sqrt(3)*0.02, +sqrt(3)*0.02),
     the uniform law with the same 0.02 standard deviation.  zipf_s > 0 adds
     bias[e] = -zipf_s * ln(rank[e]) with rank a seeded permutation of 1..E, so
-    that softmax popularity falls off as rank^-s.
+    that softmax popularity falls off as rank^-s.  correction_std > 0 gives the
+    sigmoid router's correction bias, bias[e] ~ N(0, correction_std).
     """
     E, H = shape.num_experts, shape.hidden
     g = _gen(device, seed, "router", kind)
@@ -109,6 +129,9 @@ def make_router(shape: LayerShape, seed: int = 0, device="cpu", kind: str = "nor
     else:
         raise ValueError(f"unknown router kind {kind!r}")
     bias = None
+    if correction_std > 0:
+        gb = _gen(device, seed, "correction_bias")
+        bias = (torch.randn(E, generator=gb, device=device) * correction_std).contiguous()
     if zipf_s > 0:
         gp = _gen("cpu", seed, "zipf_rank")
         rank = torch.randperm(E, generator=gp).to(torch.float64) + 1.0
@@ -169,12 +192,15 @@ def make_experts(shape: LayerShape, seed: int = 0, device="cpu", experts=None) -
             out[name] = q.contiguous()
             if s is not None:
                 out["ss" + name[2]] = s
+    if shape.shared_gate:
+        g = _gen(device, seed, "shared_gate")
+        out["shared_gate"] = (torch.randn(H, generator=g, device=device) * WEIGHT_STD).contiguous()
     return out
 
 
 def make_layer(workload: Workload, seed: int = 0, device="cpu", experts=None) -> dict:
     """Router + experts for a workload, as one dict of tensors."""
-    wr, bias = make_router(workload.shape, seed, device, workload.router, workload.zipf_s)
+    wr, bias = make_router(workload.shape, seed, device, workload.router, workload.zipf_s, workload.correction_std)
     layer = make_experts(workload.shape, seed, device, experts)
     layer["router_w"] = wr
     layer["router_bias"] = bias

@@ -37,6 +37,7 @@ class _Layer(ctypes.Structure):
         ("s1", _vp), ("s3", _vp), ("s2", _vp),
         ("ws1", _vp), ("ws3", _vp), ("ws2", _vp),
         ("ss1", _vp), ("ss3", _vp), ("ss2", _vp),
+        ("shared_gate", _vp),
     ]
 
 
@@ -70,6 +71,8 @@ def _lib(fp64: bool = False):
             lib.oracle_act_quant.argtypes = [_vp, _i64, _vp, _vp, _vp]
             lib.oracle_router_logits.argtypes = [_vp, _i64, _C.c_int, _vp, _vp, _C.c_int, _vp]
             lib.oracle_topk_softmax.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _vp, _vp]
+            lib.oracle_topk_sigmoid.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _C.c_int, _C.c_float,
+                                                _vp, _vp, _vp]
             lib.oracle_permute.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _vp, _vp]
             lib.oracle_moe_forward.argtypes = [ctypes.POINTER(_Layer), _vp, _i64, _vp, _i64, _vp, _vp, _vp]
             lib.oracle_moe_forward.restype = _C.c_int
@@ -159,6 +162,20 @@ def topk_softmax(logits, k: int):
     return ids, w, margin
 
 
+def topk_sigmoid(logits, k: int, bias=None, norm: bool = True, scale: float = 1.0):
+    """Sigmoid scores, selection by score + bias -> ids int32 [m,k], weights
+    float32 [m,k], margin float32 [m] (in selection-key units)."""
+    L = _np(logits, np.float32)
+    m, E = L.shape
+    b = None if bias is None else _np(bias, np.float32)
+    ids = np.empty((m, k), np.int32)
+    w = np.empty((m, k), np.float32)
+    margin = np.empty(m, np.float32)
+    _lib().oracle_topk_sigmoid(_ptr(L), m, E, k, _ptr(b), int(bool(norm)), float(scale), _ptr(ids), _ptr(w),
+                               _ptr(margin))
+    return ids, w, margin
+
+
 def permute(ids, num_experts: int):
     """-> expert_offsets int32 [E+1], sorted_pair int32 [P], slot_of_pair int32 [P]."""
     a = _np(ids, np.int32)
@@ -190,6 +207,7 @@ def _layer_struct(shape, layer, keep):
     for name in ("s1", "s3", "s2", "ss1", "ss3", "ss2"):
         a = arr(name, np.float32)
         setattr(s, name, _ptr(a))
+    s.shared_gate = _ptr(arr("shared_gate", np.float32)) if getattr(shape, "shared_gate", False) else None
     return s
 
 
@@ -214,7 +232,15 @@ def moe_forward(shape, layer, x, ids, w, rows=None, fp64: bool = False) -> np.nd
 
 
 def route(shape, layer, x, fp64: bool = False):
-    """Router logits + softmax top-k for all tokens -> (logits, ids, w, margin)."""
+    """Router logits + top-k for all tokens -> (logits, ids, w, margin).
+
+    softmax scoring: the bias (if any) is part of the logits.  sigmoid scoring:
+    the logits carry no bias; it only selects (oracle_topk_sigmoid)."""
+    if getattr(shape, "scoring", "softmax") == "sigmoid":
+        L = router_logits(x, layer["router_w"], None, fp64=fp64)
+        ids, w, margin = topk_sigmoid(L, shape.top_k, layer.get("router_bias"), shape.norm_topk_prob,
+                                      shape.routed_scaling)
+        return L, ids, w, margin
     L = router_logits(x, layer["router_w"], layer.get("router_bias"), fp64=fp64)
     ids, w, margin = topk_softmax(L, shape.top_k)
     return L, ids, w, margin

@@ -22,6 +22,10 @@
  *     y[o]   = sum_i a[i] W2[e,o,i]                               (step 6)
  *     out    = sum_j w[j] y_j  (+ shared expert, weight 1)        (steps 7-8)
  *
+ * with two variants of the same page: the sigmoid + correction-bias router
+ * of step 2 (oracle_topk_sigmoid) and the sigmoid-gated shared expert of
+ * step 8, out += sigmoid(dot(x, gate)) * shared.
+ *
  * The accumulation type is float (the default build) or double (the build
  * with ORACLE_FP64 defined, used to bound the float build's own rounding).
  * Every sum runs in ascending index order.  Routing weights are formed in
@@ -210,6 +214,60 @@ EXPORT void oracle_topk_softmax(const float* L, int64_t m, int E, int k, int32_t
 }
 
 /*
+ * Step "2. Batched topK dispatch", the sigmoid + correction-bias branch
+ * (DeepSeek-V3-style scoring): score s[e] = 1 / (1 + exp(-L[e])); the experts
+ * are chosen by s[e] + bias[e] (bias may be NULL), the k largest in
+ * descending order with ties to the lower index -- the bias selects experts,
+ * the weights gather the pre-bias scores: w[j] = s[ids[j]], divided by their
+ * sum when norm is set, then multiplied by scale (routed_scaling_factor).
+ * The selection keys are formed in float, the precision the GPU decides in;
+ * the weights in double, rounded to float.  margin[t] (optional) = key of the
+ * k-th pick minus the best unpicked key (+inf when k == E).
+ */
+EXPORT void oracle_topk_sigmoid(const float* L, int64_t m, int E, int k, const float* bias, int norm,
+                                float scale, int32_t* ids, float* w, float* margin) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < m; ++t) {
+        const float* lt = L + t * (int64_t)E;
+        float* key = (float*)malloc(sizeof(float) * (size_t)E);
+        unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+        for (int e = 0; e < E; ++e) {
+            const float sf = 1.0f / (1.0f + expf(-lt[e]));
+            key[e] = bias ? sf + bias[e] : sf;
+        }
+        int32_t* it = ids + t * (int64_t)k;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || key[e] > key[best]) best = e; /* strict: ties keep the lower index */
+            }
+            taken[best] = 1;
+            it[j] = best;
+        }
+        double sum = 0.0;
+        for (int j = 0; j < k; ++j) sum += 1.0 / (1.0 + exp(-(double)lt[it[j]]));
+        for (int j = 0; j < k; ++j) {
+            double v = 1.0 / (1.0 + exp(-(double)lt[it[j]]));
+            if (norm) v /= sum;
+            w[t * (int64_t)k + j] = (float)(v * (double)scale);
+        }
+        if (margin) {
+            if (k >= E) {
+                margin[t] = INFINITY;
+            } else {
+                int best = -1;
+                for (int e = 0; e < E; ++e)
+                    if (!taken[e] && (best < 0 || key[e] > key[best])) best = e;
+                margin[t] = key[it[k - 1]] - key[best];
+            }
+        }
+        free(key);
+        free(taken);
+    }
+}
+
+/*
  * Step "3. Sort tokens by expert": a stable counting sort of the pairs
  * p = t*k + j by their expert ids[p].  offsets[E+1] is the exclusive prefix
  * sum of the per-expert counts; sorted_pair[s] is the pair at sorted slot s
@@ -239,6 +297,7 @@ typedef struct {
     const float *s1, *s3, *s2; /* fp8 only: [E,I/128,H/128], [E,I/128,H/128], [E,H/128,I/128] */
     const void *ws1, *ws3, *ws2; /* shared expert, [Is,H], [Is,H], [H,Is] */
     const float *ss1, *ss3, *ss2;
+    const float* shared_gate;    /* [H] or NULL: shared expert scaled by sigmoid(dot(x, gate)) */
 } oracle_layer;
 
 /* Element (r, c) of one expert's [R, C] weight matrix, dequantised. */
@@ -294,7 +353,10 @@ static void expert_ffn(const oracle_layer* Lr, int I, const void* w1, const floa
  * rows is NULL), given the routing (ids, w: [m,k]).  out: [nrows, H] float.
  * Per token: acc = sum_j w[j] * FFN_{ids[j]}(xin) (j ascending), then
  * acc += FFN_shared(xin) when a shared expert exists (metrale moe_v41
- * forward.rs, shared_expert_tail: acc += sd).  Returns 0, or -1 on a bad id.
+ * forward.rs, shared_expert_tail: acc += sd), or with a shared gate
+ * acc += sigmoid(sum_h x[h] * gate[h]) * FFN_shared(xin) (forward_prefill
+ * step "8. Blend shared expert"; x is the bf16 input, the sum in acc_t).
+ * Returns 0, or -1 on a bad id.
  */
 EXPORT int oracle_moe_forward(const oracle_layer* Lr, const uint16_t* x, int64_t m,
                               const int64_t* rows, int64_t nrows, const int32_t* ids,
@@ -343,7 +405,13 @@ EXPORT int oracle_moe_forward(const oracle_layer* Lr, const uint16_t* x, int64_t
         }
         if (Is > 0) {
             expert_ffn(Lr, Is, Lr->ws1, Lr->ss1, Lr->ws3, Lr->ss3, Lr->ws2, Lr->ss2, 0, 0, xin, a, y);
-            for (int h = 0; h < H; ++h) acc[h] += y[h];
+            acc_t gs = 1;
+            if (Lr->shared_gate) {
+                acc_t d = 0;
+                for (int h = 0; h < H; ++h) d += (acc_t)bf16_to_float(xt[h]) * (acc_t)Lr->shared_gate[h];
+                gs = (acc_t)1 / ((acc_t)1 + ACC_EXP(-d));
+            }
+            for (int h = 0; h < H; ++h) acc[h] += gs * y[h];
         }
         for (int h = 0; h < H; ++h) out[r * (int64_t)H + h] = (float)acc[h];
         free(xin); free(a); free(y); free(acc);

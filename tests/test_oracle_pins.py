@@ -15,6 +15,12 @@
                           alone equals the same MLP; fp8 path equals a torch
                           dequantise / fake-quantise float64 pipeline.
   * combine           -> dense-gating reformulation (torch float64 einsum).
+  * sigmoid routing   -> brute force over all k-subsets of score + bias (with the
+                          keys formed in float32 by numpy), scipy's expit for the
+                          weights, closed forms (zero logits: ids 0..k-1, weights
+                          scale/k or scale/2), a bias that forces the selection.
+  * gated shared      -> torch float64: routed sum + sigmoid(x . gate) times the
+                          dense SwiGLU of the shared expert; a zero gate halves it.
   * structure         -> token independence, expert relabelling invariance,
                           float vs double oracle builds agree to ~1e-6.
 """
@@ -178,6 +184,73 @@ def test_routing_weights_softmax_closed_forms(oracle_mod):
         assert np.array_equal(idz, np.tile(np.arange(k, dtype=np.int32), (4, 1)))
         assert np.all(wz == np.float32(1.0 / k))
         assert np.all(mz == 0)
+
+
+def _sigmoid_keys32(L, bias):
+    s = (np.float32(1.0) / (np.float32(1.0) + np.exp(-L.astype(np.float32)))).astype(np.float32)
+    return s + (bias.astype(np.float32) if bias is not None else np.float32(0.0))
+
+
+def test_topk_sigmoid_brute_force_and_weights(oracle_mod):
+    from scipy.special import expit
+    rng = np.random.default_rng(11)
+    E, k, m = 10, 3, 200
+    L = rng.normal(0, 1.5, size=(m, E)).astype(np.float32)
+    bias = rng.normal(0, 0.05, size=E).astype(np.float32)
+    for norm, scale in ((True, 2.5), (False, 1.0), (False, 0.7)):
+        ids, w, margin = oracle_mod.topk_sigmoid(L, k, bias, norm, scale)
+        key = _sigmoid_keys32(L, bias)
+        for t in range(m):
+            best = max(itertools.combinations(range(E), k), key=lambda sub: sorted(key[t, list(sub)].tolist()))
+            if margin[t] > 1e-6:  # not a near-tie between numpy's and libm's float exp
+                assert set(best) == set(ids[t].tolist())
+            assert all(key[t, ids[t, j]] >= key[t, ids[t, j + 1]] for j in range(k - 1))
+        s = expit(np.take_along_axis(L, ids, axis=1).astype(np.float64))  # pre-bias scores
+        ref = s / s.sum(1, keepdims=True) * scale if norm else s * scale
+        assert np.abs(w - ref).max() < 1e-6 * max(1.0, scale)
+
+
+def test_topk_sigmoid_closed_forms(oracle_mod):
+    Z = np.zeros((3, 12), np.float32)
+    for k in (1, 4, 12):
+        ids, w, margin = oracle_mod.topk_sigmoid(Z, k, None, True, 2.5)
+        assert np.array_equal(ids, np.tile(np.arange(k, dtype=np.int32), (3, 1)))  # all scores 0.5: lowest ids
+        assert np.all(w == np.float32(2.5 / k))
+        _, w2, _ = oracle_mod.topk_sigmoid(Z, k, None, False, 2.5)
+        assert np.all(w2 == np.float32(1.25))  # sigmoid(0) * 2.5
+    # a large correction bias on a chosen set selects exactly that set, while
+    # the weights still come from the unbiased scores
+    rng = np.random.default_rng(12)
+    L = rng.normal(0, 1, size=(50, 16)).astype(np.float32)
+    chosen = np.array([13, 2, 7], np.int32)
+    bias = np.zeros(16, np.float32)
+    bias[chosen] = np.array([30.0, 20.0, 10.0], np.float32)
+    ids, w, _ = oracle_mod.topk_sigmoid(L, 3, bias, False, 1.0)
+    assert np.array_equal(ids, np.tile(chosen, (50, 1)))
+    assert np.allclose(w, 1.0 / (1.0 + np.exp(-L[:, chosen].astype(np.float64))), atol=1e-7)
+
+
+def test_gated_shared_expert_matches_torch(oracle_mod):
+    shape = I.LayerShape(hidden=256, num_experts=4, top_k=2, inter=128, shared_inter=256, shared_gate=True)
+    layer = I.make_experts(shape, seed=13)
+    x = I.make_x(shape, 6, seed=13)
+    ids = np.array([[0, 1], [2, 3], [1, 0], [3, 2], [0, 2], [1, 3]], np.int32)
+    w = np.random.default_rng(13).uniform(0.1, 0.9, size=(6, 2)).astype(np.float32)
+    x64 = _f64(x.float())
+    routed = torch.zeros(6, 256, dtype=torch.float64)
+    for t in range(6):
+        for j in range(2):
+            e = int(ids[t, j])
+            routed[t] += float(w[t, j]) * _dense_swiglu64(x64[t:t + 1], layer["w1"][e].float(), layer["w3"][e].float(),
+                                                          layer["w2"][e].float())[0]
+    shared = _dense_swiglu64(x64, layer["ws1"].float(), layer["ws3"].float(), layer["ws2"].float())
+    gate = torch.sigmoid(x64 @ _f64(layer["shared_gate"]))
+    ref = (routed + gate[:, None] * shared).numpy()
+    out = oracle_mod.moe_forward(shape, layer, x, ids, w, fp64=True)
+    assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 1e-7
+    layer["shared_gate"] = torch.zeros(256)  # sigmoid(0) = 1/2
+    half = oracle_mod.moe_forward(shape, layer, x, ids, w, fp64=True)
+    assert np.linalg.norm(half - (routed + 0.5 * shared).numpy()) / np.linalg.norm(ref) < 1e-7
 
 
 def test_permute_matches_stable_argsort(oracle_mod):
