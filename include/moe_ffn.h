@@ -62,6 +62,15 @@ extern "C" {
  * s = amax / 448, round-to-nearest-even, saturating. */
 #define MOE_WEIGHTS_FP8_E4M3_B128 1
 
+/* ---- router scoring ("2. Batched topK dispatch" of forward_prefill.rs) */
+/* softmax over the k picks; a router bias, if given, is added to the logits */
+#define MOE_SCORING_SOFTMAX 0
+/* sigmoid scores with a correction bias (the DeepSeek-V3 / MiniMax-M2
+ * branch): s = sigmoid(L); the experts are chosen by s + bias, the weights
+ * gather the pre-bias scores, divided by their sum when norm_topk_prob is
+ * set, then multiplied by routed_scaling_factor */
+#define MOE_SCORING_SIGMOID 1
+
 /* ---- expert arms for moe_experts / moe_forward */
 #define MOE_ARM_AUTO 0 /* pick by rows per expert (moe_select_arm) */
 #define MOE_ARM_GEMV 1 /* small-m arm: each selected expert's weights streamed once */
@@ -74,6 +83,9 @@ typedef struct moe_config {
     int32_t inter;        /* I: expert intermediate size, multiple of 128 (of 512 for fp8) */
     int32_t shared_inter; /* 0 = no shared expert; otherwise must equal inter */
     int32_t weights;      /* MOE_WEIGHTS_BF16 or MOE_WEIGHTS_FP8_E4M3_B128 */
+    int32_t scoring;      /* MOE_SCORING_SOFTMAX (0) or MOE_SCORING_SIGMOID */
+    int32_t norm_topk_prob;      /* sigmoid scoring: 1 = renormalise the k weights to sum 1 */
+    float routed_scaling_factor; /* sigmoid scoring: weight multiplier, finite and > 0 */
 } moe_config;
 
 /* Stacked expert weights in nn.Linear (out, in) layout.
@@ -81,6 +93,10 @@ typedef struct moe_config {
  *   shared:  w1, w3 [I, H]      w2 [H, I]        (E = 1 of the same layout)
  *   fp8 only: s1, s3 [E, I/128, H/128]  s2 [E, H/128, I/128]  (fp32)
  * Element type: bf16 or e4m3 codes (uint8) per moe_config.weights.
+ * gate (shared expert only, else NULL): fp32 [H]; when set, the shared
+ * expert's output is scaled per token by sigmoid(sum_h x[h] gate[h])
+ * (forward_prefill.rs step "8. Blend shared expert"); NULL adds it with
+ * weight 1.
  * Pointers must be 16-byte aligned.  The weights must outlive the layer. */
 typedef struct moe_expert_weights {
     const void* w1;
@@ -89,6 +105,7 @@ typedef struct moe_expert_weights {
     const float* s1;
     const float* s3;
     const float* s2;
+    const float* gate;
 } moe_expert_weights;
 
 typedef struct moe_layer moe_layer;
@@ -108,11 +125,14 @@ MOE_API int moe_workspace_size(const moe_layer* layer, int64_t m, size_t* bytes)
 /* Which arm MOE_ARM_AUTO takes for m tokens (MOE_ARM_GEMV or MOE_ARM_GEMM). */
 MOE_API int moe_select_arm(const moe_layer* layer, int64_t m);
 
-/* Steps 1-2 of forward_prefill ("Gate GEMM", "Batched topK dispatch", softmax
- * with norm_topk_prob): logits[t,e] = sum_h x[t,h] Wr[e,h] (+ bias[e]) in
- * fp32; topk_ids[t,:] = the k largest logits in descending order (equal
- * logits: lower expert index first); topk_w[t,j] = exp(L_j - L_0) / sum over
- * the k selected of exp(L_i - L_0).
+/* Steps 1-2 of forward_prefill ("Gate GEMM", "Batched topK dispatch").
+ * Softmax scoring (norm_topk_prob): logits[t,e] = sum_h x[t,h] Wr[e,h]
+ * (+ bias[e]) in fp32; topk_ids[t,:] = the k largest logits in descending
+ * order (equal logits: lower expert index first); topk_w[t,j] =
+ * exp(L_j - L_0) / sum over the k selected of exp(L_i - L_0).
+ * Sigmoid scoring: logits carry no bias; with s = sigmoid(L) (fp32),
+ * topk_ids = the k largest s + bias (same order rules); topk_w[t,j] =
+ * s_j (/ sum of the k s when norm_topk_prob) * routed_scaling_factor.
  *   x        bf16 [m, H]           router_w fp32 [E, H]
  *   router_bias fp32 [E] or NULL   logits_out fp32 [m, E] or NULL
  *   topk_ids int32 [m, k]          topk_w fp32 [m, k]                       */
@@ -156,7 +176,8 @@ MOE_API int moe_permute_noalloc(const int32_t* topk_ids, int64_t m, int32_t top_
 
 /* Steps 3-8 for a given routing: permute, grouped gate/up + SiLU(gate)*up,
  * grouped down, then out[t] = sum_j topk_w[t,j] * y_{t,j} (+ shared expert
- * output, weight 1), accumulated in fp32 in j order and stored as bf16.
+ * output, weight 1 or its sigmoid gate), accumulated in fp32 in j order and
+ * stored as bf16.
  *   x bf16 [m, H]; topk_ids int32 [m, k]; topk_w fp32 [m, k]; out bf16 [m, H]
  * out is fully overwritten (metrale moe_v41 forward.rs: acc is cleared before
  * any routed or shared row is added).  arm: MOE_ARM_*.                      */

@@ -17,6 +17,7 @@ from .build import LIB, build_library, up_to_date
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
 MOE_WEIGHTS_BF16, MOE_WEIGHTS_FP8_E4M3_B128 = 0, 1
+MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 MOE_ARM_AUTO, MOE_ARM_GEMV, MOE_ARM_GEMM = 0, 1, 2
 ARMS = {"auto": MOE_ARM_AUTO, "gemv": MOE_ARM_GEMV, "gemm": MOE_ARM_GEMM}
 
@@ -32,11 +33,12 @@ _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [("hidden", _i32), ("num_experts", _i32), ("top_k", _i32), ("inter", _i32),
-                ("shared_inter", _i32), ("weights", _i32)]
+                ("shared_inter", _i32), ("weights", _i32), ("scoring", _i32), ("norm_topk_prob", _i32),
+                ("routed_scaling_factor", ctypes.c_float)]
 
 
 class MoeExpertWeights(ctypes.Structure):
-    _fields_ = [("w1", _vp), ("w3", _vp), ("w2", _vp), ("s1", _vp), ("s3", _vp), ("s2", _vp)]
+    _fields_ = [("w1", _vp), ("w3", _vp), ("w2", _vp), ("s1", _vp), ("s3", _vp), ("s2", _vp), ("gate", _vp)]
 
 
 class MoeError(RuntimeError):
@@ -129,12 +131,17 @@ class MoeLayer:
         self.lib = load_library()
         self.shape = shape
         self._keep = dict(tensors)
+        sigmoid = getattr(shape, "scoring", "softmax") == "sigmoid"
         cfg = MoeConfig(shape.hidden, shape.num_experts, shape.top_k, shape.inter, shape.shared_inter,
-                        MOE_WEIGHTS_FP8_E4M3_B128 if shape.fp8 else MOE_WEIGHTS_BF16)
+                        MOE_WEIGHTS_FP8_E4M3_B128 if shape.fp8 else MOE_WEIGHTS_BF16,
+                        MOE_SCORING_SIGMOID if sigmoid else MOE_SCORING_SOFTMAX,
+                        int(bool(getattr(shape, "norm_topk_prob", True))),
+                        float(getattr(shape, "routed_scaling", 1.0)))
         routed = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("w1", "w3", "w2", "s1", "s3", "s2")])
         shared = None
         if shape.shared_inter:
-            shared = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2")])
+            shared = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2")],
+                                      _p(tensors.get("shared_gate")) if getattr(shape, "shared_gate", False) else None)
         handle = _vp()
         _check(self.lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(routed),
                                          ctypes.byref(shared) if shared is not None else None,

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -22,11 +23,11 @@ namespace {
 // stream, resolved when the totals are read.
 enum KernelId : int {
     K_ROUTER_SPLIT = 0, K_ROUTER, K_TOPK, K_ROUTE_PERMUTE, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
-    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_H_QUANT, K_COUNT
+    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_H_QUANT, K_SHARED_GATE, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "router_split", "router", "topk_softmax", "route_permute", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
-    "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine", "h_quant_fp8",
+    "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine", "h_quant_fp8", "shared_gate",
 };
 
 struct Pending {
@@ -86,6 +87,7 @@ struct moe_layer {
     mutable int last_launches;
     mutable KernelTimer timer;
     GemmWeights gemm;  // host-side TMA descriptors of the weights
+    RouteMode rm;      // router scoring
 };
 
 namespace {
@@ -96,7 +98,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
     size_t hdr, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile, sorted_pair, slot_of_pair;
-    size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, total;
+    size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, sgate, total;
     int S, P, rows, nchunk;
     bool router_tc;
 };
@@ -140,6 +142,7 @@ Layout layout(const moe_layer* L, int64_t m) {
         o.hf = take((size_t)o.rows * I * 4);  // GEMV arm: fp32 h before quantisation
     }
     o.y = take((size_t)o.rows * H * 4);
+    o.sgate = L->shared.gate ? take((size_t)m * 4) : 0;  // the shared expert's per-token gate
     o.total = off;
     return o;
 }
@@ -208,7 +211,7 @@ int run_route(const moe_layer* L, const Layout& lo, const void* x, int m, const 
     } else {
         MOE_LAUNCH(K_ROUTER, launch_router(xb, m, c.hidden, wr, c.num_experts, part, lo.S, st));
     }
-    MOE_LAUNCH(K_TOPK, launch_topk(part, lo.S, m, c.num_experts, c.top_k, bias, logits_out, ids, w, st));
+    MOE_LAUNCH(K_TOPK, launch_topk(part, lo.S, m, c.num_experts, c.top_k, bias, L->rm, logits_out, ids, w, st));
     return MOE_OK;
 }
 
@@ -241,6 +244,13 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     }
     if (arm == MOE_ARM_AUTO) arm = moe_select_arm(L, m);
     const int has_shared = L->has_shared ? 1 : 0;
+    // the shared expert's sigmoid gate per token (forward_prefill step 8), or
+    // null: weight 1
+    float* sg = nullptr;
+    if (L->shared.gate) {
+        sg = at<float>(ws, lo.sgate);
+        MOE_LAUNCH(K_SHARED_GATE, launch_shared_gate(static_cast<const uint16_t*>(x), m, H, L->shared.gate, sg, st));
+    }
     if (arm == MOE_ARM_GEMV) {
         GemvArgs a;
         a.hdr = hdr;
@@ -275,7 +285,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
             MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_bf16(a, static_cast<const uint16_t*>(x), h, st));
             MOE_LAUNCH(K_GEMV_DOWN, launch_gemv_down_bf16(a, h, y, st));
         }
-        MOE_LAUNCH(K_COMBINE, launch_combine_f32(y, po.slot_of_pair, w, m, k, H, lo.P, has_shared, static_cast<uint16_t*>(out),
+        MOE_LAUNCH(K_COMBINE, launch_combine_f32(y, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, static_cast<uint16_t*>(out),
                                       st));
         return MOE_OK;
     }
@@ -316,7 +326,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     if (rc != MOE_OK) return rc;
     MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(gl, st));
     MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(gl, st));
-    MOE_LAUNCH(K_COMBINE, launch_combine_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, static_cast<uint16_t*>(out),
+    MOE_LAUNCH(K_COMBINE, launch_combine_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, static_cast<uint16_t*>(out),
                                    st));
     return MOE_OK;
 }
@@ -346,10 +356,16 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
     if (c.hidden % 128 != 0 || c.inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (fp8 && (c.inter % 512 != 0 || c.hidden % 512 != 0)) return MOE_ERR_UNSUPPORTED;
     if (c.shared_inter != 0 && c.shared_inter != c.inter) return MOE_ERR_UNSUPPORTED;
-    if (!weights_ok(routed, fp8)) return MOE_ERR_INVALID_ARG;
+    if (c.scoring != MOE_SCORING_SOFTMAX && c.scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (c.scoring == MOE_SCORING_SIGMOID &&
+        (!(c.routed_scaling_factor > 0.f) || !std::isfinite(c.routed_scaling_factor) ||
+         (c.norm_topk_prob != 0 && c.norm_topk_prob != 1)))
+        return MOE_ERR_INVALID_ARG;
+    if (!weights_ok(routed, fp8) || routed->gate) return MOE_ERR_INVALID_ARG;  // a gate is for the shared expert only
     const bool has_shared = c.shared_inter > 0;
     if (has_shared != (shared != nullptr)) return MOE_ERR_INVALID_ARG;
     if (has_shared && !weights_ok(shared, fp8)) return MOE_ERR_INVALID_ARG;
+    if (has_shared && shared->gate && !aligned(shared->gate, 16)) return MOE_ERR_INVALID_ARG;
     moe_layer* L = new (std::nothrow) moe_layer();
     if (!L) return MOE_ERR_INVALID_ARG;
     L->cfg = c;
@@ -357,6 +373,8 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
     if (has_shared) L->shared = *shared;
     L->has_shared = has_shared;
     L->fp8 = fp8;
+    L->rm = RouteMode{c.scoring == MOE_SCORING_SIGMOID ? 1 : 0, c.norm_topk_prob ? 1 : 0,
+                      c.scoring == MOE_SCORING_SIGMOID ? c.routed_scaling_factor : 1.0f};
     L->last_launches = 0;
     if (cudaGetDevice(&L->device) != cudaSuccess) {
         delete L;
@@ -464,6 +482,7 @@ int moe_forward(const moe_layer* layer, const void* x, int64_t m, const float* r
         MOE_LAUNCH(K_ROUTE_PERMUTE,
                    launch_route_permute_small(static_cast<const uint16_t*>(x), (int)m, c.hidden, router_w,
                                               c.num_experts, at<float>(workspace, lo.part), lo.S, c.top_k, router_bias,
+                                              layer->rm,
                                               ids, w, layer->has_shared ? 1 : 0, po, at<WsHeader>(workspace, lo.hdr),
                                               fuse_q ? at<uint8_t>(workspace, lo.xq) : nullptr,
                                               fuse_q ? at<float>(workspace, lo.xsc) : nullptr, st));

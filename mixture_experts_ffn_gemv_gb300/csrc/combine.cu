@@ -3,9 +3,11 @@
 // (moe_unpermute_reduce_indexed) and shared_expert_tail of metrale
 // moe_v41/forward.rs (acc += sd, then out = bf16(acc)).
 //
-// out[t, :] = sum_{j < k} w[t, j] * Y[slot_of_pair[t*k + j], :]  (+ Y[P + t, :])
+// out[t, :] = sum_{j < k} w[t, j] * Y[slot_of_pair[t*k + j], :]  (+ g[t] * Y[P + t, :])
 // accumulated in fp32 in ascending j, a gather (no atomics), so the result is
-// deterministic and out is fully overwritten.
+// deterministic and out is fully overwritten.  g[t] is 1, or the shared
+// expert's sigmoid gate of forward_prefill step "8. Blend shared expert":
+// output += sigmoid(dot(input, gate)) * shared (shared_gate below).
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -28,7 +30,7 @@ __device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
 template <typename YT>
 __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
                                                const float* __restrict__ w, int k, int H, int P, int has_shared,
-                                               uint16_t* __restrict__ out) {
+                                               const float* __restrict__ shared_g, uint16_t* __restrict__ out) {
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.y;
@@ -63,10 +65,11 @@ __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const i
             for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], v[u][i], acc[i]);
     }
     if (has_shared) {
+        const float g = shared_g ? shared_g[t] : 1.0f;
         float v[8];
         load8(y + (size_t)(P + t) * H + h0, v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += v[i];
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, v[i], acc[i]);
     }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);
@@ -77,16 +80,44 @@ __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const i
 }
 
 cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
-                               int P, int has_shared, uint16_t* out, cudaStream_t st) {
+                               int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st) {
     const dim3 grid(ceil_div(H, 1024), m);
-    launch_pdl(combine<float>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, out);
+    launch_pdl(combine<float>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
-                                int H, int P, int has_shared, uint16_t* out, cudaStream_t st) {
+                                int H, int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st) {
     const dim3 grid(ceil_div(H, 1024), m);
-    launch_pdl(combine<uint16_t>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, out);
+    launch_pdl(combine<uint16_t>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- shared gate
+// g[t] = sigmoid(sum_h x[t, h] * gate[h]): one warp per token, fp32 sums over
+// lane-strided chunks of 4, then a warp sum.  H % 128 == 0.
+__global__ __launch_bounds__(256) void shared_gate(const uint16_t* __restrict__ x, int m, int H,
+                                                   const float* __restrict__ gate, float* __restrict__ g) {
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= m) return;
+    const uint16_t* xt = x + (size_t)t * H;
+    float d = 0.f;
+    for (int h = lane * 4; h < H; h += 128) {
+        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(xt + h));
+        const float4 gv = __ldg(reinterpret_cast<const float4*>(gate + h));
+        d = fmaf(bf16lo(xv.x), gv.x, d);
+        d = fmaf(bf16hi(xv.x), gv.y, d);
+        d = fmaf(bf16lo(xv.y), gv.z, d);
+        d = fmaf(bf16hi(xv.y), gv.w, d);
+    }
+    d = warp_sum(d);
+    if (lane == 0) g[t] = 1.0f / (1.0f + expf(-d));
+}
+
+cudaError_t launch_shared_gate(const uint16_t* x, int m, int H, const float* gate, float* g, cudaStream_t st) {
+    launch_pdl(shared_gate, dim3(ceil_div(m, 8)), dim3(256), 0, st, x, m, H, gate, g);
     return cudaGetLastError();
 }
 

@@ -8,6 +8,15 @@ namespace moe {
 
 struct WsHeader;
 
+// Scoring of the top-k step: softmax (a bias is added to the logits), or
+// sigmoid with a correction bias that only selects; the sigmoid weights are
+// the picked scores, renormalised when norm, times scale.
+struct RouteMode {
+    int sigmoid;
+    int norm;
+    float scale;
+};
+
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kRouterSmallMaxM = 64;  // up to this m the router is a split-H GEMV
@@ -30,7 +39,7 @@ size_t router_tc_split_bytes(int E, int H);
 cudaError_t launch_router_split(const float* wr, int E, int H, uint16_t* planes, cudaStream_t st);
 cudaError_t launch_router_tc(const uint16_t* x, int m, int H, const uint16_t* planes, int E, float* part, int S,
                              WsHeader* hdr, cudaStream_t st);
-cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const float* bias, float* logits_out,
+cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const float* bias, RouteMode rm, float* logits_out,
                         int32_t* ids, float* w, cudaStream_t st);
 
 // permute: groups g < E are the routed experts, g == E the shared expert
@@ -54,7 +63,7 @@ cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, cons
 // quantises x to e4m3 codes xq [m, H] and scales xsc [m, H/128]
 bool route_permute_fusable(int m, int k, int E);
 cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
-                                       int k, const float* bias, int32_t* ids, float* w, int has_shared,
+                                       int k, const float* bias, RouteMode rm, int32_t* ids, float* w, int has_shared,
                                        const PermuteOut& o, WsHeader* hdr, uint8_t* xq, float* xsc,
                                        cudaStream_t st);
 
@@ -87,10 +96,12 @@ cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const f
 cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
                                  cudaStream_t st);
 
-// combine: out[t] = sum_j w[t,j] * Y[slot(t,j)] (+ Y[P+t] when has_shared)
+// the shared expert's gate per token: g[t] = sigmoid(sum_h x[t,h] gate[h])
+cudaError_t launch_shared_gate(const uint16_t* x, int m, int H, const float* gate, float* g, cudaStream_t st);
+// combine: out[t] = sum_j w[t,j] * Y[slot(t,j)] (+ g[t] * Y[P+t] when has_shared; g = 1 when null)
 cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
-                               int P, int has_shared, uint16_t* out, cudaStream_t st);
+                               int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st);
 cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
-                                int H, int P, int has_shared, uint16_t* out, cudaStream_t st);
+                                int H, int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st);
 
 }  // namespace moe

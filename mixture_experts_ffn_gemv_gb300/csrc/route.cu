@@ -119,7 +119,7 @@ __global__ __launch_bounds__(256) void router_logits_tiled(const uint16_t* __res
 // One warp per token; lane l holds logits e = l + 32 v.
 template <int VPL>
 __global__ __launch_bounds__(256) void topk_softmax(const float* __restrict__ part, int S, int m, int E, int k,
-                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
+                                                    const float* __restrict__ bias, RouteMode rm, float* __restrict__ logits_out,
                                                     int32_t* __restrict__ ids, float* __restrict__ wts) {
     pdl_wait();
     pdl_trigger();
@@ -128,7 +128,7 @@ __global__ __launch_bounds__(256) void topk_softmax(const float* __restrict__ pa
     if (t >= m) return;
     int id;
     float wt;
-    warp_topk_softmax<VPL, false>(part, S, m, E, k, bias, logits_out, t, lane, &id, &wt);
+    warp_topk<VPL, false>(part, S, m, E, k, bias, rm, logits_out, t, lane, &id, &wt);
     if (lane < k) {
         ids[(size_t)t * k + lane] = id;
         wts[(size_t)t * k + lane] = wt;
@@ -155,7 +155,7 @@ __global__ __launch_bounds__(256) void topk_softmax(const float* __restrict__ pa
 // permute.  Shared scratch: ids_s [kPermChunk], tail_buf [kRouteFuseLogits]
 // (the logits, then the permute's tables), wsum [9].
 template <int VPL>
-__device__ __forceinline__ void route_tail(const float* part, int S, int m, int E, int k, const float* bias,
+__device__ __forceinline__ void route_tail(const float* part, int S, int m, int E, int k, const float* bias, RouteMode rm,
                                            int32_t* ids, float* wts, int has_shared, const PermuteOut& o,
                                            WsHeader* hdr, int* ids_s, int* tail_buf, int* wsum) {
     static_assert(kRouteFuseLogits >= 8 * 256 + 2 * (256 + 2) + 27, "permute tables fit the logits buffer");
@@ -182,7 +182,7 @@ __device__ __forceinline__ void route_tail(const float* part, int S, int m, int 
     for (int t = warp; t < m; t += 8) {
         int id;
         float wt;
-        warp_topk_softmax<VPL, false>(logits_s, 1, m, E, k, bias, nullptr, t, lane, &id, &wt);
+        warp_topk<VPL, false>(logits_s, 1, m, E, k, bias, rm, nullptr, t, lane, &id, &wt);
         if (lane < k) {
             ids[(size_t)t * k + lane] = id;
             wts[(size_t)t * k + lane] = wt;
@@ -247,7 +247,7 @@ template <int VPL, int MT>
 __global__ __launch_bounds__(256) void route_permute_whole(const uint16_t* __restrict__ x, int m, int H,
                                                            const float* __restrict__ wr, int E,
                                                            float* __restrict__ logits, int k,
-                                                           const float* __restrict__ bias, int32_t* __restrict__ ids,
+                                                           const float* __restrict__ bias, RouteMode rm, int32_t* __restrict__ ids,
                                                            float* __restrict__ wts, int has_shared, PermuteOut o,
                                                            WsHeader* hdr, uint8_t* __restrict__ xq,
                                                            float* __restrict__ xsc) {
@@ -305,14 +305,14 @@ __global__ __launch_bounds__(256) void route_permute_whole(const uint16_t* __res
         __syncthreads();  // red is reused by the next pass
     }
     if (!last_block(hdr, &is_last)) return;
-    route_tail<VPL>(logits, 1, m, E, k, bias, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
+    route_tail<VPL>(logits, 1, m, E, k, bias, rm, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
 }
 
 template <int VPL>
 __global__ __launch_bounds__(256) void route_permute_sliced(const uint16_t* __restrict__ x, int m, int H,
                                                             const float* __restrict__ wr, int E, int HS,
                                                             float* __restrict__ part, int k,
-                                                            const float* __restrict__ bias, int32_t* __restrict__ ids,
+                                                            const float* __restrict__ bias, RouteMode rm, int32_t* __restrict__ ids,
                                                             float* __restrict__ wts, int has_shared, PermuteOut o,
                                                             WsHeader* hdr, uint8_t* __restrict__ xq,
                                                             float* __restrict__ xsc) {
@@ -356,7 +356,7 @@ __global__ __launch_bounds__(256) void route_permute_sliced(const uint16_t* __re
         }
     }
     if (!last_block(hdr, &is_last)) return;
-    route_tail<VPL>(part, gridDim.y, m, E, k, bias, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
+    route_tail<VPL>(part, gridDim.y, m, E, k, bias, rm, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -390,39 +390,39 @@ bool route_permute_fusable(int m, int k, int E) {
 
 template <int VPL>
 static void launch_rps(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S, int k,
-                       const float* bias, int32_t* ids, float* w, int has_shared, const PermuteOut& o, WsHeader* hdr,
-                       uint8_t* xq, float* xsc, cudaStream_t st) {
+                       const float* bias, RouteMode rm, int32_t* ids, float* w, int has_shared, const PermuteOut& o,
+                       WsHeader* hdr, uint8_t* xq, float* xsc, cudaStream_t st) {
     const dim3 whole(ceil_div(E, kWholeEB));
     if (m <= 1)
-        launch_pdl(route_permute_whole<VPL, 1>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, ids, w, has_shared, o, hdr, xq, xsc);
+        launch_pdl(route_permute_whole<VPL, 1>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc);
     else if (m <= 4)
-        launch_pdl(route_permute_whole<VPL, 4>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, ids, w, has_shared, o, hdr, xq, xsc);
+        launch_pdl(route_permute_whole<VPL, 4>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc);
     else
-        launch_pdl(route_permute_sliced<VPL>, dim3(ceil_div(E, 8), S), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, ids, w, has_shared, o, hdr, xq, xsc);
+        launch_pdl(route_permute_sliced<VPL>, dim3(ceil_div(E, 8), S), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc);
 }
 
 cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const float* wr, int E, float* part, int S,
-                                       int k, const float* bias, int32_t* ids, float* w, int has_shared,
+                                       int k, const float* bias, RouteMode rm, int32_t* ids, float* w, int has_shared,
                                        const PermuteOut& o, WsHeader* hdr, uint8_t* xq, float* xsc,
                                        cudaStream_t st) {
     const int vpl = ceil_div(E, 32);
-    if (vpl <= 1) launch_rps<1>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, xq, xsc, st);
-    else if (vpl <= 2) launch_rps<2>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, xq, xsc, st);
-    else if (vpl <= 4) launch_rps<4>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, xq, xsc, st);
-    else launch_rps<8>(x, m, H, wr, E, part, S, k, bias, ids, w, has_shared, o, hdr, xq, xsc, st);
+    if (vpl <= 1) launch_rps<1>(x, m, H, wr, E, part, S, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc, st);
+    else if (vpl <= 2) launch_rps<2>(x, m, H, wr, E, part, S, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc, st);
+    else if (vpl <= 4) launch_rps<4>(x, m, H, wr, E, part, S, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc, st);
+    else launch_rps<8>(x, m, H, wr, E, part, S, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc, st);
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const float* bias, float* logits_out,
+cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const float* bias, RouteMode rm, float* logits_out,
                         int32_t* ids, float* w, cudaStream_t st) {
     const int vpl = ceil_div(E, 32);
     dim3 grid(ceil_div(m, 8));
-    if (vpl <= 1) launch_pdl(topk_softmax<1>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
-    else if (vpl <= 2) launch_pdl(topk_softmax<2>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
-    else if (vpl <= 4) launch_pdl(topk_softmax<4>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
-    else if (vpl <= 8) launch_pdl(topk_softmax<8>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
-    else if (vpl <= 16) launch_pdl(topk_softmax<16>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
-    else launch_pdl(topk_softmax<32>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, logits_out, ids, w);
+    if (vpl <= 1) launch_pdl(topk_softmax<1>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, rm, logits_out, ids, w);
+    else if (vpl <= 2) launch_pdl(topk_softmax<2>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, rm, logits_out, ids, w);
+    else if (vpl <= 4) launch_pdl(topk_softmax<4>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, rm, logits_out, ids, w);
+    else if (vpl <= 8) launch_pdl(topk_softmax<8>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, rm, logits_out, ids, w);
+    else if (vpl <= 16) launch_pdl(topk_softmax<16>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, rm, logits_out, ids, w);
+    else launch_pdl(topk_softmax<32>, dim3(grid), dim3(256), 0, st, part, S, m, E, k, bias, rm, logits_out, ids, w);
     return cudaGetLastError();
 }
 

@@ -85,21 +85,27 @@ __device__ __forceinline__ float from_key(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Top-k softmax of token t by one warp ("2. Batched topK dispatch", softmax
-// with norm_topk_prob): logits = sum of the S partial slices in slice order
-// (+ bias); k picks, each the largest remaining logit with ties to the lowest
-// expert index -- one warp-wide max of the order keys and one min of the
-// indices holding it per pick (redux.sync); weights = softmax over the k
-// picks.  Lane j < k returns pick j in (*id, *wt).  LDCG: read the partials
-// through L2 (they were written by other blocks of the same launch).
+// Top-k of token t by one warp ("2. Batched topK dispatch"): logits = the S
+// partial slices summed in slice order.
+//   softmax (rm.sigmoid == 0, norm_topk_prob): the bias is added to the
+//     logits; the k picks are the largest logits; weights = softmax over them.
+//   sigmoid (the correction-bias branch): s = sigmoid(L) in fp32; the picks
+//     are the largest s + bias; weights = the picked s (pre-bias), divided by
+//     their sum when rm.norm, times rm.scale.
+// Each pick is the largest remaining key with ties to the lowest expert index
+// -- one warp-wide max of the order keys and one min of the indices holding
+// it (redux.sync).  Lane j < k returns pick j in (*id, *wt).  LDCG: read the
+// partials through L2 (they were written by other blocks of the same launch).
 template <int VPL, bool LDCG>
-__device__ __forceinline__ void warp_topk_softmax(const float* part, int S, int m, int E, int k, const float* bias,
-                                                  float* logits_out, int t, int lane, int* id, float* wt) {
+__device__ __forceinline__ void warp_topk(const float* part, int S, int m, int E, int k, const float* bias,
+                                          RouteMode rm, float* logits_out, int t, int lane, int* id, float* wt) {
     uint32_t key[VPL];  // 0 = not a candidate (outside [0, E), or already picked)
+    float val[VPL];     // softmax: the logit; sigmoid: the pre-bias score
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
         key[i] = 0u;
+        val[i] = 0.f;
         if (e < E) {
             float a = 0.f;
 #pragma unroll 8
@@ -107,41 +113,57 @@ __device__ __forceinline__ void warp_topk_softmax(const float* part, int S, int 
                 const float* src = part + ((size_t)s * m + t) * E + e;
                 a += LDCG ? __ldcg(src) : *src;
             }
-            if (bias) a += bias[e];
-            key[i] = order_key(a);
+            if (!rm.sigmoid) {
+                if (bias) a += bias[e];
+                val[i] = a;
+                key[i] = order_key(a);
+            } else {
+                const float sc = 1.0f / (1.0f + expf(-a));
+                val[i] = sc;
+                key[i] = order_key(bias ? sc + bias[e] : sc);
+            }
             if (logits_out) logits_out[(size_t)t * E + e] = a;
         }
     }
-    float my_l = 0.f;
+    float my_v = 0.f;
     int my_id = 0;
     for (int j = 0; j < k; ++j) {
         uint32_t bk = 0u;  // this lane's largest key, lowest i among equals
         int bi = 0;
+        float bv = val[0];
 #pragma unroll
         for (int i = 0; i < VPL; ++i)
             if (key[i] > bk) {
                 bk = key[i];
                 bi = i;
+                bv = val[i];
             }
         const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
         const uint32_t ge = __reduce_min_sync(0xffffffffu, bk == gk ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+        const float v = __shfl_sync(0xffffffffu, bv, (int)(ge & 31u));  // the owner's local best is the pick
         if ((int)(ge & 31u) == lane) {
 #pragma unroll
             for (int i = 0; i < VPL; ++i)
                 if (i == (int)(ge >> 5)) key[i] = 0u;
         }
         if (lane == j) {
-            my_l = from_key(gk);
+            my_v = v;
             my_id = (int)ge;
         }
     }
-    const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
-    const float ex = lane < k ? expf(my_l - l0) : 0.f;
-    float den = ex;
+    float num, den;
+    if (!rm.sigmoid) {
+        const float l0 = __shfl_sync(0xffffffffu, my_v, 0);
+        num = lane < k ? expf(my_v - l0) : 0.f;
+    } else {
+        num = lane < k ? my_v : 0.f;
+    }
+    den = num;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     *id = my_id;
-    *wt = ex / den;
+    if (!rm.sigmoid) *wt = num / den;
+    else *wt = (rm.norm ? num / den : num) * rm.scale;
 }
 
 // Stable counting sort of P <= kPermChunk pairs (ids in shared memory, all in

@@ -47,6 +47,19 @@ def check_ids(gpu_ids, ref_ids, ref_logits, margin=INDEX_MARGIN):
     return swapped, bad
 
 
+def selection_keys(shape, logits, bias):
+    """What the top-k ranks, as the oracle forms it: the logits (softmax
+    scoring, bias already inside) or fp32 sigmoid(L) + bias (sigmoid scoring),
+    for check_ids' margin rule."""
+    L = np.asarray(logits, np.float32)
+    if getattr(shape, "scoring", "softmax") != "sigmoid":
+        return L
+    s = (np.float32(1.0) / (np.float32(1.0) + np.exp(-L))).astype(np.float32)
+    if bias is not None:
+        s = s + np.asarray(bias.cpu() if isinstance(bias, torch.Tensor) else bias, np.float32)
+    return s
+
+
 def compact_experts(shape, layer, expert_ids):
     """CPU copies of only the listed experts (stacked in the listed order)."""
     idx = torch.as_tensor(sorted(set(int(e) for e in expert_ids)), dtype=torch.long)
@@ -55,7 +68,7 @@ def compact_experts(shape, layer, expert_ids):
     for n in ("w1", "w3", "w2", "s1", "s3", "s2"):
         if n in layer and layer[n] is not None:
             sub[n] = layer[n].index_select(0, idx.to(dev)).cpu()
-    for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2"):
+    for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2", "shared_gate"):
         if n in layer and layer[n] is not None:
             sub[n] = layer[n].cpu()
     remap = {int(e): i for i, e in enumerate(idx.tolist())}

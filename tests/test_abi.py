@@ -68,6 +68,10 @@ def _weights(fp8=False):
     (dict(shared_inter=256), 2),        # shared expert of another width
     (dict(weights=1, inter=384), 2),    # fp8 needs I % 512 == 0
     (dict(weights=1, inter=512, hidden=384), 2),  # ... and H % 512 == 0
+    (dict(scoring=2), 1),                          # no such scoring
+    (dict(scoring=1, routed_scaling_factor=0.0), 1),  # sigmoid scoring needs a positive scaling factor
+    (dict(scoring=1, routed_scaling_factor=float("inf")), 1),
+    (dict(scoring=1, routed_scaling_factor=2.5, norm_topk_prob=3), 1),
 ])
 def test_create_rejects_unsupported_shapes(lib, kw, want):
     from mixture_experts_ffn_gemv_gb300.binding import MoeExpertWeights
@@ -91,6 +95,19 @@ def test_create_rejects_null_and_misaligned(lib):
     missing_scales = _weights(fp8=False)
     cfg8 = _cfg(weights=1, inter=512, hidden=512)
     assert lib.moe_layer_create(ctypes.byref(cfg8), ctypes.byref(missing_scales), None, ctypes.byref(out)) == 1
+
+
+def test_gate_only_on_the_shared_expert(lib):
+    from mixture_experts_ffn_gemv_gb300.binding import MoeExpertWeights
+    out = ctypes.c_void_p()
+    cfg = _cfg()
+    gated_routed = MoeExpertWeights(0x10000, 0x10000, 0x10000, None, None, None, 0x10000)
+    assert lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(gated_routed), None, ctypes.byref(out)) == 1
+    cfg_s = _cfg(shared_inter=128)
+    misaligned_gate = MoeExpertWeights(0x10000, 0x10000, 0x10000, None, None, None, 0x10004)
+    assert lib.moe_layer_create(ctypes.byref(cfg_s), ctypes.byref(_weights()), ctypes.byref(misaligned_gate),
+                                ctypes.byref(out)) == 1
+    assert not out.value
 
 
 def test_null_layer_calls_are_rejected(lib):

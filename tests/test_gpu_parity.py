@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from mixture_experts_ffn_gemv_gb300 import inputs as I
-from _parity import TOL, check_ids, oracle_rows, rel_l2, to_np
+from _parity import TOL, check_ids, oracle_rows, rel_l2, selection_keys, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -138,6 +138,57 @@ def test_route_parity(cuda, oracle_mod, wl_name, m):
     assert len(swapped) <= max(2, m // 200)
 
 
+@pytest.mark.parametrize("m", [1, 16, 100, 512])
+def test_route_parity_sigmoid_correction_bias(cuda, oracle_mod, m):
+    """The sigmoid + correction-bias router (DeepSeek-V3 shape, routed scaling
+    2.5): raw logits, ids by score + bias (margin rule on those keys), weights
+    the renormalised pre-bias scores times 2.5.  m = 1, 16 take the fused
+    decode kernel, 100 and 512 the router + top-k kernels."""
+    wl = I.WORKLOADS["deepseek_v3_sigmoid"]
+    shape = wl.shape
+    x = I.make_x(shape, m, seed=91, device=cuda)
+    wr, bias = I.make_router(shape, seed=91, device=cuda, correction_std=wl.correction_std)
+    from mixture_experts_ffn_gemv_gb300 import binding
+    small = dataclasses.replace(shape, inter=512, shared_inter=0)  # only the router matters here
+    zeros = {"w1": torch.zeros(shape.num_experts, 512, shape.hidden, dtype=torch.uint8, device=cuda),
+             "w3": torch.zeros(shape.num_experts, 512, shape.hidden, dtype=torch.uint8, device=cuda),
+             "w2": torch.zeros(shape.num_experts, shape.hidden, 512, dtype=torch.uint8, device=cuda)}
+    for n, (r, c) in (("s1", (4, shape.hidden // 128)), ("s3", (4, shape.hidden // 128)), ("s2", (shape.hidden // 128, 4))):
+        zeros[n] = torch.ones(shape.num_experts, r, c, dtype=torch.float32, device=cuda)
+    layer = binding.MoeLayer(small, zeros)
+    ids, w, logits = layer.moe_route(x, wr, bias, logits=True)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    L, r_ids, r_w, _ = oracle_mod.route(small, {"router_w": wr.cpu(), "router_bias": bias.cpu()}, x.cpu())
+    assert np.abs(to_np(logits) - L).max() <= 1e-5 * max(np.abs(L).max(), 1.0)  # no bias in the logits
+    swapped, bad = check_ids(to_np(ids), r_ids, selection_keys(small, L, bias))
+    assert not bad, bad[:5]
+    same = np.ones(m, bool)
+    same[swapped] = False
+    assert np.abs(to_np(w)[same] - r_w[same]).max() < 2e-5 * shape.routed_scaling
+    assert np.abs(to_np(w).astype(np.float64).sum(1) - shape.routed_scaling).max() < 1e-5 * shape.routed_scaling
+
+
+@pytest.mark.parametrize("arm", ["gemv", "gemm"])
+@pytest.mark.parametrize("m", [5, 16, 300])
+def test_whole_layer_gated_shared_expert(cuda, oracle_mod, arm, m):
+    """The shared expert blended through its sigmoid gate (forward_prefill step
+    8), through moe_forward on both arms, against the oracle."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    shape = I.GATED_SHARED
+    tensors, x = _small_case(shape, m, seed=93, device=cuda)
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
+    ref = oracle_mod.reference(shape, host, x.cpu())
+    layer = binding.MoeLayer(shape, tensors)
+    out, ids, w = layer.moe_forward(x, tensors["router_w"], arm=arm, return_routing=True)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    swapped, bad = check_ids(to_np(ids), ref["ids"], ref["logits"])
+    assert not bad, bad[:5]
+    keep = np.array([r for r in range(m) if r not in set(swapped)])
+    assert rel_l2(to_np(out)[keep], ref["out"][keep]) < TOL[False]
+
+
 @pytest.mark.parametrize("shape,m", [(I.TINY, 300), (ODD_E, 500), (MEDIUM_BF16, 129)])
 def test_route_tensor_core_path_odd_shapes(cuda, oracle_mod, shape, m):
     """m > 64 takes the tensor-core router (bf16 x3 split of the fp32 weight);
@@ -236,7 +287,8 @@ def test_route_and_permute_at_the_largest_expert_count(cuda, oracle_mod, m):
 
 FULL_CASES = [("tiny", 16)] + [("qwen3_decode", m) for m in (1, 4, 16, 64)] + \
              [("qwen3_prefill", m) for m in (512, 4096, 16384)] + \
-             [("deepseek_v3_fp8", m) for m in (1, 16, 4096)] + [("qwen3_zipf", 8192)]
+             [("deepseek_v3_fp8", m) for m in (1, 16, 4096)] + [("qwen3_zipf", 8192)] + \
+             [("deepseek_v3_sigmoid", m) for m in (1, 16, 512)] + [("gated_shared", m) for m in (16, 512)]
 
 
 @pytest.mark.parametrize("wl_name,m", FULL_CASES)
@@ -254,7 +306,7 @@ def test_forward_full_size(cuda, oracle_mod, wl_name, m):
     torch.cuda.synchronize()
     assert layer.device_status() == 0
     L, r_ids, r_w, margin = oracle_route(oracle_mod, wl.shape, tensors, x)
-    swapped, bad = check_ids(to_np(ids), r_ids, L)
+    swapped, bad = check_ids(to_np(ids), r_ids, selection_keys(wl.shape, L, tensors["router_bias"]))
     assert not bad, bad[:5]
     rows = np.array([r for r in sample_rows(m) if r not in set(swapped)])
     ref = oracle_rows(oracle_mod, wl.shape, tensors, x, r_ids, r_w, rows)
