@@ -373,7 +373,8 @@ def sweep(device, steps, warmup):
     bw = pk["hbm_gbs"] * 1e9
     tc = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1e12
     res = []
-    for name in ("qwen3_decode", "qwen3_prefill", "deepseek_v3_fp8", "qwen3_zipf"):
+    for name in ("qwen3_decode", "qwen3_prefill", "deepseek_v3_fp8", "qwen3_zipf", "deepseek_v3_sigmoid",
+                 "gated_shared"):
         wl = I.WORKLOADS[name]
         for m in wl.ms:
             try:

@@ -74,6 +74,7 @@ def _lib(fp64: bool = False):
             lib.oracle_topk_sigmoid.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _C.c_int, _C.c_float,
                                                 _vp, _vp, _vp]
             lib.oracle_permute.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _vp, _vp]
+            lib.oracle_residual_rmsnorm.argtypes = [_vp, _i64, _C.c_int, _vp, _vp, _C.c_float, _vp]
             lib.oracle_moe_forward.argtypes = [ctypes.POINTER(_Layer), _vp, _i64, _vp, _i64, _vp, _vp, _vp]
             lib.oracle_moe_forward.restype = _C.c_int
             lib.oracle_set_threads.argtypes = [_C.c_int]
@@ -229,6 +230,18 @@ def moe_forward(shape, layer, x, ids, w, rows=None, fp64: bool = False) -> np.nd
     if rc != 0:
         raise ValueError("oracle_moe_forward: token row or expert id out of range")
     return out
+
+
+def residual_rmsnorm(moe_out, residual, weight, eps: float, fp64: bool = False):
+    """Layer tail: -> (new residual bf16 as uint16 [m,H], norm_out uint16 [m,H])."""
+    o = _np(moe_out, np.float32)
+    r = _np(residual).copy()
+    assert r.dtype == np.uint16, "residual must be bf16"
+    wv = _np(weight, np.float32)
+    m, H = o.shape
+    out = np.empty((m, H), np.uint16)
+    _lib(fp64).oracle_residual_rmsnorm(_ptr(o), m, H, _ptr(r), _ptr(wv), float(eps), _ptr(out))
+    return r, out
 
 
 def route(shape, layer, x, fp64: bool = False):

@@ -419,6 +419,44 @@ EXPORT int oracle_moe_forward(const oracle_layer* Lr, const uint16_t* x, int64_t
     return bad ? -1 : 0;
 }
 
+/* bf16 bits of a float, round to nearest even (NaN kept quiet). */
+static uint16_t float_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/*
+ * The layer tail folded into the combine (ferrum qwen3_moe/forward_layer.rs,
+ * "weighted_sum_residual_norm": the weighted sum is written into the residual
+ * stream and the next layer's rms_norm is taken of the result):
+ *   residual[t,h] <- bf16(residual[t,h] + moe_out[t,h])
+ *   r = the new residual's values; inv = 1 / sqrt(sum_h r^2 / H + eps)
+ *   norm_out[t,h] = bf16(r[h] * inv * w[h])
+ * moe_out fp32 [m,H] (the layer output before its bf16 rounding); residual and
+ * norm_out bf16 bits [m,H]; w fp32 [H].  The sum of squares runs in acc_t in
+ * ascending h, inv in double.
+ */
+EXPORT void oracle_residual_rmsnorm(const float* moe_out, int64_t m, int H, uint16_t* residual, const float* w,
+                                    float eps, uint16_t* norm_out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < m; ++t) {
+        uint16_t* rt = residual + t * (int64_t)H;
+        const float* ot = moe_out + t * (int64_t)H;
+        acc_t ss = 0;
+        for (int h = 0; h < H; ++h) {
+            rt[h] = float_to_bf16(bf16_to_float(rt[h]) + ot[h]);
+            const acc_t r = (acc_t)bf16_to_float(rt[h]);
+            ss += r * r;
+        }
+        const double inv = 1.0 / sqrt((double)ss / (double)H + (double)eps);
+        for (int h = 0; h < H; ++h)
+            norm_out[t * (int64_t)H + h] = float_to_bf16((float)((double)bf16_to_float(rt[h]) * inv * (double)w[h]));
+    }
+}
+
 /* Threads the OpenMP loops use (0 leaves the runtime default). */
 EXPORT int oracle_set_threads(int n) {
 #ifdef _OPENMP

@@ -21,6 +21,9 @@
                           scale/k or scale/2), a bias that forces the selection.
   * gated shared      -> torch float64: routed sum + sigmoid(x . gate) times the
                           dense SwiGLU of the shared expert; a zero gate halves it.
+  * residual + norm   -> torch: the new residual bit for bit ((res + out) cast to
+                          bf16); the norm against a float64 RMSNorm of it; closed
+                          forms (a constant row normalises to sign * w at eps 0).
   * structure         -> token independence, expert relabelling invariance,
                           float vs double oracle builds agree to ~1e-6.
 """
@@ -251,6 +254,34 @@ def test_gated_shared_expert_matches_torch(oracle_mod):
     layer["shared_gate"] = torch.zeros(256)  # sigmoid(0) = 1/2
     half = oracle_mod.moe_forward(shape, layer, x, ids, w, fp64=True)
     assert np.linalg.norm(half - (routed + 0.5 * shared).numpy()) / np.linalg.norm(ref) < 1e-7
+
+
+def test_residual_rmsnorm_matches_torch(oracle_mod):
+    g = torch.Generator().manual_seed(17)
+    m, H, eps = 9, 384, 1e-6
+    res = torch.randn(m, H, generator=g).to(torch.bfloat16)
+    out = torch.randn(m, H, generator=g) * 0.3
+    w = torch.randn(H, generator=g) * 0.5 + 1.0
+    r_new, normed = oracle_mod.residual_rmsnorm(out, res, w, eps, fp64=True)
+    ref_r = (res.float() + out).to(torch.bfloat16)
+    assert np.array_equal(r_new, ref_r.view(torch.int16).numpy().view(np.uint16))  # exact
+    r64 = ref_r.double()
+    ref_n = (r64 * torch.rsqrt((r64 * r64).mean(1, keepdim=True) + eps) * w.double()).float()
+    got = torch.from_numpy(normed.view(np.int16)).view(torch.bfloat16).float()
+    # both round the same float64 value to bf16: equal but for a rare last-bit tie
+    rel = ((got - ref_n).abs() / ref_n.abs().clamp_min(1e-30)).max().item()
+    assert rel <= 2.0 ** -8
+    assert (got != ref_n.to(torch.bfloat16).float()).float().mean().item() < 0.01
+
+
+def test_residual_rmsnorm_closed_forms(oracle_mod):
+    H = 256
+    for c in (0.5, -3.0, 1e-3):
+        res = torch.full((2, H), c).to(torch.bfloat16)
+        r_new, normed = oracle_mod.residual_rmsnorm(np.zeros((2, H), np.float32), res, np.ones(H, np.float32), 0.0)
+        got = torch.from_numpy(normed.view(np.int16)).view(torch.bfloat16).float()
+        assert torch.all(got == math.copysign(1.0, c))  # c / |c| * 1
+        assert np.array_equal(r_new, res.view(torch.int16).numpy().view(np.uint16))  # + 0 leaves it alone
 
 
 def test_permute_matches_stable_argsort(oracle_mod):
