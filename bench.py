@@ -415,6 +415,47 @@ def sweep(device, steps, warmup):
     return res
 
 
+def tail_timing(reps, n, device, eps=1e-6):
+    """The layer tail (residual add + the next layer's RMSNorm) folded into the
+    combine (moe_forward_residual_rmsnorm) against moe_forward followed by the
+    same add and norm as separate torch ops; us per step, same replicas."""
+    H = reps[0]["layer"].shape.hidden
+    m = reps[0]["x"].shape[0]
+    g = torch.Generator(device=device).manual_seed(5)
+    norm_w = (torch.randn(H, generator=g, device=device) * 0.2 + 1.0).contiguous()
+    residual = torch.randn(m, H, generator=g, device=device).to(torch.bfloat16)
+    normed = torch.empty(m, H, dtype=torch.bfloat16, device=device)
+
+    def fused(i):
+        r = reps[i % len(reps)]
+        t = r["tensors"]
+        r["layer"].moe_forward_residual_rmsnorm(r["x"], t["router_w"], residual, norm_w, eps, t["router_bias"],
+                                                norm_out=normed)
+
+    def unfused(i):
+        r = reps[i % len(reps)]
+        t = r["tensors"]
+        out = r["layer"].moe_forward(r["x"], t["router_w"], t["router_bias"], out=r["out"])
+        residual.copy_((residual.float() + out.float()).to(torch.bfloat16))
+        rf = residual.float()
+        normed.copy_((rf * torch.rsqrt(rf.pow(2).mean(1, keepdim=True) + eps) * norm_w).to(torch.bfloat16))
+
+    res = {}
+    for name, fn in (("fused_us", fused), ("unfused_us", unfused)):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize(device)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(n):
+            fn(i)
+        b.record()
+        torch.cuda.synchronize(device)
+        res[name] = a.elapsed_time(b) * 1e3 / n
+    return res
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     dist = init_dist(ws)
@@ -482,6 +523,9 @@ def run_ours(args):
     }
     if rank == 0 and ws == 1:
         line["cpu_baseline"] = cpu_baseline(wl, m, (host_copy(reps[0]["tensors"]), reps[0]["x"].cpu()))
+        if not args.no_sweep:
+            line["layer_tail"] = dict(tail_timing(reps, args.steps, device), workload=args.workload, m=m,
+                                      what="residual add + next RMSNorm: fused into the combine vs separate ops")
         if not args.no_sweep:
             reps = None
             torch.cuda.empty_cache()

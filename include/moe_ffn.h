@@ -192,6 +192,22 @@ MOE_API int moe_forward(const moe_layer* layer, const void* x, int64_t m, const 
                 const float* router_bias, void* out, int32_t* topk_ids_out, float* topk_w_out,
                 int arm, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The whole layer with the layer tail folded into its combine (ferrum
+ * qwen3_moe/forward_layer.rs: weighted_sum_residual_norm writes the weighted
+ * sum into the residual stream and takes the next layer's rms_norm of the
+ * result).  In place of out:
+ *   residual[t,h] <- bf16(residual[t,h] + moe_out[t,h])   (moe_out: the layer
+ *                    output in fp32, before moe_forward would round it)
+ *   norm_out[t,h]  = bf16(r[t,h] / sqrt(sum_h r[t,h]^2 / H + eps) * norm_w[h]),
+ *                    r = the new residual's values
+ *   residual bf16 [m, H], in/out, aliasing neither x nor norm_out;
+ *   norm_w fp32 [H]; norm_out bf16 [m, H]; eps >= 0; H <= 24576.
+ * Everything else (routing outputs, arm, workspace, stream) as moe_forward. */
+MOE_API int moe_forward_residual_rmsnorm(const moe_layer* layer, const void* x, int64_t m, const float* router_w,
+                const float* router_bias, void* residual, const float* norm_w, float eps, void* norm_out,
+                int32_t* topk_ids_out, float* topk_w_out, int arm, void* workspace, size_t workspace_bytes,
+                void* stream);
+
 /* Activation quantisation of the fp8 layers (the expert input and the down
  * projection's input): per row, per block of 128 contiguous elements,
  * s = amax / 448 (IEEE fp32 divide), code = e4m3(x / s) rounded to nearest

@@ -23,7 +23,8 @@ ARMS = {"auto": MOE_ARM_AUTO, "gemv": MOE_ARM_GEMV, "gemm": MOE_ARM_GEMM}
 
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_workspace_size", "moe_select_arm", "moe_route",
-    "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_forward", "moe_act_quant_fp8", "moe_device_status",
+    "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_forward", "moe_forward_residual_rmsnorm",
+    "moe_act_quant_fp8", "moe_device_status",
     "moe_last_launch_count", "moe_kernel_timing_enable", "moe_kernel_timing_read", "moe_kernel_count",
     "moe_kernel_name", "moe_status_string",
 )
@@ -73,6 +74,8 @@ def load_library(path: str | None = None, build: bool = True):
         lib.moe_permute_noalloc.argtypes = [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp]
         lib.moe_experts.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         lib.moe_forward.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+        lib.moe_forward_residual_rmsnorm.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
+                                                     _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         lib.moe_act_quant_fp8.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp]
         lib.moe_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
         lib.moe_last_launch_count.argtypes = [_vp]
@@ -251,3 +254,22 @@ class MoeLayer:
         _check(self.lib.moe_forward(self.handle, _p(x), m, _p(router_w), _p(router_bias), _p(out), _p(ids), _p(w),
                                     ARMS[arm], _p(ws), ws.numel(), _stream(stream)), "moe_forward")
         return (out, ids, w) if return_routing else out
+
+    def moe_forward_residual_rmsnorm(self, x, router_w, residual, norm_w, eps=1e-6, router_bias=None, arm="auto",
+                                     norm_out=None, return_routing=False, stream=None):
+        """The layer with its tail: residual (bf16 [m, H], updated in place) +=
+        the layer output, and norm_out = RMSNorm(residual) * norm_w (fp32 [H])."""
+        m = x.shape[0]
+        dev = x.device
+        if norm_out is None:
+            norm_out = torch.empty(m, self.shape.hidden, dtype=torch.bfloat16, device=dev)
+        ids = w = None
+        if return_routing:
+            ids = torch.empty(m, self.shape.top_k, dtype=torch.int32, device=dev)
+            w = torch.empty(m, self.shape.top_k, dtype=torch.float32, device=dev)
+        ws = self.workspace(m)
+        _check(self.lib.moe_forward_residual_rmsnorm(self.handle, _p(x), m, _p(router_w), _p(router_bias),
+                                                     _p(residual), _p(norm_w), float(eps), _p(norm_out), _p(ids),
+                                                     _p(w), ARMS[arm], _p(ws), ws.numel(), _stream(stream)),
+               "moe_forward_residual_rmsnorm")
+        return (norm_out, ids, w) if return_routing else norm_out

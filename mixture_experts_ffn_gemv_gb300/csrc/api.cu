@@ -232,7 +232,8 @@ PermuteOut permute_out(const Layout& lo, void* ws, int32_t* sorted_pair, int32_t
 // permuted: the permute tables are already in the workspace; x_quantized: so
 // are the fp8 codes and scales of x (both written by the fused decode routing)
 int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, const int32_t* ids, const float* w,
-                void* out, int arm, void* ws, Launcher& ln, bool permuted = false, bool x_quantized = false) {
+                void* out, int arm, void* ws, Launcher& ln, bool permuted = false, bool x_quantized = false,
+                const TailArgs* tail = nullptr) {
     const moe_config& c = L->cfg;
     const cudaStream_t st = ln.st;
     const int E = c.num_experts, k = c.top_k, H = c.hidden, I = c.inter;
@@ -285,8 +286,11 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
             MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_bf16(a, static_cast<const uint16_t*>(x), h, st));
             MOE_LAUNCH(K_GEMV_DOWN, launch_gemv_down_bf16(a, h, y, st));
         }
-        MOE_LAUNCH(K_COMBINE, launch_combine_f32(y, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, static_cast<uint16_t*>(out),
-                                      st));
+        if (tail)
+            MOE_LAUNCH(K_COMBINE, launch_combine_tail_f32(y, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, *tail, st));
+        else
+            MOE_LAUNCH(K_COMBINE, launch_combine_f32(y, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg,
+                                                     static_cast<uint16_t*>(out), st));
         return MOE_OK;
     }
     if (arm != MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
@@ -326,9 +330,52 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     if (rc != MOE_OK) return rc;
     MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(gl, st));
     MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(gl, st));
-    MOE_LAUNCH(K_COMBINE, launch_combine_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, static_cast<uint16_t*>(out),
-                                   st));
+    if (tail)
+        MOE_LAUNCH(K_COMBINE, launch_combine_tail_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, *tail, st));
+    else
+        MOE_LAUNCH(K_COMBINE, launch_combine_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg,
+                                                  static_cast<uint16_t*>(out), st));
     return MOE_OK;
+}
+
+// moe_forward and moe_forward_residual_rmsnorm (tail != null: the combine
+// writes the residual and the norm instead of out)
+int forward_impl(const moe_layer* layer, const void* x, int64_t m, const float* router_w, const float* router_bias,
+                 void* out, int32_t* topk_ids_out, float* topk_w_out, int arm, void* workspace,
+                 size_t workspace_bytes, void* stream, const TailArgs* tail) {
+    Layout lo;
+    int rc = check_call(layer, m, workspace, workspace_bytes, &lo);
+    if (rc != MOE_OK || m == 0) return rc;
+    if (!x || !router_w || !aligned(x, 16) || !aligned(router_w, 16)) return MOE_ERR_INVALID_ARG;
+    if (!tail && (!out || !aligned(out, 16))) return MOE_ERR_INVALID_ARG;
+    if (arm < MOE_ARM_AUTO || arm > MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, lo.ids);
+    float* w = topk_w_out ? topk_w_out : at<float>(workspace, lo.w);
+    Launcher ln{layer, st};
+    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
+    const moe_config& c = layer->cfg;
+    if (!lo.router_tc && route_permute_fusable((int)m, c.top_k, c.num_experts)) {
+        // decode: router, top-k and the permute in one launch.  For fp8 layers
+        // with m > 4 the same launch also quantises x; at m <= 4 the separate
+        // quantiser launch measured faster (DeepSeek-V3 shape, m = 1: 105 vs
+        // 133 us per layer step).
+        const PermuteOut po = permute_out(lo, workspace, nullptr, nullptr, nullptr);
+        const bool fuse_q = layer->fp8 && m > 4;
+        MOE_LAUNCH(K_ROUTE_PERMUTE,
+                   launch_route_permute_small(static_cast<const uint16_t*>(x), (int)m, c.hidden, router_w,
+                                              c.num_experts, at<float>(workspace, lo.part), lo.S, c.top_k, router_bias,
+                                              layer->rm,
+                                              ids, w, layer->has_shared ? 1 : 0, po, at<WsHeader>(workspace, lo.hdr),
+                                              fuse_q ? at<uint8_t>(workspace, lo.xq) : nullptr,
+                                              fuse_q ? at<float>(workspace, lo.xsc) : nullptr, st));
+        rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln, true, fuse_q, tail);
+    } else {
+        rc = run_route(layer, lo, x, (int)m, router_w, router_bias, nullptr, ids, w, workspace, ln);
+        if (rc == MOE_OK) rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln, false, false, tail);
+    }
+    layer->last_launches = ln.n;
+    return rc;
 }
 
 bool weights_ok(const moe_expert_weights* w, bool fp8) {
@@ -457,42 +504,27 @@ int moe_experts(const moe_layer* layer, const void* x, int64_t m, const int32_t*
     return rc;
 }
 
+
 int moe_forward(const moe_layer* layer, const void* x, int64_t m, const float* router_w, const float* router_bias,
                 void* out, int32_t* topk_ids_out, float* topk_w_out, int arm, void* workspace, size_t workspace_bytes,
                 void* stream) {
-    Layout lo;
-    int rc = check_call(layer, m, workspace, workspace_bytes, &lo);
-    if (rc != MOE_OK || m == 0) return rc;
-    if (!x || !router_w || !out || !aligned(x, 16) || !aligned(out, 16) || !aligned(router_w, 16))
+    return forward_impl(layer, x, m, router_w, router_bias, out, topk_ids_out, topk_w_out, arm, workspace,
+                        workspace_bytes, stream, nullptr);
+}
+
+int moe_forward_residual_rmsnorm(const moe_layer* layer, const void* x, int64_t m, const float* router_w,
+                                 const float* router_bias, void* residual, const float* norm_w, float eps,
+                                 void* norm_out, int32_t* topk_ids_out, float* topk_w_out, int arm, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    if (!layer) return MOE_ERR_INVALID_ARG;
+    if (layer->cfg.hidden > kTailMaxH) return MOE_ERR_UNSUPPORTED;
+    if (m > 0 && (!residual || !norm_w || !norm_out || !aligned(residual, 16) || !aligned(norm_w, 16) ||
+                  !aligned(norm_out, 16) || residual == norm_out || residual == x || !(eps >= 0.f) ||
+                  !std::isfinite(eps)))
         return MOE_ERR_INVALID_ARG;
-    if (arm < MOE_ARM_AUTO || arm > MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, lo.ids);
-    float* w = topk_w_out ? topk_w_out : at<float>(workspace, lo.w);
-    Launcher ln{layer, st};
-    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
-    const moe_config& c = layer->cfg;
-    if (!lo.router_tc && route_permute_fusable((int)m, c.top_k, c.num_experts)) {
-        // decode: router, top-k and the permute in one launch.  For fp8 layers
-        // with m > 4 the same launch also quantises x; at m <= 4 the separate
-        // quantiser launch measured faster (DeepSeek-V3 shape, m = 1: 105 vs
-        // 133 us per layer step).
-        const PermuteOut po = permute_out(lo, workspace, nullptr, nullptr, nullptr);
-        const bool fuse_q = layer->fp8 && m > 4;
-        MOE_LAUNCH(K_ROUTE_PERMUTE,
-                   launch_route_permute_small(static_cast<const uint16_t*>(x), (int)m, c.hidden, router_w,
-                                              c.num_experts, at<float>(workspace, lo.part), lo.S, c.top_k, router_bias,
-                                              layer->rm,
-                                              ids, w, layer->has_shared ? 1 : 0, po, at<WsHeader>(workspace, lo.hdr),
-                                              fuse_q ? at<uint8_t>(workspace, lo.xq) : nullptr,
-                                              fuse_q ? at<float>(workspace, lo.xsc) : nullptr, st));
-        rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln, true, fuse_q);
-    } else {
-        rc = run_route(layer, lo, x, (int)m, router_w, router_bias, nullptr, ids, w, workspace, ln);
-        if (rc == MOE_OK) rc = run_experts(layer, lo, x, (int)m, ids, w, out, arm, workspace, ln);
-    }
-    layer->last_launches = ln.n;
-    return rc;
+    const TailArgs tail{static_cast<uint16_t*>(residual), norm_w, eps, static_cast<uint16_t*>(norm_out)};
+    return forward_impl(layer, x, m, router_w, router_bias, nullptr, topk_ids_out, topk_w_out, arm, workspace,
+                        workspace_bytes, stream, &tail);
 }
 
 int moe_act_quant_fp8(const void* x, int64_t rows, int64_t n, uint8_t* codes, float* scales, void* stream) {

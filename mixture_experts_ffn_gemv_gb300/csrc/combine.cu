@@ -26,19 +26,16 @@ __device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
     v[4] = bf16lo(a.z); v[5] = bf16hi(a.z); v[6] = bf16lo(a.w); v[7] = bf16hi(a.w);
 }
 
-// grid (ceil(H / 1024), m), 128 threads x 8 columns
+// acc[i] = out[t, h0 + i] in fp32 before rounding, i < 8: the k pairs' rows in
+// ascending j (slots and weights of 8 pairs first, then their 8 rows, then the
+// sums, so the loads overlap instead of forming a dependent chain), then the
+// shared row times its gate (1 when shared_g is null).
 template <typename YT>
-__global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
-                                               const float* __restrict__ w, int k, int H, int P, int has_shared,
-                                               const float* __restrict__ shared_g, uint16_t* __restrict__ out) {
-    pdl_wait();
-    pdl_trigger();
-    const int t = blockIdx.y;
-    const int h0 = (blockIdx.x * 128 + threadIdx.x) * 8;
-    if (h0 >= H) return;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // slots and weights of 8 pairs first, then their 8 rows, then the sums in
-    // ascending j: the loads overlap instead of forming a dependent chain
+__device__ __forceinline__ void pair_sum(const YT* __restrict__ y, const int32_t* __restrict__ slot,
+                                         const float* __restrict__ w, int k, int H, int P, int has_shared,
+                                         const float* __restrict__ shared_g, int t, int h0, float (&acc)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
     for (int j0 = 0; j0 < k; j0 += 8) {
         int sl[8];
         float wj[8];
@@ -71,6 +68,20 @@ __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const i
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, v[i], acc[i]);
     }
+}
+
+// grid (ceil(H / 1024), m), 128 threads x 8 columns
+template <typename YT>
+__global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
+                                               const float* __restrict__ w, int k, int H, int P, int has_shared,
+                                               const float* __restrict__ shared_g, uint16_t* __restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.y;
+    const int h0 = (blockIdx.x * 128 + threadIdx.x) * 8;
+    if (h0 >= H) return;
+    float acc[8];
+    pair_sum(y, slot, w, k, H, P, has_shared, shared_g, t, h0, acc);
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);
     o.y = pack_bf16x2(acc[2], acc[3]);
@@ -91,6 +102,84 @@ cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, 
     const dim3 grid(ceil_div(H, 1024), m);
     launch_pdl(combine<uint16_t>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- combine + layer tail
+// One block per token, 256 threads x 8 columns per step: the same pair sum,
+// then residual <- bf16(residual + sum), the new residual's values staged in
+// shared memory, a block sum of their squares in a fixed order (per thread
+// ascending h, warp butterfly, warps in order), and norm_out =
+// bf16(r * (1 / sqrt(ss / H + eps)) * norm_w).
+template <typename YT>
+__global__ __launch_bounds__(256) void combine_tail(const YT* __restrict__ y, const int32_t* __restrict__ slot,
+                                                    const float* __restrict__ w, int k, int H, int P, int has_shared,
+                                                    const float* __restrict__ shared_g, TailArgs tail) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ float rs[];  // [H]: the new residual's values
+    __shared__ float wsum[8];
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint16_t* res = tail.residual + (size_t)t * H;
+    float ss = 0.f;
+    for (int h0 = threadIdx.x * 8; h0 < H; h0 += 256 * 8) {
+        float acc[8];
+        pair_sum(y, slot, w, k, H, P, has_shared, shared_g, t, h0, acc);
+        float rv[8];
+        load8(res + h0, rv);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t p = pack_bf16x2(rv[2 * i] + acc[2 * i], rv[2 * i + 1] + acc[2 * i + 1]);
+            o[i] = p;
+            const float a = bf16lo(p), b = bf16hi(p);
+            rs[h0 + 2 * i] = a;
+            rs[h0 + 2 * i + 1] = b;
+            ss = fmaf(a, a, ss);
+            ss = fmaf(b, b, ss);
+        }
+        *reinterpret_cast<uint4*>(res + h0) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) wsum[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tot += wsum[i];
+    const float inv = 1.0f / sqrtf(tot / (float)H + tail.eps);
+    uint16_t* no = tail.norm_out + (size_t)t * H;
+    for (int h0 = threadIdx.x * 8; h0 < H; h0 += 256 * 8) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(tail.norm_w + h0));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(tail.norm_w + h0 + 4));
+        const float nw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = pack_bf16x2(rs[h0 + 2 * i] * inv * nw[2 * i], rs[h0 + 2 * i + 1] * inv * nw[2 * i + 1]);
+        *reinterpret_cast<uint4*>(no + h0) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+template <typename YT>
+static cudaError_t launch_tail(const YT* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H, int P,
+                               int has_shared, const float* shared_g, const TailArgs& tail, cudaStream_t st) {
+    static cudaError_t attr = cudaFuncSetAttribute(combine_tail<YT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   kTailMaxH * 4);
+    if (attr != cudaSuccess) return attr;
+    launch_pdl(combine_tail<YT>, dim3(m), dim3(256), (size_t)H * 4, st, y, slot_of_pair, w, k, H, P, has_shared,
+               shared_g, tail);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_tail_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
+                                    int P, int has_shared, const float* shared_g, const TailArgs& tail,
+                                    cudaStream_t st) {
+    return launch_tail(y, slot_of_pair, w, m, k, H, P, has_shared, shared_g, tail, st);
+}
+
+cudaError_t launch_combine_tail_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
+                                     int H, int P, int has_shared, const float* shared_g, const TailArgs& tail,
+                                     cudaStream_t st) {
+    return launch_tail(y, slot_of_pair, w, m, k, H, P, has_shared, shared_g, tail, st);
 }
 
 // ---------------------------------------------------------------- shared gate

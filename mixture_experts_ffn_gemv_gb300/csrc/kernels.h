@@ -101,6 +101,21 @@ cudaError_t launch_shared_gate(const uint16_t* x, int m, int H, const float* gat
 // combine: out[t] = sum_j w[t,j] * Y[slot(t,j)] (+ g[t] * Y[P+t] when has_shared; g = 1 when null)
 cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
                                int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st);
+// the same sum with the layer tail (moe_forward_residual_rmsnorm): residual
+// += out (bf16), norm_out = RMSNorm(residual) * norm_w; one block per token
+struct TailArgs {
+    uint16_t* residual;
+    const float* norm_w;
+    float eps;
+    uint16_t* norm_out;
+};
+constexpr int kTailMaxH = 24576;
+cudaError_t launch_combine_tail_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
+                                    int P, int has_shared, const float* shared_g, const TailArgs& tail,
+                                    cudaStream_t st);
+cudaError_t launch_combine_tail_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
+                                     int H, int P, int has_shared, const float* shared_g, const TailArgs& tail,
+                                     cudaStream_t st);
 cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
                                 int H, int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st);
 

@@ -189,6 +189,50 @@ def test_whole_layer_gated_shared_expert(cuda, oracle_mod, arm, m):
     assert rel_l2(to_np(out)[keep], ref["out"][keep]) < TOL[False]
 
 
+def _bf16_np(t):
+    return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("arm", ["gemv", "gemm"])
+@pytest.mark.parametrize("shape,m", [(MEDIUM_BF16, 16), (MEDIUM_BF16, 300), (SMALL_FP8, 24), (SMALL_FP8, 200),
+                                     (I.GATED_SHARED, 40)])
+def test_forward_residual_rmsnorm_tail(cuda, oracle_mod, arm, shape, m):
+    """The layer tail in the combine: with a zero residual the new residual is
+    moe_forward's output bit for bit (the same fp32 sum rounded once); with a
+    random one it is that sum added in fp32 and rounded; norm_out equals the
+    oracle's RMSNorm of the new residual to the last bf16 bit (rare ties)."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    tensors, x = _small_case(shape, m, seed=97, device=cuda)
+    layer = binding.MoeLayer(shape, tensors)
+    g = torch.Generator(device=cuda).manual_seed(97)
+    norm_w = (torch.randn(shape.hidden, generator=g, device=cuda) * 0.2 + 1.0).contiguous()
+    eps = 1e-6
+    try:
+        out = layer.moe_forward(x, tensors["router_w"], tensors["router_bias"], arm=arm)
+    except binding.MoeError as e:
+        if e.status == binding.MOE_ERR_UNSUPPORTED and arm == "gemm":
+            pytest.skip("grouped GEMM arm not available for this shape")
+        raise
+    res0 = torch.zeros(m, shape.hidden, dtype=torch.bfloat16, device=cuda)
+    n0 = layer.moe_forward_residual_rmsnorm(x, tensors["router_w"], res0, norm_w, eps, tensors["router_bias"], arm=arm)
+    res1_in = torch.randn(m, shape.hidden, generator=g, device=cuda).to(torch.bfloat16)
+    res1 = res1_in.clone()
+    n1 = layer.moe_forward_residual_rmsnorm(x, tensors["router_w"], res1, norm_w, eps, tensors["router_bias"], arm=arm)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert np.array_equal(_bf16_np(res0), _bf16_np(out))
+    want1 = res1_in.float() + out.float()  # out is the same sum rounded: within half a bf16 ulp of it
+    assert ((res1.float() - want1).abs() <= 2.0 ** -8 * (want1.abs() + out.float().abs()) + 1e-30).all()
+    for res, normed in ((res0, n0), (res1, n1)):
+        _, ref = oracle_mod.residual_rmsnorm(np.zeros((m, shape.hidden), np.float32), _bf16_np(res),
+                                             norm_w.cpu().numpy(), eps, fp64=True)
+        got = normed.float().cpu()
+        exp = torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float()
+        rel = ((got - exp).abs() / exp.abs().clamp_min(1e-30))
+        assert rel.max().item() <= 2.0 ** -7
+        assert (got != exp).float().mean().item() < 0.01
+
+
 @pytest.mark.parametrize("shape,m", [(I.TINY, 300), (ODD_E, 500), (MEDIUM_BF16, 129)])
 def test_route_tensor_core_path_odd_shapes(cuda, oracle_mod, shape, m):
     """m > 64 takes the tensor-core router (bf16 x3 split of the fp32 weight);
