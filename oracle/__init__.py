@@ -32,13 +32,18 @@ _i64, _i32, _vp = _C.c_int64, _C.c_int32, _C.c_void_p
 class _Layer(ctypes.Structure):
     _fields_ = [
         ("hidden", _i32), ("num_experts", _i32), ("top_k", _i32), ("inter", _i32),
-        ("shared_inter", _i32), ("fp8", _i32),
+        ("shared_inter", _i32), ("wfmt", _i32),
         ("w1", _vp), ("w3", _vp), ("w2", _vp),
         ("s1", _vp), ("s3", _vp), ("s2", _vp),
         ("ws1", _vp), ("ws3", _vp), ("ws2", _vp),
         ("ss1", _vp), ("ss3", _vp), ("ss2", _vp),
         ("shared_gate", _vp),
+        ("sb1", _vp), ("sb3", _vp), ("sb2", _vp),
+        ("ssb1", _vp), ("ssb3", _vp), ("ssb2", _vp),
     ]
+
+# weight formats of the oracle layer struct
+FMT_BF16, FMT_FP8, FMT_NVFP4 = 0, 1, 2
 
 
 def lib_path(fp64: bool = False) -> str:
@@ -69,6 +74,9 @@ def _lib(fp64: bool = False):
             lib.oracle_e4m3_decode.argtypes = [_vp, _vp, _i64]
             lib.oracle_e4m3_encode.argtypes = [_vp, _vp, _i64]
             lib.oracle_act_quant.argtypes = [_vp, _i64, _vp, _vp, _vp]
+            lib.oracle_e2m1_decode.argtypes = [_vp, _vp, _i64]
+            lib.oracle_e2m1_encode.argtypes = [_vp, _vp, _i64]
+            lib.oracle_nvfp4_quant.argtypes = [_vp, _i64, _vp, _vp, _vp, _vp]
             lib.oracle_router_logits.argtypes = [_vp, _i64, _C.c_int, _vp, _vp, _C.c_int, _vp]
             lib.oracle_topk_softmax.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _vp, _vp]
             lib.oracle_topk_sigmoid.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _C.c_int, _C.c_float,
@@ -140,6 +148,41 @@ def act_quant(values):
     return q, s, d
 
 
+def e2m1_decode(codes) -> np.ndarray:
+    """Values of e2m1 codes (the low 4 bits of each byte)."""
+    c = _np(codes, np.uint8)
+    out = np.empty(c.shape, np.float32)
+    _lib().oracle_e2m1_decode(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def e2m1_encode(values) -> np.ndarray:
+    """e2m1 codes (one per byte) of float values: nearest, ties to even, saturating."""
+    v = _np(values, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _lib().oracle_e2m1_encode(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def nvfp4_quant(values):
+    """NVFP4 quantisation of each row of a [rows, n] array (n a multiple of 16)
+    -> (packed codes uint8 [rows, n/2], e4m3 block-scale codes uint8
+    [rows, n/16], row scales float32 [rows], dequantised float32 [rows, n])."""
+    v = _np(values, np.float32)
+    if v.ndim == 1:
+        v = v.reshape(1, -1)
+    rows, n = v.shape
+    assert n % 16 == 0
+    q = np.empty((rows, n // 2), np.uint8)
+    sb = np.empty((rows, n // 16), np.uint8)
+    g = np.empty(rows, np.float32)
+    d = np.empty((rows, n), np.float32)
+    lib = _lib()
+    for r in range(rows):
+        lib.oracle_nvfp4_quant(_ptr(v[r]), n, _ptr(q[r]), _ptr(sb[r]), g[r:].ctypes.data, _ptr(d[r]))
+    return q, sb, g, d
+
+
 def router_logits(x, router_w, router_bias=None, fp64: bool = False) -> np.ndarray:
     xb = _np(x)
     assert xb.dtype == np.uint16, "x must be bf16"
@@ -198,15 +241,20 @@ def _layer_struct(shape, layer, keep):
         keep.append(a)
         return a
 
-    wdt = np.uint8 if shape.fp8 else None
+    nvfp4 = bool(getattr(shape, "nvfp4", False))
+    wdt = np.uint8 if (shape.fp8 or nvfp4) else None
     s = _Layer()
     s.hidden, s.num_experts, s.top_k = shape.hidden, shape.num_experts, shape.top_k
-    s.inter, s.shared_inter, s.fp8 = shape.inter, shape.shared_inter, int(shape.fp8)
+    s.inter, s.shared_inter = shape.inter, shape.shared_inter
+    s.wfmt = FMT_NVFP4 if nvfp4 else (FMT_FP8 if shape.fp8 else FMT_BF16)
     for name in ("w1", "w3", "w2", "ws1", "ws3", "ws2"):
         a = arr(name, wdt)
         setattr(s, name, _ptr(a))
     for name in ("s1", "s3", "s2", "ss1", "ss3", "ss2"):
         a = arr(name, np.float32)
+        setattr(s, name, _ptr(a))
+    for name in ("sb1", "sb3", "sb2", "ssb1", "ssb3", "ssb2"):
+        a = arr(name, np.uint8) if nvfp4 else None
         setattr(s, name, _ptr(a))
     s.shared_gate = _ptr(arr("shared_gate", np.float32)) if getattr(shape, "shared_gate", False) else None
     return s

@@ -38,6 +38,19 @@
  * * s; an all-zero block takes s = 1 and codes 0.  The e4m3 codec here is
  * written from the format's definition (1 sign, 4 exponent bits with bias 7,
  * 3 mantissa bits, no infinities, S.1111.111 is NaN, largest finite 448).
+ *
+ * NVFP4 weights and activations (the "NVFP4 W4A4 block-scaled MMA MoE" of
+ * span-02 gpu_model/forward.rs's module comment; the page names the format
+ * and nothing more, so the format's usual definition is taken): each value is
+ * an e2m1 code (1 sign, 2 exponent bits with bias 1, 1 mantissa bit: the
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) times an e4m3 scale shared by 16
+ * contiguous inputs, times one fp32 scale per tensor.  A weight tensor is one
+ * expert's matrix; an activation tensor is one row (a token's x, a pair's h),
+ * which keeps tokens independent.  Activation rows are quantised as:
+ *   g  = amax(row) / (6 * 448)           (g = 1 for an all-zero row)
+ *   sb = e4m3(RNE, saturating)(amax(block) / (6 * g))
+ *   code = e2m1(RNE, saturating to +-6)(v / (decode(sb) * g))  (0 when that scale is 0)
+ *   value = decode(code) * decode(sb) * g
  */
 #include <math.h>
 #include <stdint.h>
@@ -144,6 +157,82 @@ EXPORT void oracle_act_quant(const float* v, int64_t n, uint8_t* q, float* s, fl
         for (int64_t i = b0; i < b1; ++i) {
             q[i] = amax > 0.0f ? e4m3_encode_one(v[i] / sc) : 0;
             if (deq) deq[i] = e4m3_decode_one(q[i]) * sc;
+        }
+    }
+}
+
+/* e2m1 code (low 4 bits) -> float, from the format definition. */
+static float e2m1_decode_one(uint8_t c) {
+    int sign = (c >> 3) & 1;
+    int expo = (c >> 1) & 0x3;
+    int mant = c & 0x1;
+    float v = expo == 0 ? 0.5f * (float)mant : ldexpf(1.0f + 0.5f * (float)mant, expo - 1);
+    return sign ? -v : v;
+}
+
+/* float -> e2m1 code, nearest, ties to the even code, saturating to +-6;
+ * exhaustive over the 8 magnitudes, like e4m3_encode_one. */
+static uint8_t e2m1_encode_one(float x) {
+    int neg = signbit(x) ? 1 : 0;
+    double a = fabs((double)x);
+    if (isnan(x)) return 0;
+    if (a >= 6.0) return (uint8_t)((neg << 3) | 0x7);
+    int best = 0;
+    double best_err = a;
+    for (int c = 1; c <= 7; ++c) {
+        double err = fabs((double)e2m1_decode_one((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)((neg << 3) | best);
+}
+
+EXPORT void oracle_e2m1_decode(const uint8_t* in, float* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e2m1_decode_one(in[i] & 0xF);
+}
+
+EXPORT void oracle_e2m1_encode(const float* in, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e2m1_encode_one(in[i]);
+}
+
+/* Element i of an NVFP4 vector: two codes per byte, element 2j in the low
+ * nibble of byte j. */
+static uint8_t nibble_at(const uint8_t* q, int64_t i) {
+    uint8_t b = q[i >> 1];
+    return (i & 1) ? (uint8_t)(b >> 4) : (uint8_t)(b & 0xF);
+}
+
+/*
+ * NVFP4 quantisation of one activation row of n elements (n a multiple of 16),
+ * per the recipe in the header comment.  q: [n/2] packed codes; sb: [n/16]
+ * e4m3 block-scale codes; g: the row's fp32 scale; deq (optional): the values
+ * decode(code) * decode(sb) * g.
+ */
+EXPORT void oracle_nvfp4_quant(const float* v, int64_t n, uint8_t* q, uint8_t* sb, float* g, float* deq) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+    const float gs = amax > 0.0f ? amax / 2688.0f : 1.0f;
+    *g = gs;
+    for (int64_t i = 0; i < n / 2; ++i) q[i] = 0;
+    for (int64_t b0 = 0; b0 < n; b0 += 16) {
+        float bmax = 0.0f;
+        for (int64_t i = b0; i < b0 + 16; ++i) {
+            float a = fabsf(v[i]);
+            if (a > bmax) bmax = a;
+        }
+        const float six_g = 6.0f * gs;
+        const uint8_t sc = e4m3_encode_one(bmax / six_g);
+        sb[b0 / 16] = sc;
+        const float scale = e4m3_decode_one(sc) * gs;
+        for (int64_t i = b0; i < b0 + 16; ++i) {
+            const uint8_t c = scale != 0.0f ? e2m1_encode_one(v[i] / scale) : 0;
+            q[i >> 1] |= (uint8_t)((i & 1) ? (c << 4) : c);
+            if (deq) deq[i] = e2m1_decode_one(c) * e4m3_decode_one(sc) * gs;
         }
     }
 }
@@ -291,60 +380,126 @@ EXPORT void oracle_permute(const int32_t* ids, int64_t m, int k, int E, int32_t*
 
 /* ---------------------------------------------------------------- experts */
 
+#define FMT_BF16 0
+#define FMT_FP8 1
+#define FMT_NVFP4 2
+
 typedef struct {
-    int32_t hidden, num_experts, top_k, inter, shared_inter, fp8;
-    const void *w1, *w3, *w2;  /* [E,I,H], [E,I,H], [E,H,I]: bf16 bits or e4m3 codes */
-    const float *s1, *s3, *s2; /* fp8 only: [E,I/128,H/128], [E,I/128,H/128], [E,H/128,I/128] */
+    int32_t hidden, num_experts, top_k, inter, shared_inter;
+    int32_t wfmt;              /* FMT_BF16, FMT_FP8 or FMT_NVFP4 */
+    const void *w1, *w3, *w2;  /* [E,I,H], [E,I,H], [E,H,I]: bf16 bits, e4m3 codes or packed e2m1 codes */
+    /* fp8: block scales [E,I/128,H/128], [E,I/128,H/128], [E,H/128,I/128];
+     * nvfp4: the per-matrix fp32 scale, [E] each */
+    const float *s1, *s3, *s2;
     const void *ws1, *ws3, *ws2; /* shared expert, [Is,H], [Is,H], [H,Is] */
-    const float *ss1, *ss3, *ss2;
+    const float *ss1, *ss3, *ss2; /* fp8: its block scales; nvfp4: [1] each */
     const float* shared_gate;    /* [H] or NULL: shared expert scaled by sigmoid(dot(x, gate)) */
+    /* nvfp4 only: e4m3 block-scale codes, one per 16 inputs: [E,I,H/16],
+     * [E,I,H/16], [E,H,I/16]; the shared expert's [Is,H/16], [Is,H/16], [H,Is/16] */
+    const uint8_t *sb1, *sb3, *sb2;
+    const uint8_t *ssb1, *ssb3, *ssb2;
 } oracle_layer;
 
+/* One expert's [R, C] weight matrix: its codes, and its scales. */
+typedef struct {
+    const void* w;      /* this expert's codes (element (0,0)) */
+    const float* sc;    /* fp8: its 128x128 block scales; nvfp4: its fp32 matrix scale */
+    const uint8_t* sb;  /* nvfp4: its [R, C/16] e4m3 block-scale codes */
+} wmat;
+
 /* Element (r, c) of one expert's [R, C] weight matrix, dequantised. */
-static acc_t weight_at(const void* w, const float* sc, int fp8, int64_t base, int C, int r, int c) {
-    if (!fp8) return (acc_t)bf16_to_float(((const uint16_t*)w)[base + (int64_t)r * C + c]);
-    int cb = (C + 127) / 128;
-    float code = g_e4m3[((const uint8_t*)w)[base + (int64_t)r * C + c]];
-    return (acc_t)(code * sc[(int64_t)(r / 128) * cb + (c / 128)]);
+static acc_t weight_at(const wmat* W, int fmt, int C, int r, int c) {
+    const int64_t i = (int64_t)r * C + c;
+    if (fmt == FMT_BF16) return (acc_t)bf16_to_float(((const uint16_t*)W->w)[i]);
+    if (fmt == FMT_FP8) {
+        int cb = (C + 127) / 128;
+        float code = g_e4m3[((const uint8_t*)W->w)[i]];
+        return (acc_t)(code * W->sc[(int64_t)(r / 128) * cb + (c / 128)]);
+    }
+    const float q = e2m1_decode_one(nibble_at((const uint8_t*)W->w, i));
+    const float sb = g_e4m3[W->sb[(int64_t)r * (C / 16) + c / 16]];
+    return (acc_t)(q * sb) * (acc_t)W->sc[0];
+}
+
+/* Quantise a float row in place to its fp8 or nvfp4 activation values. */
+static void act_emulate(int fmt, float* v, int64_t n) {
+    float* d = (float*)malloc(sizeof(float) * (size_t)n);
+    uint8_t* q = (uint8_t*)malloc((size_t)n);
+    float* s = (float*)malloc(sizeof(float) * (size_t)((n + 127) / 128));
+    if (fmt == FMT_FP8) {
+        oracle_act_quant(v, n, q, s, d);
+    } else {
+        uint8_t* sb = (uint8_t*)malloc((size_t)(n / 16));
+        float g;
+        oracle_nvfp4_quant(v, n, q, sb, &g, d);
+        free(sb);
+    }
+    for (int64_t i = 0; i < n; ++i) v[i] = d[i];
+    free(d); free(q); free(s);
 }
 
 /*
  * One expert's SwiGLU FFN on one input row (metrale moe_v41 forward.rs, the
  * swiglu launch, without its clamp; the routing weight is applied by the
  * caller after the down projection, as in forward_prefill step 7).
- *   xin: [H] (already fp8-emulated when fp8); y: [H] out.
- * w1/w3 base offsets are in elements; sc1/sc3/sc2 point at this expert's scales.
+ *   xin: [H] (already quantisation-emulated for fp8 / nvfp4); y: [H] out.
  */
-static void expert_ffn(const oracle_layer* Lr, int I, const void* w1, const float* sc1,
-                       const void* w3, const float* sc3, const void* w2, const float* sc2,
-                       int64_t b13, int64_t b2, const acc_t* xin, acc_t* a, acc_t* y) {
+static void expert_ffn(const oracle_layer* Lr, int I, const wmat* W1, const wmat* W3, const wmat* W2,
+                       const acc_t* xin, acc_t* a, acc_t* y) {
     int H = Lr->hidden;
-    int fp8 = Lr->fp8;
+    int fmt = Lr->wfmt;
     if (I <= 0 || H <= 0) return;
     for (int i = 0; i < I; ++i) {
         acc_t g = 0, u = 0;
         for (int h = 0; h < H; ++h) {
-            g += xin[h] * weight_at(w1, sc1, fp8, b13, H, i, h);
-            u += xin[h] * weight_at(w3, sc3, fp8, b13, H, i, h);
+            g += xin[h] * weight_at(W1, fmt, H, i, h);
+            u += xin[h] * weight_at(W3, fmt, H, i, h);
         }
         acc_t silu = g / ((acc_t)1 + ACC_EXP(-g));
         a[i] = silu * u;
     }
-    if (fp8) {
-        /* the down projection's input is quantised per 128 elements along I */
+    if (fmt != FMT_BF16) {
+        /* the down projection's input is quantised along I: per 128 elements
+         * (fp8) or per 16 elements with a per-row scale (nvfp4) */
         float* af = (float*)malloc(sizeof(float) * (size_t)I);
-        float* ad = (float*)malloc(sizeof(float) * (size_t)I);
-        uint8_t* q = (uint8_t*)malloc((size_t)I);
-        float* s = (float*)malloc(sizeof(float) * (size_t)((I + 127) / 128));
         for (int i = 0; i < I; ++i) af[i] = (float)a[i];
-        oracle_act_quant(af, I, q, s, ad);
-        for (int i = 0; i < I; ++i) a[i] = (acc_t)ad[i];
-        free(af); free(ad); free(q); free(s);
+        act_emulate(fmt, af, I);
+        for (int i = 0; i < I; ++i) a[i] = (acc_t)af[i];
+        free(af);
     }
     for (int o = 0; o < H; ++o) {
         acc_t acc = 0;
-        for (int i = 0; i < I; ++i) acc += a[i] * weight_at(w2, sc2, fp8, b2, I, o, i);
+        for (int i = 0; i < I; ++i) acc += a[i] * weight_at(W2, fmt, I, o, i);
         y[o] = acc;
+    }
+}
+
+/* Expert e's three matrices (e = -1: the shared expert, Is rows). */
+static void expert_mats(const oracle_layer* Lr, int e, wmat* W1, wmat* W3, wmat* W2) {
+    const int H = Lr->hidden, I = e < 0 ? Lr->shared_inter : Lr->inter;
+    const int fmt = Lr->wfmt;
+    const int64_t n = e < 0 ? 0 : (int64_t)e * I * H; /* elements before this expert */
+    const size_t esz = fmt == FMT_BF16 ? 2 : 1;
+    const int64_t wofs = fmt == FMT_NVFP4 ? n / 2 : n;
+    W1->w = (const char*)(e < 0 ? Lr->ws1 : Lr->w1) + wofs * esz;
+    W3->w = (const char*)(e < 0 ? Lr->ws3 : Lr->w3) + wofs * esz;
+    W2->w = (const char*)(e < 0 ? Lr->ws2 : Lr->w2) + wofs * esz;
+    W1->sb = W3->sb = W2->sb = 0;
+    W1->sc = W3->sc = W2->sc = 0;
+    if (fmt == FMT_FP8) {
+        const int hb = (H + 127) / 128, ib = (I + 127) / 128;
+        const int64_t so = e < 0 ? 0 : (int64_t)e * ib * hb;
+        W1->sc = (e < 0 ? Lr->ss1 : Lr->s1) + so;
+        W3->sc = (e < 0 ? Lr->ss3 : Lr->s3) + so;
+        W2->sc = (e < 0 ? Lr->ss2 : Lr->s2) + so;
+    } else if (fmt == FMT_NVFP4) {
+        const int64_t bo = n / 16, so = e < 0 ? 0 : e;
+        W1->sc = (e < 0 ? Lr->ss1 : Lr->s1) + so;
+        W3->sc = (e < 0 ? Lr->ss3 : Lr->s3) + so;
+        W2->sc = (e < 0 ? Lr->ss2 : Lr->s2) + so;
+        W1->sb = (e < 0 ? Lr->ssb1 : Lr->sb1) + bo;
+        W3->sb = (e < 0 ? Lr->ssb3 : Lr->sb3) + bo;
+        W2->sb = (e < 0 ? Lr->ssb2 : Lr->sb2) + bo;
     }
 }
 
@@ -367,7 +522,6 @@ EXPORT int oracle_moe_forward(const oracle_layer* Lr, const uint16_t* x, int64_t
     int bad = 0;
     e4m3_table_init();
     int Imax = I > Is ? I : Is;
-    int hb = (H + 127) / 128, ib = (I + 127) / 128;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
     for (int64_t r = 0; r < n; ++r) {
         int64_t t = rows ? rows[r] : r;
@@ -377,34 +531,28 @@ EXPORT int oracle_moe_forward(const oracle_layer* Lr, const uint16_t* x, int64_t
         acc_t* y = (acc_t*)malloc(sizeof(acc_t) * (size_t)H);
         acc_t* acc = (acc_t*)calloc((size_t)H, sizeof(acc_t));
         const uint16_t* xt = x + t * (int64_t)H;
-        if (Lr->fp8) {
+        if (Lr->wfmt != FMT_BF16) {
             float* xf = (float*)malloc(sizeof(float) * (size_t)H);
-            float* xd = (float*)malloc(sizeof(float) * (size_t)H);
-            uint8_t* q = (uint8_t*)malloc((size_t)H);
-            float* s = (float*)malloc(sizeof(float) * (size_t)hb);
             for (int h = 0; h < H; ++h) xf[h] = bf16_to_float(xt[h]);
-            oracle_act_quant(xf, H, q, s, xd);
-            for (int h = 0; h < H; ++h) xin[h] = (acc_t)xd[h];
-            free(xf); free(xd); free(q); free(s);
+            act_emulate(Lr->wfmt, xf, H);
+            for (int h = 0; h < H; ++h) xin[h] = (acc_t)xf[h];
+            free(xf);
         } else {
             for (int h = 0; h < H; ++h) xin[h] = (acc_t)bf16_to_float(xt[h]);
         }
         for (int j = 0; j < k; ++j) {
             int e = ids[t * (int64_t)k + j];
             if (e < 0 || e >= E) { bad |= 1; break; }
-            int64_t b13 = (int64_t)e * I * H, b2 = (int64_t)e * H * I;
-            const float *c1 = 0, *c3 = 0, *c2 = 0;
-            if (Lr->fp8) {
-                c1 = Lr->s1 + (int64_t)e * ib * hb;
-                c3 = Lr->s3 + (int64_t)e * ib * hb;
-                c2 = Lr->s2 + (int64_t)e * hb * ib;
-            }
-            expert_ffn(Lr, I, Lr->w1, c1, Lr->w3, c3, Lr->w2, c2, b13, b2, xin, a, y);
+            wmat W1, W3, W2;
+            expert_mats(Lr, e, &W1, &W3, &W2);
+            expert_ffn(Lr, I, &W1, &W3, &W2, xin, a, y);
             acc_t wj = (acc_t)w[t * (int64_t)k + j];
             for (int h = 0; h < H; ++h) acc[h] += wj * y[h];
         }
         if (Is > 0) {
-            expert_ffn(Lr, Is, Lr->ws1, Lr->ss1, Lr->ws3, Lr->ss3, Lr->ws2, Lr->ss2, 0, 0, xin, a, y);
+            wmat W1, W3, W2;
+            expert_mats(Lr, -1, &W1, &W3, &W2);
+            expert_ffn(Lr, Is, &W1, &W3, &W2, xin, a, y);
             acc_t gs = 1;
             if (Lr->shared_gate) {
                 acc_t d = 0;

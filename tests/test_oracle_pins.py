@@ -24,6 +24,16 @@
   * residual + norm   -> torch: the new residual bit for bit ((res + out) cast to
                           bf16); the norm against a float64 RMSNorm of it; closed
                           forms (a constant row normalises to sign * w at eps 0).
+  * e2m1 codec        -> golden code/value table from the format definition;
+                          encode against numpy's round-half-even on each binade's
+                          grid (every tie midpoint, saturation, signed zero).
+  * NVFP4 quantiser   -> an independent pipeline (torch's float8 cast for the
+                          block scales, numpy round-half-even for the codes);
+                          exact reconstruction of rows built from codes; an
+                          all-zero row; power-of-two scale invariance.
+  * NVFP4 expert      -> a torch float64 pipeline on the table-decoded weights
+                          and the independently fake-quantised activations;
+                          token independence of the per-row activation scale.
   * structure         -> token independence, expert relabelling invariance,
                           float vs double oracle builds agree to ~1e-6.
 """
@@ -122,6 +132,187 @@ def test_act_quant_matches_torch_cast(oracle_mod):
         ref = torch.from_numpy(blk / sc).to(torch.float8_e4m3fn)
         assert np.array_equal(q[b * 128:(b + 1) * 128], ref.view(torch.uint8).numpy())
         assert np.array_equal(d[b * 128:(b + 1) * 128], (ref.float() * float(sc)).numpy().astype(np.float32))
+
+
+# ----------------------------------------------------------------- e2m1 / NVFP4
+
+def _e2m1_table():
+    with open(os.path.join(GOLDEN, "e2m1_codes.json")) as f:
+        g = json.load(f)
+    return {int(c, 16): float(v) for c, v in g["pairs"]}
+
+
+def test_e2m1_golden_codes(oracle_mod):
+    tab = _e2m1_table()
+    codes = np.array(sorted(tab), np.uint8)
+    got = oracle_mod.e2m1_decode(codes)
+    want = np.array([tab[int(c)] for c in codes], np.float32)
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))  # -0.0 for 0x8
+    # only the low nibble is read
+    assert np.array_equal(oracle_mod.e2m1_decode(codes | 0xA0), want)
+
+
+def _e2m1_round_numpy(v):
+    """Round-to-nearest-even onto the e2m1 grid via numpy's half-even rounding:
+    spacing 0.5 below 2, 1 on [2, 4), 2 from 4; saturated at 6."""
+    a = np.abs(v.astype(np.float64))
+    step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+    r = np.minimum(np.round(a / step) * step, 6.0)
+    return np.copysign(r, v)
+
+
+def _e2m1_code_of_value(r):
+    tab = _e2m1_table()
+    inv = {(math.copysign(1.0, v), abs(v)): c for c, v in tab.items()}
+    return np.array([inv[(math.copysign(1.0, x), abs(x))] for x in r.tolist()], np.uint8)
+
+
+def test_e2m1_encode_matches_numpy_half_even(oracle_mod):
+    mags = np.array(sorted(set(abs(v) for v in _e2m1_table().values())))
+    mids = (mags[:-1] + mags[1:]) / 2.0  # every tie point
+    rng = np.random.default_rng(3)
+    cand = np.concatenate([
+        mags, mids,
+        np.nextafter(mids.astype(np.float32), np.float32(np.inf)),
+        np.nextafter(mids.astype(np.float32), np.float32(0)),
+        rng.uniform(0, 7, 100_000), rng.normal(0, 2, 20_000),
+        np.array([6.0, 6.5, 7.0, 1e6, 0.0, 1e-30]),
+    ]).astype(np.float32)
+    cand = np.concatenate([cand, -cand])
+    ours = oracle_mod.e2m1_encode(cand)
+    ref = _e2m1_code_of_value(_e2m1_round_numpy(cand))
+    bad = np.nonzero(ours != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, e.g. {cand[bad[:5]]} -> {ours[bad[:5]]} vs {ref[bad[:5]]}"
+
+
+def _nvfp4_quant_independent(v):
+    """The row quantiser written with library routines: the row scale in
+    float32, each block scale by torch's e4m3 cast, codes by numpy's
+    half-even rounding.  -> (codes one per element, block-scale codes, g)."""
+    v = np.asarray(v, np.float32)
+    amax = np.float32(np.abs(v).max())
+    g = np.float32(amax / np.float32(2688.0)) if amax > 0 else np.float32(1.0)
+    blocks = v.reshape(-1, 16)
+    bmax = np.abs(blocks).max(axis=1).astype(np.float32)
+    t = (bmax / np.float32(np.float32(6.0) * g)).astype(np.float32)
+    sbt = torch.from_numpy(t).to(torch.float8_e4m3fn)
+    sb = sbt.view(torch.uint8).numpy()
+    scale = (sbt.float().numpy() * g).astype(np.float32)
+    codes = np.zeros(blocks.shape, np.uint8)
+    nz = scale != 0
+    r = _e2m1_round_numpy((blocks[nz] / scale[nz, None]).astype(np.float32))
+    codes[nz] = _e2m1_code_of_value(r.reshape(-1)).reshape(r.shape)
+    return codes.reshape(-1), sb, g
+
+
+def _pack(codes):
+    c = codes.reshape(-1, 2)
+    return (c[:, 0] | (c[:, 1] << 4)).astype(np.uint8)
+
+
+def test_nvfp4_quant_matches_independent_pipeline(oracle_mod):
+    rng = np.random.default_rng(4)
+    rows = rng.normal(0, 1, (6, 512)).astype(np.float32)
+    rows[1, 64:80] = 0.0                 # an all-zero block
+    rows[2, :256] *= 1e-4                # blocks far below the row's amax
+    rows[3] = rng.standard_cauchy(512)   # heavy tails
+    rows[4, 100] = 50.0                  # one outlier sets the row scale
+    q, sb, g, d = oracle_mod.nvfp4_quant(rows)
+    for r in range(rows.shape[0]):
+        codes, sbr, gr = _nvfp4_quant_independent(rows[r])
+        assert g[r] == gr
+        assert np.array_equal(sb[r], sbr)
+        assert np.array_equal(q[r], _pack(codes))
+        vals = np.array([_e2m1_table()[int(c)] for c in codes], np.float64)
+        sc = torch.from_numpy(sbr).view(torch.float8_e4m3fn).double().numpy()
+        np.testing.assert_allclose(d[r], (vals * np.repeat(sc, 16) * float(gr)).astype(np.float32), rtol=1e-7, atol=0)
+
+
+def test_nvfp4_quant_reconstructs_exact_rows(oracle_mod):
+    # rows built from codes: every block holds a +-6, one block has scale 448
+    # and the row scale is a power of two, so quantising gives them back
+    rng = np.random.default_rng(5)
+    tab = _e2m1_table()
+    for trial in range(20):
+        n = 256
+        codes = rng.integers(0, 16, n).astype(np.uint8)
+        codes[::16] = rng.choice([0x7, 0xF], n // 16)
+        sb = rng.integers(0x08, 0x7F, n // 16).astype(np.uint8)  # normal e4m3 scales
+        sb[rng.integers(0, n // 16)] = 0x7E
+        g = np.float32(2.0 ** rng.integers(-20, 5))
+        sc = torch.from_numpy(sb).view(torch.float8_e4m3fn).double().numpy()
+        v = (np.array([tab[int(c)] for c in codes]) * np.repeat(sc, 16) * float(g)).astype(np.float32)
+        q, sbo, go, d = oracle_mod.nvfp4_quant(v)
+        assert go[0] == g
+        assert np.array_equal(sbo[0], sb)
+        # a zero code may come back with the other sign: compare values
+        assert np.array_equal(d[0], v)
+        assert np.array_equal(oracle_mod.e2m1_decode(q[0] & 0xF), oracle_mod.e2m1_decode(_pack(codes) & 0xF))
+        assert np.array_equal(oracle_mod.e2m1_decode(q[0] >> 4), oracle_mod.e2m1_decode(_pack(codes) >> 4))
+
+
+def test_nvfp4_quant_zero_row_and_scale_invariance(oracle_mod):
+    q, sb, g, d = oracle_mod.nvfp4_quant(np.zeros((1, 64), np.float32))
+    assert g[0] == 1.0 and not q.any() and not sb.any() and not d.any()
+    rng = np.random.default_rng(6)
+    v = rng.normal(0, 1, (1, 256)).astype(np.float32)
+    q0, sb0, g0, d0 = oracle_mod.nvfp4_quant(v)
+    for p in (-8, 3, 20):
+        q1, sb1, g1, d1 = oracle_mod.nvfp4_quant(v * np.float32(2.0 ** p))
+        assert np.array_equal(q1, q0) and np.array_equal(sb1, sb0)
+        assert g1[0] == g0[0] * np.float32(2.0 ** p)
+        assert np.array_equal(d1, d0 * np.float32(2.0 ** p))
+
+
+def _nvfp4_dequant_torch(q, sb, s):
+    """[R, C/2] packed codes, [R, C/16] e4m3 scales, matrix scale -> float64 [R, C]."""
+    tab = torch.tensor([_e2m1_table()[c] for c in range(16)], dtype=torch.float64)
+    q = q.long()
+    vals = torch.stack([tab[q & 15], tab[q >> 4]], dim=-1).reshape(q.shape[0], -1)
+    sc = sb.view(torch.float8_e4m3fn).double().repeat_interleave(16, 1)
+    return vals * sc * float(s)
+
+
+def _nvfp4_fake_quant_rows(v64):
+    out = np.empty(v64.shape, np.float64)
+    tab = _e2m1_table()
+    for r in range(v64.shape[0]):
+        codes, sb, g = _nvfp4_quant_independent(v64[r].numpy().astype(np.float32))
+        sc = torch.from_numpy(sb).view(torch.float8_e4m3fn).double().numpy()
+        out[r] = np.array([tab[int(c)] for c in codes]) * np.repeat(sc, 16) * float(g)
+    return torch.from_numpy(out)
+
+
+def test_nvfp4_expert_matches_torch_pipeline(oracle_mod):
+    shape = I.LayerShape(hidden=256, num_experts=2, top_k=1, inter=128, nvfp4=True)
+    layer = I.make_experts(shape, seed=14)
+    x = I.make_x(shape, 5, seed=14)
+    ids = np.ones((5, 1), np.int32)
+    w = np.ones((5, 1), np.float32)
+    x64 = _nvfp4_fake_quant_rows(_f64(x.float()))
+    w1 = _nvfp4_dequant_torch(layer["w1"][1], layer["sb1"][1], layer["s1"][1])
+    w3 = _nvfp4_dequant_torch(layer["w3"][1], layer["sb3"][1], layer["s3"][1])
+    w2 = _nvfp4_dequant_torch(layer["w2"][1], layer["sb2"][1], layer["s2"][1])
+    a = torch.nn.functional.silu(x64 @ w1.T) * (x64 @ w3.T)
+    ref = (_nvfp4_fake_quant_rows(a) @ w2.T).numpy()
+    out64 = oracle_mod.moe_forward(shape, layer, x, ids, w, fp64=True)
+    out32 = oracle_mod.moe_forward(shape, layer, x, ids, w)
+    assert np.linalg.norm(out64 - ref) / np.linalg.norm(ref) < 1e-6
+    # the float build may flip an h code at a rounding boundary
+    assert np.linalg.norm(out32 - ref) / np.linalg.norm(ref) < 2e-3
+
+
+def test_nvfp4_layer_tokens_independent_and_builds_agree(oracle_mod):
+    wl = I.WORKLOADS["small_nvfp4"]
+    layer = I.make_layer(wl, seed=15)
+    x = I.make_x(wl.shape, 8, seed=15)
+    r = oracle_mod.reference(wl.shape, layer, x)
+    for t in (0, 5):
+        one = oracle_mod.reference(wl.shape, layer, x[t:t + 1])
+        assert np.array_equal(one["out"][0], r["out"][t])
+    r64 = oracle_mod.reference(wl.shape, layer, x, fp64=True)
+    assert np.linalg.norm(r["out"] - r64["out"]) / np.linalg.norm(r64["out"]) < 1e-4
 
 
 # ----------------------------------------------------------------- routing
