@@ -147,9 +147,22 @@ class ClockSampler:
 # ----------------------------------------------------------------- algorithmic bytes / flops
 
 
+NVFP4_B = 0.5 + 1.0 / 16  # bytes per NVFP4 element: a 4-bit code + an e4m3 scale per 16
+
+
+def _dtype(shape) -> str:
+    """The arithmetic type of the expert path."""
+    if getattr(shape, "nvfp4", False):
+        return "nvfp4_e2m1"
+    return "fp8_e4m3" if shape.fp8 else "bf16"
+
+
 def expert_bytes(shape):
-    """Bytes of one expert's three matrices (+ fp8 block scales)."""
+    """Bytes of one expert's three matrices (+ fp8 block scales, or NVFP4
+    block scales and per-matrix scales)."""
     H, I_ = shape.hidden, shape.inter
+    if getattr(shape, "nvfp4", False):
+        return int(3 * H * I_ * NVFP4_B) + 3 * 4
     wb = 1 if shape.fp8 else 2
     b = 3 * H * I_ * wb
     if shape.fp8:
@@ -164,6 +177,16 @@ def kernel_alg_bytes(kernel, shape, m, U):
     H, I_, E, k = shape.hidden, shape.inter, shape.num_experts, shape.top_k
     P = m * k
     rows = P + (m if shape.shared_inter else 0)
+    if getattr(shape, "nvfp4", False):
+        # codes + block scales in, row scales, fp32 h out of gate/up
+        if kernel == "gemv_gateup":
+            return int(U * 2 * I_ * H * NVFP4_B + m * (H * NVFP4_B + 4) + rows * I_ * 4)
+        if kernel == "gemv_down":
+            return int(U * H * I_ * NVFP4_B + rows * (I_ * NVFP4_B + 4) + rows * H * 4)
+        if kernel == "act_quant_nvfp4":
+            return int(m * H * 2 + m * (H * NVFP4_B + 4))
+        if kernel == "h_quant_nvfp4":
+            return int(rows * I_ * 4 + rows * (I_ * NVFP4_B + 4))
     wb = 1 if shape.fp8 else 2
     ab = 1 if shape.fp8 else 2
     sc = 4 * (H // 128) * (I_ // 128) if shape.fp8 else 0
@@ -374,7 +397,7 @@ def sweep(device, steps, warmup):
     tc = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1e12
     res = []
     for name in ("qwen3_decode", "qwen3_prefill", "deepseek_v3_fp8", "qwen3_zipf", "deepseek_v3_sigmoid",
-                 "gated_shared"):
+                 "gated_shared", "qwen3_nvfp4"):
         wl = I.WORKLOADS[name]
         for m in wl.ms:
             try:
@@ -507,7 +530,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8_e4m3" if shape.fp8 else "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": _dtype(shape), "data": "synthetic",
         "config": {"workload": args.workload + (f" (experts overridden: {args.experts})" if args.experts else ""), "m": m, "hidden": shape.hidden, "experts": shape.num_experts,
                    "top_k": shape.top_k, "inter": shape.inter, "shared_inter": shape.shared_inter,
                    "global_batch": ws * m, "parallelism": f"token-parallel x{ws} (replicas, no collective)",
@@ -563,7 +586,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3" if wl.shape.fp8 else "bf16", "data": "synthetic",
+        "dtype": _dtype(wl.shape), "data": "synthetic",
         "config": {"workload": args.workload + (f" (experts overridden: {args.experts})" if args.experts else ""), "m": m, "hidden": wl.shape.hidden, "experts": wl.shape.num_experts,
                    "top_k": wl.shape.top_k, "inter": wl.shape.inter, "global_batch": m},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",

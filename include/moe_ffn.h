@@ -61,6 +61,17 @@ extern "C" {
  * to e4m3 with one fp32 scale per token per 128 contiguous inputs,
  * s = amax / 448, round-to-nearest-even, saturating. */
 #define MOE_WEIGHTS_FP8_E4M3_B128 1
+/* NVFP4 weights and activations (W4A4; span-02 gpu_model/forward.rs names an
+ * "NVFP4 W4A4 block-scaled MMA MoE" and nothing more, so the format's usual
+ * definition is taken): e2m1 codes (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6)
+ * packed two per byte, element 2j in the low nibble of byte j; one e4m3
+ * scale code per 16 contiguous inputs of a row; one fp32 scale per tensor.
+ * A weight tensor is one expert's matrix.  Activations (x, and the down
+ * projection's input h) are quantised per row: g = amax(row) / 2688 (1 for
+ * an all-zero row); per 16-block sb = e4m3(RNE, saturating)(amax / (6 g));
+ * code = e2m1(RNE, saturating)(v / (decode(sb) * g)), 0 where that scale is
+ * 0.  Only the GEMV arm takes NVFP4 layers. */
+#define MOE_WEIGHTS_NVFP4 2
 
 /* ---- router scoring ("2. Batched topK dispatch" of forward_prefill.rs) */
 /* softmax over the k picks; a router bias, if given, is added to the logits */
@@ -77,12 +88,12 @@ extern "C" {
 #define MOE_ARM_GEMM 2 /* tcgen05/TMEM grouped GEMM arm fed by TMA */
 
 typedef struct moe_config {
-    int32_t hidden;       /* H: multiple of 128 (of 512 for fp8 weights) */
+    int32_t hidden;       /* H: multiple of 128 (of 512 for fp8, of 256 for nvfp4 weights) */
     int32_t num_experts;  /* E: 1..1024 */
     int32_t top_k;        /* k: 1..min(E, 32) */
-    int32_t inter;        /* I: expert intermediate size, multiple of 128 (of 512 for fp8) */
+    int32_t inter;        /* I: expert intermediate size, multiple of 128 (of 512 for fp8, 256 for nvfp4) */
     int32_t shared_inter; /* 0 = no shared expert; otherwise must equal inter */
-    int32_t weights;      /* MOE_WEIGHTS_BF16 or MOE_WEIGHTS_FP8_E4M3_B128 */
+    int32_t weights;      /* MOE_WEIGHTS_BF16, MOE_WEIGHTS_FP8_E4M3_B128 or MOE_WEIGHTS_NVFP4 */
     int32_t scoring;      /* MOE_SCORING_SOFTMAX (0) or MOE_SCORING_SIGMOID */
     int32_t norm_topk_prob;      /* sigmoid scoring: 1 = renormalise the k weights to sum 1 */
     float routed_scaling_factor; /* sigmoid scoring: weight multiplier, finite and > 0 */
@@ -93,6 +104,10 @@ typedef struct moe_config {
  *   shared:  w1, w3 [I, H]      w2 [H, I]        (E = 1 of the same layout)
  *   fp8 only: s1, s3 [E, I/128, H/128]  s2 [E, H/128, I/128]  (fp32)
  * Element type: bf16 or e4m3 codes (uint8) per moe_config.weights.
+ * nvfp4: w1, w3 uint8 [E, I, H/2], w2 uint8 [E, H, I/2] (packed codes);
+ *   sb1, sb3 uint8 [E, I, H/16], sb2 uint8 [E, H, I/16] (e4m3 block scales);
+ *   s1, s3, s2 fp32 [E] (one scale per expert matrix; [1] for the shared
+ *   expert).  sb* must be NULL for the other formats.
  * gate (shared expert only, else NULL): fp32 [H]; when set, the shared
  * expert's output is scaled per token by sigmoid(sum_h x[h] gate[h])
  * (forward_prefill.rs step "8. Blend shared expert"); NULL adds it with
@@ -106,6 +121,9 @@ typedef struct moe_expert_weights {
     const float* s3;
     const float* s2;
     const float* gate;
+    const uint8_t* sb1;
+    const uint8_t* sb3;
+    const uint8_t* sb2;
 } moe_expert_weights;
 
 typedef struct moe_layer moe_layer;
@@ -216,6 +234,14 @@ MOE_API int moe_forward_residual_rmsnorm(const moe_layer* layer, const void* x, 
  *   n a multiple of 128.  Needs no layer and no workspace.                  */
 MOE_API int moe_act_quant_fp8(const void* x, int64_t rows, int64_t n, uint8_t* codes, float* scales,
                               void* stream);
+
+/* Activation quantisation of the NVFP4 layers, per row as described at
+ * MOE_WEIGHTS_NVFP4 (the same kernel quantises x inside moe_forward).
+ *   x bf16 [rows, n]; codes uint8 [rows, n/2] (packed); block_scales uint8
+ *   [rows, n/16] (e4m3 codes); row_scales fp32 [rows]; n a multiple of 16.
+ * Needs no layer and no workspace.                                          */
+MOE_API int moe_act_quant_nvfp4(const void* x, int64_t rows, int64_t n, uint8_t* codes, uint8_t* block_scales,
+                                float* row_scales, void* stream);
 
 /* Synchronises `stream` and reads the device error word a previous call left
  * in `workspace` (0 = none).  Returns MOE_OK, MOE_ERR_DEVICE when the word is

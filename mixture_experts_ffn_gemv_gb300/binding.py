@@ -16,7 +16,7 @@ import torch
 from .build import LIB, build_library, up_to_date
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
-MOE_WEIGHTS_BF16, MOE_WEIGHTS_FP8_E4M3_B128 = 0, 1
+MOE_WEIGHTS_BF16, MOE_WEIGHTS_FP8_E4M3_B128, MOE_WEIGHTS_NVFP4 = 0, 1, 2
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 MOE_ARM_AUTO, MOE_ARM_GEMV, MOE_ARM_GEMM = 0, 1, 2
 ARMS = {"auto": MOE_ARM_AUTO, "gemv": MOE_ARM_GEMV, "gemm": MOE_ARM_GEMM}
@@ -24,7 +24,7 @@ ARMS = {"auto": MOE_ARM_AUTO, "gemv": MOE_ARM_GEMV, "gemm": MOE_ARM_GEMM}
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_workspace_size", "moe_select_arm", "moe_route",
     "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_forward", "moe_forward_residual_rmsnorm",
-    "moe_act_quant_fp8", "moe_device_status",
+    "moe_act_quant_fp8", "moe_act_quant_nvfp4", "moe_device_status",
     "moe_last_launch_count", "moe_kernel_timing_enable", "moe_kernel_timing_read", "moe_kernel_count",
     "moe_kernel_name", "moe_status_string",
 )
@@ -39,7 +39,8 @@ class MoeConfig(ctypes.Structure):
 
 
 class MoeExpertWeights(ctypes.Structure):
-    _fields_ = [("w1", _vp), ("w3", _vp), ("w2", _vp), ("s1", _vp), ("s3", _vp), ("s2", _vp), ("gate", _vp)]
+    _fields_ = [("w1", _vp), ("w3", _vp), ("w2", _vp), ("s1", _vp), ("s3", _vp), ("s2", _vp), ("gate", _vp),
+                ("sb1", _vp), ("sb3", _vp), ("sb2", _vp)]
 
 
 class MoeError(RuntimeError):
@@ -77,6 +78,7 @@ def load_library(path: str | None = None, build: bool = True):
         lib.moe_forward_residual_rmsnorm.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
                                                      _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         lib.moe_act_quant_fp8.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp]
+        lib.moe_act_quant_nvfp4.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp]
         lib.moe_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
         lib.moe_last_launch_count.argtypes = [_vp]
         lib.moe_kernel_timing_enable.argtypes = [_vp, ctypes.c_int]
@@ -122,11 +124,25 @@ def moe_act_quant_fp8(x, stream=None):
     return codes, scales
 
 
+def moe_act_quant_nvfp4(x, stream=None):
+    """x bf16 [rows, n] (device) -> (packed codes uint8 [rows, n/2], e4m3
+    block-scale codes uint8 [rows, n/16], row scales fp32 [rows])."""
+    lib = load_library()
+    rows, n = x.shape
+    codes = torch.empty(rows, n // 2, dtype=torch.uint8, device=x.device)
+    sb = torch.empty(rows, n // 16, dtype=torch.uint8, device=x.device)
+    g = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(lib.moe_act_quant_nvfp4(_p(x), rows, n, _p(codes), _p(sb), _p(g), _stream(stream)),
+           "moe_act_quant_nvfp4")
+    return codes, sb, g
+
+
 class MoeLayer:
     """A layer handle over caller-owned device weights (see include/moe_ffn.h).
 
-    tensors: dict with w1, w3, w2 (and s1, s3, s2 for fp8), optionally ws1,
-    ws3, ws2 (+ ss1, ss3, ss2) for the shared expert, as produced by
+    tensors: dict with w1, w3, w2 (and s1, s3, s2 for fp8; s1, s3, s2 and
+    sb1, sb3, sb2 for NVFP4), optionally ws1, ws3, ws2 (+ ss1, ss3, ss2, and
+    ssb1, ssb3, ssb2) for the shared expert, as produced by
     ``inputs.make_experts`` and moved to the device.
     """
 
@@ -135,16 +151,20 @@ class MoeLayer:
         self.shape = shape
         self._keep = dict(tensors)
         sigmoid = getattr(shape, "scoring", "softmax") == "sigmoid"
-        cfg = MoeConfig(shape.hidden, shape.num_experts, shape.top_k, shape.inter, shape.shared_inter,
-                        MOE_WEIGHTS_FP8_E4M3_B128 if shape.fp8 else MOE_WEIGHTS_BF16,
+        nvfp4 = bool(getattr(shape, "nvfp4", False))
+        wfmt = MOE_WEIGHTS_NVFP4 if nvfp4 else (MOE_WEIGHTS_FP8_E4M3_B128 if shape.fp8 else MOE_WEIGHTS_BF16)
+        cfg = MoeConfig(shape.hidden, shape.num_experts, shape.top_k, shape.inter, shape.shared_inter, wfmt,
                         MOE_SCORING_SIGMOID if sigmoid else MOE_SCORING_SOFTMAX,
                         int(bool(getattr(shape, "norm_topk_prob", True))),
                         float(getattr(shape, "routed_scaling", 1.0)))
-        routed = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("w1", "w3", "w2", "s1", "s3", "s2")])
+        sbn = ("sb1", "sb3", "sb2") if nvfp4 else ()
+        routed = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("w1", "w3", "w2", "s1", "s3", "s2")], None,
+                                  *[_p(tensors.get(n)) for n in sbn])
         shared = None
         if shape.shared_inter:
+            gate = _p(tensors.get("shared_gate")) if getattr(shape, "shared_gate", False) else None
             shared = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2")],
-                                      _p(tensors.get("shared_gate")) if getattr(shape, "shared_gate", False) else None)
+                                      gate, *[_p(tensors.get("s" + n)) for n in sbn])
         handle = _vp()
         _check(self.lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(routed),
                                          ctypes.byref(shared) if shared is not None else None,

@@ -23,11 +23,12 @@ namespace {
 // stream, resolved when the totals are read.
 enum KernelId : int {
     K_ROUTER_SPLIT = 0, K_ROUTER, K_TOPK, K_ROUTE_PERMUTE, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
-    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_H_QUANT, K_SHARED_GATE, K_COUNT
+    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_H_QUANT, K_SHARED_GATE, K_ACT_QUANT_NVFP4, K_H_QUANT_NVFP4, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "router_split", "router", "topk_softmax", "route_permute", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
     "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine", "h_quant_fp8", "shared_gate",
+    "act_quant_nvfp4", "h_quant_nvfp4",
 };
 
 struct Pending {
@@ -83,6 +84,7 @@ struct moe_layer {
     moe_expert_weights shared;
     bool has_shared;
     bool fp8;
+    bool nvfp4;  // NVFP4 weights and activations (GEMV arm only)
     int device;
     mutable int last_launches;
     mutable KernelTimer timer;
@@ -99,6 +101,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Layout {
     size_t hdr, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile, sorted_pair, slot_of_pair;
     size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, sgate, total;
+    size_t xsb, xg, hsb, hg;  // nvfp4: block scales and row scales of x and h
     int S, P, rows, nchunk;
     bool router_tc;
 };
@@ -130,6 +133,20 @@ Layout layout(const moe_layer* L, int64_t m) {
     o.act_tile = take((size_t)(E + 2) * 4);
     o.sorted_pair = take((size_t)o.P * 4);
     o.slot_of_pair = take((size_t)o.P * 4);
+    if (L->nvfp4) {
+        // x and h as packed codes + block scales + row scales, and fp32 h
+        o.xq = take((size_t)m * H / 2);
+        o.xsb = take((size_t)m * H / 16);
+        o.xg = take((size_t)m * 4);
+        o.h = take((size_t)o.rows * I / 2);
+        o.hsb = take((size_t)o.rows * I / 16);
+        o.hg = take((size_t)o.rows * 4);
+        o.hf = take((size_t)o.rows * I * 4);
+        o.y = take((size_t)o.rows * H * 4);
+        o.sgate = L->shared.gate ? take((size_t)m * 4) : 0;
+        o.total = off;
+        return o;
+    }
     if (L->fp8) {
         o.xq = take((size_t)m * H);
         o.xsc = take((size_t)m * (H / 128) * 4);
@@ -269,8 +286,23 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
         a.s1 = L->routed.s1; a.s3 = L->routed.s3; a.s2 = L->routed.s2;
         a.sw1 = L->shared.w1; a.sw3 = L->shared.w3; a.sw2 = L->shared.w2;
         a.ss1 = L->shared.s1; a.ss3 = L->shared.s3; a.ss2 = L->shared.s2;
+        a.sb1 = L->routed.sb1; a.sb3 = L->routed.sb3; a.sb2 = L->routed.sb2;
+        a.ssb1 = L->shared.sb1; a.ssb3 = L->shared.sb3; a.ssb2 = L->shared.sb2;
         float* y = at<float>(ws, lo.y);
-        if (L->fp8) {
+        if (L->nvfp4) {
+            uint8_t* xq = at<uint8_t>(ws, lo.xq);
+            uint8_t* xsb = at<uint8_t>(ws, lo.xsb);
+            float* xg = at<float>(ws, lo.xg);
+            uint8_t* hq = at<uint8_t>(ws, lo.h);
+            uint8_t* hsb = at<uint8_t>(ws, lo.hsb);
+            float* hg = at<float>(ws, lo.hg);
+            float* hf = at<float>(ws, lo.hf);
+            MOE_LAUNCH(K_ACT_QUANT_NVFP4,
+                       launch_act_quant_nvfp4_bf16(static_cast<const uint16_t*>(x), m, H, xq, xsb, xg, st));
+            MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_nvfp4(a, xq, xsb, xg, hf, st));
+            MOE_LAUNCH(K_H_QUANT_NVFP4, launch_act_quant_nvfp4_f32(hf, lo.rows, I, hq, hsb, hg, st));
+            MOE_LAUNCH(K_GEMV_DOWN, launch_gemv_down_nvfp4(a, hq, hsb, hg, y, st));
+        } else if (L->fp8) {
             uint8_t* xq = at<uint8_t>(ws, lo.xq);
             float* xsc = at<float>(ws, lo.xsc);
             uint8_t* hq = at<uint8_t>(ws, lo.h);
@@ -294,7 +326,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
         return MOE_OK;
     }
     if (arm != MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
-    if (!gemm_supported(L->cfg)) return MOE_ERR_UNSUPPORTED;
+    if (L->nvfp4 || !gemm_supported(L->cfg)) return MOE_ERR_UNSUPPORTED;
     GemmCall g{};
     g.hdr = hdr;
     g.grp_off = po.grp_off;
@@ -378,10 +410,16 @@ int forward_impl(const moe_layer* layer, const void* x, int64_t m, const float* 
     return rc;
 }
 
-bool weights_ok(const moe_expert_weights* w, bool fp8) {
+bool weights_ok(const moe_expert_weights* w, int fmt) {
     if (!w || !w->w1 || !w->w3 || !w->w2) return false;
     if (!aligned(w->w1, 16) || !aligned(w->w3, 16) || !aligned(w->w2, 16)) return false;
-    if (fp8 && (!w->s1 || !w->s3 || !w->s2)) return false;
+    if (fmt != MOE_WEIGHTS_BF16 && (!w->s1 || !w->s3 || !w->s2)) return false;
+    if (fmt == MOE_WEIGHTS_NVFP4) {
+        if (!w->sb1 || !w->sb3 || !w->sb2) return false;
+        if (!aligned(w->sb1, 16) || !aligned(w->sb3, 16) || !aligned(w->sb2, 16)) return false;
+    } else if (w->sb1 || w->sb3 || w->sb2) {
+        return false;
+    }
     return true;
 }
 
@@ -394,24 +432,27 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
     if (!cfg || !out) return MOE_ERR_INVALID_ARG;
     *out = nullptr;
     const moe_config& c = *cfg;
-    if (c.weights != MOE_WEIGHTS_BF16 && c.weights != MOE_WEIGHTS_FP8_E4M3_B128) return MOE_ERR_INVALID_ARG;
+    if (c.weights != MOE_WEIGHTS_BF16 && c.weights != MOE_WEIGHTS_FP8_E4M3_B128 && c.weights != MOE_WEIGHTS_NVFP4)
+        return MOE_ERR_INVALID_ARG;
     const bool fp8 = c.weights == MOE_WEIGHTS_FP8_E4M3_B128;
+    const bool nvfp4 = c.weights == MOE_WEIGHTS_NVFP4;
     if (c.hidden <= 0 || c.inter <= 0 || c.num_experts <= 0 || c.top_k <= 0 || c.shared_inter < 0)
         return MOE_ERR_INVALID_ARG;
     if (c.top_k > c.num_experts) return MOE_ERR_INVALID_ARG;
     if (c.num_experts > kMaxExperts || c.top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
     if (c.hidden % 128 != 0 || c.inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
     if (fp8 && (c.inter % 512 != 0 || c.hidden % 512 != 0)) return MOE_ERR_UNSUPPORTED;
+    if (nvfp4 && (c.inter % 256 != 0 || c.hidden % 256 != 0)) return MOE_ERR_UNSUPPORTED;
     if (c.shared_inter != 0 && c.shared_inter != c.inter) return MOE_ERR_UNSUPPORTED;
     if (c.scoring != MOE_SCORING_SOFTMAX && c.scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c.scoring == MOE_SCORING_SIGMOID &&
         (!(c.routed_scaling_factor > 0.f) || !std::isfinite(c.routed_scaling_factor) ||
          (c.norm_topk_prob != 0 && c.norm_topk_prob != 1)))
         return MOE_ERR_INVALID_ARG;
-    if (!weights_ok(routed, fp8) || routed->gate) return MOE_ERR_INVALID_ARG;  // a gate is for the shared expert only
+    if (!weights_ok(routed, c.weights) || routed->gate) return MOE_ERR_INVALID_ARG;  // a gate is for the shared expert only
     const bool has_shared = c.shared_inter > 0;
     if (has_shared != (shared != nullptr)) return MOE_ERR_INVALID_ARG;
-    if (has_shared && !weights_ok(shared, fp8)) return MOE_ERR_INVALID_ARG;
+    if (has_shared && !weights_ok(shared, c.weights)) return MOE_ERR_INVALID_ARG;
     if (has_shared && shared->gate && !aligned(shared->gate, 16)) return MOE_ERR_INVALID_ARG;
     moe_layer* L = new (std::nothrow) moe_layer();
     if (!L) return MOE_ERR_INVALID_ARG;
@@ -420,6 +461,7 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
     if (has_shared) L->shared = *shared;
     L->has_shared = has_shared;
     L->fp8 = fp8;
+    L->nvfp4 = nvfp4;
     L->rm = RouteMode{c.scoring == MOE_SCORING_SIGMOID ? 1 : 0, c.norm_topk_prob ? 1 : 0,
                       c.scoring == MOE_SCORING_SIGMOID ? c.routed_scaling_factor : 1.0f};
     L->last_launches = 0;
@@ -534,6 +576,19 @@ int moe_act_quant_fp8(const void* x, int64_t rows, int64_t n, uint8_t* codes, fl
     if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 16)) return MOE_ERR_INVALID_ARG;
     if (launch_act_quant_fp8(static_cast<const uint16_t*>(x), (int)rows, (int)n, codes, scales,
                              static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_act_quant_nvfp4(const void* x, int64_t rows, int64_t n, uint8_t* codes, uint8_t* block_scales,
+                        float* row_scales, void* stream) {
+    if (rows < 0 || n <= 0 || n % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (rows > INT32_MAX / 2 || n > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (!x || !codes || !block_scales || !row_scales || !aligned(x, 16) || !aligned(codes, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (launch_act_quant_nvfp4_bf16(static_cast<const uint16_t*>(x), (int)rows, (int)n, codes, block_scales,
+                                    row_scales, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -18,6 +18,15 @@
 // 128 inputs: each 128-wide K block is accumulated into a fresh partial that
 // is then scaled by s_w * s_x and added (the two-level fp32 block-scale
 // accumulation of spark_model forward_prefill's fp8 grouped GEMM).
+//
+// NVFP4 (W4A4, the block-scaled fp4 MoE of span-02 gpu_model/forward.rs):
+// weights and activations are e2m1 codes with an e4m3 scale per 16 inputs and
+// an fp32 scale per tensor.  A 16-byte load holds 32 codes of one row, two
+// scale blocks.  Each code pair is widened to f16x2 and multiplied by its
+// block scale; e2m1 times e4m3 has at most 6 significant bits and lies in
+// [2^-10, 2688], so that product is exact in f16 and the f16 mma.sync sums
+// exact products of the block-scaled values.  The two fp32 tensor scales
+// multiply the finished sum.
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -62,6 +71,63 @@ __device__ __forceinline__ void mma2_e4m3(float (&c)[4], const uint4& ag, const 
 template <int RT>
 __device__ __forceinline__ uint4 ldw(const uint4* p) {
     return RT == 2 ? ld_stream_v4_l2pf(p) : ld_stream_v4(p);
+}
+
+// ---- NVFP4
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// The two e4m3 block-scale codes of a 16-byte chunk (block 0 in the low byte)
+// -> each scale as an f16x2 splat.
+__device__ __forceinline__ void nvfp4_scales(uint32_t two_codes, uint32_t& s0, uint32_t& s1) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_codes));
+    s0 = __byte_perm(h2, 0, 0x1010);
+    s1 = __byte_perm(h2, 0, 0x3232);
+}
+
+// Four bytes of e2m1 code pairs -> four f16x2 values, each times the scale s.
+// The halves of every pair come out in one fixed order; weights and
+// activations are widened the same way, so a dot product over them is
+// unchanged by it.
+__device__ __forceinline__ void nvfp4_word(uint32_t w, uint32_t s, uint32_t (&v)[4]) {
+    uint32_t d0, d1, d2, d3;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+        : "r"(w));
+    v[0] = hmul2(d0, s);
+    v[1] = hmul2(d1, s);
+    v[2] = hmul2(d2, s);
+    v[3] = hmul2(d3, s);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& q, int i) {
+    return i == 0 ? q.x : (i == 1 ? q.y : (i == 2 ? q.z : q.w));
+}
+
+// Two MMAs over one 4-byte word (8 elements of K) of weight rows g and g+8
+// (already widened: wa, wb) and of the token column (xv).
+__device__ __forceinline__ void mma_word_f16(float (&c)[4], const uint32_t (&wa)[4], const uint32_t (&wb)[4],
+                                             const uint32_t (&xv)[4]) {
+    mma_f16(c, wa[0], wb[0], wa[1], wb[1], xv[0], xv[1]);
+    mma_f16(c, wa[2], wb[2], wa[3], wb[3], xv[2], xv[3]);
 }
 
 struct Group {
@@ -423,6 +489,227 @@ __global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uin
     }
 }
 
+// ============================================================ gate/up, NVFP4
+// CTA: RT row tiles (16 rows of I) x 8/RT K-slices of H, as for bf16; chunks
+// of 32 codes (16 bytes).  h = silu(g) * u, with g and u carrying both tensor
+// scales, is stored as fp32 [rows, I] for the row quantiser.
+template <int NT, int RT>
+__global__ __launch_bounds__(256, (NT == 1 ? 3 : 2)) void gemv_gateup_nvfp4(
+    const GemvArgs a, const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xsb,
+    const float* __restrict__ xg, float* __restrict__ hf, int n_slices) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int KS = 8 / RT;
+    __shared__ float red[KS][RT][32][NT * 8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int rt = warp % RT, kq = warp / RT;
+    Group gr;
+    if (!load_group(a, blockIdx.x / n_slices, gr)) return;
+    const int H = a.H, I = a.I, hq = H / 2, hs = H / 16;
+    const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
+    const bool routed = gr.g < a.E;
+    const uint8_t* W1 = routed ? (const uint8_t*)a.w1 + (size_t)gr.g * I * hq : (const uint8_t*)a.sw1;
+    const uint8_t* W3 = routed ? (const uint8_t*)a.w3 + (size_t)gr.g * I * hq : (const uint8_t*)a.sw3;
+    const uint8_t* B1 = routed ? a.sb1 + (size_t)gr.g * I * hs : a.ssb1;
+    const uint8_t* B3 = routed ? a.sb3 + (size_t)gr.g * I * hs : a.ssb3;
+    const float gw1 = routed ? __ldg(a.s1 + gr.g) : __ldg(a.ss1);
+    const float gw3 = routed ? __ldg(a.s3 + gr.g) : __ldg(a.ss3);
+    const uint4* w1g = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8) * hq);
+    const uint4* w1g8 = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8 + 8) * hq);
+    const uint4* w3g = reinterpret_cast<const uint4*>(W3 + (size_t)(row0 + g8) * hq);
+    const uint4* w3g8 = reinterpret_cast<const uint4*>(W3 + (size_t)(row0 + g8 + 8) * hq);
+    const uint16_t* b1g = reinterpret_cast<const uint16_t*>(B1 + (size_t)(row0 + g8) * hs);
+    const uint16_t* b1g8 = reinterpret_cast<const uint16_t*>(B1 + (size_t)(row0 + g8 + 8) * hs);
+    const uint16_t* b3g = reinterpret_cast<const uint16_t*>(B3 + (size_t)(row0 + g8) * hs);
+    const uint16_t* b3g8 = reinterpret_cast<const uint16_t*>(B3 + (size_t)(row0 + g8 + 8) * hs);
+    const int nch = H / 32;
+    const int kc0 = kq * nch / KS, kc1 = (kq + 1) * nch / KS;
+    for (int r0 = 0; r0 < gr.cnt; r0 += 8 * NT) {
+        const int R = min(8 * NT, gr.cnt - r0);
+        const uint4* xr[NT];
+        const uint16_t* xs[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g8;
+            const int tok = row_token(a, gr.off + r0 + (col < R ? col : 0));
+            xr[nt] = reinterpret_cast<const uint4*>(xq + (size_t)tok * hq);
+            xs[nt] = reinterpret_cast<const uint16_t*>(xsb + (size_t)tok * hs);
+        }
+        float c1[NT][4], c3[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c1[nt][i] = c3[nt][i] = 0.f;
+        // warp-uniform trip count (a K-slice need not hold whole 4-chunk
+        // steps): lanes past the slice's end take zero codes, which add 0
+#pragma unroll 2
+        for (int kb = kc0; kb < kc1; kb += 4) {
+            const int kc = kb + tig;
+            const bool in = kc < kc1;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 q1 = in ? ldw<RT>(w1g + kc) : z, q18 = in ? ldw<RT>(w1g8 + kc) : z;
+            const uint4 q3 = in ? ldw<RT>(w3g + kc) : z, q38 = in ? ldw<RT>(w3g8 + kc) : z;
+            uint32_t s1[2], s18[2], s3[2], s38[2];
+            nvfp4_scales(in ? __ldg(b1g + kc) : 0, s1[0], s1[1]);
+            nvfp4_scales(in ? __ldg(b1g8 + kc) : 0, s18[0], s18[1]);
+            nvfp4_scales(in ? __ldg(b3g + kc) : 0, s3[0], s3[1]);
+            nvfp4_scales(in ? __ldg(b3g8 + kc) : 0, s38[0], s38[1]);
+            uint4 xb[NT];
+            uint32_t sx[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                xb[nt] = in ? __ldg(xr[nt] + kc) : z;
+                nvfp4_scales(in ? __ldg(xs[nt] + kc) : 0, sx[nt][0], sx[nt][1]);
+            }
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+                const int blk = wi >> 1;
+                uint32_t v1[4], v18[4], v3[4], v38[4];
+                nvfp4_word(word_of(q1, wi), s1[blk], v1);
+                nvfp4_word(word_of(q18, wi), s18[blk], v18);
+                nvfp4_word(word_of(q3, wi), s3[blk], v3);
+                nvfp4_word(word_of(q38, wi), s38[blk], v38);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    uint32_t xv[4];
+                    nvfp4_word(word_of(xb[nt], wi), sx[nt][blk], xv);
+                    mma_word_f16(c1[nt], v1, v18, xv);
+                    mma_word_f16(c3[nt], v3, v38, xv);
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                red[kq][rt][lane][nt * 8 + i] = c1[nt][i];
+                red[kq][rt][lane][nt * 8 + 4 + i] = c3[nt][i];
+            }
+        __syncthreads();
+        if (kq == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float gs = red[0][rt][lane][nt * 8 + i], us = red[0][rt][lane][nt * 8 + 4 + i];
+#pragma unroll
+                    for (int q = 1; q < KS; ++q) {
+                        gs += red[q][rt][lane][nt * 8 + i];
+                        us += red[q][rt][lane][nt * 8 + 4 + i];
+                    }
+                    const int col = nt * 8 + tig * 2 + (i & 1);
+                    const int row = row0 + g8 + (i >> 1) * 8;
+                    if (col < R) {
+                        const float gx = __ldg(xg + row_token(a, gr.off + r0 + col));
+                        hf[(size_t)(gr.off + r0 + col) * I + row] = swiglu(gs * gw1 * gx, us * gw3 * gx);
+                    }
+                }
+        }
+        __syncthreads();
+    }
+}
+
+// ============================================================ down, NVFP4
+// CTA: RT row tiles (16 rows of H) x 8/RT K-slices of I; y fp32 [rows, H].
+template <int NT, int RT>
+__global__ __launch_bounds__(256, (NT == 1 ? 4 : 3)) void gemv_down_nvfp4(const GemvArgs a, const uint8_t* __restrict__ hq,
+                                                       const uint8_t* __restrict__ hsb,
+                                                       const float* __restrict__ hg, float* __restrict__ y,
+                                                       int n_slices) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int KS = 8 / RT;
+    __shared__ float red[KS][RT][32][NT * 4];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int rt = warp % RT, kq = warp / RT;
+    Group gr;
+    if (!load_group(a, blockIdx.x / n_slices, gr)) return;
+    const int H = a.H, I = a.I, iq = I / 2, is = I / 16;
+    const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
+    const bool routed = gr.g < a.E;
+    const uint8_t* W2 = routed ? (const uint8_t*)a.w2 + (size_t)gr.g * H * iq : (const uint8_t*)a.sw2;
+    const uint8_t* B2 = routed ? a.sb2 + (size_t)gr.g * H * is : a.ssb2;
+    const float gw2 = routed ? __ldg(a.s2 + gr.g) : __ldg(a.ss2);
+    const uint4* wg = reinterpret_cast<const uint4*>(W2 + (size_t)(row0 + g8) * iq);
+    const uint4* wg8 = reinterpret_cast<const uint4*>(W2 + (size_t)(row0 + g8 + 8) * iq);
+    const uint16_t* bg = reinterpret_cast<const uint16_t*>(B2 + (size_t)(row0 + g8) * is);
+    const uint16_t* bg8 = reinterpret_cast<const uint16_t*>(B2 + (size_t)(row0 + g8 + 8) * is);
+    const int nch = I / 32;
+    const int kc0 = kq * nch / KS, kc1 = (kq + 1) * nch / KS;
+    for (int r0 = 0; r0 < gr.cnt; r0 += 8 * NT) {
+        const int R = min(8 * NT, gr.cnt - r0);
+        const uint4* hr[NT];
+        const uint16_t* hs[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = nt * 8 + g8;
+            const size_t row = (size_t)(gr.off + r0 + (col < R ? col : 0));
+            hr[nt] = reinterpret_cast<const uint4*>(hq + row * iq);
+            hs[nt] = reinterpret_cast<const uint16_t*>(hsb + row * is);
+        }
+        float c[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
+        // warp-uniform trip count, as in gate/up
+#pragma unroll 2
+        for (int kb = kc0; kb < kc1; kb += 4) {
+            const int kc = kb + tig;
+            const bool in = kc < kc1;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 q0 = in ? ldw<RT>(wg + kc) : z, q8 = in ? ldw<RT>(wg8 + kc) : z;
+            uint32_t s0[2], s8[2];
+            nvfp4_scales(in ? __ldg(bg + kc) : 0, s0[0], s0[1]);
+            nvfp4_scales(in ? __ldg(bg8 + kc) : 0, s8[0], s8[1]);
+            uint4 hb[NT];
+            uint32_t sx[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                hb[nt] = in ? __ldg(hr[nt] + kc) : z;
+                nvfp4_scales(in ? __ldg(hs[nt] + kc) : 0, sx[nt][0], sx[nt][1]);
+            }
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+                const int blk = wi >> 1;
+                uint32_t v0[4], v8[4];
+                nvfp4_word(word_of(q0, wi), s0[blk], v0);
+                nvfp4_word(word_of(q8, wi), s8[blk], v8);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    uint32_t xv[4];
+                    nvfp4_word(word_of(hb[nt], wi), sx[nt][blk], xv);
+                    mma_word_f16(c[nt], v0, v8, xv);
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[kq][rt][lane][nt * 4 + i] = c[nt][i];
+        __syncthreads();
+        if (kq == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float v = red[0][rt][lane][nt * 4 + i];
+#pragma unroll
+                    for (int q = 1; q < KS; ++q) v += red[q][rt][lane][nt * 4 + i];
+                    const int col = nt * 8 + tig * 2 + (i & 1);
+                    const int row = row0 + g8 + (i >> 1) * 8;
+                    if (col < R) {
+                        const size_t srow = (size_t)(gr.off + r0 + col);
+                        y[srow * H + row] = v * gw2 * __ldg(hg + srow);
+                    }
+                }
+        }
+        __syncthreads();
+    }
+}
+
 // ============================================================ launchers
 // Token columns per pass: 16 when the groups average more than 4 rows (a
 // group with more rows than one pass covers takes further passes, re-reading
@@ -481,6 +768,18 @@ cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const f
 cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
                                  cudaStream_t st) {
     MOE_GEMV_LAUNCH(gemv_down_fp8, false, a.H, a.I, 128, hq, hsc, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_gateup_nvfp4(const GemvArgs& a, const uint8_t* xq, const uint8_t* xsb, const float* xg,
+                                     float* hf, cudaStream_t st) {
+    MOE_GEMV_LAUNCH(gemv_gateup_nvfp4, true, a.I, a.H, 128, xq, xsb, xg, hf);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_down_nvfp4(const GemvArgs& a, const uint8_t* hq, const uint8_t* hsb, const float* hg,
+                                   float* y, cudaStream_t st) {
+    MOE_GEMV_LAUNCH(gemv_down_nvfp4, false, a.H, a.I, 128, hq, hsb, hg, y);
     return cudaGetLastError();
 }
 

@@ -87,7 +87,10 @@ struct GemvArgs {
     int P, k, E, H, I, max_groups;
     // routed weights (stacked) and the shared expert's (g == E)
     const void *w1, *w3, *w2, *sw1, *sw3, *sw2;
+    // fp8: 128x128 block scales; nvfp4: one fp32 scale per expert matrix
     const float *s1, *s3, *s2, *ss1, *ss3, *ss2;
+    // nvfp4: e4m3 block-scale codes, one per 16 inputs
+    const uint8_t *sb1, *sb3, *sb2, *ssb1, *ssb3, *ssb2;
 };
 cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st);
 cudaError_t launch_gemv_down_bf16(const GemvArgs& a, const uint16_t* h, float* y, cudaStream_t st);
@@ -95,6 +98,18 @@ cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const f
                                    cudaStream_t st);
 cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
                                  cudaStream_t st);
+
+// NVFP4 (W4A4): activation rows quantised to packed e2m1 codes q [rows, n/2],
+// e4m3 block-scale codes sb [rows, n/16] and a row scale g [rows]; the GEMVs
+// take those and write fp32 h / y like the fp8 ones
+cudaError_t launch_act_quant_nvfp4_bf16(const uint16_t* x, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
+                                        cudaStream_t st);
+cudaError_t launch_act_quant_nvfp4_f32(const float* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
+                                       cudaStream_t st);
+cudaError_t launch_gemv_gateup_nvfp4(const GemvArgs& a, const uint8_t* xq, const uint8_t* xsb, const float* xg,
+                                     float* hf, cudaStream_t st);
+cudaError_t launch_gemv_down_nvfp4(const GemvArgs& a, const uint8_t* hq, const uint8_t* hsb, const float* hg,
+                                   float* y, cudaStream_t st);
 
 // the shared expert's gate per token: g[t] = sigmoid(sum_h x[t,h] gate[h])
 cudaError_t launch_shared_gate(const uint16_t* x, int m, int H, const float* gate, float* g, cudaStream_t st);

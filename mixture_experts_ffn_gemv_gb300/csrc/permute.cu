@@ -11,8 +11,8 @@
 //                   the grouped GEMM's m-tile starts;
 //   permute_scatter per chunk, warp-level ranks (match_any) give each pair
 //                   its slot: pairs keep ascending order within an expert.
-// Plus the activation gathers for the grouped GEMM and the fp8 activation
-// quantiser (one e4m3 code + fp32 scale per 128 inputs).
+// Plus the activation gathers for the grouped GEMM, the fp8 activation
+// quantiser (one e4m3 code + fp32 scale per 128 inputs) and the NVFP4 one.
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -236,6 +236,115 @@ cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, f
 cudaError_t launch_quant_rows_fp8(const float* v, int rows, int n, uint8_t* q, float* s, cudaStream_t st) {
     const int blocks = rows * (n / 128);
     launch_pdl(act_quant_fp8<float>, dim3(ceil_div(blocks, 8)), dim3(256), 0, st, v, rows, n, q, s);
+    return cudaGetLastError();
+}
+
+// ---- NVFP4 activation rows
+// e2m1 code of a finite float: nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with
+// ties to the even code (<= at the midpoints toward an even code, < toward
+// an odd one), saturating at 6; the sign bit is kept, zero included.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+    const float a = fabsf(v);
+    uint32_t c;
+    if (a <= 0.25f) c = 0;
+    else if (a < 0.75f) c = 1;
+    else if (a <= 1.25f) c = 2;
+    else if (a < 1.75f) c = 3;
+    else if (a <= 2.5f) c = 4;
+    else if (a < 3.5f) c = 5;
+    else if (a <= 5.0f) c = 6;
+    else c = 7;
+    return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+template <typename T>
+__device__ __forceinline__ void load16(const T* p, float (&f)[16]);
+template <>
+__device__ __forceinline__ void load16<uint16_t>(const uint16_t* p, float (&f)[16]) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint4 u = __ldg(q + i);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[i * 8 + 2 * j] = bf16lo(w[j]);
+            f[i * 8 + 2 * j + 1] = bf16hi(w[j]);
+        }
+    }
+}
+template <>
+__device__ __forceinline__ void load16<float>(const float* p, float (&f)[16]) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 u = __ldg(q + i);
+        f[4 * i] = u.x;
+        f[4 * i + 1] = u.y;
+        f[4 * i + 2] = u.z;
+        f[4 * i + 3] = u.w;
+    }
+}
+
+// One block of 128 threads per row of n (a multiple of 16) values:
+//   g = amax(row) / 2688 (1 for an all-zero row), 2688 = 6 * 448;
+//   per 16-block: sb = e4m3(RNE, satfinite)(amax(block) / (6 g));
+//   code = e2m1(v / (decode(sb) * g)), 0 when that scale is 0.
+// Codes are packed two per byte, element 2j in the low nibble of byte j.
+template <typename T>
+__global__ __launch_bounds__(128) void act_quant_nvfp4(const T* __restrict__ v, int rows, int n,
+                                                       uint8_t* __restrict__ q, uint8_t* __restrict__ sb,
+                                                       float* __restrict__ g) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float wmax[4];
+    const int r = blockIdx.x;
+    const int nb = n / 16;
+    const T* row = v + (size_t)r * n;
+    float am = 0.f;
+    for (int b = threadIdx.x; b < nb; b += 128) {
+        float f[16];
+        load16(row + (size_t)b * 16, f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(f[i]));
+    }
+    am = warp_max(am);
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = am;
+    __syncthreads();
+    am = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    const float gs = am > 0.f ? __fdiv_rn(am, 2688.0f) : 1.0f;
+    if (threadIdx.x == 0) g[r] = gs;
+    const float six_g = __fmul_rn(6.0f, gs);
+    for (int b = threadIdx.x; b < nb; b += 128) {
+        float f[16];
+        load16(row + (size_t)b * 16, f);
+        float bm = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(f[i]));
+        const uint32_t sc = f32x2_to_e4m3x2(__fdiv_rn(bm, six_g), 0.f) & 0xffu;
+        const float scale = __fmul_rn(e4m3x2_to_f32x2(sc).x, gs);
+        uint32_t lo = 0, hi = 0;
+        if (scale != 0.f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                lo |= e2m1_code(__fdiv_rn(f[i], scale)) << (4 * i);
+                hi |= e2m1_code(__fdiv_rn(f[8 + i], scale)) << (4 * i);
+            }
+        }
+        *reinterpret_cast<uint2*>(q + (size_t)r * (n / 2) + (size_t)b * 8) = make_uint2(lo, hi);
+        sb[(size_t)r * nb + b] = (uint8_t)sc;
+    }
+}
+
+cudaError_t launch_act_quant_nvfp4_bf16(const uint16_t* x, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
+                                        cudaStream_t st) {
+    launch_pdl(act_quant_nvfp4<uint16_t>, dim3(rows), dim3(128), 0, st, x, rows, n, q, sb, g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant_nvfp4_f32(const float* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
+                                       cudaStream_t st) {
+    launch_pdl(act_quant_nvfp4<float>, dim3(rows), dim3(128), 0, st, v, rows, n, q, sb, g);
     return cudaGetLastError();
 }
 

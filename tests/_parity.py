@@ -9,6 +9,12 @@ INDEX_MARGIN = 1e-4          # ids may differ only where oracle logits are this 
 TOL = {False: 1e-2, True: 2e-2}  # rel L2 bound: bf16 weights / fp8 block-scaled weights
 
 
+def tol(shape) -> float:
+    """rel L2 bound of a layer shape: 1e-2 for bf16 weights, 2e-2 for the
+    block-scaled formats (fp8, NVFP4)."""
+    return TOL[bool(shape.fp8 or getattr(shape, "nvfp4", False))]
+
+
 def rel_l2(got, ref) -> float:
     g = np.asarray(got, np.float64)
     r = np.asarray(ref, np.float64)
@@ -65,10 +71,10 @@ def compact_experts(shape, layer, expert_ids):
     idx = torch.as_tensor(sorted(set(int(e) for e in expert_ids)), dtype=torch.long)
     dev = layer["w1"].device
     sub = {}
-    for n in ("w1", "w3", "w2", "s1", "s3", "s2"):
+    for n in ("w1", "w3", "w2", "s1", "s3", "s2", "sb1", "sb3", "sb2"):
         if n in layer and layer[n] is not None:
             sub[n] = layer[n].index_select(0, idx.to(dev)).cpu()
-    for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2", "shared_gate"):
+    for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2", "ssb1", "ssb3", "ssb2", "shared_gate"):
         if n in layer and layer[n] is not None:
             sub[n] = layer[n].cpu()
     remap = {int(e): i for i, e in enumerate(idx.tolist())}

@@ -52,10 +52,12 @@ def _cfg(**kw):
     return MoeConfig(**c)
 
 
-def _weights(fp8=False):
+def _weights(fp8=False, nvfp4=False):
     from mixture_experts_ffn_gemv_gb300.binding import MoeExpertWeights
     fake = 0x10000  # never dereferenced: creation fails or stops before any device access
-    return MoeExpertWeights(fake, fake, fake, fake if fp8 else None, fake if fp8 else None, fake if fp8 else None)
+    sc = fake if (fp8 or nvfp4) else None
+    sb = fake if nvfp4 else None
+    return MoeExpertWeights(fake, fake, fake, sc, sc, sc, None, sb, sb, sb)
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -68,6 +70,8 @@ def _weights(fp8=False):
     (dict(shared_inter=256), 2),        # shared expert of another width
     (dict(weights=1, inter=384), 2),    # fp8 needs I % 512 == 0
     (dict(weights=1, inter=512, hidden=384), 2),  # ... and H % 512 == 0
+    (dict(weights=2, inter=384), 2),    # NVFP4 needs I % 256 == 0
+    (dict(weights=2, inter=256, hidden=384), 2),  # ... and H % 256 == 0
     (dict(scoring=2), 1),                          # no such scoring
     (dict(scoring=1, routed_scaling_factor=0.0), 1),  # sigmoid scoring needs a positive scaling factor
     (dict(scoring=1, routed_scaling_factor=float("inf")), 1),
@@ -76,7 +80,7 @@ def _weights(fp8=False):
 def test_create_rejects_unsupported_shapes(lib, kw, want):
     from mixture_experts_ffn_gemv_gb300.binding import MoeExpertWeights
     cfg = _cfg(**kw)
-    w = _weights(fp8=cfg.weights == 1)
+    w = _weights(fp8=cfg.weights == 1, nvfp4=cfg.weights == 2)
     shared = MoeExpertWeights(0x10000, 0x10000, 0x10000) if cfg.shared_inter else None
     out = ctypes.c_void_p()
     rc = lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(shared) if shared else None,
@@ -95,6 +99,23 @@ def test_create_rejects_null_and_misaligned(lib):
     missing_scales = _weights(fp8=False)
     cfg8 = _cfg(weights=1, inter=512, hidden=512)
     assert lib.moe_layer_create(ctypes.byref(cfg8), ctypes.byref(missing_scales), None, ctypes.byref(out)) == 1
+
+
+def test_create_checks_nvfp4_block_scales(lib):
+    from mixture_experts_ffn_gemv_gb300.binding import MoeExpertWeights
+    out = ctypes.c_void_p()
+    cfg4 = _cfg(weights=2, inter=256, hidden=512)
+    f = 0x10000
+    no_blocks = MoeExpertWeights(f, f, f, f, f, f)                       # NVFP4 without block scales
+    assert lib.moe_layer_create(ctypes.byref(cfg4), ctypes.byref(no_blocks), None, ctypes.byref(out)) == 1
+    no_tensor = MoeExpertWeights(f, f, f, None, None, None, None, f, f, f)  # ... or without tensor scales
+    assert lib.moe_layer_create(ctypes.byref(cfg4), ctypes.byref(no_tensor), None, ctypes.byref(out)) == 1
+    odd = MoeExpertWeights(f, f, f, f, f, f, None, f, f + 2, f)          # misaligned block scales
+    assert lib.moe_layer_create(ctypes.byref(cfg4), ctypes.byref(odd), None, ctypes.byref(out)) == 1
+    bf16_with_blocks = MoeExpertWeights(f, f, f, None, None, None, None, f, f, f)
+    assert lib.moe_layer_create(ctypes.byref(_cfg()), ctypes.byref(bf16_with_blocks), None,
+                                ctypes.byref(out)) == 1
+    assert not out.value
 
 
 def test_gate_only_on_the_shared_expert(lib):
@@ -118,3 +139,6 @@ def test_null_layer_calls_are_rejected(lib):
     assert lib.moe_last_launch_count(None) == -1
     assert lib.moe_act_quant_fp8(None, 4, 100, None, None, None) == 1  # n % 128 != 0
     assert lib.moe_act_quant_fp8(None, 0, 128, None, None, None) == 0  # nothing to do
+    assert lib.moe_act_quant_nvfp4(None, 4, 100, None, None, None, None) == 1  # n % 16 != 0
+    assert lib.moe_act_quant_nvfp4(None, 0, 128, None, None, None, None) == 0
+    assert lib.moe_act_quant_nvfp4(None, 4, 128, None, None, None, None) == 1  # null pointers
