@@ -183,6 +183,10 @@ def kernel_alg_bytes(kernel, shape, m, U):
             return int(U * 2 * I_ * H * NVFP4_B + m * (H * NVFP4_B + 4) + rows * I_ * 4)
         if kernel == "gemv_down":
             return int(U * H * I_ * NVFP4_B + rows * (I_ * NVFP4_B + 4) + rows * H * 4)
+        if kernel == "gemm_gateup":  # f16 A rows in, packed weights, fp32 h out
+            return int(U * 2 * I_ * H * NVFP4_B + rows * (H * 2 + 4) + rows * I_ * 4)
+        if kernel == "gemm_down":
+            return int(U * H * I_ * NVFP4_B + rows * (I_ * 2 + 4) + rows * H * 2)
         if kernel == "act_quant_nvfp4":
             return int(m * H * 2 + m * (H * NVFP4_B + 4))
         if kernel == "h_quant_nvfp4":
@@ -397,7 +401,7 @@ def sweep(device, steps, warmup):
     tc = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1e12
     res = []
     for name in ("qwen3_decode", "qwen3_prefill", "deepseek_v3_fp8", "qwen3_zipf", "deepseek_v3_sigmoid",
-                 "gated_shared", "qwen3_nvfp4"):
+                 "gated_shared", "qwen3_nvfp4", "qwen3_nvfp4_prefill"):
         wl = I.WORKLOADS[name]
         for m in wl.ms:
             try:

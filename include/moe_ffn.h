@@ -70,7 +70,7 @@ extern "C" {
  * projection's input h) are quantised per row: g = amax(row) / 2688 (1 for
  * an all-zero row); per 16-block sb = e4m3(RNE, saturating)(amax / (6 g));
  * code = e2m1(RNE, saturating)(v / (decode(sb) * g)), 0 where that scale is
- * 0.  Only the GEMV arm takes NVFP4 layers. */
+ * 0.  Both arms take NVFP4 layers. */
 #define MOE_WEIGHTS_NVFP4 2
 
 /* ---- router scoring ("2. Batched topK dispatch" of forward_prefill.rs) */

@@ -102,6 +102,7 @@ struct Layout {
     size_t hdr, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile, sorted_pair, slot_of_pair;
     size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, sgate, total;
     size_t xsb, xg, hsb, hg;  // nvfp4: block scales and row scales of x and h
+    size_t xs_g, h16;         // nvfp4 GEMM arm: gathered rows' scales, f16 h
     int S, P, rows, nchunk;
     bool router_tc;
 };
@@ -144,6 +145,10 @@ Layout layout(const moe_layer* L, int64_t m) {
         o.hf = take((size_t)o.rows * I * 4);
         o.y = take((size_t)o.rows * H * 4);
         o.sgate = L->shared.gate ? take((size_t)m * 4) : 0;
+        // grouped-GEMM arm: the sorted rows widened to f16, their scales, f16 h
+        o.xs = take((size_t)o.rows * H * 2);
+        o.xs_g = take((size_t)o.rows * 4);
+        o.h16 = take((size_t)o.rows * I * 2);
         o.total = off;
         return o;
     }
@@ -300,7 +305,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
             MOE_LAUNCH(K_ACT_QUANT_NVFP4,
                        launch_act_quant_nvfp4_bf16(static_cast<const uint16_t*>(x), m, H, xq, xsb, xg, st));
             MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_nvfp4(a, xq, xsb, xg, hf, st));
-            MOE_LAUNCH(K_H_QUANT_NVFP4, launch_act_quant_nvfp4_f32(hf, lo.rows, I, hq, hsb, hg, st));
+            MOE_LAUNCH(K_H_QUANT_NVFP4, launch_act_quant_nvfp4_f32(hf, lo.rows, I, hq, hsb, hg, nullptr, st));
             MOE_LAUNCH(K_GEMV_DOWN, launch_gemv_down_nvfp4(a, hq, hsb, hg, y, st));
         } else if (L->fp8) {
             uint8_t* xq = at<uint8_t>(ws, lo.xq);
@@ -326,7 +331,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
         return MOE_OK;
     }
     if (arm != MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
-    if (L->nvfp4 || !gemm_supported(L->cfg)) return MOE_ERR_UNSUPPORTED;
+    if (!gemm_supported(L->cfg)) return MOE_ERR_UNSUPPORTED;
     GemmCall g{};
     g.hdr = hdr;
     g.grp_off = po.grp_off;
@@ -339,7 +344,21 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     g.I = I;
     g.max_tiles = gemm_max_tiles(lo.P, E, has_shared, m);
     uint16_t* ybf = at<uint16_t>(ws, lo.y);
-    if (L->fp8) {
+    if (L->nvfp4) {
+        // x to NVFP4, then the sorted rows widened to f16 (the A operand)
+        uint8_t* xq = at<uint8_t>(ws, lo.xq);
+        uint8_t* xsb = at<uint8_t>(ws, lo.xsb);
+        float* xg = at<float>(ws, lo.xg);
+        MOE_LAUNCH(K_ACT_QUANT_NVFP4,
+                   launch_act_quant_nvfp4_bf16(static_cast<const uint16_t*>(x), m, H, xq, xsb, xg, st));
+        MOE_LAUNCH(K_GATHER, launch_gather_nvfp4(xq, xsb, xg, po.sorted_pair, k, lo.P, lo.rows, H,
+                                                 at<uint32_t>(ws, lo.xs), at<float>(ws, lo.xs_g), st));
+        g.xs = at<void>(ws, lo.xs);
+        g.xs_g = at<float>(ws, lo.xs_g);
+        g.h = at<void>(ws, lo.h16);
+        g.h_g = at<float>(ws, lo.hg);
+        g.hf = at<float>(ws, lo.hf);
+    } else if (L->fp8) {
         uint8_t* xq = at<uint8_t>(ws, lo.xq);
         float* xsc = at<float>(ws, lo.xsc);
         if (!x_quantized)
@@ -361,6 +380,10 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     int rc = gemm_plan(L->gemm, g, &gl);
     if (rc != MOE_OK) return rc;
     MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(gl, st));
+    if (L->nvfp4)  // h (fp32, both scales applied) to NVFP4 and to the down GEMM's f16 A operand
+        MOE_LAUNCH(K_H_QUANT_NVFP4, launch_act_quant_nvfp4_f32(at<float>(ws, lo.hf), lo.rows, I, at<uint8_t>(ws, lo.h),
+                                                               at<uint8_t>(ws, lo.hsb), at<float>(ws, lo.hg),
+                                                               at<uint32_t>(ws, lo.h16), st));
     MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(gl, st));
     if (tail)
         MOE_LAUNCH(K_COMBINE, launch_combine_tail_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, *tail, st));

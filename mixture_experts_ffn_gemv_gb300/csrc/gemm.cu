@@ -290,8 +290,9 @@ cudaError_t set_smem_attr() {
 }  // namespace
 
 bool gemm_supported(const moe_config& c) {
-    return (c.weights == MOE_WEIGHTS_BF16 || c.weights == MOE_WEIGHTS_FP8_E4M3_B128) && c.hidden % 256 == 0 &&
-           c.inter % 128 == 0 && c.num_experts <= kMaxExperts;
+    return (c.weights == MOE_WEIGHTS_BF16 || c.weights == MOE_WEIGHTS_FP8_E4M3_B128 ||
+            c.weights == MOE_WEIGHTS_NVFP4) &&
+           c.hidden % 256 == 0 && c.inter % 128 == 0 && c.num_experts <= kMaxExperts;
 }
 
 int gemm_max_tiles(int P, int E, int has_shared, int m) {
@@ -303,6 +304,34 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
     out->ready = false;
     if (!gemm_supported(c)) return MOE_OK;
     out->fp8 = c.weights == MOE_WEIGHTS_FP8_E4M3_B128;
+    out->nvfp4 = c.weights == MOE_WEIGHTS_NVFP4;
+    if (out->nvfp4) {
+        // packed codes, unswizzled 32-byte boxes (64 codes of K) of 128 (W1, W3)
+        // or 256 (W2) rows: the converter warps widen them in shared memory
+        const uint64_t H = c.hidden, I = c.inter, E = c.num_experts;
+        const uint64_t d13[3] = {H / 2, I, E}, d2[3] = {I / 2, H, E};
+        const uint64_t s13[3] = {H / 2, I, 1}, s2[3] = {I / 2, H, 1};
+        if (!tmap_encode(&out->w1, routed->w1, 3, d13, 1, 32, 128, false) ||
+            !tmap_encode(&out->w3, routed->w3, 3, d13, 1, 32, 128, false) ||
+            !tmap_encode(&out->w2, routed->w2, 3, d2, 1, 32, BN, false))
+            return MOE_ERR_CUDA;
+        out->s1 = routed->s1; out->s3 = routed->s3; out->s2 = routed->s2;
+        out->sb1 = routed->sb1; out->sb3 = routed->sb3; out->sb2 = routed->sb2;
+        if (shared) {
+            if (!tmap_encode(&out->sw1, shared->w1, 3, s13, 1, 32, 128, false) ||
+                !tmap_encode(&out->sw3, shared->w3, 3, s13, 1, 32, 128, false) ||
+                !tmap_encode(&out->sw2, shared->w2, 3, s2, 1, 32, BN, false))
+                return MOE_ERR_CUDA;
+            out->ss1 = shared->s1; out->ss3 = shared->s3; out->ss2 = shared->s2;
+            out->ssb1 = shared->sb1; out->ssb3 = shared->sb3; out->ssb2 = shared->sb2;
+        } else {
+            out->sw1 = out->w1; out->sw3 = out->w3; out->sw2 = out->w2;
+            out->ss1 = out->s1; out->ss3 = out->s3; out->ss2 = out->s2;
+            out->ssb1 = out->sb1; out->ssb3 = out->sb3; out->ssb2 = out->sb2;
+        }
+        out->ready = true;
+        return MOE_OK;
+    }
     const int es = out->fp8 ? 1 : 2;
     const uint32_t bc = 128 / es;  // one 128-byte swizzle row of K per box
     const uint64_t H = c.hidden, I = c.inter, E = c.num_experts;
@@ -348,6 +377,7 @@ int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out) {
 }
 
 cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
+    if (L.w->nvfp4) return launch_gemm_nvfp4_gateup(L, st);
     if (L.w->fp8) return launch_gemm_fp8_gateup(L, st);
     cudaError_t e = set_smem_attr<true>();
     if (e != cudaSuccess) return e;
@@ -360,6 +390,7 @@ cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
 }
 
 cudaError_t launch_gemm_down(const GemmLaunch& L, cudaStream_t st) {
+    if (L.w->nvfp4) return launch_gemm_nvfp4_down(L, st);
     if (L.w->fp8) return launch_gemm_fp8_down(L, st);
     cudaError_t e = set_smem_attr<false>();
     if (e != cudaSuccess) return e;

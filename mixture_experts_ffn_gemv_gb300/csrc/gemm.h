@@ -14,10 +14,12 @@ struct WsHeader;
 // TMA descriptors of the stacked weights, built once per layer on the host.
 struct GemmWeights {
     bool ready;
-    bool fp8;  // e4m3 codes with 128x128 fp32 block scales
+    bool fp8;    // e4m3 codes with 128x128 fp32 block scales
+    bool nvfp4;  // packed e2m1 codes: unswizzled maps of 32-byte boxes (64 codes of K)
     CUtensorMap w1, w3, w2;
     CUtensorMap sw1, sw3, sw2;
-    const float *s1, *s3, *s2, *ss1, *ss3, *ss2;  // fp8 block scales (routed, shared)
+    const float *s1, *s3, *s2, *ss1, *ss3, *ss2;  // fp8 block scales / nvfp4 matrix scales (routed, shared)
+    const uint8_t *sb1, *sb3, *sb2, *ssb1, *ssb3, *ssb2;  // nvfp4 e4m3 block scales
 };
 
 struct GemmCall {
@@ -29,9 +31,14 @@ struct GemmCall {
     int rows, E, H, I, max_tiles;
     void* xs;      // gathered activations [rows, H] (bf16 or e4m3)
     float* xs_sc;  // fp8: [rows, H/128]
-    void* h;       // [rows, I] (bf16 or e4m3)
+    void* h;       // [rows, I] (bf16, e4m3, or for nvfp4 the f16 block-scaled values)
     float* hsc;    // fp8: [rows, I/128]
     uint16_t* y;   // [rows, H] bf16
+    // nvfp4: row scales of the gathered x rows and of h, and the fp32 h the
+    // gate/up GEMM writes for the row quantiser
+    const float* xs_g;
+    const float* h_g;
+    float* hf;
 };
 
 // Everything the two grouped-GEMM launches of one call need (tensor maps of
@@ -53,5 +60,7 @@ cudaError_t launch_gemm_gateup(const GemmLaunch& p, cudaStream_t st);
 cudaError_t launch_gemm_down(const GemmLaunch& p, cudaStream_t st);
 cudaError_t launch_gemm_fp8_gateup(const GemmLaunch& p, cudaStream_t st);
 cudaError_t launch_gemm_fp8_down(const GemmLaunch& p, cudaStream_t st);
+cudaError_t launch_gemm_nvfp4_gateup(const GemmLaunch& p, cudaStream_t st);
+cudaError_t launch_gemm_nvfp4_down(const GemmLaunch& p, cudaStream_t st);
 
 }  // namespace moe

@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
+#include "nvfp4.cuh"
 
 namespace moe {
 
@@ -81,41 +82,6 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// The two e4m3 block-scale codes of a 16-byte chunk (block 0 in the low byte)
-// -> each scale as an f16x2 splat.
-__device__ __forceinline__ void nvfp4_scales(uint32_t two_codes, uint32_t& s0, uint32_t& s1) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_codes));
-    s0 = __byte_perm(h2, 0, 0x1010);
-    s1 = __byte_perm(h2, 0, 0x3232);
-}
-
-// Four bytes of e2m1 code pairs -> four f16x2 values, each times the scale s.
-// The halves of every pair come out in one fixed order; weights and
-// activations are widened the same way, so a dot product over them is
-// unchanged by it.
-__device__ __forceinline__ void nvfp4_word(uint32_t w, uint32_t s, uint32_t (&v)[4]) {
-    uint32_t d0, d1, d2, d3;
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
-        : "r"(w));
-    v[0] = hmul2(d0, s);
-    v[1] = hmul2(d1, s);
-    v[2] = hmul2(d2, s);
-    v[3] = hmul2(d3, s);
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int i) {

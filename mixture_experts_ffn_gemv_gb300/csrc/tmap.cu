@@ -29,7 +29,7 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool tmap_encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, int esize, uint32_t box_cols,
-                 uint32_t box_rows) {
+                 uint32_t box_rows, bool swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || rank < 2 || rank > 3) return false;
     cuuint64_t gdim[3], gstride[2];
@@ -39,7 +39,9 @@ bool tmap_encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dim
     if (rank == 3) gstride[1] = dims[0] * dims[1] * esize;
     const CUresult r = fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                           (cuuint32_t)rank, const_cast<void*>(base), gdim, gstride, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

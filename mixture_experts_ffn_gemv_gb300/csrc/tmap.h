@@ -8,10 +8,11 @@
 namespace moe {
 
 // Row-major tensor of `rank` (2 or 3) dims, dims[0] innermost, elements of
-// esize bytes (2 = bf16, 1 = e4m3 codes); box of box_cols x box_rows (x 1);
-// 128-byte swizzle; out-of-range elements read as zero.
+// esize bytes (2 = bf16 / f16, 1 = byte codes); box of box_cols x box_rows
+// (x 1); 128-byte swizzle unless swizzle is false (the box then lands densely,
+// row after row); out-of-range elements read as zero.
 bool tmap_encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, int esize, uint32_t box_cols,
-                 uint32_t box_rows);
+                 uint32_t box_rows, bool swizzle = true);
 
 int device_sm_count();
 

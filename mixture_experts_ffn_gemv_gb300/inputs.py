@@ -98,6 +98,7 @@ WORKLOADS = {
     "deepseek_v3_sigmoid": Workload("deepseek_v3_sigmoid", DEEPSEEK_V3_SIGMOID, (1, 16, 512), correction_std=0.01),
     "gated_shared": Workload("gated_shared", GATED_SHARED, (16, 512)),
     "qwen3_nvfp4": Workload("qwen3_nvfp4", QWEN3_NVFP4, (1, 16, 64)),
+    "qwen3_nvfp4_prefill": Workload("qwen3_nvfp4_prefill", QWEN3_NVFP4, (512, 4096, 16384), router="uniform"),
     "small_nvfp4": Workload("small_nvfp4", SMALL_NVFP4, (16, 512)),
 }
 

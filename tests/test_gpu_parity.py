@@ -354,7 +354,8 @@ FULL_CASES = [("tiny", 16)] + [("qwen3_decode", m) for m in (1, 4, 16, 64)] + \
              [("qwen3_prefill", m) for m in (512, 4096, 16384)] + \
              [("deepseek_v3_fp8", m) for m in (1, 16, 4096)] + [("qwen3_zipf", 8192)] + \
              [("deepseek_v3_sigmoid", m) for m in (1, 16, 512)] + [("gated_shared", m) for m in (16, 512)] + \
-             [("qwen3_nvfp4", m) for m in (1, 16, 64)] + [("small_nvfp4", m) for m in (16, 512)]
+             [("qwen3_nvfp4", m) for m in (1, 16, 64)] + [("small_nvfp4", m) for m in (16, 512)] + \
+             [("qwen3_nvfp4_prefill", m) for m in (512, 4096)]
 
 
 @pytest.mark.parametrize("wl_name,m", FULL_CASES)
