@@ -287,38 +287,49 @@ __device__ __forceinline__ void load16<float>(const float* p, float (&f)[16]) {
     }
 }
 
-// One block of 128 threads per row of n (a multiple of 16) values:
+// WPR warps per row of n (a multiple of 16) values, 8 / WPR rows per block
+// (four warps per row while rows are few, one warp per row when there are
+// many):
 //   g = amax(row) / 2688 (1 for an all-zero row), 2688 = 6 * 448;
 //   per 16-block: sb = e4m3(RNE, satfinite)(amax(block) / (6 g));
 //   code = e2m1(v / (decode(sb) * g)), 0 when that scale is 0.
 // Codes are packed two per byte, element 2j in the low nibble of byte j.
 // deq (optional): the f16 values decode(code) * decode(sb) (without g), as
 // nvfp4_word widens them -- the grouped GEMM's A operand.
-template <typename T>
-__global__ __launch_bounds__(128) void act_quant_nvfp4(const T* __restrict__ v, int rows, int n,
+template <typename T, int WPR>
+__global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, int rows, int n,
                                                        uint8_t* __restrict__ q, uint8_t* __restrict__ sb,
                                                        float* __restrict__ g, uint32_t* __restrict__ deq) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float wmax[4];
-    const int r = blockIdx.x;
+    constexpr int TPR = 32 * WPR;  // threads per row
+    __shared__ float wmax[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (8 / WPR) + warp / WPR;
+    const int tr = (warp % WPR) * 32 + lane;  // thread index within the row
+    const bool live = r < rows;                // rows past the end still meet the barrier
     const int nb = n / 16;
-    const T* row = v + (size_t)r * n;
+    const T* row = v + (size_t)(live ? r : 0) * n;
     float am = 0.f;
-    for (int b = threadIdx.x; b < nb; b += 128) {
+    for (int b = tr; live && b < nb; b += TPR) {
         float f[16];
         load16(row + (size_t)b * 16, f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(f[i]));
     }
     am = warp_max(am);
-    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = am;
-    __syncthreads();
-    am = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    if (WPR > 1) {
+        if (lane == 0) wmax[warp] = am;
+        __syncthreads();
+        const int w0 = (warp / WPR) * WPR;
+#pragma unroll
+        for (int i = 0; i < WPR; ++i) am = fmaxf(am, wmax[w0 + i]);
+    }
+    if (!live) return;
     const float gs = am > 0.f ? __fdiv_rn(am, 2688.0f) : 1.0f;
-    if (threadIdx.x == 0) g[r] = gs;
+    if (tr == 0) g[r] = gs;
     const float six_g = __fmul_rn(6.0f, gs);
-    for (int b = threadIdx.x; b < nb; b += 128) {
+    for (int b = tr; b < nb; b += TPR) {
         float f[16];
         load16(row + (size_t)b * 16, f);
         float bm = 0.f;
@@ -346,6 +357,18 @@ __global__ __launch_bounds__(128) void act_quant_nvfp4(const T* __restrict__ v, 
             d[1] = make_uint4(c[0], c[1], c[2], c[3]);
         }
     }
+}
+
+// rows up to this take four warps per row
+constexpr int kQuantFewRows = 1024;
+
+template <typename T>
+static void launch_act_quant_nvfp4(const T* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g, uint32_t* deq,
+                                   cudaStream_t st) {
+    if (rows <= kQuantFewRows)
+        launch_pdl(act_quant_nvfp4<T, 4>, dim3(ceil_div(rows, 2)), dim3(256), 0, st, v, rows, n, q, sb, g, deq);
+    else
+        launch_pdl(act_quant_nvfp4<T, 1>, dim3(ceil_div(rows, 8)), dim3(256), 0, st, v, rows, n, q, sb, g, deq);
 }
 
 // Grouped-GEMM A operand of an NVFP4 layer: row s of the sorted order gets
@@ -387,13 +410,13 @@ cudaError_t launch_gather_nvfp4(const uint8_t* xq, const uint8_t* xsb, const flo
 
 cudaError_t launch_act_quant_nvfp4_bf16(const uint16_t* x, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                         cudaStream_t st) {
-    launch_pdl(act_quant_nvfp4<uint16_t>, dim3(rows), dim3(128), 0, st, x, rows, n, q, sb, g, (uint32_t*)nullptr);
+    launch_act_quant_nvfp4<uint16_t>(x, rows, n, q, sb, g, nullptr, st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_act_quant_nvfp4_f32(const float* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                        uint32_t* deq, cudaStream_t st) {
-    launch_pdl(act_quant_nvfp4<float>, dim3(rows), dim3(128), 0, st, v, rows, n, q, sb, g, deq);
+    launch_act_quant_nvfp4<float>(v, rows, n, q, sb, g, deq, st);
     return cudaGetLastError();
 }
 

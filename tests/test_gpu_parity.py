@@ -80,11 +80,12 @@ def test_act_quant_fp8_bitwise(cuda, oracle_mod):
         assert np.array_equal(scales[r].cpu().numpy(), s), f"row {r}"
 
 
-@pytest.mark.parametrize("n", [768, 2048, 7168])
-def test_act_quant_nvfp4_bitwise(cuda, oracle_mod, n):
+@pytest.mark.parametrize("n,rows", [(768, 23), (2048, 23), (7168, 23), (768, 1100)])
+def test_act_quant_nvfp4_bitwise(cuda, oracle_mod, n, rows):
+    """Both launch shapes: four warps per row (few rows), one warp per row (many)."""
     from mixture_experts_ffn_gemv_gb300 import binding
     shape = I.LayerShape(hidden=n, num_experts=1, top_k=1, inter=256)
-    x = I.make_x(shape, 23, seed=22, device=cuda)
+    x = I.make_x(shape, rows, seed=22, device=cuda)
     x[1] = 0                     # an all-zero row: g = 1, codes and scales 0
     x[2, 16:32] = 0              # an all-zero block
     x[3, :n // 2] *= 1e-4        # blocks far below the row's amax (small / zero scales)
