@@ -10,11 +10,12 @@
 //   A  f16 [rows, K], widened once before the GEMM (the NVFP4 gather for
 //      gate/up, the row quantiser for down), loaded by TMA (128B swizzle);
 //   B  the packed weight codes of the tile (64 of K = 32 bytes per row) land
-//      by TMA in a staging area of the stage; eight converter warps widen them
-//      into the stage's f16 B tile in the 128-byte swizzled K-major layout the
-//      MMA descriptor reads, then arrive on the stage's conversion barrier.
-// Warps: 0 TMA producer, 1 MMA issuer, 2..9 epilogue (as in gemm.cu),
-// 10..17 converters.  Every mbarrier wait is bounded (2 s); on expiry the CTA
+//      by TMA beside A in a 5-deep ring; sixteen converter warps widen them
+//      into one of three f16 B tiles in the 128-byte swizzled K-major layout
+//      the MMA descriptor reads.  The rings decouple load latency, conversion
+//      and the tensor core: each runs ahead of the next by its ring depth.
+// Warps: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (one per TMEM lane
+// quarter), 6..21 converters.  Every mbarrier wait is bounded (2 s); on expiry the CTA
 // records DEV_ERR_TIMEOUT, stops, drains its tensor-core work and frees TMEM.
 #include <cuda_runtime.h>
 
@@ -33,14 +34,19 @@ namespace {
 using namespace sm100;
 
 constexpr int BM = 128, BN = 256, BK = 64;  // BK f16 = one 128-byte swizzle row
-constexpr int STAGES = 3;
+constexpr int STAGES = 5;                    // TMA ring: A tile + the B tile's codes
+constexpr int BBUFS = 3;                     // f16 B tiles between converters and MMA
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int C_BYTES = BN * BK / 2;  // the B tile's packed codes, 32 bytes per weight row
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + C_BYTES;
+constexpr int A_OFF = 0;
+constexpr int B_OFF = STAGES * A_BYTES;
+constexpr int C_OFF = B_OFF + BBUFS * B_BYTES;
+constexpr int BAR_OFF = C_OFF + STAGES * C_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int EPI_WARPS = 8;
-constexpr int CONV_WARPS = 8;
+constexpr int EPI_WARPS = 4;    // one per TMEM lane quarter: a tile's epilogue overlaps the next tile's MMAs
+constexpr int EPI_SPLIT = EPI_WARPS / 4;
+constexpr int CONV_WARPS = 16;  // conversion, not the MMA, paces this kernel
 constexpr int CONV0 = 2 + EPI_WARPS;  // first converter warp
 constexpr int THREADS = 32 * (CONV0 + CONV_WARPS);
 constexpr int CONV_THREADS = 32 * CONV_WARPS;
@@ -48,8 +54,9 @@ constexpr int TASKS = BN * 8;  // (weight row, 16-byte f16 chunk) pairs of one B
 constexpr int TASKS_PER_THREAD = TASKS / CONV_THREADS;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 constexpr int TABLE_INTS = 2 * kMaxExperts + 4;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + TABLE_INTS * 4;
-static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256 + TABLE_INTS * 4;
+static_assert(A_BYTES % 1024 == 0 && B_OFF % 1024 == 0, "swizzled tiles keep 1024-byte alignment");
+static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM's shared memory");
 static_assert(TASKS % CONV_THREADS == 0, "whole conversion tasks per thread");
 
 // kind::f16 instruction descriptor with f16 A and B (format code 0), fp32 D,
@@ -106,13 +113,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    const uint32_t full0 = smem_u32(bars), conv0 = smem_u32(bars + STAGES), empty0 = smem_u32(bars + 2 * STAGES);
-    const uint32_t tfull0 = smem_u32(bars + 3 * STAGES), tempty0 = smem_u32(bars + 3 * STAGES + 2);
-    const uint32_t drain = smem_u32(bars + 3 * STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+    // full: A + codes landed; aempty: MMA done with the A slot; cempty:
+    // converters done with the codes slot; bfull / bempty: an f16 B tile
+    // written / consumed
+    const uint32_t full0 = smem_u32(bars), aempty0 = smem_u32(bars + STAGES), cempty0 = smem_u32(bars + 2 * STAGES);
+    const uint32_t bfull0 = smem_u32(bars + 3 * STAGES), bempty0 = smem_u32(bars + 3 * STAGES + BBUFS);
+    const uint32_t tfull0 = smem_u32(bars + 3 * STAGES + 2 * BBUFS), tempty0 = tfull0 + 16;
+    const uint32_t drain = tempty0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2 * BBUFS + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* s_tile = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+    int* s_tile = reinterpret_cast<int*>(smem + BAR_OFF + 256);
     int* s_group = s_tile + kMaxExperts + 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,8 +134,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(conv0 + 8 * s, CONV_WARPS);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(aempty0 + 8 * s, 1);
+            mbar_init(cempty0 + 8 * s, CONV_WARPS);
+        }
+        for (int b = 0; b < BBUFS; ++b) {
+            mbar_init(bfull0 + 8 * b, CONV_WARPS);
+            mbar_init(bempty0 + 8 * b, 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull0 + 8 * a, 1);
@@ -161,11 +176,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int gz = routed ? g : 0;
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, WAIT_NS)) {
+                    if (!mbar_wait(aempty0 + 8 * s, ph ^ 1u, WAIT_NS) || !mbar_wait(cempty0 + 8 * s, ph ^ 1u, WAIT_NS)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = sbase + s * STAGE_BYTES, sc = sa + A_BYTES + B_BYTES;
+                    const uint32_t sa = sbase + A_OFF + s * A_BYTES, sc = sbase + C_OFF + s * C_BYTES;
                     mbar_arrive_expect_tx(full0 + 8 * s, A_BYTES + C_BYTES);
                     tma_load_2d(sa, &tmA, kb * BK, row0, full0 + 8 * s);
                     if (GATEUP) {
@@ -200,17 +215,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d = tmem_base + acc * BN;
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS) || !mbar_wait(conv0 + 8 * s, ph, WAIT_NS)) {
+                    const uint32_t b = it % BBUFS, bph = (it / BBUFS) & 1u;
+                    if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS) || !mbar_wait(bfull0 + 8 * b, bph, WAIT_NS)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = desc_sw128(sbase + s * STAGE_BYTES);
-                    const uint64_t bd = desc_sw128(sbase + s * STAGE_BYTES + A_BYTES);
+                    const uint64_t ad = desc_sw128(sbase + A_OFF + s * A_BYTES);
+                    const uint64_t bd = desc_sw128(sbase + B_OFF + b * B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per MMA
                         mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-                    mma_commit(empty0 + 8 * s);
+                    mma_commit(aempty0 + 8 * s);
+                    mma_commit(bempty0 + 8 * b);
                 }
                 if (!ok) break;
                 mma_commit(tfull0 + 8 * acc);
@@ -247,17 +264,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 srow[i] = reinterpret_cast<const uint32_t*>(base);
             }
             bool ok = true;
+            // each row's 4 block scales of a K step, loaded one step ahead
+            uint32_t sw[TASKS_PER_THREAD], swn[TASKS_PER_THREAD];
+#pragma unroll
+            for (int i = 0; i < TASKS_PER_THREAD; ++i) sw[i] = __ldg(srow[i]);
             for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                 const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                uint32_t sw[TASKS_PER_THREAD];  // the row's 4 block scales of this K step
+                const uint32_t b = it % BBUFS, bph = (it / BBUFS) & 1u;
+                const int kn = kb + 1 < p.kblocks ? kb + 1 : kb;
 #pragma unroll
-                for (int i = 0; i < TASKS_PER_THREAD; ++i) sw[i] = __ldg(srow[i] + kb);
-                if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS)) {
+                for (int i = 0; i < TASKS_PER_THREAD; ++i) swn[i] = __ldg(srow[i] + kn);
+                if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS) || !mbar_wait(bempty0 + 8 * b, bph ^ 1u, WAIT_NS)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* stg = smem + s * STAGE_BYTES + A_BYTES + B_BYTES;
-                const uint32_t bt = sbase + s * STAGE_BYTES + A_BYTES;
+                const uint8_t* stg = smem + C_OFF + s * C_BYTES;
+                const uint32_t bt = sbase + B_OFF + b * B_BYTES;
 #pragma unroll
                 for (int i = 0; i < TASKS_PER_THREAD; ++i) {
                     const int task = ct + i * CONV_THREADS;
@@ -270,7 +292,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 fence_async_shared();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(conv0 + 8 * s);
+                if (lane == 0) {
+                    mbar_arrive(cempty0 + 8 * s);
+                    mbar_arrive(bfull0 + 8 * b);
+                }
+#pragma unroll
+                for (int i = 0; i < TASKS_PER_THREAD; ++i) sw[i] = swn[i];
             }
             if (!ok) {
                 set_error(p.hdr, DEV_ERR_TIMEOUT, 13);
@@ -279,8 +306,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else {
-        const int q = warp & 3;            // the TMEM lane quarter this warp may read
-        const int half = (warp - 2) >> 2;  // which half of the tile's output columns
+        const int q = warp & 3;                    // the TMEM lane quarter this warp may read
+        const int half = (warp - 2) >> 2;          // which part of the tile's output columns
+        constexpr int CG = (BN / 2 / 32) / EPI_SPLIT, CD = (BN / 32) / EPI_SPLIT;  // 32-column chunks per warp
         const int r = q * 32 + lane;
         uint32_t tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
@@ -307,7 +335,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const float su = ar * (routed ? __ldg(p.g1 + g) : __ldg(p.sg1));
                 float* orow = static_cast<float*>(p.out) + srow * p.ldo + nt * (BN / 2);
 #pragma unroll 1
-                for (int c = 2 * half; c < 2 * half + 2; ++c) {
+                for (int c = half * CG; c < (half + 1) * CG; ++c) {
                     uint32_t gv[32], uv[32];
                     tmem_ld32(taddr + c * 32, gv);
                     tmem_ld32(taddr + BN / 2 + c * 32, uv);
@@ -328,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const float sy = ar * (routed ? __ldg(p.g0 + g) : __ldg(p.sg0));
                 uint16_t* orow = static_cast<uint16_t*>(p.out) + srow * p.ldo + nt * BN;
 #pragma unroll 1
-                for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+                for (int c = half * CD; c < (half + 1) * CD; ++c) {
                     uint32_t dv[32];
                     tmem_ld32(taddr + c * 32, dv);
                     tmem_wait_ld();
