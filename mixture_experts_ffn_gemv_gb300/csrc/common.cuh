@@ -14,7 +14,8 @@ struct WsHeader {
     int done;         // permute: chunks finished (last chunk does the scan)
     int n_active;     // groups with at least one row
     int total_tiles;  // grouped GEMM: m-tiles over all active groups
-    int pad[59];
+    int group_done[32];  // fused decode routing: slices finished per group of 8 experts
+    int pad[27];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

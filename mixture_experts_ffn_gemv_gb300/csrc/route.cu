@@ -147,8 +147,9 @@ __global__ __launch_bounds__(256) void topk_softmax(const float* __restrict__ pa
 //            order.  No partial slices for the tail to add.
 //   m > 4    route_permute_sliced: split-H partials [S, m, E] exactly as
 //            router_partial_small (8 experts x one H-slice per block, 16-token
-//            passes), which re-reads x least; the tail adds the S slices in
-//            slice order.
+//            passes), which re-reads x least.  The last of the S blocks of an
+//            expert group (a ticket per group) adds its S slices in slice
+//            order into slice 0; the tail then reads whole logits.
 
 // Shared tail, run by the last block: logits = the S slices of part summed in
 // slice order (into shared memory), then the top-k of every token, then the
@@ -355,8 +356,29 @@ __global__ __launch_bounds__(256) void route_permute_sliced(const uint16_t* __re
             }
         }
     }
-    if (!last_block(hdr, &is_last)) return;
-    route_tail<VPL>(part, gridDim.y, m, E, k, bias, rm, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
+    // the last block of this expert group sums its S slices (in slice order)
+    // into slice 0, spread over all 256 threads
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(&hdr->group_done[blockIdx.x], 1) == (int)gridDim.y - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const int ne = min(8, E - (int)blockIdx.x * 8);
+    for (int i = threadIdx.x; i < m * ne; i += 256) {
+        const int t = i / ne, ee = blockIdx.x * 8 + i % ne;
+        float v = 0.f;
+        for (int q = 0; q < (int)gridDim.y; ++q) v += __ldcg(part + ((size_t)q * m + t) * E + ee);
+        part[(size_t)t * E + ee] = v;
+    }
+    // the last group to finish runs the tail on the whole logits
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(&hdr->done, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    route_tail<VPL>(part, 1, m, E, k, bias, rm, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
 }
 
 // ---------------------------------------------------------------- launchers
