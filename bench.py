@@ -2,19 +2,28 @@
 """Benchmark of the MoE FFN layer forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload qwen3_decode] [--tokens 16] [--no-sweep]
+                    [--workload qwen3_prefill] [--tokens 4096] [--no-sweep]
+                    [--sweep-out FILE]
 
 One step = one forward of the whole layer (router, top-k, permute, experts,
-combine) over one batch of m synthetic tokens.  Steps rotate over R layer
-replicas (different seeds) whose weights together exceed L2 several times, so
-no step finds its experts in L2.  Prints one JSON line (rank 0).
+combine) over one batch of m synthetic tokens.  The default workload is the
+Qwen3-30B-A3B-shaped layer at prefill, m = 4096 tokens, bf16.  Steps rotate
+over R layer replicas (different seeds) whose weights together exceed L2
+several times, so no step finds its experts in L2.
+
+Output: the LAST line of stdout is the one headline JSON object (rank 0).
+The per-size sweep over every workload and the layer-tail comparison go to
+stderr as one compact JSON object per line (and to --sweep-out when given),
+so the headline stays short and last.
 
 Under torchrun (N > 1) every rank runs its own replica set on its own GPU
 with its own tokens (token-parallel, no data-path collective) and the
 whole-job throughput is the tokens of all ranks over the slowest rank's time.
 
 --impl reference times the CPU oracle (the plain per-token loops) on the
-host cores on the same workload; under torchrun only rank 0 runs it.
+host cores on the same workload: every step is one oracle forward of a
+bounded sample of the batch (its first tokens; tokens are independent, so
+those rows are exactly the full batch's); under torchrun only rank 0 runs it.
 """
 from __future__ import annotations
 
@@ -178,15 +187,20 @@ def kernel_alg_bytes(kernel, shape, m, U):
     P = m * k
     rows = P + (m if shape.shared_inter else 0)
     if getattr(shape, "nvfp4", False):
-        # codes + block scales in, row scales, fp32 h out of gate/up
+        # W4A4: weights and activations both count as NVFP4 (a half-byte code
+        # + an e4m3 scale per 16 + an fp32 scale per row); the kernels' own
+        # wider intermediates (f16 A rows, fp32 h) are implementation choices
+        # and are not counted as algorithmic bytes.
+        xa = H * NVFP4_B + 4    # one quantised x row
+        ha = I_ * NVFP4_B + 4   # one quantised h row
         if kernel == "gemv_gateup":
-            return int(U * 2 * I_ * H * NVFP4_B + m * (H * NVFP4_B + 4) + rows * I_ * 4)
+            return int(U * 2 * I_ * H * NVFP4_B + m * xa + rows * ha)
         if kernel == "gemv_down":
-            return int(U * H * I_ * NVFP4_B + rows * (I_ * NVFP4_B + 4) + rows * H * 4)
-        if kernel == "gemm_gateup":  # f16 A rows in, packed weights, fp32 h out
-            return int(U * 2 * I_ * H * NVFP4_B + rows * (H * 2 + 4) + rows * I_ * 4)
+            return int(U * H * I_ * NVFP4_B + rows * ha + rows * H * 2)
+        if kernel == "gemm_gateup":
+            return int(U * 2 * I_ * H * NVFP4_B + rows * xa + rows * ha)
         if kernel == "gemm_down":
-            return int(U * H * I_ * NVFP4_B + rows * (I_ * 2 + 4) + rows * H * 2)
+            return int(U * H * I_ * NVFP4_B + rows * ha + rows * H * 2)
         if kernel == "act_quant_nvfp4":
             return int(m * H * 2 + m * (H * NVFP4_B + 4))
         if kernel == "h_quant_nvfp4":
@@ -372,30 +386,44 @@ def e2e_steps(reps, n, device, dist, m, shape):
     return a.elapsed_time(b), bytes_in, m * shape.hidden * 2
 
 
+def oracle_sample_tokens(shape, m, target_flop=12e9):
+    """Tokens of the bounded oracle sample: about target_flop of expert work
+    (roughly a second on the GPU machine's host cores), at least one, at most m."""
+    per_tok = 2 * 3 * shape.hidden * shape.inter * shape.top_k
+    if shape.shared_inter:
+        per_tok += 2 * 3 * shape.hidden * shape.shared_inter
+    return int(max(1, min(m, round(target_flop / per_tok))))
+
+
 def cpu_baseline(wl, m, reps_host, budget_s=12.0):
-    """The oracle, as it stands, on the host cores: whole-layer forwards of the
-    same m-token batch repeated until ~budget_s of wall time."""
+    """The oracle, as it stands, on the host cores: whole-layer forwards of a
+    bounded sample of the m-token batch (its first tokens, routed and summed
+    exactly as in the full batch, since tokens are independent), repeated
+    until ~budget_s of wall time."""
     import oracle
     cores = oracle.set_threads(os.cpu_count() or 1)
     tensors, x = reps_host
+    ns = oracle_sample_tokens(wl.shape, m)
+    xs = x[:ns].contiguous()
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle.reference(wl.shape, tensors, x)
+        oracle.reference(wl.shape, tensors, xs)
         n += 1
         if time.perf_counter() - t0 >= budget_s or n >= 1000:
             break
     dt = time.perf_counter() - t0
-    return {"value": n * m / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} whole-layer forwards of the {m}-token batch ({wl.name}, seed 0), {dt:.1f} s wall"}
+    return {"value": n * ns / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} oracle forwards of the first {ns} of the {m} tokens, {dt:.1f} s"}
 
 
 def host_copy(tensors):
     return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
 
 
-def sweep(device, steps, warmup):
-    """tokens/s and layer roofline fraction of every workload size (N=1)."""
+def sweep(device, steps, warmup, emit):
+    """tokens/s and layer roofline fraction of every workload size (N=1);
+    emit(row) receives each row as soon as it is measured."""
     pk, _ = peaks()
     bw = pk["hbm_gbs"] * 1e9
     tc = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1e12
@@ -439,7 +467,22 @@ def sweep(device, steps, warmup):
                 reps = None
                 torch.cuda.synchronize(device)
                 torch.cuda.empty_cache()
+            emit(_compact_row(res[-1]))
     return res
+
+
+def _compact_row(row):
+    """A sweep row with its figures rounded (one short line per size)."""
+    out = {}
+    for k, v in row.items():
+        if isinstance(v, float):
+            out[k] = _r(v)
+        elif isinstance(v, dict):
+            out[k] = {kk: ({a: _r(b) for a, b in vv.items()} if isinstance(vv, dict) else _r(vv))
+                      for kk, vv in v.items()}
+        else:
+            out[k] = v
+    return out
 
 
 def tail_timing(reps, n, device, eps=1e-6):
@@ -483,6 +526,33 @@ def tail_timing(reps, n, device, eps=1e-6):
     return res
 
 
+def _r(v, sig=4):
+    """Round a float to `sig` significant digits (keeps the headline short)."""
+    if v is None or not isinstance(v, float) or v == 0.0 or not math.isfinite(v):
+        return v
+    return round(v, sig - 1 - int(math.floor(math.log10(abs(v)))))
+
+
+class SideOutput:
+    """Where the long results go: stderr, one compact JSON object per line,
+    and optionally a JSON-lines file."""
+
+    def __init__(self, path):
+        self.f = open(path, "w") if path else None
+
+    def emit(self, kind, obj):
+        row = dict(kind=kind, **obj)
+        s = json.dumps(row, separators=(",", ":"))
+        print(s, file=sys.stderr, flush=True)
+        if self.f:
+            self.f.write(s + "\n")
+            self.f.flush()
+
+    def close(self):
+        if self.f:
+            self.f.close()
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     dist = init_dist(ws)
@@ -514,6 +584,8 @@ def run_ours(args):
     flops = kernel_flops(dname, shape, m)
     alg = kernel_alg_bytes(dname, shape, m, Umean)
     bw = pk["hbm_gbs"]
+    # a kernel timed inside a step that lasts over a second is held to the
+    # sustained tensor peak, a shorter one to the burst peak
     tc_key = "bf16_tflops_sustained" if ms_max > 1000 else "bf16_tflops"
     tc = pk.get(tc_key, FALLBACK_PEAKS["bf16_tflops"]) * (2.0 if shape.fp8 else 1.0)
     if flops and alg and flops / (tc * 1e12) > alg / (bw * 1e9):
@@ -522,43 +594,50 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": alg / avg_s / 1e9, "peak": bw, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(dname, args.workload, m)
-    roof.update({"kernel": dname, "avg_launch_us": avg_s * 1e6, "alg_bytes_per_launch": alg,
-                 "peak_source": f"{pk_kind} ({'MEASURED_PEAKS.json' if pk_kind == 'measured' else 'fallback'})"})
+    roof.update({"kernel": dname, "launch_us": avg_s * 1e6, "alg_bytes": alg,
+                 "peak_src": "measured" if pk_kind == "measured" else "fallback"})
     lay_b, lay_f = layer_alg(shape, m, Umean)
     t_step = ms_max / args.steps / 1e3
     layer_roof = max(lay_b / (bw * 1e9), lay_f / (tc * 1e12)) / t_step
 
     e2e_ms, bi, bo = e2e_steps(reps, args.steps, device, dist, m, shape)
     e2e_max = max_over_ranks(dist, e2e_ms, device)
+    ktot = sum(t[0] for t in totals.values())
+    top = sorted(totals.items(), key=lambda kv: -kv[1][0])
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": _dtype(shape), "data": "synthetic",
-        "config": {"workload": args.workload + (f" (experts overridden: {args.experts})" if args.experts else ""), "m": m, "hidden": shape.hidden, "experts": shape.num_experts,
-                   "top_k": shape.top_k, "inter": shape.inter, "shared_inter": shape.shared_inter,
-                   "global_batch": ws * m, "parallelism": f"token-parallel x{ws} (replicas, no collective)",
-                   "l2": f"inputs larger than L2: {R} rotating layer replicas, {rep_bytes / 1e9:.1f} GB of weights"},
+        "metric": METRIC, "value": _r(value), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": _r(ms_max / args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": _dtype(shape), "data": "synthetic",
+        "config": {"workload": args.workload + (f"(E={args.experts})" if args.experts else ""), "m": m,
+                   "hidden": shape.hidden, "experts": shape.num_experts, "top_k": shape.top_k,
+                   "inter": shape.inter, "shared_inter": shape.shared_inter, "global_batch": ws * m,
+                   "parallelism": f"token-parallel x{ws}",
+                   "l2": f"inputs > L2: {R} rotating replicas, {rep_bytes / 1e9:.1f} GB"},
         "gpu_launches": launches,
-        "roofline": roof,
-        "layer_roofline": {"frac": layer_roof, "alg_bytes": lay_b, "alg_flops": lay_f, "active_groups": Umean},
-        "kernels": {k: {"total_ms": v[0], "launches": v[1], "share": v[0] / sum(t[0] for t in totals.values())}
-                    for k, v in sorted(totals.items(), key=lambda kv: -kv[1][0])},
-        "e2e": {"value": ws * m * args.steps / (e2e_max / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo},
-        "clocks": clk.summary(),
+        "roofline": {k: _r(v) if isinstance(v, float) else v for k, v in roof.items()},
+        "layer_roofline": {"frac": _r(layer_roof), "alg_bytes": _r(float(lay_b)), "alg_flops": _r(float(lay_f))},
+        "kernel_share": {k: _r(v[0] / ktot, 3) for k, v in top[:5]},
+        "e2e": {"value": _r(ws * m * args.steps / (e2e_max / 1e3)), "unit": "tokens/s",
+                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "clocks": {k: v for k, v in clk.summary().items() if k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
+    side = SideOutput(args.sweep_out if rank == 0 else None)
+    if rank == 0:
+        side.emit("kernels", {"workload": args.workload, "m": m, "us_per_launch": {
+            k: _r(v[0] / v[1] * 1e3) for k, v in top}, "launches_per_step": {k: v[1] / args.steps for k, v in top}})
     if rank == 0 and ws == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, m, (host_copy(reps[0]["tensors"]), reps[0]["x"].cpu()))
+        cb = cpu_baseline(wl, m, (host_copy(reps[0]["tensors"]), reps[0]["x"].cpu()))
+        line["cpu_baseline"] = {k: _r(v) if isinstance(v, float) else v for k, v in cb.items()}
         if not args.no_sweep:
-            line["layer_tail"] = dict(tail_timing(reps, args.steps, device), workload=args.workload, m=m,
-                                      what="residual add + next RMSNorm: fused into the combine vs separate ops")
-        if not args.no_sweep:
+            side.emit("layer_tail", dict(tail_timing(reps, args.steps, device), workload=args.workload, m=m))
             reps = None
             torch.cuda.empty_cache()
-            line["sweep"] = sweep(device, args.steps, args.warmup)
+            sweep(device, args.steps, args.warmup, lambda row: side.emit("sweep", row))
+    side.close()
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        sys.stderr.flush()
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 
@@ -578,26 +657,31 @@ def run_reference(args):
     m = args.m
     tensors = I.make_layer(wl, seed=0, device="cpu")
     x = I.make_x(wl.shape, m, seed=0, device="cpu")
+    # every step: one oracle forward of the batch's first ns tokens (tokens are
+    # independent, so these rows equal the full batch's first ns rows)
+    ns = oracle_sample_tokens(wl.shape, m)
+    xs = x[:ns].contiguous()
     cores = oracle.set_threads(os.cpu_count() or 1)
     for _ in range(max(0, min(args.warmup, 1))):
-        oracle.reference(wl.shape, tensors, x)
+        oracle.reference(wl.shape, tensors, xs)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.reference(wl.shape, tensors, x)
+        oracle.reference(wl.shape, tensors, xs)
     dt = time.perf_counter() - t0
-    value = m * args.steps / dt
+    value = ns * args.steps / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "impl": "reference", "metric": METRIC, "value": _r(value), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": _r(dt / args.steps * 1e3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": _dtype(wl.shape), "data": "synthetic",
-        "config": {"workload": args.workload + (f" (experts overridden: {args.experts})" if args.experts else ""), "m": m, "hidden": wl.shape.hidden, "experts": wl.shape.num_experts,
-                   "top_k": wl.shape.top_k, "inter": wl.shape.inter, "global_batch": m},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} whole-layer forwards of the {m}-token batch on the host cores"},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": {"workload": args.workload + (f"(E={args.experts})" if args.experts else ""), "m": m,
+                   "hidden": wl.shape.hidden, "experts": wl.shape.num_experts, "top_k": wl.shape.top_k,
+                   "inter": wl.shape.inter, "shared_inter": wl.shape.shared_inter, "global_batch": m},
+        "cpu_baseline": {"value": _r(value), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: oracle forward of the first {ns} of the {m} tokens"},
+        "e2e": {"value": _r(value), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(line, separators=(",", ":")), flush=True)
 
 
 def main():
@@ -606,9 +690,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen3_decode", choices=sorted(I.WORKLOADS))
-    ap.add_argument("--tokens", dest="m", type=int, default=16, help="tokens per step (m)")
+    ap.add_argument("--workload", default="qwen3_prefill", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--tokens", dest="m", type=int, default=4096, help="tokens per step (m)")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-out", default=None, help="also write the stderr result rows to this JSON-lines file")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the workload's expert count (small cases for profiling captures)")
     ap.add_argument("--replicas", type=int, default=0, help="override the number of rotating layer replicas")

@@ -163,7 +163,10 @@ MOE_API int moe_route(const moe_layer* layer, const void* x, int64_t m, const fl
  *   expert_offsets int32 [E+1]: exclusive prefix sum of per-expert counts
  *   sorted_pair    int32 [m*k]: pair at sorted slot s (ascending p within an expert)
  *   slot_of_pair   int32 [m*k]: inverse of sorted_pair
- * Ids outside [0, E) set the device error word (MOE_ERR_DEVICE).            */
+ * Ids outside [0, E) set the device error word (MOE_ERR_DEVICE).  Such a pair
+ * is dropped: its slot_of_pair entry is -1, expert_offsets[E] counts only the
+ * valid pairs (so it is then below m*k), and sorted_pair is written only up
+ * to that count.                                                            */
 MOE_API int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t m,
                 int32_t* expert_offsets, int32_t* sorted_pair, int32_t* slot_of_pair,
                 void* workspace, size_t workspace_bytes, void* stream);
@@ -185,9 +188,14 @@ MOE_API int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t
  * All calls on a device share that one array and it keeps the last call's
  * contents: each call clears the part that must start at zero itself, but two
  * calls that overlap on the GPU (different streams without ordering between
- * them) race on it; order them on one stream.  The first call on a device
- * looks up the array's device address (with that device current), so make it
- * before any stream capture begins.                                        */
+ * them) race on it; order them on one stream.  Every call looks up the
+ * array's device address on the current device (a host-side query); the
+ * first lookup on a device loads this library's device code there, so make
+ * the first call before any stream capture begins.
+ * Out-of-range ids are handled as in moe_permute (the pair is dropped,
+ * slot_of_pair -1, expert_offsets[E] counts only the valid pairs), but with
+ * no workspace there is no error word the caller can read: a caller that may
+ * pass such ids checks expert_offsets[E] == m * top_k after the stream.     */
 MOE_API int moe_permute_noalloc(const int32_t* topk_ids, int64_t m, int32_t top_k, int32_t num_experts,
                                 int32_t* expert_offsets, int32_t* sorted_pair, int32_t* slot_of_pair,
                                 void* stream);
@@ -247,6 +255,28 @@ MOE_API int moe_act_quant_nvfp4(const void* x, int64_t rows, int64_t n, uint8_t*
  * in `workspace` (0 = none).  Returns MOE_OK, MOE_ERR_DEVICE when the word is
  * set, or MOE_ERR_CUDA.                                                     */
 MOE_API int moe_device_status(const void* workspace, void* stream, int32_t* device_code);
+
+/* Limit, in nanoseconds of GPU wall time, of every bounded wait inside the
+ * grouped-GEMM kernels (the mbarrier waits between their TMA producer,
+ * tensor-core issuer and epilogue warps); 0 restores the default of 2 s.
+ * A wait that runs out makes its kernel record DEV_ERR_TIMEOUT (2) in the
+ * workspace's device error word, stop issuing work, wait (2 s at most) for
+ * the copies and MMAs it already issued, free its tensor memory and return;
+ * that call's outputs are then unspecified and moe_device_status reports
+ * MOE_ERR_DEVICE.  The next call clears the word.  For tests of this
+ * failure path (with moe_layer_stall_test) and for callers that want a hung
+ * pipeline reported sooner; it takes effect from the next call on `layer`.
+ * (The failure handling of forward_prefill.rs is Rust's Result/ensure!; this
+ * is its device-side counterpart.)                                           */
+MOE_API int moe_layer_set_wait_limit(moe_layer* layer, uint64_t ns);
+
+/* Test of that failure path without any fault: while enabled (1), the bf16
+ * grouped-GEMM kernels of calls on `layer` make their tensor-core issuer
+ * first wait on an mbarrier that no thread ever completes, so that wait runs
+ * out after the wait limit and the kernel takes the abort path above (no MMA
+ * is issued; the TMA copies already issued are waited for; tensor memory is
+ * freed).  0 turns it off.  Other weight formats and the GEMV arm ignore it. */
+MOE_API int moe_layer_stall_test(moe_layer* layer, int enable);
 
 /* Kernels the last successful call on `layer` launched (for launch counting). */
 MOE_API int moe_last_launch_count(const moe_layer* layer);

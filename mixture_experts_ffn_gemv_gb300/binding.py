@@ -24,7 +24,8 @@ ARMS = {"auto": MOE_ARM_AUTO, "gemv": MOE_ARM_GEMV, "gemm": MOE_ARM_GEMM}
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_workspace_size", "moe_select_arm", "moe_route",
     "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_forward", "moe_forward_residual_rmsnorm",
-    "moe_act_quant_fp8", "moe_act_quant_nvfp4", "moe_device_status",
+    "moe_act_quant_fp8", "moe_act_quant_nvfp4", "moe_device_status", "moe_layer_set_wait_limit",
+    "moe_layer_stall_test",
     "moe_last_launch_count", "moe_kernel_timing_enable", "moe_kernel_timing_read", "moe_kernel_count",
     "moe_kernel_name", "moe_status_string",
 )
@@ -81,6 +82,8 @@ def load_library(path: str | None = None, build: bool = True):
         lib.moe_act_quant_nvfp4.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp]
         lib.moe_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
         lib.moe_last_launch_count.argtypes = [_vp]
+        lib.moe_layer_set_wait_limit.argtypes = [_vp, ctypes.c_uint64]
+        lib.moe_layer_stall_test.argtypes = [_vp, ctypes.c_int]
         lib.moe_kernel_timing_enable.argtypes = [_vp, ctypes.c_int]
         lib.moe_kernel_timing_read.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                                ctypes.POINTER(_i64)]
@@ -198,6 +201,14 @@ class MoeLayer:
 
     def select_arm(self, m: int) -> int:
         return self.lib.moe_select_arm(self.handle, int(m))
+
+    def set_wait_limit(self, ns: int):
+        """Limit (ns) of the grouped GEMMs' bounded waits; 0 restores 2 s."""
+        _check(self.lib.moe_layer_set_wait_limit(self.handle, int(ns)), "moe_layer_set_wait_limit")
+
+    def stall_test(self, enable: bool):
+        """Make the bf16 grouped GEMMs wait on a barrier nothing completes."""
+        _check(self.lib.moe_layer_stall_test(self.handle, int(bool(enable))), "moe_layer_stall_test")
 
     def last_launch_count(self) -> int:
         return self.lib.moe_last_launch_count(self.handle)

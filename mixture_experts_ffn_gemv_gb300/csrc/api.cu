@@ -90,11 +90,14 @@ struct moe_layer {
     mutable KernelTimer timer;
     GemmWeights gemm;  // host-side TMA descriptors of the weights
     RouteMode rm;      // router scoring
+    uint64_t wait_ns;  // grouped GEMMs: limit of every bounded mbarrier wait
+    int stall_test;    // bf16 grouped GEMMs: stall on purpose (failure-path test)
 };
 
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -343,6 +346,8 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     g.H = H;
     g.I = I;
     g.max_tiles = gemm_max_tiles(lo.P, E, has_shared, m);
+    g.wait_ns = L->wait_ns;
+    g.stall_test = L->stall_test;
     uint16_t* ybf = at<uint16_t>(ws, lo.y);
     if (L->nvfp4) {
         // x to NVFP4, then the sorted rows widened to f16 (the A operand)
@@ -488,6 +493,8 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
     L->rm = RouteMode{c.scoring == MOE_SCORING_SIGMOID ? 1 : 0, c.norm_topk_prob ? 1 : 0,
                       c.scoring == MOE_SCORING_SIGMOID ? c.routed_scaling_factor : 1.0f};
     L->last_launches = 0;
+    L->wait_ns = kDefaultWaitNs;
+    L->stall_test = 0;
     if (cudaGetDevice(&L->device) != cudaSuccess) {
         delete L;
         return MOE_ERR_CUDA;
@@ -627,6 +634,18 @@ int moe_device_status(const void* workspace, void* stream, int32_t* device_code)
 }
 
 int moe_last_launch_count(const moe_layer* layer) { return layer ? layer->last_launches : -1; }
+
+int moe_layer_set_wait_limit(moe_layer* layer, uint64_t ns) {
+    if (!layer) return MOE_ERR_INVALID_ARG;
+    layer->wait_ns = ns ? ns : kDefaultWaitNs;
+    return MOE_OK;
+}
+
+int moe_layer_stall_test(moe_layer* layer, int enable) {
+    if (!layer || (enable != 0 && enable != 1)) return MOE_ERR_INVALID_ARG;
+    layer->stall_test = enable;
+    return MOE_OK;
+}
 
 int moe_kernel_timing_enable(moe_layer* layer, int enable) {
     if (!layer) return MOE_ERR_INVALID_ARG;

@@ -17,8 +17,9 @@
 // The work list is (m-tile, n-tile) over the non-empty groups the permute
 // left in the workspace (group m-tile starts in act_tile); every tile costs
 // the same K work, so CTAs take tiles round-robin.  Every mbarrier wait is
-// bounded: on expiry the CTA records DEV_ERR_TIMEOUT, stops issuing, drains
-// its tensor-core work and frees TMEM before returning.
+// bounded (by the layer's wait limit, 2 s unless a caller lowered it): on
+// expiry the CTA records DEV_ERR_TIMEOUT, stops issuing, waits (2 s at most)
+// for its TMA copies and MMAs in flight, frees TMEM and returns.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -44,7 +45,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half the columns
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
+constexpr uint64_t DRAIN_NS = 2000000000ull;  // 2 s: drains of in-flight copies / MMAs
 constexpr int TABLE_INTS = 2 * kMaxExperts + 4;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + TABLE_INTS * 4;
 
@@ -60,6 +61,8 @@ struct GemmParams {
     int ldo;       // output row stride (elements)
     int n_rows_b;  // weight rows per B load box (128 gate/up, 256 down)
     uint16_t* out;
+    uint64_t wait_ns;  // limit of every protocol wait
+    int stall_test;    // 1: the MMA issuer first waits on a barrier nothing completes
 };
 
 __device__ __forceinline__ int find_group(const int* tile_start, int n_active, int mt) {
@@ -87,6 +90,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
     const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    const uint32_t never = smem_u32(bars + 2 * STAGES + 6);  // stall test: no thread ever arrives here
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_tile = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
     int* s_group = s_tile + kMaxExperts + 2;
@@ -106,6 +110,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(tempty0 + 8 * a, EPI_WARPS);
         }
         mbar_init(drain, 1);
+        mbar_init(never, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int gz = routed ? g : 0;
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, WAIT_NS)) {
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -157,17 +162,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // every issued load has landed before the CTA can exit
             for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
-                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, WAIT_NS);
+                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, DRAIN_NS);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(BM, BN);
             uint32_t it = 0, tc = 0;
-            bool ok = true;
+            // the stall test: a stalled pipeline, made by waiting on a barrier
+            // that nothing completes, must end in the bounded-wait abort path
+            bool ok = !p.stall_test || mbar_wait(never, 0, p.wait_ns);
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
                 if (*abort_flag) break;
                 const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
-                if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, WAIT_NS)) {
+                if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -175,7 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d = tmem_base + acc * BN;
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS)) {
+                    if (!mbar_wait(full0 + 8 * s, ph, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *abort_flag = 1;
             }
             mma_commit(drain);
-            mbar_wait(drain, 0, WAIT_NS);
+            mbar_wait(drain, 0, DRAIN_NS);
         }
         __syncwarp();
     } else {
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             if (*abort_flag) break;
             const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
-            if (!mbar_wait(tfull0 + 8 * acc, aph, WAIT_NS)) {
+            if (!mbar_wait(tfull0 + 8 * acc, aph, p.wait_ns)) {
                 set_error(p.hdr, DEV_ERR_TIMEOUT, 3);
                 *abort_flag = 1;
                 break;
@@ -383,7 +390,7 @@ cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;
     GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.I / 128, g.H / BK, g.I, 128,
-                 static_cast<uint16_t*>(g.h)};
+                 static_cast<uint16_t*>(g.h), g.wait_ns, g.stall_test};
     const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
     launch_pdl(grouped_gemm_bf16<true>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_xs, L.w->w1, L.w->w3, L.w->sw1, L.w->sw3, p);
     return cudaGetLastError();
@@ -395,7 +402,7 @@ cudaError_t launch_gemm_down(const GemmLaunch& L, cudaStream_t st) {
     cudaError_t e = set_smem_attr<false>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;
-    GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.H / BN, g.I / BK, g.H, BN, g.y};
+    GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.H / BN, g.I / BK, g.H, BN, g.y, g.wait_ns, g.stall_test};
     const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
     launch_pdl(grouped_gemm_bf16<false>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_h, L.w->w2, L.w->w2, L.w->sw2, L.w->sw2, p);
     return cudaGetLastError();

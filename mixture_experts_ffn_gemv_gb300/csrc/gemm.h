@@ -29,6 +29,8 @@ struct GemmCall {
     const int* act_group;
     const int* act_tile;
     int rows, E, H, I, max_tiles;
+    uint64_t wait_ns;  // limit of every protocol wait (drains keep their own 2 s limit)
+    int stall_test;    // bf16 kernels: wait first on a barrier nothing completes (failure-path test)
     void* xs;      // gathered activations [rows, H] (bf16 or e4m3)
     float* xs_sc;  // fp8: [rows, H/128]
     void* h;       // [rows, I] (bf16, e4m3, or for nvfp4 the f16 block-scaled values)

@@ -47,7 +47,7 @@ constexpr int QC = EPI_WARPS / 4;           // column groups per row
 constexpr int NC = BN / QC;                 // accumulator columns per epilogue thread
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int THREADS = 64 + EPI_THREADS;
-constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr uint64_t DRAIN_NS = 2000000000ull;  // drains of in-flight copies / MMAs
 constexpr int TABLE_INTS = 2 * kMaxExperts + 4;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256 + TABLE_INTS * 4 + 2 * BM * QC * 4;
 
@@ -67,6 +67,7 @@ struct Fp8Params {
     uint8_t* out_q;    // gate/up: h codes [rows, I]
     float* out_sc;     // gate/up: h scales [rows, I/128]
     uint16_t* out_y;   // down: y [rows, H]
+    uint64_t wait_ns;  // limit of every protocol wait
 };
 
 __device__ __forceinline__ int find_group(const int* tile_start, int n_active, int mt) {
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int gz = routed ? g : 0;
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, WAIT_NS)) {
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *abort_flag = 1;
             }
             for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
-                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, WAIT_NS);
+                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, DRAIN_NS);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t b = it & 1u, pph = (it >> 1) & 1u;
-                    if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS) || !mbar_wait(pempty0 + 8 * b, pph ^ 1u, WAIT_NS)) {
+                    if (!mbar_wait(full0 + 8 * s, ph, p.wait_ns) || !mbar_wait(pempty0 + 8 * b, pph ^ 1u, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *abort_flag = 1;
             }
             mma_commit(drain);
-            mbar_wait(drain, 0, WAIT_NS);
+            mbar_wait(drain, 0, DRAIN_NS);
         }
         __syncwarp();
     } else {
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t b = it & 1u, pph = (it >> 1) & 1u;
                 const float sx = __ldg(asc + kb);
                 const float f_lo = sx * __ldg(sc_lo + kb), f_hi = sx * __ldg(sc_hi + kb);
-                if (!mbar_wait(pfull0 + 8 * b, pph, WAIT_NS)) {
+                if (!mbar_wait(pfull0 + 8 * b, pph, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 float* slot = xchg + (par * BM + r) * QC;
                 slot[cg] = amax;
                 mbar_arrive(xbar0 + 8 * par);
-                if (!mbar_wait(xbar0 + 8 * par, (tc >> 1) & 1u, WAIT_NS)) {
+                if (!mbar_wait(xbar0 + 8 * par, (tc >> 1) & 1u, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -338,7 +339,7 @@ cudaError_t launch_gemm_fp8_gateup(const GemmLaunch& L, cudaStream_t st) {
     const GemmCall& g = L.call;
     const GemmWeights& w = *L.w;
     Fp8Params p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.xs_sc, w.s1, w.s3, w.ss1, w.ss3,
-                g.E, g.rows, g.I / 128, g.H / BK, g.I, g.I / 128, static_cast<uint8_t*>(g.h), g.hsc, nullptr};
+                g.E, g.rows, g.I / 128, g.H / BK, g.I, g.I / 128, static_cast<uint8_t*>(g.h), g.hsc, nullptr, g.wait_ns};
     const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
     launch_pdl(grouped_gemm_fp8<true>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
     return cudaGetLastError();
@@ -350,7 +351,7 @@ cudaError_t launch_gemm_fp8_down(const GemmLaunch& L, cudaStream_t st) {
     const GemmCall& g = L.call;
     const GemmWeights& w = *L.w;
     Fp8Params p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.hsc, w.s2, w.s2, w.ss2, w.ss2,
-                g.E, g.rows, g.H / BN, g.I / BK, g.H, g.H / 128, nullptr, nullptr, g.y};
+                g.E, g.rows, g.H / BN, g.I / BK, g.H, g.H / 128, nullptr, nullptr, g.y, g.wait_ns};
     const int grid = std::max(1, std::min(num_sms(), g.max_tiles * p.n_tiles));
     launch_pdl(grouped_gemm_fp8<false>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_h, w.w2, w.w2, w.sw2, w.sw2, p);
     return cudaGetLastError();

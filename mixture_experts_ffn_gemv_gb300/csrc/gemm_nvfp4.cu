@@ -15,7 +15,7 @@
 //      the MMA descriptor reads.  The rings decouple load latency, conversion
 //      and the tensor core: each runs ahead of the next by its ring depth.
 // Warps: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (one per TMEM lane
-// quarter), 6..21 converters.  Every mbarrier wait is bounded (2 s); on expiry the CTA
+// quarter), 6..21 converters.  Every mbarrier wait is bounded (the layer's wait limit, 2 s by default); on expiry the CTA
 // records DEV_ERR_TIMEOUT, stops, drains its tensor-core work and frees TMEM.
 #include <cuda_runtime.h>
 
@@ -52,7 +52,7 @@ constexpr int THREADS = 32 * (CONV0 + CONV_WARPS);
 constexpr int CONV_THREADS = 32 * CONV_WARPS;
 constexpr int TASKS = BN * 8;  // (weight row, 16-byte f16 chunk) pairs of one B tile
 constexpr int TASKS_PER_THREAD = TASKS / CONV_THREADS;
-constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
+constexpr uint64_t DRAIN_NS = 2000000000ull;  // 2 s: drains of in-flight copies / MMAs
 constexpr int TABLE_INTS = 2 * kMaxExperts + 4;
 constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256 + TABLE_INTS * 4;
 static_assert(A_BYTES % 1024 == 0 && B_OFF % 1024 == 0, "swizzled tiles keep 1024-byte alignment");
@@ -82,6 +82,7 @@ struct Nvfp4Params {
     const float *g0, *g1, *sg0, *sg1;        // matrix scales: routed [E], shared [1]
     const float* arow;                       // activation row scale per sorted row
     void* out;                               // gate/up: fp32 h [rows, I]; down: bf16 y [rows, H]
+    uint64_t wait_ns;                        // limit of every protocol wait
 };
 
 __device__ __forceinline__ int find_group(const int* tile_start, int n_active, int mt) {
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int gz = routed ? g : 0;
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(aempty0 + 8 * s, ph ^ 1u, WAIT_NS) || !mbar_wait(cempty0 + 8 * s, ph ^ 1u, WAIT_NS)) {
+                    if (!mbar_wait(aempty0 + 8 * s, ph ^ 1u, p.wait_ns) || !mbar_wait(cempty0 + 8 * s, ph ^ 1u, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // every issued load has landed before the CTA can exit
             for (uint32_t j = it > (uint32_t)STAGES ? it - STAGES : 0; j < it; ++j)
-                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, WAIT_NS);
+                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, DRAIN_NS);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
                 if (*abort_flag) break;
                 const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
-                if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, WAIT_NS)) {
+                if (!mbar_wait(tempty0 + 8 * acc, aph ^ 1u, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -216,7 +217,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     const uint32_t b = it % BBUFS, bph = (it / BBUFS) & 1u;
-                    if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS) || !mbar_wait(bfull0 + 8 * b, bph, WAIT_NS)) {
+                    if (!mbar_wait(full0 + 8 * s, ph, p.wait_ns) || !mbar_wait(bfull0 + 8 * b, bph, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 *abort_flag = 1;
             }
             mma_commit(drain);
-            mbar_wait(drain, 0, WAIT_NS);
+            mbar_wait(drain, 0, DRAIN_NS);
         }
         __syncwarp();
     } else if (warp >= CONV0) {
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int kn = kb + 1 < p.kblocks ? kb + 1 : kb;
 #pragma unroll
                 for (int i = 0; i < TASKS_PER_THREAD; ++i) swn[i] = __ldg(srow[i] + kn);
-                if (!mbar_wait(full0 + 8 * s, ph, WAIT_NS) || !mbar_wait(bempty0 + 8 * b, bph ^ 1u, WAIT_NS)) {
+                if (!mbar_wait(full0 + 8 * s, ph, p.wait_ns) || !mbar_wait(bempty0 + 8 * b, bph ^ 1u, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             if (*abort_flag) break;
             const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
-            if (!mbar_wait(tfull0 + 8 * acc, aph, WAIT_NS)) {
+            if (!mbar_wait(tfull0 + 8 * acc, aph, p.wait_ns)) {
                 set_error(p.hdr, DEV_ERR_TIMEOUT, 14);
                 *abort_flag = 1;
                 break;
@@ -406,7 +407,7 @@ cudaError_t launch_gemm_nvfp4_gateup(const GemmLaunch& L, cudaStream_t st) {
     const GemmCall& g = L.call;
     const GemmWeights& w = *L.w;
     Nvfp4Params p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.I / 128, g.H / BK, g.H, g.I, g.I,
-                  128, w.sb1, w.sb3, w.ssb1, w.ssb3, w.s1, w.s3, w.ss1, w.ss3, g.xs_g, g.hf};
+                  128, w.sb1, w.sb3, w.ssb1, w.ssb3, w.s1, w.s3, w.ss1, w.ss3, g.xs_g, g.hf, g.wait_ns};
     const int grid = std::max(1, std::min(sms(), g.max_tiles * p.n_tiles));
     launch_pdl(grouped_gemm_nvfp4<true>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_xs, w.w1, w.w3, w.sw1,
                w.sw3, p);
@@ -419,7 +420,7 @@ cudaError_t launch_gemm_nvfp4_down(const GemmLaunch& L, cudaStream_t st) {
     const GemmCall& g = L.call;
     const GemmWeights& w = *L.w;
     Nvfp4Params p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.H / BN, g.I / BK, g.I, g.H, g.H,
-                  BN, w.sb2, w.sb2, w.ssb2, w.ssb2, w.s2, w.s2, w.ss2, w.ss2, g.h_g, g.y};
+                  BN, w.sb2, w.sb2, w.ssb2, w.ssb2, w.s2, w.s2, w.ss2, w.ss2, g.h_g, g.y, g.wait_ns};
     const int grid = std::max(1, std::min(sms(), g.max_tiles * p.n_tiles));
     launch_pdl(grouped_gemm_nvfp4<false>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, L.a_h, w.w2, w.w2, w.sw2,
                w.sw2, p);

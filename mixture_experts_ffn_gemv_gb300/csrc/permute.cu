@@ -64,7 +64,7 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
     }
     if (tid == 0) hist[E] = has_shared ? m : 0;
     __syncthreads();
-    block_exclusive_scan(off, E, wsum);
+    const int valid_pairs = block_exclusive_scan(off, E, wsum);  // P unless some ids were out of range
     for (int e = tid; e < E; e += 256) {
         o.grp_off[e] = off[e];
         o.grp_cnt[e] = hist[e];
@@ -74,7 +74,7 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
     if (tid == 0) {
         o.grp_off[E] = P;
         o.grp_cnt[E] = hist[E];
-        if (o.expert_offsets) o.expert_offsets[E] = P;
+        if (o.expert_offsets) o.expert_offsets[E] = valid_pairs;
     }
     __syncthreads();
     // non-empty groups (routed experts, then the shared expert), ascending

@@ -3,12 +3,16 @@
 // caller passes only its inputs and outputs and nothing is ever allocated.
 //
 // The scratch is one file-scope __device__ array.  In host code its name is
-// only a host-side stand-in, so the device address is looked up once per
-// device with cudaGetSymbolAddress (with that device current) and passed to
-// the kernels as a plain pointer.
+// only a host-side stand-in, so each call looks up its device address with
+// cudaGetSymbolAddress (on the current device) and passes it to the kernels
+// as a plain pointer.
+//
+// Out-of-range expert ids: the kernels drop such a pair (its slot_of_pair
+// entry is -1) and leave it out of expert_offsets[E], the number of valid
+// pairs.  They also set the scratch header's error word, but no entry point
+// reads that word back here, so the caller's check is expert_offsets[E] ==
+// m * top_k.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -22,24 +26,14 @@ constexpr size_t kNoAllocScratchBytes = 320 * 1024;
 
 static __device__ __align__(256) unsigned char g_permute_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-
-// Device address of g_permute_scratch on the current device (looked up on the
-// first call per device).
+// Device address of g_permute_scratch on the current device.  Looked up on
+// every call: the lookup is a host-side query (no allocation, no stream work),
+// and repeating it keeps the address right after a cudaDeviceReset, which
+// reloads this library's device code possibly elsewhere.
 int scratch_on_current_device(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-    std::call_once(g_once[dev], [dev] {
-        void* p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_permute_scratch);
-        g_scratch_ptr[dev] = p;
-    });
-    if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev]) return MOE_ERR_CUDA;
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    *out = p;
     return MOE_OK;
 }
 

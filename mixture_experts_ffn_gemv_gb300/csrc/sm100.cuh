@@ -45,16 +45,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Waits for the phase of the given parity to complete; gives up (returns
 // false) after limit_ns of wall time so that a protocol error cannot hang the
-// GPU.
+// GPU.  The clock starts at the first unsuccessful poll and is read every 16
+// polls (a poll may itself suspend the thread for a while).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u) {
-            const uint64_t now = globaltimer();
-            if (t0 == 0) t0 = now;
-            else if (now - t0 > limit_ns) return false;
-        }
+        if ((i & 15u) == 0u && globaltimer() - t0 > limit_ns) return false;
     }
 }
 

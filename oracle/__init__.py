@@ -82,6 +82,8 @@ def _lib(fp64: bool = False):
             lib.oracle_topk_sigmoid.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _C.c_int, _C.c_float,
                                                 _vp, _vp, _vp]
             lib.oracle_permute.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _vp, _vp]
+            lib.oracle_route_weights.argtypes = [_vp, _i64, _C.c_int, _C.c_int, _vp, _C.c_int, _C.c_int,
+                                                 _C.c_float, _vp]
             lib.oracle_residual_rmsnorm.argtypes = [_vp, _i64, _C.c_int, _vp, _vp, _C.c_float, _vp]
             lib.oracle_moe_forward.argtypes = [ctypes.POINTER(_Layer), _vp, _i64, _vp, _i64, _vp, _vp, _vp]
             lib.oracle_moe_forward.restype = _C.c_int
@@ -218,6 +220,22 @@ def topk_sigmoid(logits, k: int, bias=None, norm: bool = True, scale: float = 1.
     _lib().oracle_topk_sigmoid(_ptr(L), m, E, k, _ptr(b), int(bool(norm)), float(scale), _ptr(ids), _ptr(w),
                                _ptr(margin))
     return ids, w, margin
+
+
+def route_weights(shape, logits, ids):
+    """Routing weights float32 [m,k] for a given selection ids [m,k] (the
+    forced-ids mode): the layer's scoring applied to those ids' logits."""
+    L = _np(logits, np.float32)
+    m, E = L.shape
+    a = _np(ids, np.int32)
+    k = a.shape[1]
+    assert a.shape[0] == m and a.min() >= 0 and a.max() < E
+    w = np.empty((m, k), np.float32)
+    sigmoid = getattr(shape, "scoring", "softmax") == "sigmoid"
+    _lib().oracle_route_weights(_ptr(L), m, E, k, _ptr(a), int(sigmoid),
+                                int(bool(getattr(shape, "norm_topk_prob", True))),
+                                float(getattr(shape, "routed_scaling", 1.0)), _ptr(w))
+    return w
 
 
 def permute(ids, num_experts: int):

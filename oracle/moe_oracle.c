@@ -362,6 +362,37 @@ EXPORT void oracle_topk_sigmoid(const float* L, int64_t m, int E, int k, const f
  * sum of the per-expert counts; sorted_pair[s] is the pair at sorted slot s
  * (pairs ascending within an expert); slot_of_pair[p] is its inverse.
  */
+/* Routing weights for a GIVEN selection (the forced-ids mode): the weight
+ * half of forward_prefill.rs step "2. Batched topK dispatch" applied to ids
+ * chosen elsewhere, e.g. by the GPU where a near-tie let it pick differently.
+ * scoring 0 (softmax, renormalised): w_j = exp(L_j - L_max) / sum_i exp(L_i -
+ * L_max) over the k given ids, L_max their largest logit; scoring 1 (sigmoid):
+ * w_j = sigmoid(L_j), divided by their sum when norm, times scale.  Formed in
+ * double and rounded to float, as in oracle_topk_softmax/_sigmoid. */
+EXPORT void oracle_route_weights(const float* L, int64_t m, int E, int k, const int32_t* ids, int scoring,
+                                 int norm, float scale, float* w) {
+    for (int64_t t = 0; t < m; ++t) {
+        const float* lt = L + t * (int64_t)E;
+        const int32_t* it = ids + t * (int64_t)k;
+        if (scoring == 0) {
+            double lmax = (double)lt[it[0]];
+            for (int j = 1; j < k; ++j)
+                if ((double)lt[it[j]] > lmax) lmax = (double)lt[it[j]];
+            double den = 0.0;
+            for (int j = 0; j < k; ++j) den += exp((double)lt[it[j]] - lmax);
+            for (int j = 0; j < k; ++j) w[t * (int64_t)k + j] = (float)(exp((double)lt[it[j]] - lmax) / den);
+        } else {
+            double sum = 0.0;
+            for (int j = 0; j < k; ++j) sum += 1.0 / (1.0 + exp(-(double)lt[it[j]]));
+            for (int j = 0; j < k; ++j) {
+                double v = 1.0 / (1.0 + exp(-(double)lt[it[j]]));
+                if (norm) v /= sum;
+                w[t * (int64_t)k + j] = (float)(v * (double)scale);
+            }
+        }
+    }
+}
+
 EXPORT void oracle_permute(const int32_t* ids, int64_t m, int k, int E, int32_t* offsets,
                            int32_t* sorted_pair, int32_t* slot_of_pair) {
     int64_t P = m * (int64_t)k;

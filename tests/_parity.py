@@ -93,3 +93,22 @@ def oracle_rows(oracle, shape, layer, x, ids, w, rows):
     sub_shape = dataclasses.replace(shape, num_experts=U)
     x_r = x.index_select(0, torch.as_tensor(rows, device=x.device)).cpu()
     return oracle.moe_forward(sub_shape, sub, x_r, ids_c, w_r)
+
+
+def max_swapped(m: int) -> int:
+    """How many tokens may hold a near-tie id set other than the oracle's."""
+    return max(2, m // 200)
+
+
+def forced_routing(oracle, shape, logits, ref_ids, ref_w, gpu_ids, swapped):
+    """The routing each token is compared under: the oracle's own ids and
+    weights, except for the near-tie tokens in `swapped`, which take the GPU's
+    ids with the oracle's weights for those ids (the forced-ids mode)."""
+    ids = np.array(ref_ids, np.int32, copy=True)
+    w = np.array(ref_w, np.float32, copy=True)
+    if len(swapped):
+        sw = np.asarray(swapped, np.int64)
+        g = np.asarray(gpu_ids, np.int32)[sw]
+        ids[sw] = g
+        w[sw] = oracle.route_weights(shape, np.asarray(logits, np.float32)[sw], g)
+    return ids, w

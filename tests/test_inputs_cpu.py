@@ -75,4 +75,9 @@ def test_bench_byte_accounting():
     assert g == U * 2 * 768 * 2048 * 2 + m * 2048 * 2 + m * 8 * 768 * 2
     gn = bench.kernel_alg_bytes("gemv_gateup", n, m, U)
     assert gn < g / 3  # NVFP4 weights take 0.5625 bytes per element against 2
+    # W4A4: activations count at NVFP4 size too (codes + block scales + a row scale)
+    xa, ha = 2048 * bench.NVFP4_B + 4, 768 * bench.NVFP4_B + 4
+    assert gn == int(U * 2 * 768 * 2048 * bench.NVFP4_B + m * xa + m * 8 * ha)
+    gm = bench.kernel_alg_bytes("gemm_gateup", n, 4096, 128)
+    assert gm == int(128 * 2 * 768 * 2048 * bench.NVFP4_B + 4096 * 8 * (xa + ha))
     assert bench._dtype(n) == "nvfp4_e2m1" and bench._dtype(d) == "fp8_e4m3" and bench._dtype(q) == "bf16"

@@ -8,12 +8,17 @@
   * top-k order       -> numpy stable argsort (tie-heavy inputs) and brute force
                           over all k-subsets on the tiny shape.
   * routing weights   -> scipy softmax; closed forms: zero router gives 1/k,
-                          k = E gives the full softmax; sum to 1.
+                          k = E gives the full softmax; sum to 1.  The weights
+                          of a given (forced) selection against scipy's softmax
+                          and expit over that subset.
   * permute           -> numpy stable argsort and bincount; bijection.
   * expert FFN        -> one expert with k = 1 equals a dense SwiGLU MLP
                           (torch float64 matmul + torch silu); shared expert
                           alone equals the same MLP; fp8 path equals a torch
-                          dequantise / fake-quantise float64 pipeline.
+                          dequantise / fake-quantise float64 pipeline; the fp8
+                          and NVFP4 shared experts alone (routed experts
+                          zeroed, with scales unlike the shared ones) equal the
+                          same pipelines on the shared operands.
   * combine           -> dense-gating reformulation (torch float64 einsum).
   * sigmoid routing   -> brute force over all k-subsets of score + bias (with the
                           keys formed in float32 by numpy), scipy's expit for the
@@ -37,6 +42,7 @@
   * structure         -> token independence, expert relabelling invariance,
                           float vs double oracle builds agree to ~1e-6.
 """
+import dataclasses
 import itertools
 import json
 import math
@@ -424,6 +430,27 @@ def test_topk_sigmoid_closed_forms(oracle_mod):
     assert np.allclose(w, 1.0 / (1.0 + np.exp(-L[:, chosen].astype(np.float64))), atol=1e-7)
 
 
+def test_route_weights_for_given_ids(oracle_mod):
+    """The forced-ids weights (the routing-weight half of step 2 applied to a
+    selection made elsewhere) against scipy's softmax and expit over the given
+    subset, in any order; on the oracle's own selection they are its weights."""
+    from scipy.special import expit, softmax
+    rng = np.random.default_rng(31)
+    L = rng.normal(0, 1, size=(40, 24)).astype(np.float32)
+    ids = np.stack([rng.permutation(24)[:5] for _ in range(40)]).astype(np.int32)
+    soft = I.LayerShape(hidden=128, num_experts=24, top_k=5, inter=128)
+    w = oracle_mod.route_weights(soft, L, ids)
+    ref = softmax(np.take_along_axis(L, ids, 1).astype(np.float64), axis=1)
+    assert np.abs(w - ref).max() < 1e-7
+    sig = dataclasses.replace(soft, scoring="sigmoid", routed_scaling=2.5)
+    s = expit(np.take_along_axis(L, ids, 1).astype(np.float64))
+    assert np.abs(oracle_mod.route_weights(sig, L, ids) - 2.5 * s / s.sum(1, keepdims=True)).max() < 1e-6
+    unnorm = dataclasses.replace(sig, norm_topk_prob=False)
+    assert np.abs(oracle_mod.route_weights(unnorm, L, ids) - 2.5 * s).max() < 1e-6
+    own_ids, own_w, _ = oracle_mod.topk_softmax(L, 5)
+    assert np.array_equal(oracle_mod.route_weights(soft, L, own_ids), own_w)
+
+
 def test_gated_shared_expert_matches_torch(oracle_mod):
     shape = I.LayerShape(hidden=256, num_experts=4, top_k=2, inter=128, shared_inter=256, shared_gate=True)
     layer = I.make_experts(shape, seed=13)
@@ -558,6 +585,65 @@ def test_fp8_expert_matches_torch_pipeline(oracle_mod):
     w2 = _torch_dequant(layer["w2"][1], layer["s2"][1])
     a = torch.nn.functional.silu(x64 @ w1.T) * (x64 @ w3.T)
     ref = (_torch_fake_quant_rows(a) @ w2.T).numpy()
+    out64 = oracle_mod.moe_forward(shape, layer, x, ids, w, fp64=True)
+    out32 = oracle_mod.moe_forward(shape, layer, x, ids, w)
+    assert np.linalg.norm(out64 - ref) / np.linalg.norm(ref) < 1e-6
+    assert np.linalg.norm(out32 - ref) / np.linalg.norm(ref) < 2e-3
+
+
+def test_fp8_shared_expert_alone_matches_torch_pipeline(oracle_mod):
+    # The DeepSeek-V3-shaped layer's shared expert in fp8: its own codes and
+    # 128x128 block scales (ss1, ss3, ss2), added with weight 1 after the
+    # routed sum (metrale moe_v41 forward.rs, shared_expert_tail: acc += sd).
+    # The routed experts are zeroed but keep large, different scales, so an
+    # oracle that took a routed expert's scales (or a transposed scale index)
+    # for the shared expert fails.
+    shape = I.LayerShape(hidden=256, num_experts=3, top_k=2, inter=256, shared_inter=256, fp8=True)
+    layer = I.make_experts(shape, seed=21)
+    for n in ("w1", "w3", "w2"):
+        layer[n].zero_()
+    for n in ("s1", "s3", "s2"):
+        layer[n].fill_(7.0)
+    layer["ss1"] *= torch.tensor([[1.0, 3.0], [0.5, 2.0]])
+    layer["ss3"] *= torch.tensor([[2.0, 0.5], [1.0, 0.25]])
+    layer["ss2"] *= torch.tensor([[1.0, 0.25], [4.0, 1.5]])
+    x = I.make_x(shape, 6, seed=21)
+    ids = np.tile(np.array([[2, 0]], np.int32), (6, 1))
+    w = np.full((6, 2), 0.5, np.float32)
+    x64 = _torch_fake_quant_rows(_f64(x.float()))
+    w1 = _torch_dequant(layer["ws1"], layer["ss1"])
+    w3 = _torch_dequant(layer["ws3"], layer["ss3"])
+    w2 = _torch_dequant(layer["ws2"], layer["ss2"])
+    a = torch.nn.functional.silu(x64 @ w1.T) * (x64 @ w3.T)
+    ref = (_torch_fake_quant_rows(a) @ w2.T).numpy()
+    out64 = oracle_mod.moe_forward(shape, layer, x, ids, w, fp64=True)
+    out32 = oracle_mod.moe_forward(shape, layer, x, ids, w)
+    assert np.linalg.norm(out64 - ref) / np.linalg.norm(ref) < 1e-6
+    assert np.linalg.norm(out32 - ref) / np.linalg.norm(ref) < 2e-3
+
+
+def test_nvfp4_shared_expert_alone_matches_torch_pipeline(oracle_mod):
+    # The NVFP4 shared expert: its own packed codes, e4m3 block scales (ssb*)
+    # and per-matrix scales (ss*).  Routed codes are zero (+0) while the
+    # routed scales differ from the shared ones, so reading a routed expert's
+    # scales for the shared expert fails.
+    shape = I.LayerShape(hidden=256, num_experts=2, top_k=1, inter=128, shared_inter=128, nvfp4=True)
+    layer = I.make_experts(shape, seed=22)
+    for n in ("w1", "w3", "w2"):
+        layer[n].zero_()
+    for n in ("sb1", "sb3", "sb2"):
+        layer[n].fill_(0x48)  # e4m3 4.0
+    for n in ("s1", "s3", "s2"):
+        layer[n].fill_(0.125)
+    x = I.make_x(shape, 5, seed=22)
+    ids = np.zeros((5, 1), np.int32)
+    w = np.ones((5, 1), np.float32)
+    x64 = _nvfp4_fake_quant_rows(_f64(x.float()))
+    w1 = _nvfp4_dequant_torch(layer["ws1"], layer["ssb1"], layer["ss1"][0])
+    w3 = _nvfp4_dequant_torch(layer["ws3"], layer["ssb3"], layer["ss3"][0])
+    w2 = _nvfp4_dequant_torch(layer["ws2"], layer["ssb2"], layer["ss2"][0])
+    a = torch.nn.functional.silu(x64 @ w1.T) * (x64 @ w3.T)
+    ref = (_nvfp4_fake_quant_rows(a) @ w2.T).numpy()
     out64 = oracle_mod.moe_forward(shape, layer, x, ids, w, fp64=True)
     out32 = oracle_mod.moe_forward(shape, layer, x, ids, w)
     assert np.linalg.norm(out64 - ref) / np.linalg.norm(ref) < 1e-6

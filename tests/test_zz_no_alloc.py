@@ -57,6 +57,28 @@ def test_noalloc_permute_matches_workspace_permute():
         assert torch.equal(sp, ref_sp)
         assert torch.equal(sl, ref_sl)
 
+    # an out-of-range id: both entry points drop that pair the same way, and
+    # expert_offsets[E] (the count of valid pairs) is how this caller sees it
+    m, k, E = 50, 4, 16
+    bad = _ids(m, k, E, 4)
+    bad[7, 2] = E + 3
+    ids = torch.from_numpy(bad).to(dev)
+    shape = I.LayerShape(hidden=256, num_experts=E, top_k=k, inter=128)
+    zeros = {n: torch.zeros(E, 128, 256, dtype=torch.bfloat16, device=dev) for n in ("w1", "w3")}
+    zeros["w2"] = torch.zeros(E, 256, 128, dtype=torch.bfloat16, device=dev)
+    ref_layer = binding.MoeLayer(shape, zeros)
+    ref_off, ref_sp, ref_sl = ref_layer.moe_permute(ids)
+    assert ref_layer.device_status() == 1  # the workspace path reports DEV_ERR_BAD_ID
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
+    sp = torch.full((m * k,), -7, dtype=torch.int32, device=dev)
+    sl = torch.full((m * k,), -7, dtype=torch.int32, device=dev)
+    rc = lib.moe_permute_noalloc(_ptr(ids), m, k, E, _ptr(off), _ptr(sp), _ptr(sl), stream)
+    assert rc == binding.MOE_OK
+    torch.cuda.synchronize(dev)
+    assert int(off[E]) == m * k - 1 and torch.equal(off, ref_off)
+    assert int(sl[7 * k + 2]) == -1 and torch.equal(sl, ref_sl)
+    assert torch.equal(sp[: m * k - 1], ref_sp[: m * k - 1])
+
     # a call whose histograms would not fit in the fixed scratch is refused
     big = torch.zeros(1, dtype=torch.int32, device=dev)
     rc = lib.moe_permute_noalloc(_ptr(big), 32768, 8, 1024, _ptr(big), _ptr(big), _ptr(big), stream)
