@@ -23,12 +23,13 @@ namespace {
 // stream, resolved when the totals are read.
 enum KernelId : int {
     K_ROUTER_SPLIT = 0, K_ROUTER, K_TOPK, K_ROUTE_PERMUTE, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
-    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_H_QUANT, K_SHARED_GATE, K_ACT_QUANT_NVFP4, K_H_QUANT_NVFP4, K_COUNT
+    K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_H_QUANT, K_SHARED_GATE, K_ACT_QUANT_NVFP4, K_H_QUANT_NVFP4,
+    K_DECODE_FUSED, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "router_split", "router", "topk_softmax", "route_permute", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
     "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine", "h_quant_fp8", "shared_gate",
-    "act_quant_nvfp4", "h_quant_nvfp4",
+    "act_quant_nvfp4", "h_quant_nvfp4", "decode_fused",
 };
 
 struct Pending {
@@ -102,7 +103,8 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-    size_t hdr, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile, sorted_pair, slot_of_pair;
+    size_t hdr, tickets, zero_bytes, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile,
+        sorted_pair, slot_of_pair;
     size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, sgate, total;
     size_t xsb, xg, hsb, hg;  // nvfp4: block scales and row scales of x and h
     size_t xs_g, h16;         // nvfp4 GEMM arm: gathered rows' scales, f16 h
@@ -126,6 +128,10 @@ Layout layout(const moe_layer* L, int64_t m) {
     };
     const size_t ab = L->fp8 ? 1 : 2;  // activation element bytes
     o.hdr = take(sizeof(WsHeader));
+    // per-m-tile tickets of the tensor-core router's top-k tail, right after
+    // the header: both are zeroed by one memset at the start of every call
+    o.tickets = o.router_tc ? take((size_t)router_tc_mtiles((int)m) * 4) : 0;
+    o.zero_bytes = off;
     o.part = take((size_t)o.S * m * E * 4);
     o.planes = o.router_tc ? take(router_tc_split_bytes(E, H)) : 0;
     o.ids = take((size_t)o.P * 4);
@@ -232,10 +238,11 @@ int run_route(const moe_layer* L, const Layout& lo, const void* x, int m, const 
         uint16_t* planes = at<uint16_t>(ws, lo.planes);
         WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
         MOE_LAUNCH(K_ROUTER_SPLIT, launch_router_split(wr, c.num_experts, c.hidden, planes, st));
-        MOE_LAUNCH(K_ROUTER, launch_router_tc(xb, m, c.hidden, planes, c.num_experts, part, lo.S, hdr, st));
-    } else {
-        MOE_LAUNCH(K_ROUTER, launch_router(xb, m, c.hidden, wr, c.num_experts, part, lo.S, st));
+        MOE_LAUNCH(K_ROUTER, launch_router_tc(xb, m, c.hidden, planes, c.num_experts, part, lo.S, hdr,
+                                              at<int>(ws, lo.tickets), c.top_k, bias, L->rm, logits_out, ids, w, st));
+        return MOE_OK;  // the router's tail picked the top k
     }
+    MOE_LAUNCH(K_ROUTER, launch_router(xb, m, c.hidden, wr, c.num_experts, part, lo.S, st));
     MOE_LAUNCH(K_TOPK, launch_topk(part, lo.S, m, c.num_experts, c.top_k, bias, L->rm, logits_out, ids, w, st));
     return MOE_OK;
 }
@@ -252,6 +259,31 @@ PermuteOut permute_out(const Layout& lo, void* ws, int32_t* sorted_pair, int32_t
     o.slot_of_pair = slot_of_pair ? slot_of_pair : at<int32_t>(ws, lo.slot_of_pair);
     o.expert_offsets = expert_offsets;
     return o;
+}
+
+// The GEMV kernels' view of a call: group tables in the workspace, weights.
+GemvArgs gemv_args(const moe_layer* L, const Layout& lo, void* ws) {
+    const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
+    const int E = L->cfg.num_experts;
+    GemvArgs a;
+    a.hdr = at<WsHeader>(ws, lo.hdr);
+    a.grp_off = po.grp_off;
+    a.grp_cnt = po.grp_cnt;
+    a.act_group = po.act_group;
+    a.sorted_pair = po.sorted_pair;
+    a.P = lo.P;
+    a.k = L->cfg.top_k;
+    a.E = E;
+    a.H = L->cfg.hidden;
+    a.I = L->cfg.inter;
+    a.max_groups = std::min(E, lo.P) + (L->has_shared ? 1 : 0);
+    a.w1 = L->routed.w1; a.w3 = L->routed.w3; a.w2 = L->routed.w2;
+    a.s1 = L->routed.s1; a.s3 = L->routed.s3; a.s2 = L->routed.s2;
+    a.sw1 = L->shared.w1; a.sw3 = L->shared.w3; a.sw2 = L->shared.w2;
+    a.ss1 = L->shared.s1; a.ss3 = L->shared.s3; a.ss2 = L->shared.s2;
+    a.sb1 = L->routed.sb1; a.sb3 = L->routed.sb3; a.sb2 = L->routed.sb2;
+    a.ssb1 = L->shared.sb1; a.ssb3 = L->shared.sb3; a.ssb2 = L->shared.sb2;
+    return a;
 }
 
 // permuted: the permute tables are already in the workspace; x_quantized: so
@@ -278,24 +310,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
         MOE_LAUNCH(K_SHARED_GATE, launch_shared_gate(static_cast<const uint16_t*>(x), m, H, L->shared.gate, sg, st));
     }
     if (arm == MOE_ARM_GEMV) {
-        GemvArgs a;
-        a.hdr = hdr;
-        a.grp_off = po.grp_off;
-        a.grp_cnt = po.grp_cnt;
-        a.act_group = po.act_group;
-        a.sorted_pair = po.sorted_pair;
-        a.P = lo.P;
-        a.k = k;
-        a.E = E;
-        a.H = H;
-        a.I = I;
-        a.max_groups = std::min(E, lo.P) + has_shared;
-        a.w1 = L->routed.w1; a.w3 = L->routed.w3; a.w2 = L->routed.w2;
-        a.s1 = L->routed.s1; a.s3 = L->routed.s3; a.s2 = L->routed.s2;
-        a.sw1 = L->shared.w1; a.sw3 = L->shared.w3; a.sw2 = L->shared.w2;
-        a.ss1 = L->shared.s1; a.ss3 = L->shared.s3; a.ss2 = L->shared.s2;
-        a.sb1 = L->routed.sb1; a.sb3 = L->routed.sb3; a.sb2 = L->routed.sb2;
-        a.ssb1 = L->shared.sb1; a.ssb3 = L->shared.sb3; a.ssb2 = L->shared.sb2;
+        const GemvArgs a = gemv_args(L, lo, ws);
         float* y = at<float>(ws, lo.y);
         if (L->nvfp4) {
             uint8_t* xq = at<uint8_t>(ws, lo.xq);
@@ -413,8 +428,35 @@ int forward_impl(const moe_layer* layer, const void* x, int64_t m, const float* 
     int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, lo.ids);
     float* w = topk_w_out ? topk_w_out : at<float>(workspace, lo.w);
     Launcher ln{layer, st};
-    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
     const moe_config& c = layer->cfg;
+    const int arm_used = arm == MOE_ARM_AUTO ? moe_select_arm(layer, m) : arm;
+    if (!tail && !layer->fp8 && !layer->nvfp4 && !layer->shared.gate && !lo.router_tc && arm_used == MOE_ARM_GEMV &&
+        c.hidden % 256 == 0 && decode_fused_usable((int)m, c.num_experts, c.top_k)) {
+        // decode, bf16: the whole layer in one cooperative launch
+        DecodeArgs d{};
+        d.a = gemv_args(layer, lo, workspace);
+        d.x = static_cast<const uint16_t*>(x);
+        d.m = (int)m;
+        d.wr = router_w;
+        d.bias = router_bias;
+        d.rm = layer->rm;
+        d.logits = at<float>(workspace, lo.part);
+        d.ids = ids;
+        d.w = w;
+        d.has_shared = layer->has_shared ? 1 : 0;
+        d.po = permute_out(lo, workspace, nullptr, nullptr, nullptr);
+        d.hdr = at<WsHeader>(workspace, lo.hdr);
+        d.h = at<uint16_t>(workspace, lo.h);
+        d.y = at<float>(workspace, lo.y);
+        d.out = static_cast<uint16_t*>(out);
+        d.ns_g = c.inter / 16;
+        d.ns_d = c.hidden / 32;
+        d.wait_ns = layer->wait_ns;
+        MOE_LAUNCH(K_DECODE_FUSED, launch_decode_fused(d, st));
+        layer->last_launches = ln.n;
+        return MOE_OK;
+    }
     if (!lo.router_tc && route_permute_fusable((int)m, c.top_k, c.num_experts)) {
         // decode: router, top-k and the permute in one launch.  For fp8 layers
         // with m > 4 the same launch also quantises x; at m <= 4 the separate
@@ -538,7 +580,7 @@ int moe_route(const moe_layer* layer, const void* x, int64_t m, const float* rou
     if (!x || !router_w || !topk_ids || !topk_w || !aligned(x, 16) || !aligned(router_w, 16))
         return MOE_ERR_INVALID_ARG;
     Launcher ln{layer, static_cast<cudaStream_t>(stream)};
-    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), ln.st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, ln.st) != cudaSuccess) return MOE_ERR_CUDA;
     rc = run_route(layer, lo, x, (int)m, router_w, router_bias, logits_out, topk_ids, topk_w, workspace, ln);
     layer->last_launches = ln.n;
     return rc;
@@ -570,7 +612,7 @@ int moe_experts(const moe_layer* layer, const void* x, int64_t m, const int32_t*
     if (!x || !topk_ids || !topk_w || !out || !aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
     if (arm < MOE_ARM_AUTO || arm > MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
     Launcher ln{layer, static_cast<cudaStream_t>(stream)};
-    if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), ln.st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, ln.st) != cudaSuccess) return MOE_ERR_CUDA;
     rc = run_experts(layer, lo, x, (int)m, topk_ids, topk_w, out, arm, workspace, ln);
     layer->last_launches = ln.n;
     return rc;

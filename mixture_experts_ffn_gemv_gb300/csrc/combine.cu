@@ -8,67 +8,12 @@
 // deterministic and out is fully overwritten.  g[t] is 1, or the shared
 // expert's sigmoid gate of forward_prefill step "8. Blend shared expert":
 // output += sigmoid(dot(input, gate)) * shared (shared_gate below).
+#include "combine.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
 
 namespace moe {
-
-__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-    v[0] = bf16lo(a.x); v[1] = bf16hi(a.x); v[2] = bf16lo(a.y); v[3] = bf16hi(a.y);
-    v[4] = bf16lo(a.z); v[5] = bf16hi(a.z); v[6] = bf16lo(a.w); v[7] = bf16hi(a.w);
-}
-
-// acc[i] = out[t, h0 + i] in fp32 before rounding, i < 8: the k pairs' rows in
-// ascending j (slots and weights of 8 pairs first, then their 8 rows, then the
-// sums, so the loads overlap instead of forming a dependent chain), then the
-// shared row times its gate (1 when shared_g is null).
-template <typename YT>
-__device__ __forceinline__ void pair_sum(const YT* __restrict__ y, const int32_t* __restrict__ slot,
-                                         const float* __restrict__ w, int k, int H, int P, int has_shared,
-                                         const float* __restrict__ shared_g, int t, int h0, float (&acc)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j0 = 0; j0 < k; j0 += 8) {
-        int sl[8];
-        float wj[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const bool in = j0 + u < k;
-            sl[u] = in ? slot[(size_t)t * k + j0 + u] : -1;
-            wj[u] = in ? w[(size_t)t * k + j0 + u] : 0.f;
-        }
-        float v[8][8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (sl[u] >= 0 && sl[u] < P) {  // slot -1: a pair with an invalid expert id
-                load8(y + (size_t)sl[u] * H + h0, v[u]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
-                wj[u] = 0.f;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], v[u][i], acc[i]);
-    }
-    if (has_shared) {
-        const float g = shared_g ? shared_g[t] : 1.0f;
-        float v[8];
-        load8(y + (size_t)(P + t) * H + h0, v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, v[i], acc[i]);
-    }
-}
 
 // grid (ceil(H / 1024), m), 128 threads x 8 columns
 template <typename YT>

@@ -37,8 +37,12 @@ bool router_tc_usable(int m, int H, int E);
 int router_tc_slices(int m, int H, int E);
 size_t router_tc_split_bytes(int E, int H);
 cudaError_t launch_router_split(const float* wr, int E, int H, uint16_t* planes, cudaStream_t st);
+// the tensor-core router with the top-k tail: the last CTA of each 128-token
+// m-tile (tickets [router_tc_mtiles(m)], zero at launch) writes ids and w
+int router_tc_mtiles(int m);
 cudaError_t launch_router_tc(const uint16_t* x, int m, int H, const uint16_t* planes, int E, float* part, int S,
-                             WsHeader* hdr, cudaStream_t st);
+                             WsHeader* hdr, int* tickets, int k, const float* bias, RouteMode rm, float* logits_out,
+                             int32_t* ids, float* w, cudaStream_t st);
 cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const float* bias, RouteMode rm, float* logits_out,
                         int32_t* ids, float* w, cudaStream_t st);
 
@@ -98,6 +102,33 @@ cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const f
                                    cudaStream_t st);
 cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
                                  cudaStream_t st);
+
+// Fused decode (bf16 weights, m <= kDecodeFusedMaxM, E <= 256): one
+// cooperative launch runs the whole layer -- whole router logits, the
+// routing tail (top-k and the single-block permute), gate/up, down and the
+// combine -- separated by grid barriers whose waits are bounded by wait_ns.
+constexpr int kDecodeFusedMaxM = 4;
+struct DecodeArgs {
+    GemvArgs a;                 // groups, weights and sizes (as the GEMV kernels take them)
+    const uint16_t* x;          // [m, H]
+    int m;
+    const float* wr;            // router [E, H]
+    const float* bias;          // [E] or null
+    RouteMode rm;
+    float* logits;              // scratch [m, E]
+    int32_t* ids;               // [m, k]
+    float* w;                   // [m, k]
+    int has_shared;
+    PermuteOut po;
+    WsHeader* hdr;
+    uint16_t* h;                // [rows, I]
+    float* y;                   // [rows, H]
+    uint16_t* out;              // [m, H]
+    int ns_g, ns_d;             // row slices per group: gate/up (16 rows), down (32 rows)
+    uint64_t wait_ns;
+};
+bool decode_fused_usable(int m, int E, int k);
+cudaError_t launch_decode_fused(const DecodeArgs& d, cudaStream_t st);
 
 // NVFP4 (W4A4): activation rows quantised to packed e2m1 codes q [rows, n/2],
 // e4m3 block-scale codes sb [rows, n/16] and a row scale g [rows]; the GEMVs

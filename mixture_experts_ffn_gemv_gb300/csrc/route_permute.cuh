@@ -338,4 +338,131 @@ __device__ __forceinline__ void block_permute_tiny(const int* ids_s, int P, int 
     }
 }
 
+// Recursive-halving sum over the 32 lanes of the C live values v[0, C) (C a
+// power of two), using xor offsets O, O/2, ..., 1: at each level a lane keeps
+// one half of its live values and adds the partner's copy of that half.  On
+// return lane l holds in v[0, max(C/32, 1)) the totals of values base + j
+// (lanes that differ only in bits beyond the splitting levels hold copies).
+template <int N, int C, int O>
+__device__ __forceinline__ void rhalve(float (&v)[N], int lane, int& base) {
+    if constexpr (O > 0) {
+        if constexpr (C >= 2) {
+            const bool up = (lane & O) != 0;
+#pragma unroll
+            for (int j = 0; j < C / 2; ++j) {
+                const float send = up ? v[j] : v[j + C / 2];
+                const float keep = up ? v[j + C / 2] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+            }
+            if (up) base += C / 2;
+            rhalve<N, C / 2, O / 2>(v, lane, base);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+            rhalve<N, 1, O / 2>(v, lane, base);
+        }
+    }
+}
+
+constexpr int kWholeEB = 2;  // experts per block of the whole-logit router
+
+// Whole router logits of experts [e0, e0 + kWholeEB) for all m tokens
+// (MT tokens per pass): the block's 8 warps split H into eighths, each warp
+// sums its values over the lanes by recursive halving (about one shuffle per
+// value) and the eight warp partials are added in warp order into
+// logits [m, E].  red: shared [8][kWholeEB * MT].
+template <int MT>
+__device__ __forceinline__ void whole_logits(const uint16_t* __restrict__ x, int m, int H, const float* __restrict__ wr,
+                                             int E, float* __restrict__ logits, int e0,
+                                             float (*red)[kWholeEB * MT]) {
+    constexpr int N = kWholeEB * MT;  // values per lane: [expert][token]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hs = H / 8, h0 = warp * hs, h1 = h0 + hs;  // this warp's eighth of H (a multiple of 16)
+    for (int t0 = 0; t0 < m; t0 += MT) {
+        float acc[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = 0.f;
+#pragma unroll 2
+        for (int h = h0 + lane * 4; h < h1; h += 128) {
+            float4 w[kWholeEB];
+#pragma unroll
+            for (int e = 0; e < kWholeEB; ++e)
+                w[e] = e0 + e < E ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + e) * H + h))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                if (t0 + t < m) {
+                    const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)(t0 + t) * H + h));
+                    const float x0 = bf16lo(xv.x), x1 = bf16hi(xv.x), x2 = bf16lo(xv.y), x3 = bf16hi(xv.y);
+#pragma unroll
+                    for (int e = 0; e < kWholeEB; ++e) {
+                        float& a = acc[e * MT + t];
+                        a = fmaf(w[e].x, x0, a);
+                        a = fmaf(w[e].y, x1, a);
+                        a = fmaf(w[e].z, x2, a);
+                        a = fmaf(w[e].w, x3, a);
+                    }
+                }
+            }
+        }
+        int base = 0;
+        rhalve<N, N, 16>(acc, lane, base);
+#pragma unroll
+        for (int j = 0; j < (N >= 32 ? N / 32 : 1); ++j) red[warp][base + j] = acc[j];
+        __syncthreads();
+        if (threadIdx.x < N) {
+            const int el = threadIdx.x / MT, t = threadIdx.x % MT;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) v += red[w][threadIdx.x];
+            if (t0 + t < m && e0 + el < E) logits[(size_t)(t0 + t) * E + e0 + el] = v;
+        }
+        __syncthreads();  // red is reused by the next pass
+    }
+}
+
+// Shared tail, run by the last block: logits = the S slices of part summed in
+// slice order (into shared memory), then the top-k of every token, then the
+// permute.  Shared scratch: ids_s [kPermChunk], tail_buf [kRouteFuseLogits]
+// (the logits, then the permute's tables), wsum [9].
+template <int VPL>
+__device__ __forceinline__ void route_tail(const float* part, int S, int m, int E, int k, const float* bias, RouteMode rm,
+                                           int32_t* ids, float* wts, int has_shared, const PermuteOut& o,
+                                           WsHeader* hdr, int* ids_s, int* tail_buf, int* wsum) {
+    static_assert(kRouteFuseLogits >= 8 * 256 + 2 * (256 + 2) + 27, "permute tables fit the logits buffer");
+    float* logits_s = reinterpret_cast<float*>(tail_buf);
+    int* wbase = tail_buf;
+    int* hist = tail_buf + 8 * 256;
+    int* off = hist + 256 + 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // all 256 threads reduce the slices (coalesced over e, many loads in
+    // flight); the warps then pick from shared memory
+    const int n = m * E;
+    for (int i0 = threadIdx.x; i0 < n; i0 += 4 * 256) {
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int q = 0; q < S; ++q)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i0 + u * 256 < n) v[u] += __ldcg(part + (size_t)q * n + i0 + u * 256);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i0 + u * 256 < n) logits_s[i0 + u * 256] = v[u];
+    }
+    __syncthreads();
+    for (int t = warp; t < m; t += 8) {
+        int id;
+        float wt;
+        warp_topk<VPL, false>(logits_s, 1, m, E, k, bias, rm, nullptr, t, lane, &id, &wt);
+        if (lane < k) {
+            ids[(size_t)t * k + lane] = id;
+            wts[(size_t)t * k + lane] = wt;
+            ids_s[t * k + lane] = id;
+        }
+    }
+    __syncthreads();  // logits no longer needed: the buffer becomes the permute's tables
+    if (m * k <= kPermTiny) block_permute_tiny(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, tail_buf + 8 * 256 + 2 * (256 + 2));
+    else block_permute_small(ids_s, m * k, m, E, has_shared, o, hdr, hist, off, wbase, wsum);
+    if (threadIdx.x == 0) hdr->done = 0;
+}
+
 }  // namespace moe
