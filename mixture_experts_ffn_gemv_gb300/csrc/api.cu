@@ -103,7 +103,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-    size_t hdr, tickets, zero_bytes, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile,
+    size_t hdr, zero_bytes, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile,
         sorted_pair, slot_of_pair;
     size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, sgate, total;
     size_t xsb, xg, hsb, hg;  // nvfp4: block scales and row scales of x and h
@@ -128,10 +128,7 @@ Layout layout(const moe_layer* L, int64_t m) {
     };
     const size_t ab = L->fp8 ? 1 : 2;  // activation element bytes
     o.hdr = take(sizeof(WsHeader));
-    // per-m-tile tickets of the tensor-core router's top-k tail, right after
-    // the header: both are zeroed by one memset at the start of every call
-    o.tickets = o.router_tc ? take((size_t)router_tc_mtiles((int)m) * 4) : 0;
-    o.zero_bytes = off;
+    o.zero_bytes = off;  // the header is zeroed at the start of every call
     o.part = take((size_t)o.S * m * E * 4);
     o.planes = o.router_tc ? take(router_tc_split_bytes(E, H)) : 0;
     o.ids = take((size_t)o.P * 4);
@@ -238,11 +235,10 @@ int run_route(const moe_layer* L, const Layout& lo, const void* x, int m, const 
         uint16_t* planes = at<uint16_t>(ws, lo.planes);
         WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
         MOE_LAUNCH(K_ROUTER_SPLIT, launch_router_split(wr, c.num_experts, c.hidden, planes, st));
-        MOE_LAUNCH(K_ROUTER, launch_router_tc(xb, m, c.hidden, planes, c.num_experts, part, lo.S, hdr,
-                                              at<int>(ws, lo.tickets), c.top_k, bias, L->rm, logits_out, ids, w, st));
-        return MOE_OK;  // the router's tail picked the top k
+        MOE_LAUNCH(K_ROUTER, launch_router_tc(xb, m, c.hidden, planes, c.num_experts, part, lo.S, hdr, st));
+    } else {
+        MOE_LAUNCH(K_ROUTER, launch_router(xb, m, c.hidden, wr, c.num_experts, part, lo.S, st));
     }
-    MOE_LAUNCH(K_ROUTER, launch_router(xb, m, c.hidden, wr, c.num_experts, part, lo.S, st));
     MOE_LAUNCH(K_TOPK, launch_topk(part, lo.S, m, c.num_experts, c.top_k, bias, L->rm, logits_out, ids, w, st));
     return MOE_OK;
 }

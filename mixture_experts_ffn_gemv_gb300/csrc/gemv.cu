@@ -779,10 +779,12 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+constexpr int kDecodeTailInts = 4096;  // >= the permute tables and m * E <= 4 * 256 logits
+
 template <int VPL, int MT>
 __global__ __launch_bounds__(256, 4) void decode_fused_bf16(const DecodeArgs d) {
-    __shared__ int ids_s[kPermChunk];
-    __shared__ __align__(16) int tail_buf[kRouteFuseLogits];
+    __shared__ int ids_s[kPermTiny];
+    __shared__ __align__(16) int tail_buf[kDecodeTailInts];
     __shared__ int wsum[9];
     __shared__ float red[8][kWholeEB * MT];
     __shared__ int s_res;
@@ -794,8 +796,8 @@ __global__ __launch_bounds__(256, 4) void decode_fused_bf16(const DecodeArgs d) 
     const int r = grid_arrive(d.hdr, d.wait_ns, &s_res);
     if (r < 0) return;
     if (r == 1) {
-        route_tail<VPL>(d.logits, 1, d.m, E, a.k, d.bias, d.rm, d.ids, d.w, d.has_shared, d.po, d.hdr, ids_s,
-                        tail_buf, wsum);
+        route_tail<VPL, kDecodeTailInts>(d.logits, 1, d.m, E, a.k, d.bias, d.rm, d.ids, d.w, d.has_shared, d.po,
+                                         d.hdr, ids_s, tail_buf, wsum);
         grid_release(d.hdr);
     }
     // phase G: gate/up items; then prefetch the W2 rows of this CTA's down items
@@ -830,15 +832,18 @@ __global__ __launch_bounds__(256, 4) void decode_fused_bf16(const DecodeArgs d) 
 }
 
 bool decode_fused_usable(int m, int E, int k) {
-    return m >= 1 && m <= kDecodeFusedMaxM && E <= 256 && m * k <= kPermTiny && m * E <= kRouteFuseLogits;
+    return m >= 1 && m <= kDecodeFusedMaxM && E <= 256 && m * k <= kPermTiny && m * E <= 1024;
 }
 
 template <int VPL, int MT>
 static cudaError_t launch_df(const DecodeArgs& d, cudaStream_t st) {
     static int grid = 0;
     if (grid == 0) {
+        cudaError_t e = cudaFuncSetAttribute(decode_fused_bf16<VPL, MT>,
+                                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
         int per_sm = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_bf16<VPL, MT>, 256, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_bf16<VPL, MT>, 256, 0);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         grid = std::min(per_sm, 4) * sm_count();

@@ -37,12 +37,8 @@ bool router_tc_usable(int m, int H, int E);
 int router_tc_slices(int m, int H, int E);
 size_t router_tc_split_bytes(int E, int H);
 cudaError_t launch_router_split(const float* wr, int E, int H, uint16_t* planes, cudaStream_t st);
-// the tensor-core router with the top-k tail: the last CTA of each 128-token
-// m-tile (tickets [router_tc_mtiles(m)], zero at launch) writes ids and w
-int router_tc_mtiles(int m);
 cudaError_t launch_router_tc(const uint16_t* x, int m, int H, const uint16_t* planes, int E, float* part, int S,
-                             WsHeader* hdr, int* tickets, int k, const float* bias, RouteMode rm, float* logits_out,
-                             int32_t* ids, float* w, cudaStream_t st);
+                             WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_topk(const float* part, int S, int m, int E, int k, const float* bias, RouteMode rm, float* logits_out,
                         int32_t* ids, float* w, cudaStream_t st);
 

@@ -424,11 +424,12 @@ __device__ __forceinline__ void whole_logits(const uint16_t* __restrict__ x, int
 // slice order (into shared memory), then the top-k of every token, then the
 // permute.  Shared scratch: ids_s [kPermChunk], tail_buf [kRouteFuseLogits]
 // (the logits, then the permute's tables), wsum [9].
-template <int VPL>
+// CAP: ints in tail_buf (it must also hold the m*E logits).
+template <int VPL, int CAP = kRouteFuseLogits>
 __device__ __forceinline__ void route_tail(const float* part, int S, int m, int E, int k, const float* bias, RouteMode rm,
                                            int32_t* ids, float* wts, int has_shared, const PermuteOut& o,
                                            WsHeader* hdr, int* ids_s, int* tail_buf, int* wsum) {
-    static_assert(kRouteFuseLogits >= 8 * 256 + 2 * (256 + 2) + 27, "permute tables fit the logits buffer");
+    static_assert(CAP >= 8 * 256 + 2 * (256 + 2) + 27, "permute tables fit the logits buffer");
     float* logits_s = reinterpret_cast<float*>(tail_buf);
     int* wbase = tail_buf;
     int* hist = tail_buf + 8 * 256;

@@ -10,11 +10,10 @@
 // logits keep fp32-grade accuracy at tensor-core speed.
 //
 // Grid (m-tiles of 128 tokens, S slices of H, expert blocks): each CTA
-// writes its partial logits [S, m, E].  The last CTA of an m-tile to finish
-// (an atomic ticket per m-tile; nothing ever waits) then runs step 2 of the
-// page, "Batched topK dispatch", for the tile's tokens: one warp per token
-// adds the S partials in slice order and picks the top k (the same warp
-// routine as the stand-alone top-k kernel), so no second launch is needed.
+// writes its partial logits [S, m, E] with 32-byte stores; the top-k kernel
+// adds the S partials in slice order.  (Folding the top-k into the last CTA of
+// each m-tile measured much slower: 128 tokens on 6 warps is a long serial
+// tail, 140 us against 23 + 13 us at m = 4096.)
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -22,7 +21,6 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
-#include "route_permute.cuh"
 #include "sm100.cuh"
 #include "tmap.h"
 
@@ -60,28 +58,7 @@ struct RouterParams {
     int m, E, Epad, kblocks_per_slice, stages, stage_bytes, b_plane_bytes;
     int N;  // experts per CTA (grid z splits Epad into blocks of N <= 128)
     WsHeader* hdr;
-    // the top-k tail
-    int* tickets;        // [m-tiles], zero at launch
-    int k, vpl;          // picks per token; logits per lane (E <= 32 * vpl)
-    const float* bias;   // router bias / correction bias, or null
-    RouteMode rm;
-    float* logits_out;   // [m, E] or null
-    int32_t* ids;        // [m, k]
-    float* w;            // [m, k]
 };
-
-template <int VPL>
-__device__ __forceinline__ void topk_rows(const RouterParams& p, int S, int t0, int t1, int warp, int nwarps, int lane) {
-    for (int t = t0 + warp; t < t1; t += nwarps) {
-        int id;
-        float wt;
-        warp_topk<VPL, true>(p.part, S, p.m, p.E, p.k, p.bias, p.rm, p.logits_out, t, lane, &id, &wt);
-        if (lane < p.k) {
-            p.ids[(size_t)t * p.k + lane] = id;
-            p.w[(size_t)t * p.k + lane] = wt;
-        }
-    }
-}
 
 __global__ void __launch_bounds__(R_THREADS, 1)
     router_logits_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -209,23 +186,6 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, tmem_cols);
     }
-    // the last CTA of this m-tile (over slices and expert blocks) picks the
-    // top k of the tile's tokens from the finished partials
-    __shared__ int is_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0)
-        is_last = atomicAdd(&p.tickets[blockIdx.x], 1) == (int)(gridDim.y * gridDim.z) - 1;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    const int S = (int)gridDim.y, t1 = min(m0 + RBM, p.m), nw = R_THREADS / 32;
-    switch (p.vpl) {
-        case 1: topk_rows<1>(p, S, m0, t1, warp, nw, lane); break;
-        case 2: topk_rows<2>(p, S, m0, t1, warp, nw, lane); break;
-        case 4: topk_rows<4>(p, S, m0, t1, warp, nw, lane); break;
-        default: topk_rows<8>(p, S, m0, t1, warp, nw, lane); break;
-    }
 }
 
 int sm_count() {
@@ -265,11 +225,8 @@ cudaError_t launch_router_split(const float* wr, int E, int H, uint16_t* planes,
     return cudaGetLastError();
 }
 
-int router_tc_mtiles(int m) { return ceil_div(m, RBM); }
-
 cudaError_t launch_router_tc(const uint16_t* x, int m, int H, const uint16_t* planes, int E, float* part, int S,
-                             WsHeader* hdr, int* tickets, int k, const float* bias, RouteMode rm, float* logits_out,
-                             int32_t* ids, float* w, cudaStream_t st) {
+                             WsHeader* hdr, cudaStream_t st) {
     const int Epad = router_tc_epad(E);
     CUtensorMap tx, tw;
     const int N = router_tc_n(E);
@@ -287,14 +244,6 @@ cudaError_t launch_router_tc(const uint16_t* x, int m, int H, const uint16_t* pl
     p.stage_bytes = RBM * RBK * 2 + 3 * p.b_plane_bytes;
     p.stages = std::max(1, std::min(8, (R_SMEM_MAX - 2048) / p.stage_bytes));
     p.hdr = hdr;
-    p.tickets = tickets;
-    p.k = k;
-    p.vpl = E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : 8;
-    p.bias = bias;
-    p.rm = rm;
-    p.logits_out = logits_out;
-    p.ids = ids;
-    p.w = w;
     uint32_t cols = 32;
     while ((int)cols < N) cols <<= 1;
     const int smem = 1024 + p.stages * p.stage_bytes + 256;
