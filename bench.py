@@ -205,8 +205,6 @@ def kernel_alg_bytes(kernel, shape, m, U):
             return int(m * H * 2 + m * (H * NVFP4_B + 4))
         if kernel == "h_quant_nvfp4":
             return int(rows * I_ * 4 + rows * (I_ * NVFP4_B + 4))
-    if kernel == "decode_fused":  # the whole layer in one launch
-        return layer_alg(shape, m, U)[0]
     wb = 1 if shape.fp8 else 2
     ab = 1 if shape.fp8 else 2
     sc = 4 * (H // 128) * (I_ // 128) if shape.fp8 else 0

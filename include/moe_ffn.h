@@ -97,6 +97,20 @@ typedef struct moe_config {
     int32_t scoring;      /* MOE_SCORING_SOFTMAX (0) or MOE_SCORING_SIGMOID */
     int32_t norm_topk_prob;      /* sigmoid scoring: 1 = renormalise the k weights to sum 1 */
     float routed_scaling_factor; /* sigmoid scoring: weight multiplier, finite and > 0 */
+    /* Expert parallelism (the EP path of forward_prefill.rs: an all-reduce of
+     * the bf16 [N, H] MoE output across ranks that each hold some experts,
+     * the shared expert blended once, after the all-reduce).  0, 0 = this
+     * layer holds all num_experts experts.  Otherwise it is one shard: it
+     * holds experts [expert_begin, expert_end), 0 <= begin < end <=
+     * num_experts, and its routed weight tensors are stacked over those
+     * experts only (w1, w3 [end - begin, I, H] ...).  The router still
+     * scores all num_experts experts (router_w [num_experts, H]) and the ids
+     * stay global; a shard's moe_forward / moe_experts write the partial
+     * routed sum over the pairs whose expert it holds (the other pairs are
+     * dropped, not an error) and leave the shared expert out:
+     * moe_shared_expert_add adds it after the caller's all-reduce. */
+    int32_t expert_begin;
+    int32_t expert_end;
 } moe_config;
 
 /* Stacked expert weights in nn.Linear (out, in) layout.
@@ -166,7 +180,9 @@ MOE_API int moe_route(const moe_layer* layer, const void* x, int64_t m, const fl
  * Ids outside [0, E) set the device error word (MOE_ERR_DEVICE).  Such a pair
  * is dropped: its slot_of_pair entry is -1, expert_offsets[E] counts only the
  * valid pairs (so it is then below m*k), and sorted_pair is written only up
- * to that count.                                                            */
+ * to that count.  On an expert-parallel shard E is the shard's expert count
+ * (expert_offsets [E+1] over its experts, in order) and pairs of the other
+ * shards' experts are dropped the same way without an error.               */
 MOE_API int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t m,
                 int32_t* expert_offsets, int32_t* sorted_pair, int32_t* slot_of_pair,
                 void* workspace, size_t workspace_bytes, void* stream);
@@ -210,6 +226,18 @@ MOE_API int moe_permute_noalloc(const int32_t* topk_ids, int64_t m, int32_t top_
 MOE_API int moe_experts(const moe_layer* layer, const void* x, int64_t m, const int32_t* topk_ids,
                 const float* topk_w, void* out, int arm, void* workspace,
                 size_t workspace_bytes, void* stream);
+
+/* out[t, :] = bf16(out[t, :] + shared(x[t, :])): the shared expert alone
+ * (weight 1, or its sigmoid gate), added to out in fp32 and rounded once --
+ * forward_prefill.rs's "defer shared expert blend until after all-reduce",
+ * the last step of an expert-parallel layer whose ranks each ran moe_forward
+ * on a shard and all-reduced the partial outputs.  Works on any layer with a
+ * shared expert (MOE_ERR_INVALID_ARG without one).  x bf16 [m, H]; out bf16
+ * [m, H], read and written; arm as for moe_experts (AUTO: the GEMV arm up to
+ * 64 tokens).  Workspace as for the other calls (moe_workspace_size covers
+ * it).                                                                      */
+MOE_API int moe_shared_expert_add(const moe_layer* layer, const void* x, int64_t m, void* out, int arm,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /* The whole layer: moe_route then moe_experts on one stream, no host sync.
  * topk_ids_out / topk_w_out may be NULL (the routing then stays in the

@@ -23,7 +23,8 @@ ARMS = {"auto": MOE_ARM_AUTO, "gemv": MOE_ARM_GEMV, "gemm": MOE_ARM_GEMM}
 
 EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_workspace_size", "moe_select_arm", "moe_route",
-    "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_forward", "moe_forward_residual_rmsnorm",
+    "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_shared_expert_add", "moe_forward",
+    "moe_forward_residual_rmsnorm",
     "moe_act_quant_fp8", "moe_act_quant_nvfp4", "moe_device_status", "moe_layer_set_wait_limit",
     "moe_layer_stall_test",
     "moe_last_launch_count", "moe_kernel_timing_enable", "moe_kernel_timing_read", "moe_kernel_count",
@@ -36,7 +37,7 @@ _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
 class MoeConfig(ctypes.Structure):
     _fields_ = [("hidden", _i32), ("num_experts", _i32), ("top_k", _i32), ("inter", _i32),
                 ("shared_inter", _i32), ("weights", _i32), ("scoring", _i32), ("norm_topk_prob", _i32),
-                ("routed_scaling_factor", ctypes.c_float)]
+                ("routed_scaling_factor", ctypes.c_float), ("expert_begin", _i32), ("expert_end", _i32)]
 
 
 class MoeExpertWeights(ctypes.Structure):
@@ -75,6 +76,7 @@ def load_library(path: str | None = None, build: bool = True):
         lib.moe_permute.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
         lib.moe_permute_noalloc.argtypes = [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp]
         lib.moe_experts.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+        lib.moe_shared_expert_add.argtypes = [_vp, _vp, _i64, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         lib.moe_forward.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         lib.moe_forward_residual_rmsnorm.argtypes = [_vp, _vp, _i64, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp,
                                                      _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
@@ -149,7 +151,10 @@ class MoeLayer:
     ``inputs.make_experts`` and moved to the device.
     """
 
-    def __init__(self, shape, tensors: dict):
+    def __init__(self, shape, tensors: dict, expert_range=None):
+        """expert_range: (begin, end) makes this handle one expert-parallel
+        shard holding experts [begin, end) of shape.num_experts; its tensors
+        w1, w3, w2 (and s*, sb*) are then stacked over those experts only."""
         self.lib = load_library()
         self.shape = shape
         self._keep = dict(tensors)
@@ -159,7 +164,8 @@ class MoeLayer:
         cfg = MoeConfig(shape.hidden, shape.num_experts, shape.top_k, shape.inter, shape.shared_inter, wfmt,
                         MOE_SCORING_SIGMOID if sigmoid else MOE_SCORING_SOFTMAX,
                         int(bool(getattr(shape, "norm_topk_prob", True))),
-                        float(getattr(shape, "routed_scaling", 1.0)))
+                        float(getattr(shape, "routed_scaling", 1.0)),
+                        *(expert_range if expert_range is not None else (0, 0)))
         sbn = ("sb1", "sb3", "sb2") if nvfp4 else ()
         routed = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("w1", "w3", "w2", "s1", "s3", "s2")], None,
                                   *[_p(tensors.get(n)) for n in sbn])
@@ -270,6 +276,14 @@ class MoeLayer:
         ws = self.workspace(m)
         _check(self.lib.moe_experts(self.handle, _p(x), m, _p(topk_ids), _p(topk_w), _p(out), ARMS[arm], _p(ws),
                                     ws.numel(), _stream(stream)), "moe_experts")
+        return out
+
+    def moe_shared_expert_add(self, x, out, arm="auto", stream=None):
+        """out (bf16 [m, H], in place) += the shared expert of x."""
+        m = x.shape[0]
+        ws = self.workspace(m)
+        _check(self.lib.moe_shared_expert_add(self.handle, _p(x), m, _p(out), ARMS[arm], _p(ws), ws.numel(),
+                                              _stream(stream)), "moe_shared_expert_add")
         return out
 
     def moe_forward(self, x, router_w, router_bias=None, arm="auto", out=None, return_routing=False, stream=None):

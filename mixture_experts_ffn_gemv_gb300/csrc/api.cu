@@ -24,12 +24,12 @@ namespace {
 enum KernelId : int {
     K_ROUTER_SPLIT = 0, K_ROUTER, K_TOPK, K_ROUTE_PERMUTE, K_PERMUTE_COUNT, K_PERMUTE_SCATTER, K_ACT_QUANT, K_GATHER, K_GEMV_GATEUP, K_GEMV_DOWN,
     K_GEMM_GATEUP, K_GEMM_DOWN, K_COMBINE, K_H_QUANT, K_SHARED_GATE, K_ACT_QUANT_NVFP4, K_H_QUANT_NVFP4,
-    K_DECODE_FUSED, K_COUNT
+    K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "router_split", "router", "topk_softmax", "route_permute", "permute_count", "permute_scatter", "act_quant_fp8", "gather_rows",
     "gemv_gateup", "gemv_down", "gemm_gateup", "gemm_down", "combine", "h_quant_fp8", "shared_gate",
-    "act_quant_nvfp4", "h_quant_nvfp4", "decode_fused",
+    "act_quant_nvfp4", "h_quant_nvfp4",
 };
 
 struct Pending {
@@ -93,6 +93,11 @@ struct moe_layer {
     RouteMode rm;      // router scoring
     uint64_t wait_ns;  // grouped GEMMs: limit of every bounded mbarrier wait
     int stall_test;    // bf16 grouped GEMMs: stall on purpose (failure-path test)
+    // expert parallelism: this layer holds experts [e_lo, e_lo + E_local) of
+    // cfg.num_experts; a shard (E_local < num_experts) leaves the shared
+    // expert out of moe_forward (moe_shared_expert_add adds it)
+    int e_lo, E_local;
+    bool shard;
 };
 
 namespace {
@@ -109,16 +114,22 @@ struct Layout {
     size_t xsb, xg, hsb, hg;  // nvfp4: block scales and row scales of x and h
     size_t xs_g, h16;         // nvfp4 GEMM arm: gathered rows' scales, f16 h
     int S, P, rows, nchunk;
+    int k;        // pairs per token in this call (top_k; 0 for the shared expert alone)
+    int shared;   // 1: group E (the shared expert, rows P .. P+m-1) runs in this call
     bool router_tc;
 };
 
-Layout layout(const moe_layer* L, int64_t m) {
+// shared_only: the layout of moe_shared_expert_add (no routed pairs)
+Layout layout(const moe_layer* L, int64_t m, bool shared_only = false) {
     Layout o{};
-    const int E = L->cfg.num_experts, k = L->cfg.top_k, H = L->cfg.hidden, I = L->cfg.inter;
+    const int Er = L->cfg.num_experts, E = L->E_local, H = L->cfg.hidden, I = L->cfg.inter;
+    o.k = shared_only ? 0 : L->cfg.top_k;
+    o.shared = shared_only ? 1 : ((L->has_shared && !L->shard) ? 1 : 0);
+    const int k = o.k;
     o.P = (int)(m * k);
-    o.rows = o.P + (L->has_shared ? (int)m : 0);
-    o.router_tc = router_tc_usable((int)m, H, E);
-    o.S = o.router_tc ? router_tc_slices((int)m, H, E) : router_slices(H, (int)m);
+    o.rows = o.P + (o.shared ? (int)m : 0);
+    o.router_tc = !shared_only && router_tc_usable((int)m, H, Er);
+    o.S = o.router_tc ? router_tc_slices((int)m, H, Er) : router_slices(H, (int)m);
     o.nchunk = ceil_div(std::max(o.P, 1), kPermChunk);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -129,8 +140,8 @@ Layout layout(const moe_layer* L, int64_t m) {
     const size_t ab = L->fp8 ? 1 : 2;  // activation element bytes
     o.hdr = take(sizeof(WsHeader));
     o.zero_bytes = off;  // the header is zeroed at the start of every call
-    o.part = take((size_t)o.S * m * E * 4);
-    o.planes = o.router_tc ? take(router_tc_split_bytes(E, H)) : 0;
+    o.part = take((size_t)o.S * m * Er * 4);
+    o.planes = o.router_tc ? take(router_tc_split_bytes(Er, H)) : 0;
     o.ids = take((size_t)o.P * 4);
     o.w = take((size_t)o.P * 4);
     o.chunk_base = take((size_t)o.nchunk * E * 4);
@@ -257,10 +268,20 @@ PermuteOut permute_out(const Layout& lo, void* ws, int32_t* sorted_pair, int32_t
     return o;
 }
 
+size_t l2_bytes() {
+    static size_t n = [] {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+            return (size_t)0;
+        return (size_t)v;
+    }();
+    return n;
+}
+
 // The GEMV kernels' view of a call: group tables in the workspace, weights.
 GemvArgs gemv_args(const moe_layer* L, const Layout& lo, void* ws) {
     const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
-    const int E = L->cfg.num_experts;
+    const int E = L->E_local;
     GemvArgs a;
     a.hdr = at<WsHeader>(ws, lo.hdr);
     a.grp_off = po.grp_off;
@@ -268,11 +289,16 @@ GemvArgs gemv_args(const moe_layer* L, const Layout& lo, void* ws) {
     a.act_group = po.act_group;
     a.sorted_pair = po.sorted_pair;
     a.P = lo.P;
-    a.k = L->cfg.top_k;
+    a.k = lo.k;
     a.E = E;
     a.H = L->cfg.hidden;
     a.I = L->cfg.inter;
-    a.max_groups = std::min(E, lo.P) + (L->has_shared ? 1 : 0);
+    a.max_groups = std::min(E, lo.P) + lo.shared;
+    // prefetch W2 into L2 during gate/up when the active groups' W2 (at most
+    // max_groups of them) takes under a third of L2: decode with few experts
+    const size_t w2_bytes = L->fp8 ? (size_t)a.H * a.I
+                                   : (L->nvfp4 ? (size_t)a.H * a.I / 2 + (size_t)a.H * a.I / 16 : (size_t)a.H * a.I * 2);
+    a.prefetch_w2 = !L->fp8 && (size_t)a.max_groups * w2_bytes <= l2_bytes() / 3 ? 1 : 0;
     a.w1 = L->routed.w1; a.w3 = L->routed.w3; a.w2 = L->routed.w2;
     a.s1 = L->routed.s1; a.s3 = L->routed.s3; a.s2 = L->routed.s2;
     a.sw1 = L->shared.w1; a.sw3 = L->shared.w3; a.sw2 = L->shared.w2;
@@ -289,19 +315,20 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
                 const TailArgs* tail = nullptr) {
     const moe_config& c = L->cfg;
     const cudaStream_t st = ln.st;
-    const int E = c.num_experts, k = c.top_k, H = c.hidden, I = c.inter;
+    const int E = L->E_local, k = lo.k, H = c.hidden, I = c.inter;
     WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
     const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
     if (!permuted) {
-        MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->has_shared ? 1 : 0, po, hdr, st));
-        MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(ids, m, k, E, po, st));
+        MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->e_lo, c.num_experts, lo.shared, po, hdr, st));
+        MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(ids, m, k, E, L->e_lo, c.num_experts, po, st));
     }
-    if (arm == MOE_ARM_AUTO) arm = moe_select_arm(L, m);
-    const int has_shared = L->has_shared ? 1 : 0;
+    if (arm == MOE_ARM_AUTO) arm = lo.k == 0 ? (m <= 64 || !gemm_supported(c) ? MOE_ARM_GEMV : MOE_ARM_GEMM)
+                                             : moe_select_arm(L, m);
+    const int has_shared = lo.shared;
     // the shared expert's sigmoid gate per token (forward_prefill step 8), or
     // null: weight 1
     float* sg = nullptr;
-    if (L->shared.gate) {
+    if (L->shared.gate && has_shared) {
         sg = at<float>(ws, lo.sgate);
         MOE_LAUNCH(K_SHARED_GATE, launch_shared_gate(static_cast<const uint16_t*>(x), m, H, L->shared.gate, sg, st));
     }
@@ -341,7 +368,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
             MOE_LAUNCH(K_COMBINE, launch_combine_tail_f32(y, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, *tail, st));
         else
             MOE_LAUNCH(K_COMBINE, launch_combine_f32(y, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg,
-                                                     static_cast<uint16_t*>(out), st));
+                                                     static_cast<uint16_t*>(out), st, lo.k == 0 ? 1 : 0));
         return MOE_OK;
     }
     if (arm != MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
@@ -405,7 +432,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
         MOE_LAUNCH(K_COMBINE, launch_combine_tail_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, *tail, st));
     else
         MOE_LAUNCH(K_COMBINE, launch_combine_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg,
-                                                  static_cast<uint16_t*>(out), st));
+                                                  static_cast<uint16_t*>(out), st, lo.k == 0 ? 1 : 0));
     return MOE_OK;
 }
 
@@ -426,34 +453,7 @@ int forward_impl(const moe_layer* layer, const void* x, int64_t m, const float* 
     Launcher ln{layer, st};
     if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
     const moe_config& c = layer->cfg;
-    const int arm_used = arm == MOE_ARM_AUTO ? moe_select_arm(layer, m) : arm;
-    if (!tail && !layer->fp8 && !layer->nvfp4 && !layer->shared.gate && !lo.router_tc && arm_used == MOE_ARM_GEMV &&
-        c.hidden % 256 == 0 && decode_fused_usable((int)m, c.num_experts, c.top_k)) {
-        // decode, bf16: the whole layer in one cooperative launch
-        DecodeArgs d{};
-        d.a = gemv_args(layer, lo, workspace);
-        d.x = static_cast<const uint16_t*>(x);
-        d.m = (int)m;
-        d.wr = router_w;
-        d.bias = router_bias;
-        d.rm = layer->rm;
-        d.logits = at<float>(workspace, lo.part);
-        d.ids = ids;
-        d.w = w;
-        d.has_shared = layer->has_shared ? 1 : 0;
-        d.po = permute_out(lo, workspace, nullptr, nullptr, nullptr);
-        d.hdr = at<WsHeader>(workspace, lo.hdr);
-        d.h = at<uint16_t>(workspace, lo.h);
-        d.y = at<float>(workspace, lo.y);
-        d.out = static_cast<uint16_t*>(out);
-        d.ns_g = c.inter / 16;
-        d.ns_d = c.hidden / 32;
-        d.wait_ns = layer->wait_ns;
-        MOE_LAUNCH(K_DECODE_FUSED, launch_decode_fused(d, st));
-        layer->last_launches = ln.n;
-        return MOE_OK;
-    }
-    if (!lo.router_tc && route_permute_fusable((int)m, c.top_k, c.num_experts)) {
+    if (!lo.router_tc && !layer->shard && route_permute_fusable((int)m, c.top_k, c.num_experts)) {
         // decode: router, top-k and the permute in one launch.  For fp8 layers
         // with m > 4 the same launch also quantises x; at m <= 4 the separate
         // quantiser launch measured faster (DeepSeek-V3 shape, m = 1: 105 vs
@@ -515,6 +515,9 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
         (!(c.routed_scaling_factor > 0.f) || !std::isfinite(c.routed_scaling_factor) ||
          (c.norm_topk_prob != 0 && c.norm_topk_prob != 1)))
         return MOE_ERR_INVALID_ARG;
+    if (c.expert_begin < 0 || c.expert_end < 0 || c.expert_end > c.num_experts ||
+        (c.expert_end != 0 && c.expert_begin >= c.expert_end) || (c.expert_end == 0 && c.expert_begin != 0))
+        return MOE_ERR_INVALID_ARG;
     if (!weights_ok(routed, c.weights) || routed->gate) return MOE_ERR_INVALID_ARG;  // a gate is for the shared expert only
     const bool has_shared = c.shared_inter > 0;
     if (has_shared != (shared != nullptr)) return MOE_ERR_INVALID_ARG;
@@ -533,11 +536,16 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
     L->last_launches = 0;
     L->wait_ns = kDefaultWaitNs;
     L->stall_test = 0;
+    L->e_lo = c.expert_end ? c.expert_begin : 0;
+    L->E_local = c.expert_end ? c.expert_end - c.expert_begin : c.num_experts;
+    L->shard = L->E_local < c.num_experts;
     if (cudaGetDevice(&L->device) != cudaSuccess) {
         delete L;
         return MOE_ERR_CUDA;
     }
-    const int rc = gemm_prepare_weights(c, routed, has_shared ? shared : nullptr, &L->gemm);
+    moe_config local = c;  // the weight tensors hold this layer's experts only
+    local.num_experts = L->E_local;
+    const int rc = gemm_prepare_weights(local, routed, has_shared ? shared : nullptr, &L->gemm);
     if (rc != MOE_OK) {
         delete L;
         return rc;
@@ -554,6 +562,7 @@ int moe_layer_destroy(moe_layer* layer) {
 int moe_workspace_size(const moe_layer* layer, int64_t m, size_t* bytes) {
     if (!layer || !bytes || m < 0) return MOE_ERR_INVALID_ARG;
     *bytes = layout(layer, m).total;
+    if (layer->has_shared) *bytes = std::max(*bytes, layout(layer, m, true).total);  // moe_shared_expert_add
     return MOE_OK;
 }
 
@@ -593,9 +602,9 @@ int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t m, int3
     if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
     Launcher ln{layer, st};
     const PermuteOut po = permute_out(lo, workspace, sorted_pair, slot_of_pair, expert_offsets);
-    const int k = layer->cfg.top_k, E = layer->cfg.num_experts;
-    MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(topk_ids, (int)m, k, E, 0, po, hdr, st));
-    MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(topk_ids, (int)m, k, E, po, st));
+    const int k = layer->cfg.top_k, E = layer->E_local, Et = layer->cfg.num_experts;
+    MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(topk_ids, (int)m, k, E, layer->e_lo, Et, 0, po, hdr, st));
+    MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(topk_ids, (int)m, k, E, layer->e_lo, Et, po, st));
     layer->last_launches = ln.n;
     return MOE_OK;
 }
@@ -614,6 +623,29 @@ int moe_experts(const moe_layer* layer, const void* x, int64_t m, const int32_t*
     return rc;
 }
 
+
+int moe_shared_expert_add(const moe_layer* layer, const void* x, int64_t m, void* out, int arm, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    if (!layer) return MOE_ERR_INVALID_ARG;
+    if (!layer->has_shared) return MOE_ERR_INVALID_ARG;
+    if (m < 0 || m > (int64_t)(INT32_MAX / 64)) return m < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev != layer->device) return MOE_ERR_INVALID_ARG;
+    if (m == 0) return MOE_OK;
+    if (!x || !out || !aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    if (arm < MOE_ARM_AUTO || arm > MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
+    const Layout lo = layout(layer, m, true);
+    if (!workspace || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < lo.total) return MOE_ERR_WORKSPACE;
+    Launcher ln{layer, static_cast<cudaStream_t>(stream)};
+    if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, ln.st) != cudaSuccess) return MOE_ERR_CUDA;
+    // no routed pairs (P = 0): the id and weight arrays are never read
+    const int rc = run_experts(layer, lo, x, (int)m, at<int32_t>(workspace, lo.ids), at<float>(workspace, lo.w), out,
+                               arm, workspace, ln);
+    layer->last_launches = ln.n;
+    return rc;
+}
 
 int moe_forward(const moe_layer* layer, const void* x, int64_t m, const float* router_w, const float* router_bias,
                 void* out, int32_t* topk_ids_out, float* topk_w_out, int arm, void* workspace, size_t workspace_bytes,

@@ -16,10 +16,14 @@
 namespace moe {
 
 // grid (ceil(H / 1024), m), 128 threads x 8 columns
+// accumulate = 1: out += the sum (out read as bf16, the sum added in fp32,
+// rounded once) -- the shared expert added after an expert-parallel
+// all-reduce of the routed partial outputs.
 template <typename YT>
 __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
                                                const float* __restrict__ w, int k, int H, int P, int has_shared,
-                                               const float* __restrict__ shared_g, uint16_t* __restrict__ out) {
+                                               const float* __restrict__ shared_g, uint16_t* __restrict__ out,
+                                               int accumulate) {
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.y;
@@ -27,6 +31,12 @@ __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const i
     if (h0 >= H) return;
     float acc[8];
     pair_sum(y, slot, w, k, H, P, has_shared, shared_g, t, h0, acc);
+    if (accumulate) {
+        float prev[8];
+        load8(out + (size_t)t * H + h0, prev);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = prev[i] + acc[i];
+    }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);
     o.y = pack_bf16x2(acc[2], acc[3]);
@@ -36,16 +46,20 @@ __global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const i
 }
 
 cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
-                               int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st) {
+                               int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st,
+                               int accumulate) {
     const dim3 grid(ceil_div(H, 1024), m);
-    launch_pdl(combine<float>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out);
+    launch_pdl(combine<float>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out,
+               accumulate);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
-                                int H, int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st) {
+                                int H, int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st,
+                                int accumulate) {
     const dim3 grid(ceil_div(H, 1024), m);
-    launch_pdl(combine<uint16_t>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out);
+    launch_pdl(combine<uint16_t>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out,
+               accumulate);
     return cudaGetLastError();
 }
 

@@ -1,24 +1,19 @@
 // Unpermute + routing-weighted reduce of one token's 8 output columns: the
-// body of the combine kernels (combine.cu) and of the fused decode kernel's
-// last phase.  See combine.cu for the operation and its page.
+// body of the combine kernels.  See combine.cu for the operation and its page.
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
 
-// COH: the rows were written earlier in the same kernel launch (by other
-// blocks), so they are read through L2 (ld.global.cg), not the read-only path.
-template <bool COH = false>
 __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
-    const float4 a = COH ? __ldcg(reinterpret_cast<const float4*>(p)) : __ldg(reinterpret_cast<const float4*>(p));
-    const float4 b = COH ? __ldcg(reinterpret_cast<const float4*>(p + 4)) : __ldg(reinterpret_cast<const float4*>(p + 4));
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
-template <bool COH = false>
 __device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
-    const uint4 a = COH ? __ldcg(reinterpret_cast<const uint4*>(p)) : __ldg(reinterpret_cast<const uint4*>(p));
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
     v[0] = bf16lo(a.x); v[1] = bf16hi(a.x); v[2] = bf16lo(a.y); v[3] = bf16hi(a.y);
     v[4] = bf16lo(a.z); v[5] = bf16hi(a.z); v[6] = bf16lo(a.w); v[7] = bf16hi(a.w);
 }
@@ -27,7 +22,7 @@ __device__ __forceinline__ void load8(const uint16_t* p, float (&v)[8]) {
 // ascending j (slots and weights of 8 pairs first, then their 8 rows, then the
 // sums, so the loads overlap instead of forming a dependent chain), then the
 // shared row times its gate (1 when shared_g is null).
-template <typename YT, bool COH = false>
+template <typename YT>
 __device__ __forceinline__ void pair_sum(const YT* __restrict__ y, const int32_t* __restrict__ slot,
                                          const float* __restrict__ w, int k, int H, int P, int has_shared,
                                          const float* __restrict__ shared_g, int t, int h0, float (&acc)[8]) {
@@ -39,15 +34,14 @@ __device__ __forceinline__ void pair_sum(const YT* __restrict__ y, const int32_t
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const bool in = j0 + u < k;
-            const size_t i = (size_t)t * k + j0 + u;
-            sl[u] = in ? (COH ? __ldcg(slot + i) : slot[i]) : -1;
-            wj[u] = in ? (COH ? __ldcg(w + i) : w[i]) : 0.f;
+            sl[u] = in ? slot[(size_t)t * k + j0 + u] : -1;
+            wj[u] = in ? w[(size_t)t * k + j0 + u] : 0.f;
         }
         float v[8][8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             if (sl[u] >= 0 && sl[u] < P) {  // slot -1: a pair with an invalid expert id
-                load8<COH>(y + (size_t)sl[u] * H + h0, v[u]);
+                load8(y + (size_t)sl[u] * H + h0, v[u]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
@@ -60,9 +54,9 @@ __device__ __forceinline__ void pair_sum(const YT* __restrict__ y, const int32_t
             for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], v[u][i], acc[i]);
     }
     if (has_shared) {
-        const float g = shared_g ? (COH ? __ldcg(shared_g + t) : shared_g[t]) : 1.0f;
+        const float g = shared_g ? shared_g[t] : 1.0f;
         float v[8];
-        load8<COH>(y + (size_t)(P + t) * H + h0, v);
+        load8(y + (size_t)(P + t) * H + h0, v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, v[i], acc[i]);
     }

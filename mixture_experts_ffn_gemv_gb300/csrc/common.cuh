@@ -15,9 +15,7 @@ struct WsHeader {
     int n_active;     // groups with at least one row
     int total_tiles;  // grouped GEMM: m-tiles over all active groups
     int group_done[32];  // fused decode routing: slices finished per group of 8 experts
-    int bar_count;       // fused decode kernel: blocks arrived at the current grid barrier
-    int bar_gen;         // fused decode kernel: grid barriers completed
-    int pad[25];
+    int pad[27];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -27,14 +27,10 @@
 // [2^-10, 2688], so that product is exact in f16 and the f16 mma.sync sums
 // exact products of the block-scaled values.  The two fp32 tensor scales
 // multiply the finished sum.
-#include <algorithm>
-
-#include "combine.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
 #include "nvfp4.cuh"
-#include "route_permute.cuh"
 
 namespace moe {
 
@@ -104,6 +100,21 @@ struct Group {
     int g, off, cnt;
 };
 
+// Ask L2 to fetch this work item's share of its group's down-projection
+// weight (W2 of the group is one contiguous [H, I] block of `bytes`; item
+// `slice` of n_slices takes an equal, 16-byte aligned share) while the gate/up
+// weights stream, so the down kernel that follows reads W2 from L2.  Only
+// when the host set prefetch_w2 (the active groups' W2 fits L2 with room).
+__device__ __forceinline__ void prefetch_w2_share(const void* w2, size_t bytes, int slice, int n_slices) {
+    const size_t share = (bytes / n_slices) & ~(size_t)15;
+    const char* base = static_cast<const char*>(w2) + (size_t)slice * share;
+    const int lane = threadIdx.x & 31;
+    for (size_t off = (size_t)lane * 4096; off < share; off += 32 * 4096) {
+        const uint32_t n = (uint32_t)(share - off < 4096 ? share - off : 4096);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n) : "memory");
+    }
+}
+
 __device__ __forceinline__ bool load_group(const GemvArgs& a, int ga, Group& gr) {
     if (ga >= a.hdr->n_active) return false;
     gr.g = a.act_group[ga];
@@ -123,8 +134,7 @@ __device__ __forceinline__ int row_token(const GemvArgs& a, int s) {
 // K-slice partials are summed in fixed order through shared memory, then
 // h = silu(g) * u is stored as bf16 [rows, I].
 // The body of one CTA's work item bid = (active group bid / n_slices, row
-// slice bid % n_slices); the stand-alone kernel runs one item per CTA, the
-// fused decode kernel several per CTA.
+// slice bid % n_slices).
 template <int NT, int RT>
 __device__ __forceinline__ void gateup_bf16_item(const GemvArgs& a, const uint16_t* __restrict__ x,
                                                  uint16_t* __restrict__ h, int bid, int n_slices) {
@@ -137,6 +147,9 @@ __device__ __forceinline__ void gateup_bf16_item(const GemvArgs& a, const uint16
     if (!load_group(a, bid / n_slices, gr)) return;
     const int H = a.H, I = a.I;
     const int row0 = (bid % n_slices) * (16 * RT) + rt * 16;
+    if (a.prefetch_w2 && warp == 7)
+        prefetch_w2_share(gr.g < a.E ? (const uint16_t*)a.w2 + (size_t)gr.g * H * I : (const uint16_t*)a.sw2,
+                          (size_t)H * I * 2, bid % n_slices, n_slices);
     const uint16_t* W1 = gr.g < a.E ? (const uint16_t*)a.w1 + (size_t)gr.g * I * H : (const uint16_t*)a.sw1;
     const uint16_t* W3 = gr.g < a.E ? (const uint16_t*)a.w3 + (size_t)gr.g * I * H : (const uint16_t*)a.sw3;
     const uint4* w1g = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8) * H);
@@ -216,9 +229,7 @@ __global__ __launch_bounds__(256, (NT == 1 ? 4 : 2)) void gemv_gateup_bf16(const
 
 // ============================================================ down, bf16
 // CTA: RT row tiles (16 rows of H) x 8/RT K-slices of I; y fp32 [rows, H].
-// COH: h was written earlier in the same launch (the fused decode kernel), so
-// it is read through L2 rather than the read-only path.
-template <int NT, int RT, bool COH>
+template <int NT, int RT>
 __device__ __forceinline__ void down_bf16_item(const GemvArgs& a, const uint16_t* __restrict__ h,
                                                float* __restrict__ y, int bid, int n_slices) {
     constexpr int KS = 8 / RT;
@@ -251,7 +262,7 @@ __device__ __forceinline__ void down_bf16_item(const GemvArgs& a, const uint16_t
         for (int kc = kc0 + tig; kc < kc1; kc += 4) {
             const uint4 w0 = ldw<RT>(wg + kc), w8 = ldw<RT>(wg8 + kc);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma2_bf16(c[nt], w0, w8, COH ? __ldcg(hr[nt] + kc) : __ldg(hr[nt] + kc));
+            for (int nt = 0; nt < NT; ++nt) mma2_bf16(c[nt], w0, w8, __ldg(hr[nt] + kc));
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -280,7 +291,7 @@ __global__ __launch_bounds__(256, 4) void gemv_down_bf16(const GemvArgs a, const
                                                       float* __restrict__ y, int n_slices) {
     pdl_wait();
     pdl_trigger();
-    down_bf16_item<NT, RT, false>(a, h, y, blockIdx.x, n_slices);
+    down_bf16_item<NT, RT>(a, h, y, blockIdx.x, n_slices);
 }
 
 // ============================================================ gate/up, fp8
@@ -499,6 +510,12 @@ __global__ __launch_bounds__(256, (NT == 1 ? 3 : 2)) void gemv_gateup_nvfp4(
     const int H = a.H, I = a.I, hq = H / 2, hs = H / 16;
     const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
     const bool routed = gr.g < a.E;
+    if (a.prefetch_w2 && warp == 7) {  // packed codes [H, I/2], then block scales [H, I/16]
+        prefetch_w2_share(routed ? (const uint8_t*)a.w2 + (size_t)gr.g * H * (I / 2) : (const uint8_t*)a.sw2,
+                          (size_t)H * (I / 2), blockIdx.x % n_slices, n_slices);
+        prefetch_w2_share(routed ? a.sb2 + (size_t)gr.g * H * (I / 16) : a.ssb2, (size_t)H * (I / 16),
+                          blockIdx.x % n_slices, n_slices);
+    }
     const uint8_t* W1 = routed ? (const uint8_t*)a.w1 + (size_t)gr.g * I * hq : (const uint8_t*)a.sw1;
     const uint8_t* W3 = routed ? (const uint8_t*)a.w3 + (size_t)gr.g * I * hq : (const uint8_t*)a.sw3;
     const uint8_t* B1 = routed ? a.sb1 + (size_t)gr.g * I * hs : a.ssb1;
@@ -698,181 +715,6 @@ __global__ __launch_bounds__(256, (NT == 1 ? 4 : 3)) void gemv_down_nvfp4(const 
         }
         __syncthreads();
     }
-}
-
-static int sm_count();
-
-// ============================================================ fused decode
-// The whole layer for m <= 4 tokens in one cooperative launch (every CTA is
-// resident at once), so the four dependent steps of the decode chain -- the
-// routing of span-02 gpu_model/forward.rs's moe_router_decode, its
-// moe_glu_decode and moe_down_decode, and the weighted combine -- pay no
-// launch-and-drain gap between them:
-//   phase R  CTAs take expert pairs: whole router logits (whole_logits);
-//   barrier  the last CTA to arrive runs the routing tail (top-k, the
-//            single-block permute) before it releases the others;
-//   phase G  gate/up work items (group, 16-row slice) round-robin over CTAs;
-//            each CTA then asks L2 to prefetch the W2 rows of its own down
-//            items (cp.async.bulk.prefetch), so HBM keeps streaming through
-//            the next barrier;
-//   phase D  down items (group, 32-row slice);
-//   phase C  out[t] = sum_j w[t, j] y[slot(t, j)] (+ the shared expert), 8
-//            columns per thread.
-// Every barrier wait is bounded (wait_ns): a CTA that gives up records
-// DEV_ERR_TIMEOUT and returns; the others then give up at their next wait.
-
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Arrive at a grid barrier.  Returns 1 in the last CTA to arrive (which must
-// call grid_release once its serial work is done), 0 in the others once the
-// barrier is released, -1 when the wait ran out (error recorded).
-__device__ __forceinline__ int grid_arrive(WsHeader* hdr, uint64_t limit_ns, int* s_res) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int gen = ld_acquire_gpu(&hdr->bar_gen);
-        __threadfence();
-        int res = 1;
-        if (atomicAdd(&hdr->bar_count, 1) != (int)gridDim.x - 1) {
-            res = 0;
-            uint64_t t0;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-            while (ld_acquire_gpu(&hdr->bar_gen) == gen) {
-                uint64_t now;
-                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
-                if (now - t0 > limit_ns) {
-                    set_error(hdr, DEV_ERR_TIMEOUT, 40);
-                    res = -1;
-                    break;
-                }
-                __nanosleep(100);
-            }
-        }
-        __threadfence();
-        *s_res = res;
-    }
-    __syncthreads();
-    return *s_res;
-}
-
-__device__ __forceinline__ void grid_release(WsHeader* hdr) {
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        hdr->bar_count = 0;
-        __threadfence();
-        atomicAdd(&hdr->bar_gen, 1);
-    }
-}
-
-// One plain barrier (no serial work): false when the wait ran out.
-__device__ __forceinline__ bool grid_sync(WsHeader* hdr, uint64_t limit_ns, int* s_res) {
-    const int r = grid_arrive(hdr, limit_ns, s_res);
-    if (r == 1) grid_release(hdr);
-    return r >= 0;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-constexpr int kDecodeTailInts = 4096;  // >= the permute tables and m * E <= 4 * 256 logits
-
-template <int VPL, int MT>
-__global__ __launch_bounds__(256, 4) void decode_fused_bf16(const DecodeArgs d) {
-    __shared__ int ids_s[kPermTiny];
-    __shared__ __align__(16) int tail_buf[kDecodeTailInts];
-    __shared__ int wsum[9];
-    __shared__ float red[8][kWholeEB * MT];
-    __shared__ int s_res;
-    const GemvArgs& a = d.a;
-    const int E = a.E, H = a.H, I = a.I;
-    // phase R: whole logits of expert pairs
-    for (int b = blockIdx.x; b * kWholeEB < E; b += gridDim.x)
-        whole_logits<MT>(d.x, d.m, H, d.wr, E, d.logits, b * kWholeEB, red);
-    const int r = grid_arrive(d.hdr, d.wait_ns, &s_res);
-    if (r < 0) return;
-    if (r == 1) {
-        route_tail<VPL, kDecodeTailInts>(d.logits, 1, d.m, E, a.k, d.bias, d.rm, d.ids, d.w, d.has_shared, d.po,
-                                         d.hdr, ids_s, tail_buf, wsum);
-        grid_release(d.hdr);
-    }
-    // phase G: gate/up items; then prefetch the W2 rows of this CTA's down items
-    const int n_act = ld_acquire_gpu(&d.hdr->n_active);
-    for (int it = blockIdx.x; it < n_act * d.ns_g; it += gridDim.x) gateup_bf16_item<1, 1>(a, d.x, d.h, it, d.ns_g);
-    if (threadIdx.x < 32) {  // one warp, 4 KB pieces
-        const int pieces = 32 * I * 2 / 4096;  // I a multiple of 128
-        for (int it = blockIdx.x; it < n_act * d.ns_d; it += gridDim.x) {
-            const int g = __ldcg(a.act_group + it / d.ns_d);
-            const uint16_t* W2 = g < E ? (const uint16_t*)a.w2 + (size_t)g * H * I : (const uint16_t*)a.sw2;
-            const char* base = reinterpret_cast<const char*>(W2 + (size_t)(it % d.ns_d) * 32 * I);
-            for (int q = threadIdx.x; q < pieces; q += 32) prefetch_l2(base + (size_t)q * 4096, 4096u);
-        }
-    }
-    if (!grid_sync(d.hdr, d.wait_ns, &s_res)) return;
-    // phase D: down items
-    for (int it = blockIdx.x; it < n_act * d.ns_d; it += gridDim.x) down_bf16_item<1, 2, true>(a, d.h, d.y, it, d.ns_d);
-    if (!grid_sync(d.hdr, d.wait_ns, &s_res)) return;
-    // phase C: the weighted combine, 8 columns per thread
-    const int per_tok = H / 8;
-    for (int i = blockIdx.x * 256 + threadIdx.x; i < d.m * per_tok; i += gridDim.x * 256) {
-        const int t = i / per_tok, h0 = (i % per_tok) * 8;
-        float acc[8];
-        pair_sum<float, true>(d.y, d.po.slot_of_pair, d.w, a.k, H, a.P, d.has_shared, nullptr, t, h0, acc);
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        *reinterpret_cast<uint4*>(d.out + (size_t)t * H + h0) = o;
-    }
-}
-
-bool decode_fused_usable(int m, int E, int k) {
-    return m >= 1 && m <= kDecodeFusedMaxM && E <= 256 && m * k <= kPermTiny && m * E <= 1024;
-}
-
-template <int VPL, int MT>
-static cudaError_t launch_df(const DecodeArgs& d, cudaStream_t st) {
-    static int grid = 0;
-    if (grid == 0) {
-        cudaError_t e = cudaFuncSetAttribute(decode_fused_bf16<VPL, MT>,
-                                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_fused_bf16<VPL, MT>, 256, 0);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        grid = std::min(per_sm, 4) * sm_count();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: the grid barriers can complete
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_fused_bf16<VPL, MT>, d);
-}
-
-cudaError_t launch_decode_fused(const DecodeArgs& d, cudaStream_t st) {
-    const int vpl = ceil_div(d.a.E, 32);
-    cudaError_t e;
-    if (d.m <= 1) {
-        e = vpl <= 1 ? launch_df<1, 1>(d, st) : vpl <= 2 ? launch_df<2, 1>(d, st) : vpl <= 4 ? launch_df<4, 1>(d, st)
-                                                                                           : launch_df<8, 1>(d, st);
-    } else {
-        e = vpl <= 1 ? launch_df<1, 4>(d, st) : vpl <= 2 ? launch_df<2, 4>(d, st) : vpl <= 4 ? launch_df<4, 4>(d, st)
-                                                                                           : launch_df<8, 4>(d, st);
-    }
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
 }
 
 // ============================================================ launchers

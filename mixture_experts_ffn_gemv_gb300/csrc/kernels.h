@@ -54,9 +54,12 @@ struct PermuteOut {
     int32_t* slot_of_pair;   // [P]
     int32_t* expert_offsets; // [E+1] optional copy for the caller (may be null)
 };
-cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int has_shared, const PermuteOut& o,
-                                 WsHeader* hdr, cudaStream_t st);
-cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, const PermuteOut& o, cudaStream_t st);
+// ids are global expert ids; the layer holds experts [e_lo, e_lo + E) of
+// E_total (pairs of other experts are dropped: slot -1)
+cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int e_lo, int E_total, int has_shared,
+                                 const PermuteOut& o, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, int e_lo, int E_total,
+                                   const PermuteOut& o, cudaStream_t st);
 
 // decode fusion: router sums + top-k + single-block permute in one launch
 // (part: [S, m, E] scratch, S = router_slices(H, m)); with xq non-null it also
@@ -85,6 +88,7 @@ struct GemvArgs {
     const int* act_group;
     const int32_t* sorted_pair;
     int P, k, E, H, I, max_groups;
+    int prefetch_w2;  // gate/up kernels prefetch the groups' W2 into L2 for the down kernel
     // routed weights (stacked) and the shared expert's (g == E)
     const void *w1, *w3, *w2, *sw1, *sw3, *sw2;
     // fp8: 128x128 block scales; nvfp4: one fp32 scale per expert matrix
@@ -98,33 +102,6 @@ cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const f
                                    cudaStream_t st);
 cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
                                  cudaStream_t st);
-
-// Fused decode (bf16 weights, m <= kDecodeFusedMaxM, E <= 256): one
-// cooperative launch runs the whole layer -- whole router logits, the
-// routing tail (top-k and the single-block permute), gate/up, down and the
-// combine -- separated by grid barriers whose waits are bounded by wait_ns.
-constexpr int kDecodeFusedMaxM = 4;
-struct DecodeArgs {
-    GemvArgs a;                 // groups, weights and sizes (as the GEMV kernels take them)
-    const uint16_t* x;          // [m, H]
-    int m;
-    const float* wr;            // router [E, H]
-    const float* bias;          // [E] or null
-    RouteMode rm;
-    float* logits;              // scratch [m, E]
-    int32_t* ids;               // [m, k]
-    float* w;                   // [m, k]
-    int has_shared;
-    PermuteOut po;
-    WsHeader* hdr;
-    uint16_t* h;                // [rows, I]
-    float* y;                   // [rows, H]
-    uint16_t* out;              // [m, H]
-    int ns_g, ns_d;             // row slices per group: gate/up (16 rows), down (32 rows)
-    uint64_t wait_ns;
-};
-bool decode_fused_usable(int m, int E, int k);
-cudaError_t launch_decode_fused(const DecodeArgs& d, cudaStream_t st);
 
 // NVFP4 (W4A4): activation rows quantised to packed e2m1 codes q [rows, n/2],
 // e4m3 block-scale codes sb [rows, n/16] and a row scale g [rows]; the GEMVs
@@ -148,7 +125,8 @@ cudaError_t launch_gemv_down_nvfp4(const GemvArgs& a, const uint8_t* hq, const u
 cudaError_t launch_shared_gate(const uint16_t* x, int m, int H, const float* gate, float* g, cudaStream_t st);
 // combine: out[t] = sum_j w[t,j] * Y[slot(t,j)] (+ g[t] * Y[P+t] when has_shared; g = 1 when null)
 cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, const float* w, int m, int k, int H,
-                               int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st);
+                               int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st,
+                               int accumulate = 0);
 // the same sum with the layer tail (moe_forward_residual_rmsnorm): residual
 // += out (bf16), norm_out = RMSNorm(residual) * norm_w; one block per token
 struct TailArgs {
@@ -165,6 +143,7 @@ cudaError_t launch_combine_tail_bf16(const uint16_t* y, const int32_t* slot_of_p
                                      int H, int P, int has_shared, const float* shared_g, const TailArgs& tail,
                                      cudaStream_t st);
 cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, const float* w, int m, int k,
-                                int H, int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st);
+                                int H, int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st,
+                                int accumulate = 0);
 
 }  // namespace moe

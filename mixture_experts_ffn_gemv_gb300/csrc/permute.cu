@@ -13,6 +13,8 @@
 //                   its slot: pairs keep ascending order within an expert.
 // Plus the activation gathers for the grouped GEMM, the fp8 activation
 // quantiser (one e4m3 code + fp32 scale per 128 inputs) and the NVFP4 one.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -21,8 +23,18 @@
 
 namespace moe {
 
+// Expert ids are global; this layer holds experts [e_lo, e_lo + E) of
+// E_total (all of them unless it is one shard of an expert-parallel layer).
+// A pair whose id lies in [0, E_total) but outside the shard belongs to
+// another shard and is dropped without error; an id outside [0, E_total)
+// sets DEV_ERR_BAD_ID and is dropped too.
+__device__ __forceinline__ int local_expert(int id, int e_lo, int E, int E_total) {
+    return (id >= e_lo && id < e_lo + E && id < E_total) ? id - e_lo : -1;
+}
+
 __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__ ids, int P, int m, int E,
-                                                     int has_shared, int nchunk, PermuteOut o, WsHeader* hdr) {
+                                                     int e_lo, int E_total, int has_shared, int nchunk, PermuteOut o,
+                                                     WsHeader* hdr) {
     pdl_wait();
     pdl_trigger();
     __shared__ int hist[kMaxExperts + 2];
@@ -35,12 +47,13 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
     for (int e = tid; e < E; e += 256) hist[e] = 0;
     __syncthreads();
     for (int p = p0 + tid; p < p1; p += 256) {
-        const int e = ids[p];
-        if (e < 0 || e >= E) {
+        const int id = ids[p];
+        if (id < 0 || id >= E_total) {
             set_error(hdr, DEV_ERR_BAD_ID, p);
             continue;
         }
-        atomicAdd(&hist[e], 1);
+        const int e = local_expert(id, e_lo, E, E_total);
+        if (e >= 0) atomicAdd(&hist[e], 1);
     }
     __syncthreads();
     for (int e = tid; e < E; e += 256) o.chunk_base[(size_t)c * E + e] = hist[e];
@@ -102,7 +115,8 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
     }
 }
 
-__global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict__ ids, int P, int E, PermuteOut o) {
+__global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict__ ids, int P, int E, int e_lo,
+                                                       int E_total, PermuteOut o) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ int wbase[];  // [8][E]
@@ -118,8 +132,7 @@ __global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict
         const int p = pb + lane;
         int e = -1;
         if (p < p1) {
-            e = ids[p];
-            if (e < 0 || e >= E) e = -1;
+            e = local_expert(ids[p], e_lo, E, E_total);
         }
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
@@ -139,8 +152,7 @@ __global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict
         const int p = pb + lane;
         int e = -1;
         if (p < p1) {
-            e = ids[p];
-            if (e < 0 || e >= E) e = -1;
+            e = local_expert(ids[p], e_lo, E, E_total);
         }
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0) {
@@ -148,7 +160,7 @@ __global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict
             o.sorted_pair[slot] = p;
             o.slot_of_pair[p] = slot;
         } else if (p < p1) {
-            o.slot_of_pair[p] = -1;  // invalid id (flagged by permute_count): the pair is dropped
+            o.slot_of_pair[p] = -1;  // an invalid id or another shard's expert: the pair is dropped
         }
         __syncwarp();
         if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
@@ -156,19 +168,21 @@ __global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict
     }
 }
 
-cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int has_shared, const PermuteOut& o,
-                                 WsHeader* hdr, cudaStream_t st) {
+cudaError_t launch_permute_count(const int32_t* ids, int m, int k, int E, int e_lo, int E_total, int has_shared,
+                                 const PermuteOut& o, WsHeader* hdr, cudaStream_t st) {
     const int P = m * k;
-    const int nchunk = ceil_div(P, kPermChunk);
-    launch_pdl(permute_count, dim3(nchunk), dim3(256), 0, st, ids, P, m, E, has_shared, nchunk, o, hdr);
+    const int nchunk = std::max(1, ceil_div(P, kPermChunk));  // P = 0: one block builds the shared-only tables
+    launch_pdl(permute_count, dim3(nchunk), dim3(256), 0, st, ids, P, m, E, e_lo, E_total, has_shared, nchunk, o, hdr);
     return cudaGetLastError();
 }
 
-cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, const PermuteOut& o, cudaStream_t st) {
+cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, int e_lo, int E_total,
+                                   const PermuteOut& o, cudaStream_t st) {
     const int P = m * k;
+    if (P == 0) return cudaSuccess;
     const int nchunk = ceil_div(P, kPermChunk);
     const size_t smem = sizeof(int) * 8 * (size_t)E;
-    launch_pdl(permute_scatter, dim3(nchunk), dim3(256), smem, st, ids, P, E, o);
+    launch_pdl(permute_scatter, dim3(nchunk), dim3(256), smem, st, ids, P, E, e_lo, E_total, o);
     return cudaGetLastError();
 }
 

@@ -77,7 +77,7 @@ extern "C" int moe_permute_noalloc(const int32_t* topk_ids, int64_t m, int32_t t
     o.sorted_pair = sorted_pair;
     o.slot_of_pair = slot_of_pair;
     o.expert_offsets = expert_offsets;
-    if (launch_permute_count(topk_ids, (int)m, k, E, 0, o, hdr, st) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_permute_scatter(topk_ids, (int)m, k, E, o, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_permute_count(topk_ids, (int)m, k, E, 0, E, 0, o, hdr, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_permute_scatter(topk_ids, (int)m, k, E, 0, E, o, st) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -354,59 +354,6 @@ def test_route_and_permute_at_the_largest_expert_count(cuda, oracle_mod, m):
     assert np.abs(to_np(w).astype(np.float64).sum(1) - 1).max() < 1e-5
 
 
-# ------------------------------------------------------------------ fused decode (one cooperative launch)
-
-FUSED_CASES = [(I.TINY, 1), (I.TINY, 4), (SHARED_BF16, 2), (TOP1, 3), (ODD_E, 4), (MEDIUM_BF16, 1),
-               (I.QWEN3_30B_A3B, 2), (I.QWEN3_30B_A3B, 3)]
-
-
-@pytest.mark.parametrize("shape,m", FUSED_CASES)
-def test_fused_decode_matches_oracle_and_the_kernel_chain(cuda, oracle_mod, shape, m):
-    """bf16 layers at m <= 4 run as one cooperative launch (routing, gate/up,
-    down and combine between bounded grid barriers).  Its output must match
-    the oracle, and bit for bit the separate-kernel chain (moe_experts on the
-    GEMV arm) given the same routing, since both run the same GEMV bodies and
-    the same fixed-order combine."""
-    from mixture_experts_ffn_gemv_gb300 import binding
-    tensors, x = _small_case(shape, m, seed=113, device=cuda)
-    layer = binding.MoeLayer(shape, tensors)
-    out, ids, w = layer.moe_forward(x, tensors["router_w"], tensors["router_bias"], return_routing=True)
-    torch.cuda.synchronize()
-    assert layer.device_status() == 0
-    assert layer.last_launch_count() == 1  # the fused kernel alone
-    chain = layer.moe_experts(x, ids, w, arm="gemv")
-    torch.cuda.synchronize()
-    assert torch.equal(out, chain)
-    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
-    ref = oracle_mod.reference(shape, host, x.cpu())
-    swapped, bad = check_ids(to_np(ids), ref["ids"], ref["logits"])
-    assert not bad, bad[:5]
-    assert np.abs(to_np(w)[[r for r in range(m) if r not in swapped]] -
-                  ref["w"][[r for r in range(m) if r not in swapped]]).max(initial=0.0) < 2e-5
-    f_ids, f_w = forced_routing(oracle_mod, shape, ref["logits"], ref["ids"], ref["w"], to_np(ids), swapped)
-    want = oracle_mod.moe_forward(shape, host, x.cpu(), f_ids, f_w)
-    assert rel_l2(to_np(out), want) < TOL[False]
-
-
-def test_fused_decode_stalled_barrier_times_out(cuda):
-    """The fused decode kernel's grid barriers are bounded by the layer's wait
-    limit: with a limit far below the routing phase's duration the barrier
-    waits run out, the call reports DEV_ERR_TIMEOUT, and the next call with
-    the default limit is clean and equals the kernel chain."""
-    from mixture_experts_ffn_gemv_gb300 import binding
-    wl = I.WORKLOADS["qwen3_decode"]
-    tensors, layer = layer_for(wl, cuda)
-    x = I.make_x(wl.shape, 1, device=cuda)
-    layer.set_wait_limit(1)  # 1 ns: any wait at a barrier runs out
-    layer.moe_forward(x, tensors["router_w"])
-    code = layer.device_status()
-    layer.set_wait_limit(0)
-    out, ids, w = layer.moe_forward(x, tensors["router_w"], return_routing=True)
-    assert layer.device_status() == 0
-    assert torch.equal(out, layer.moe_experts(x, ids, w, arm="gemv"))
-    assert code in (0, 2)  # 2 unless every CTA happened to arrive before the last one released
-
-
 # ------------------------------------------------------------------ whole layer, full sizes
 
 FULL_CASES = [("tiny", 16)] + [("qwen3_decode", m) for m in (1, 2, 4, 16, 64)] + \
