@@ -174,6 +174,7 @@ class MoeLayer:
             gate = _p(tensors.get("shared_gate")) if getattr(shape, "shared_gate", False) else None
             shared = MoeExpertWeights(*[_p(tensors.get(n)) for n in ("ws1", "ws3", "ws2", "ss1", "ss3", "ss2")],
                                       gate, *[_p(tensors.get("s" + n)) for n in sbn])
+        self.expert_range = tuple(expert_range) if expert_range is not None else (0, shape.num_experts)
         handle = _vp()
         _check(self.lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(routed),
                                          ctypes.byref(shared) if shared is not None else None,
@@ -261,7 +262,8 @@ class MoeLayer:
         m = topk_ids.shape[0]
         dev = topk_ids.device
         P = m * self.shape.top_k
-        off = torch.empty(self.shape.num_experts + 1, dtype=torch.int32, device=dev)
+        n_local = self.expert_range[1] - self.expert_range[0]  # this handle's experts
+        off = torch.empty(n_local + 1, dtype=torch.int32, device=dev)
         sp = torch.empty(P, dtype=torch.int32, device=dev)
         sl = torch.empty(P, dtype=torch.int32, device=dev)
         ws = self.workspace(m)
