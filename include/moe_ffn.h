@@ -179,8 +179,8 @@ MOE_API int moe_route(const moe_layer* layer, const void* x, int64_t m, const fl
  *   slot_of_pair   int32 [m*k]: inverse of sorted_pair
  * Ids outside [0, E) set the device error word (MOE_ERR_DEVICE).  Such a pair
  * is dropped: its slot_of_pair entry is -1, expert_offsets[E] counts only the
- * valid pairs (so it is then below m*k), and sorted_pair is written only up
- * to that count.  On an expert-parallel shard E is the shard's expert count
+ * valid pairs (so it is then below m*k), and sorted_pair holds -1 from that
+ * count on.  On an expert-parallel shard E is the shard's expert count
  * (expert_offsets [E+1] over its experts, in order) and pairs of the other
  * shards' experts are dropped the same way without an error.               */
 MOE_API int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t m,
@@ -209,7 +209,8 @@ MOE_API int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t
  * first lookup on a device loads this library's device code there, so make
  * the first call before any stream capture begins.
  * Out-of-range ids are handled as in moe_permute (the pair is dropped,
- * slot_of_pair -1, expert_offsets[E] counts only the valid pairs), but with
+ * slot_of_pair -1, expert_offsets[E] counts only the valid pairs, sorted_pair
+ * -1 from there on), but with
  * no workspace there is no error word the caller can read: a caller that may
  * pass such ids checks expert_offsets[E] == m * top_k after the stream.     */
 MOE_API int moe_permute_noalloc(const int32_t* topk_ids, int64_t m, int32_t top_k, int32_t num_experts,

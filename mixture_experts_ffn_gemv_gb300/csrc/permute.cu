@@ -77,7 +77,7 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
     }
     if (tid == 0) hist[E] = has_shared ? m : 0;
     __syncthreads();
-    const int valid_pairs = block_exclusive_scan(off, E, wsum);  // P unless some ids were out of range
+    const int valid_pairs = block_exclusive_scan(off, E, wsum);  // P unless some pairs were dropped
     for (int e = tid; e < E; e += 256) {
         o.grp_off[e] = off[e];
         o.grp_cnt[e] = hist[e];
@@ -89,6 +89,8 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
         o.grp_cnt[E] = hist[E];
         if (o.expert_offsets) o.expert_offsets[E] = valid_pairs;
     }
+    // the sorted slots past the valid pairs hold no pair: mark them
+    for (int sl = valid_pairs + tid; sl < P; sl += 256) o.sorted_pair[sl] = -1;
     __syncthreads();
     // non-empty groups (routed experts, then the shared expert), ascending
     for (int g = tid; g <= E; g += 256) off[g] = hist[g] > 0 ? 1 : 0;
@@ -187,6 +189,15 @@ cudaError_t launch_permute_scatter(const int32_t* ids, int m, int k, int E, int 
 }
 
 // ---------------------------------------------------------------- gathers
+// Token of row s of the grouped-GEMM input, or -1 for a routed slot that
+// holds no pair (past the valid pairs when some were dropped: ids out of
+// range, or another shard's experts; the permute marks those slots -1).
+__device__ __forceinline__ int gather_token(const int32_t* sorted_pair, int s, int k, int P) {
+    if (s >= P) return s - P;  // the shared expert's rows
+    const int p = sorted_pair[s];
+    return (p >= 0 && p < P) ? p / k : -1;
+}
+
 // Row s of the grouped-GEMM input: token sorted_pair[s] / k for s < P (routed
 // pairs), token s - P for the shared expert's rows.  One warp per row.
 __global__ __launch_bounds__(256) void gather_bf16(const uint16_t* __restrict__ x,
@@ -196,7 +207,8 @@ __global__ __launch_bounds__(256) void gather_bf16(const uint16_t* __restrict__ 
     pdl_trigger();
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (s >= rows) return;
-    const int t = s < P ? sorted_pair[s] / k : s - P;
+    const int t = gather_token(sorted_pair, s, k, P);
+    if (t < 0) return;  // an unused slot: no tile reads a valid row from it
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
     for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
@@ -209,7 +221,8 @@ __global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq
     pdl_trigger();
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (s >= rows) return;
-    const int t = s < P ? sorted_pair[s] / k : s - P;
+    const int t = gather_token(sorted_pair, s, k, P);
+    if (t < 0) return;  // an unused slot: no tile reads a valid row from it
     const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
     for (int c = lane; c < H / 16; c += 32) dst[c] = __ldg(src + c);
@@ -396,7 +409,8 @@ __global__ __launch_bounds__(256) void gather_nvfp4(const uint8_t* __restrict__ 
     pdl_trigger();
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (s >= rows) return;
-    const int t = s < P ? sorted_pair[s] / k : s - P;
+    const int t = gather_token(sorted_pair, s, k, P);
+    if (t < 0) return;  // an unused slot: no tile reads a valid row from it
     const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * (H / 2));
     const uint16_t* ssrc = reinterpret_cast<const uint16_t*>(xsb + (size_t)t * (H / 16));
     uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * (H / 2));

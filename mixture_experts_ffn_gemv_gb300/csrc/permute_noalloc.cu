@@ -8,8 +8,8 @@
 // as a plain pointer.
 //
 // Out-of-range expert ids: the kernels drop such a pair (its slot_of_pair
-// entry is -1) and leave it out of expert_offsets[E], the number of valid
-// pairs.  They also set the scratch header's error word, but no entry point
+// entry is -1; sorted_pair is -1 past the valid pairs) and leave it out of
+// expert_offsets[E], the number of valid pairs.  They also set the scratch header's error word, but no entry point
 // reads that word back here, so the caller's check is expert_offsets[E] ==
 // m * top_k.
 #include <cuda_runtime.h>

@@ -462,16 +462,23 @@ def test_single_expert_top1_is_dense_mlp(cuda, oracle_mod):
     assert rel_l2(to_np(out), dense.cpu().numpy()) < TOL[False]
 
 
-def test_bad_expert_id_sets_device_flag(cuda):
-    from mixture_experts_ffn_gemv_gb300 import binding
+@pytest.mark.parametrize("arm", ["gemv", "gemm"])
+def test_bad_expert_id_sets_device_flag(cuda, oracle_mod, arm):
+    """Out-of-range ids set the device flag and their pairs are dropped on
+    both arms (the grouped-GEMM arm's gather skips the sorted slots they
+    leave empty); the other pairs still give the oracle's sum."""
     wl = I.WORKLOADS["tiny"]
     tensors, layer = layer_for(wl, cuda)
     x = I.make_x(wl.shape, 4, device=cuda)
     ids = torch.tensor([[0, 1], [2, 8], [3, 4], [5, -1]], dtype=torch.int32, device=cuda)
     w = torch.full((4, 2), 0.5, device=cuda)
-    layer.moe_experts(x, ids, w, arm="gemv")
+    out = layer.moe_experts(x, ids, w, arm=arm)
     assert layer.device_status() == 1  # DEV_ERR_BAD_ID
-    layer.moe_experts(x, ids.clamp(0, 7), w, arm="gemv")
+    host = {n: tensors[n].cpu() for n in ("w1", "w3", "w2")}
+    keep = np.array([[0.5, 0.5], [0.5, 0.0], [0.5, 0.5], [0.5, 0.0]], np.float32)
+    ref = oracle_mod.moe_forward(wl.shape, host, x.cpu(), to_np(ids.clamp(0, 7)).astype(np.int32), keep)
+    assert rel_l2(to_np(out), ref) < TOL[False]
+    layer.moe_experts(x, ids.clamp(0, 7), w, arm=arm)
     assert layer.device_status() == 0  # the next call starts clean
 
 

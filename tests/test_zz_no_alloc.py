@@ -77,7 +77,7 @@ def test_noalloc_permute_matches_workspace_permute():
     torch.cuda.synchronize(dev)
     assert int(off[E]) == m * k - 1 and torch.equal(off, ref_off)
     assert int(sl[7 * k + 2]) == -1 and torch.equal(sl, ref_sl)
-    assert torch.equal(sp[: m * k - 1], ref_sp[: m * k - 1])
+    assert torch.equal(sp, ref_sp) and int(sp[-1]) == -1
 
     # a call whose histograms would not fit in the fixed scratch is refused
     big = torch.zeros(1, dtype=torch.int32, device=dev)
