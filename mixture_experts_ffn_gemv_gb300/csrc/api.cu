@@ -268,16 +268,6 @@ PermuteOut permute_out(const Layout& lo, void* ws, int32_t* sorted_pair, int32_t
     return o;
 }
 
-size_t l2_bytes() {
-    static size_t n = [] {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
-            return (size_t)0;
-        return (size_t)v;
-    }();
-    return n;
-}
-
 // The GEMV kernels' view of a call: group tables in the workspace, weights.
 GemvArgs gemv_args(const moe_layer* L, const Layout& lo, void* ws) {
     const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
@@ -294,11 +284,6 @@ GemvArgs gemv_args(const moe_layer* L, const Layout& lo, void* ws) {
     a.H = L->cfg.hidden;
     a.I = L->cfg.inter;
     a.max_groups = std::min(E, lo.P) + lo.shared;
-    // prefetch W2 into L2 during gate/up when the active groups' W2 (at most
-    // max_groups of them) takes under a third of L2: decode with few experts
-    const size_t w2_bytes = L->fp8 ? (size_t)a.H * a.I
-                                   : (L->nvfp4 ? (size_t)a.H * a.I / 2 + (size_t)a.H * a.I / 16 : (size_t)a.H * a.I * 2);
-    a.prefetch_w2 = !L->fp8 && (size_t)a.max_groups * w2_bytes <= l2_bytes() / 3 ? 1 : 0;
     a.w1 = L->routed.w1; a.w3 = L->routed.w3; a.w2 = L->routed.w2;
     a.s1 = L->routed.s1; a.s3 = L->routed.s3; a.s2 = L->routed.s2;
     a.sw1 = L->shared.w1; a.sw3 = L->shared.w3; a.sw2 = L->shared.w2;

@@ -100,21 +100,6 @@ struct Group {
     int g, off, cnt;
 };
 
-// Ask L2 to fetch this work item's share of its group's down-projection
-// weight (W2 of the group is one contiguous [H, I] block of `bytes`; item
-// `slice` of n_slices takes an equal, 16-byte aligned share) while the gate/up
-// weights stream, so the down kernel that follows reads W2 from L2.  Only
-// when the host set prefetch_w2 (the active groups' W2 fits L2 with room).
-__device__ __forceinline__ void prefetch_w2_share(const void* w2, size_t bytes, int slice, int n_slices) {
-    const size_t share = (bytes / n_slices) & ~(size_t)15;
-    const char* base = static_cast<const char*>(w2) + (size_t)slice * share;
-    const int lane = threadIdx.x & 31;
-    for (size_t off = (size_t)lane * 4096; off < share; off += 32 * 4096) {
-        const uint32_t n = (uint32_t)(share - off < 4096 ? share - off : 4096);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n) : "memory");
-    }
-}
-
 __device__ __forceinline__ bool load_group(const GemvArgs& a, int ga, Group& gr) {
     if (ga >= a.hdr->n_active) return false;
     gr.g = a.act_group[ga];
@@ -147,9 +132,6 @@ __device__ __forceinline__ void gateup_bf16_item(const GemvArgs& a, const uint16
     if (!load_group(a, bid / n_slices, gr)) return;
     const int H = a.H, I = a.I;
     const int row0 = (bid % n_slices) * (16 * RT) + rt * 16;
-    if (a.prefetch_w2 && warp == 7)
-        prefetch_w2_share(gr.g < a.E ? (const uint16_t*)a.w2 + (size_t)gr.g * H * I : (const uint16_t*)a.sw2,
-                          (size_t)H * I * 2, bid % n_slices, n_slices);
     const uint16_t* W1 = gr.g < a.E ? (const uint16_t*)a.w1 + (size_t)gr.g * I * H : (const uint16_t*)a.sw1;
     const uint16_t* W3 = gr.g < a.E ? (const uint16_t*)a.w3 + (size_t)gr.g * I * H : (const uint16_t*)a.sw3;
     const uint4* w1g = reinterpret_cast<const uint4*>(W1 + (size_t)(row0 + g8) * H);
@@ -510,12 +492,6 @@ __global__ __launch_bounds__(256, (NT == 1 ? 3 : 2)) void gemv_gateup_nvfp4(
     const int H = a.H, I = a.I, hq = H / 2, hs = H / 16;
     const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
     const bool routed = gr.g < a.E;
-    if (a.prefetch_w2 && warp == 7) {  // packed codes [H, I/2], then block scales [H, I/16]
-        prefetch_w2_share(routed ? (const uint8_t*)a.w2 + (size_t)gr.g * H * (I / 2) : (const uint8_t*)a.sw2,
-                          (size_t)H * (I / 2), blockIdx.x % n_slices, n_slices);
-        prefetch_w2_share(routed ? a.sb2 + (size_t)gr.g * H * (I / 16) : a.ssb2, (size_t)H * (I / 16),
-                          blockIdx.x % n_slices, n_slices);
-    }
     const uint8_t* W1 = routed ? (const uint8_t*)a.w1 + (size_t)gr.g * I * hq : (const uint8_t*)a.sw1;
     const uint8_t* W3 = routed ? (const uint8_t*)a.w3 + (size_t)gr.g * I * hq : (const uint8_t*)a.sw3;
     const uint8_t* B1 = routed ? a.sb1 + (size_t)gr.g * I * hs : a.ssb1;

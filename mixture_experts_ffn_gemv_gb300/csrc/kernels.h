@@ -88,7 +88,6 @@ struct GemvArgs {
     const int* act_group;
     const int32_t* sorted_pair;
     int P, k, E, H, I, max_groups;
-    int prefetch_w2;  // gate/up kernels prefetch the groups' W2 into L2 for the down kernel
     // routed weights (stacked) and the shared expert's (g == E)
     const void *w1, *w3, *w2, *sw1, *sw3, *sw2;
     // fp8: 128x128 block scales; nvfp4: one fp32 scale per expert matrix
