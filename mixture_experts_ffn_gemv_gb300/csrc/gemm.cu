@@ -22,6 +22,7 @@
 // for its TMA copies and MMAs in flight, frees TMEM and returns.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -280,6 +281,260 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// The same bf16 GEMMs on pairs of CTAs (a cluster of two, tcgen05
+// cta_group::2): a work item is 256 sorted rows of one group (the two CTAs'
+// 128-row m-tiles 2j and 2j+1) times one n-tile.  Each CTA loads its own 128
+// token rows and half of the 256 weight rows (gate/up: the leader W1, the
+// peer W3; down: one half each), the leader issues M = 256, N = 256 MMAs and
+// each CTA's TMEM receives its own rows of the result, so the epilogue is the
+// one-CTA kernel's.  Per SM and K step that is 32 KB written to and read from
+// shared memory for 128 x 256 x 64 MACs, against 48 KB for the one-CTA tile.
+// Barriers: the leader's full barrier counts both CTAs' TMA bytes (the peer's
+// copies signal it); the MMA commits are multicast to both CTAs' empty and
+// accumulator-full barriers; both CTAs' epilogue warps arrive on the
+// leader's accumulator-empty barrier.  Every wait is bounded as above.
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = BM * BK * 2;   // this CTA's 128 token rows
+constexpr int P_B_BYTES = 128 * BK * 2;  // this CTA's half of the 256 weight rows
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_TABLE_INTS = 3 * (kMaxExperts + 2);
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 256 + P_TABLE_INTS * 4;
+static_assert(P_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_bf16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                           const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
+                           const __grid_constant__ CUtensorMap tmS1, const GemmParams p) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + P_STAGES);
+    const uint32_t tfull0 = smem_u32(bars + 2 * P_STAGES), tempty0 = smem_u32(bars + 2 * P_STAGES + 2);
+    const uint32_t drain = smem_u32(bars + 2 * P_STAGES + 4);
+    const uint32_t never = smem_u32(bars + 2 * P_STAGES + 5);  // stall test: no thread ever arrives here
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 6);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_tile = reinterpret_cast<int*>(smem + P_STAGES * P_STAGE_BYTES + 256);
+    int* s_group = s_tile + (kMaxExperts + 2);
+    int* s_pair = s_group + (kMaxExperts + 2);  // pair counts, then their exclusive prefix
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int n_active = p.hdr->n_active;
+    for (int i = threadIdx.x; i <= n_active; i += THREADS) s_tile[i] = p.act_tile[i];
+    for (int i = threadIdx.x; i < n_active; i += THREADS) s_group[i] = p.act_group[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, 2 * EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        mbar_init(never, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_active; i += THREADS) s_pair[i] = (s_tile[i + 1] - s_tile[i] + 1) >> 1;
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of the pair counts (entry n_active = total)
+        int carry = 0;
+        for (int base = 0; base <= n_active; base += 32) {
+            const int i = base + lane;
+            const int v = i < n_active ? s_pair[i] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            if (i <= n_active) s_pair[i] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before either signals the other
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = s_pair[n_active] * p.n_tiles;
+    const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const uint32_t lead_full0 = mapa(full0, 0), lead_tempty0 = mapa(tempty0, 0);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB0);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = cl; t < total && ok; t += ncl) {
+                if (*abort_flag) break;
+                const int pt = t / p.n_tiles, nt = t % p.n_tiles;
+                const int a = find_group(s_pair, n_active, pt);
+                const int g = s_group[a];
+                const int row0 = p.grp_off[g] + (2 * (pt - s_pair[a]) + (int)rank) * BM;
+                const bool routed = g < p.E;
+                const CUtensorMap* b0 = routed ? &tmB0 : &tmS0;
+                const CUtensorMap* b1 = routed ? &tmB1 : &tmS1;
+                const int gz = routed ? g : 0;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % P_STAGES, ph = (it / P_STAGES) & 1u;
+                    if (!mbar_wait_cluster(empty0 + 8 * s, ph ^ 1u, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + s * P_STAGE_BYTES, sb = sa + P_A_BYTES;
+                    if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * P_STAGE_BYTES);
+                    tma_load_2d_pair(sa, &tmA, kb * BK, row0, lead_full0 + 8 * s);
+                    if (GATEUP)
+                        tma_load_3d_pair(sb, rank ? b1 : b0, kb * BK, nt * 128, gz, lead_full0 + 8 * s);
+                    else
+                        tma_load_3d_pair(sb, b0, kb * BK, nt * 256 + (int)rank * 128, gz, lead_full0 + 8 * s);
+                }
+            }
+            if (!ok) {
+                set_error(p.hdr, DEV_ERR_TIMEOUT, 1);
+                *abort_flag = 1;
+            }
+            if (leader) {
+                // every issued copy of both CTAs has landed before either can exit
+                for (uint32_t j = it > (uint32_t)P_STAGES ? it - P_STAGES : 0; j < it; ++j)
+                    mbar_wait_cluster(full0 + 8 * (j % P_STAGES), (j / P_STAGES) & 1u, DRAIN_NS);
+            } else if (!ok || *abort_flag) {
+                // the peer's copies complete on the leader's barriers: after an
+                // abort, give any still in flight time to land
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 50000ull) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_bf16(2 * BM, BN);
+            uint32_t it = 0, tc = 0;
+            bool ok = !p.stall_test || mbar_wait(never, 0, p.wait_ns);
+            for (int t = cl; t < total && ok; t += ncl, ++tc) {
+                if (*abort_flag) break;
+                const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+                if (!mbar_wait_cluster(tempty0 + 8 * acc, aph ^ 1u, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.kblocks; ++kb, ++it) {
+                    const uint32_t s = it % P_STAGES, ph = (it / P_STAGES) & 1u;
+                    if (!mbar_wait_cluster(full0 + 8 * s, ph, p.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(sbase + s * P_STAGE_BYTES);
+                    const uint64_t bd = desc_sw128(sbase + s * P_STAGE_BYTES + P_A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per MMA
+                        mma_bf16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    mma_commit_pair(empty0 + 8 * s);
+                }
+                if (!ok) break;
+                mma_commit_pair(tfull0 + 8 * acc);
+            }
+            if (!ok) {
+                set_error(p.hdr, DEV_ERR_TIMEOUT, 2);
+                *abort_flag = 1;
+            }
+            mma_commit_pair(drain);
+            mbar_wait_cluster(drain, 0, DRAIN_NS);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;            // the TMEM lane quarter this warp may read
+        const int half = (warp - 2) >> 2;  // which half of the tile's output columns
+        const int r = q * 32 + lane;
+        uint32_t tc = 0;
+        for (int t = cl; t < total; t += ncl, ++tc) {
+            if (*abort_flag) break;
+            const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
+            if (!mbar_wait_cluster(tfull0 + 8 * acc, aph, p.wait_ns)) {
+                set_error(p.hdr, DEV_ERR_TIMEOUT, 3);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int pt = t / p.n_tiles, nt = t % p.n_tiles;
+            const int a = find_group(s_pair, n_active, pt);
+            const int g = s_group[a];
+            const int j = 2 * (pt - s_pair[a]) + (int)rank;  // this CTA's m-tile of the group
+            const int valid = p.grp_cnt[g] - j * BM;
+            const bool ok = r < valid;
+            uint16_t* orow = p.out + (size_t)(p.grp_off[g] + j * BM + r) * p.ldo;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            if (GATEUP) {
+#pragma unroll 1
+                for (int c = 2 * half; c < 2 * half + 2; ++c) {
+                    uint32_t gv[32], uv[32];
+                    tmem_ld32(taddr + c * 32, gv);
+                    tmem_ld32(taddr + 128 + c * 32, uv);
+                    tmem_wait_ld();
+                    if (ok) {
+                        uint16_t* dst = orow + nt * 128 + c * 32;
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            uint32_t o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                o[i] = pack_bf16x2(swiglu(__uint_as_float(gv[16 * v + 2 * i]), __uint_as_float(uv[16 * v + 2 * i])),
+                                                   swiglu(__uint_as_float(gv[16 * v + 2 * i + 1]),
+                                                          __uint_as_float(uv[16 * v + 2 * i + 1])));
+                            st_global_v8(dst + 16 * v, o);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+                    uint32_t dv[32];
+                    tmem_ld32(taddr + c * 32, dv);
+                    tmem_wait_ld();
+                    if (ok) {
+                        uint16_t* dst = orow + nt * BN + c * 32;
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            uint32_t o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                o[i] = pack_bf16x2(__uint_as_float(dv[16 * v + 2 * i]), __uint_as_float(dv[16 * v + 2 * i + 1]));
+                            st_global_v8(dst + 16 * v, o);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lead_tempty0 + 8 * acc);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still signal it or read its TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 int num_sms() {
@@ -346,7 +601,8 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
     const uint64_t s13[3] = {H, I, 1}, s2[3] = {I, H, 1};
     if (!tmap_encode(&out->w1, routed->w1, 3, d13, es, bc, 128) ||
         !tmap_encode(&out->w3, routed->w3, 3, d13, es, bc, 128) ||
-        !tmap_encode(&out->w2, routed->w2, 3, d2, es, bc, BN))
+        !tmap_encode(&out->w2, routed->w2, 3, d2, es, bc, BN) ||
+        !tmap_encode(&out->w2h, routed->w2, 3, d2, es, bc, 128))
         return MOE_ERR_CUDA;
     out->s1 = routed->s1;
     out->s3 = routed->s3;
@@ -354,7 +610,8 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
     if (shared) {
         if (!tmap_encode(&out->sw1, shared->w1, 3, s13, es, bc, 128) ||
             !tmap_encode(&out->sw3, shared->w3, 3, s13, es, bc, 128) ||
-            !tmap_encode(&out->sw2, shared->w2, 3, s2, es, bc, BN))
+            !tmap_encode(&out->sw2, shared->w2, 3, s2, es, bc, BN) ||
+            !tmap_encode(&out->sw2h, shared->w2, 3, s2, es, bc, 128))
             return MOE_ERR_CUDA;
         out->ss1 = shared->s1;
         out->ss3 = shared->s3;
@@ -363,6 +620,7 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
         out->sw1 = out->w1;
         out->sw3 = out->w3;
         out->sw2 = out->w2;
+        out->sw2h = out->w2h;
         out->ss1 = out->s1;
         out->ss3 = out->s3;
         out->ss2 = out->s2;
@@ -383,9 +641,49 @@ int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out) {
     return MOE_OK;
 }
 
+// The bf16 GEMMs run on CTA pairs unless MOE_GEMM_PAIR=0 (the one-CTA kernels).
+bool use_pairs() {
+    static const bool on = [] {
+        const char* v = getenv("MOE_GEMM_PAIR");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+
+template <bool GATEUP>
+cudaError_t launch_pair(const GemmLaunch& L, cudaStream_t st) {
+    static cudaError_t attr = cudaFuncSetAttribute(grouped_gemm_bf16_pair<GATEUP>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+    if (attr != cudaSuccess) return attr;
+    const GemmCall& g = L.call;
+    GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E,
+                 GATEUP ? g.I / 128 : g.H / BN, (GATEUP ? g.H : g.I) / BK, GATEUP ? g.I : g.H, 128,
+                 GATEUP ? static_cast<uint16_t*>(g.h) : g.y, g.wait_ns, g.stall_test};
+    const int pairs = std::max(1, std::min(num_sms() / 2, g.max_tiles * p.n_tiles));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 2;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    const GemmWeights& w = *L.w;
+    if (GATEUP)
+        return cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<true>, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<false>, L.a_h, w.w2h, w.w2h, w.sw2h, w.sw2h, p);
+}
+
 cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
     if (L.w->nvfp4) return launch_gemm_nvfp4_gateup(L, st);
     if (L.w->fp8) return launch_gemm_fp8_gateup(L, st);
+    if (use_pairs()) return launch_pair<true>(L, st);
     cudaError_t e = set_smem_attr<true>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;
@@ -399,6 +697,7 @@ cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
 cudaError_t launch_gemm_down(const GemmLaunch& L, cudaStream_t st) {
     if (L.w->nvfp4) return launch_gemm_nvfp4_down(L, st);
     if (L.w->fp8) return launch_gemm_fp8_down(L, st);
+    if (use_pairs()) return launch_pair<false>(L, st);
     cudaError_t e = set_smem_attr<false>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;
