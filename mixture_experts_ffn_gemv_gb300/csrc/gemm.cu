@@ -282,13 +282,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------- CTA pairs
-// The same bf16 GEMMs on pairs of CTAs (a cluster of two, tcgen05
+// The bf16 gate/up GEMM on pairs of CTAs (a cluster of two, tcgen05
 // cta_group::2): a work item is 256 sorted rows of one group (the two CTAs'
 // 128-row m-tiles 2j and 2j+1) times one n-tile.  Each CTA loads its own 128
-// token rows and half of the 256 weight rows (gate/up: the leader W1, the
-// peer W3; down: one half each), the leader issues M = 256, N = 256 MMAs and
-// each CTA's TMEM receives its own rows of the result, so the epilogue is the
-// one-CTA kernel's.  Per SM and K step that is 32 KB written to and read from
+// token rows and half of the 256 weight rows (the leader the 128 rows of W1,
+// the peer the same rows of W3), the leader issues M = 256, N = 256 MMAs and
+// each CTA's TMEM receives its own rows of the result -- G and U side by side,
+// as in the one-CTA kernel, whose epilogue this is.  Per SM and K step that is 32 KB written to and read from
 // shared memory for 128 x 256 x 64 MACs, against 48 KB for the one-CTA tile.
 // Barriers: the leader's full barrier counts both CTAs' TMA bytes (the peer's
 // copies signal it); the MMA commits are multicast to both CTAs' empty and
@@ -302,7 +302,6 @@ constexpr int P_TABLE_INTS = 3 * (kMaxExperts + 2);
 constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 256 + P_TABLE_INTS * 4;
 static_assert(P_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
-template <bool GATEUP>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_bf16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
@@ -399,10 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sa = sbase + s * P_STAGE_BYTES, sb = sa + P_A_BYTES;
                     if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * P_STAGE_BYTES);
                     tma_load_2d_pair(sa, &tmA, kb * BK, row0, lead_full0 + 8 * s);
-                    if (GATEUP)
-                        tma_load_3d_pair(sb, rank ? b1 : b0, kb * BK, nt * 128, gz, lead_full0 + 8 * s);
-                    else
-                        tma_load_3d_pair(sb, b0, kb * BK, nt * 256 + (int)rank * 128, gz, lead_full0 + 8 * s);
+                    tma_load_3d_pair(sb, rank ? b1 : b0, kb * BK, nt * 128, gz, lead_full0 + 8 * s);
                 }
             }
             if (!ok) {
@@ -481,7 +477,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool ok = r < valid;
             uint16_t* orow = p.out + (size_t)(p.grp_off[g] + j * BM + r) * p.ldo;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            if (GATEUP) {
+            {
 #pragma unroll 1
                 for (int c = 2 * half; c < 2 * half + 2; ++c) {
                     uint32_t gv[32], uv[32];
@@ -498,24 +494,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 o[i] = pack_bf16x2(swiglu(__uint_as_float(gv[16 * v + 2 * i]), __uint_as_float(uv[16 * v + 2 * i])),
                                                    swiglu(__uint_as_float(gv[16 * v + 2 * i + 1]),
                                                           __uint_as_float(uv[16 * v + 2 * i + 1])));
-                            st_global_v8(dst + 16 * v, o);
-                        }
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
-                    uint32_t dv[32];
-                    tmem_ld32(taddr + c * 32, dv);
-                    tmem_wait_ld();
-                    if (ok) {
-                        uint16_t* dst = orow + nt * BN + c * 32;
-#pragma unroll
-                        for (int v = 0; v < 2; ++v) {
-                            uint32_t o[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                o[i] = pack_bf16x2(__uint_as_float(dv[16 * v + 2 * i]), __uint_as_float(dv[16 * v + 2 * i + 1]));
                             st_global_v8(dst + 16 * v, o);
                         }
                     }
@@ -601,8 +579,7 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
     const uint64_t s13[3] = {H, I, 1}, s2[3] = {I, H, 1};
     if (!tmap_encode(&out->w1, routed->w1, 3, d13, es, bc, 128) ||
         !tmap_encode(&out->w3, routed->w3, 3, d13, es, bc, 128) ||
-        !tmap_encode(&out->w2, routed->w2, 3, d2, es, bc, BN) ||
-        !tmap_encode(&out->w2h, routed->w2, 3, d2, es, bc, 128))
+        !tmap_encode(&out->w2, routed->w2, 3, d2, es, bc, BN))
         return MOE_ERR_CUDA;
     out->s1 = routed->s1;
     out->s3 = routed->s3;
@@ -610,8 +587,7 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
     if (shared) {
         if (!tmap_encode(&out->sw1, shared->w1, 3, s13, es, bc, 128) ||
             !tmap_encode(&out->sw3, shared->w3, 3, s13, es, bc, 128) ||
-            !tmap_encode(&out->sw2, shared->w2, 3, s2, es, bc, BN) ||
-            !tmap_encode(&out->sw2h, shared->w2, 3, s2, es, bc, 128))
+            !tmap_encode(&out->sw2, shared->w2, 3, s2, es, bc, BN))
             return MOE_ERR_CUDA;
         out->ss1 = shared->s1;
         out->ss3 = shared->s3;
@@ -620,7 +596,6 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
         out->sw1 = out->w1;
         out->sw3 = out->w3;
         out->sw2 = out->w2;
-        out->sw2h = out->w2h;
         out->ss1 = out->s1;
         out->ss3 = out->s3;
         out->ss2 = out->s2;
@@ -641,24 +616,28 @@ int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out) {
     return MOE_OK;
 }
 
-// The bf16 GEMMs run on CTA pairs unless MOE_GEMM_PAIR=0 (the one-CTA kernels).
-bool use_pairs() {
-    static const bool on = [] {
+// The bf16 gate/up GEMM runs on CTA pairs once the routed rows average 256
+// per active group (a pair's tile); below that the pairs' padding rows cost
+// more than the shared-memory traffic they save.  Measured on the Qwen3 shape:
+// gate/up 202 -> 196 us at m = 4096, 541 -> 520 us at m = 16384; slower at
+// m = 512, and the down GEMM (K = 768) was slower on pairs at every size.
+// MOE_GEMM_PAIR=0 keeps the one-CTA kernel everywhere.
+bool use_pairs(const GemmCall& g) {
+    static const bool allowed = [] {
         const char* v = getenv("MOE_GEMM_PAIR");
         return !(v && v[0] == '0');
     }();
-    return on;
+    const int groups = std::max(1, std::min(g.E, g.rows));
+    return allowed && g.rows / groups >= 2 * BM;
 }
 
-template <bool GATEUP>
-cudaError_t launch_pair(const GemmLaunch& L, cudaStream_t st) {
-    static cudaError_t attr = cudaFuncSetAttribute(grouped_gemm_bf16_pair<GATEUP>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+cudaError_t launch_pair_gateup(const GemmLaunch& L, cudaStream_t st) {
+    static cudaError_t attr = cudaFuncSetAttribute(grouped_gemm_bf16_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   P_SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
     const GemmCall& g = L.call;
-    GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E,
-                 GATEUP ? g.I / 128 : g.H / BN, (GATEUP ? g.H : g.I) / BK, GATEUP ? g.I : g.H, 128,
-                 GATEUP ? static_cast<uint16_t*>(g.h) : g.y, g.wait_ns, g.stall_test};
+    GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.I / 128, g.H / BK, g.I, 128,
+                 static_cast<uint16_t*>(g.h), g.wait_ns, g.stall_test};
     const int pairs = std::max(1, std::min(num_sms() / 2, g.max_tiles * p.n_tiles));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
@@ -675,15 +654,13 @@ cudaError_t launch_pair(const GemmLaunch& L, cudaStream_t st) {
     cfg.attrs = at;
     cfg.numAttrs = 2;
     const GemmWeights& w = *L.w;
-    if (GATEUP)
-        return cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<true>, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<false>, L.a_h, w.w2h, w.w2h, w.sw2h, w.sw2h, p);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
 }
 
 cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
     if (L.w->nvfp4) return launch_gemm_nvfp4_gateup(L, st);
     if (L.w->fp8) return launch_gemm_fp8_gateup(L, st);
-    if (use_pairs()) return launch_pair<true>(L, st);
+    if (use_pairs(L.call)) return launch_pair_gateup(L, st);
     cudaError_t e = set_smem_attr<true>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;
@@ -697,7 +674,6 @@ cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
 cudaError_t launch_gemm_down(const GemmLaunch& L, cudaStream_t st) {
     if (L.w->nvfp4) return launch_gemm_nvfp4_down(L, st);
     if (L.w->fp8) return launch_gemm_fp8_down(L, st);
-    if (use_pairs()) return launch_pair<false>(L, st);
     cudaError_t e = set_smem_attr<false>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;

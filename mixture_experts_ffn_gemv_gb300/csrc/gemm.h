@@ -18,7 +18,6 @@ struct GemmWeights {
     bool nvfp4;  // packed e2m1 codes: unswizzled maps of 32-byte boxes (64 codes of K)
     CUtensorMap w1, w3, w2;
     CUtensorMap sw1, sw3, sw2;
-    CUtensorMap w2h, sw2h;  // bf16 W2 in 128-row boxes: one CTA's half of a pair's n-tile
     const float *s1, *s3, *s2, *ss1, *ss3, *ss2;  // fp8 block scales / nvfp4 matrix scales (routed, shared)
     const uint8_t *sb1, *sb3, *sb2, *ssb1, *ssb3, *ssb2;  // nvfp4 e4m3 block scales
 };

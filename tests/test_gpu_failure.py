@@ -2,10 +2,10 @@
 
 Every mbarrier wait in the grouped-GEMM kernels is bounded.  Here a wait is
 made to run out on purpose -- the tensor-core issuer first waits on a barrier
-that no thread ever completes (moe_layer_stall_test) under a short wait limit
--- and the call must come back with the device error word set to
-DEV_ERR_TIMEOUT, the context usable, and the next call clean and equal to the
-oracle.  (forward_prefill.rs reports failures through Rust's Result; the
+that no thread ever completes (moe_layer_stall_test) under a short wait limit,
+on the one-CTA kernel and on the CTA-pair gate/up kernel -- and the call must
+come back with the device error word set to DEV_ERR_TIMEOUT, the context
+usable, and the next call clean and equal to the oracle.  (forward_prefill.rs reports failures through Rust's Result; the
 bounded wait is this library's device-side counterpart.)
 """
 import numpy as np
@@ -30,13 +30,18 @@ def cuda():
     return torch.device("cuda", 0)
 
 
-def test_stalled_gemm_times_out_and_the_next_call_is_clean(cuda, oracle_mod):
+# 400 routed rows over 8 experts: the one-CTA grouped GEMM; 600 rows over 2
+# experts: gate/up on CTA pairs
+PAIR_SHAPE = I.LayerShape(hidden=1024, num_experts=2, top_k=1, inter=256)
+
+
+@pytest.mark.parametrize("shape,m", [(SHAPE, 200), (PAIR_SHAPE, 600)])
+def test_stalled_gemm_times_out_and_the_next_call_is_clean(cuda, oracle_mod, shape, m):
     from mixture_experts_ffn_gemv_gb300 import binding
-    m = 200  # 400 routed rows over 8 experts: the grouped-GEMM arm
-    wl = I.Workload("stall", SHAPE, (m,))
+    wl = I.Workload("stall", shape, (m,))
     tensors = I.make_layer(wl, seed=61, device=cuda)
-    x = I.make_x(SHAPE, m, seed=61, device=cuda)
-    layer = binding.MoeLayer(SHAPE, tensors)
+    x = I.make_x(shape, m, seed=61, device=cuda)
+    layer = binding.MoeLayer(shape, tensors)
     assert layer.select_arm(m) == binding.MOE_ARM_GEMM
 
     layer.set_wait_limit(200_000)  # 200 us
@@ -51,11 +56,11 @@ def test_stalled_gemm_times_out_and_the_next_call_is_clean(cuda, oracle_mod):
     torch.cuda.synchronize()
     assert layer.device_status() == 0
     host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
-    ref = oracle_mod.reference(SHAPE, host, x.cpu())
+    ref = oracle_mod.reference(shape, host, x.cpu())
     swapped, bad = check_ids(to_np(ids), ref["ids"], ref["logits"])
     assert not bad, bad[:5]
-    f_ids, f_w = forced_routing(oracle_mod, SHAPE, ref["logits"], ref["ids"], ref["w"], to_np(ids), swapped)
-    want = oracle_mod.moe_forward(SHAPE, host, x.cpu(), f_ids, f_w)
+    f_ids, f_w = forced_routing(oracle_mod, shape, ref["logits"], ref["ids"], ref["w"], to_np(ids), swapped)
+    want = oracle_mod.moe_forward(shape, host, x.cpu(), f_ids, f_w)
     assert rel_l2(to_np(out), want) < TOL[False]
 
 

@@ -305,6 +305,32 @@ def test_experts_given_oracle_routing(cuda, oracle_mod, arm, shape, m):
     assert err < tol(shape), err
 
 
+# few experts, many rows each: the bf16 gate/up GEMM runs on CTA pairs
+# (256-row tiles over two SMs) once the rows average 256 per group
+PAIR_BF16 = I.LayerShape(hidden=512, num_experts=4, top_k=2, inter=256)
+PAIR_SHARED = I.LayerShape(hidden=512, num_experts=4, top_k=1, inter=256, shared_inter=256)
+
+
+@pytest.mark.parametrize("shape,m", [(PAIR_BF16, 600), (PAIR_BF16, 1000), (PAIR_SHARED, 900)])
+def test_gateup_on_cta_pairs(cuda, oracle_mod, shape, m):
+    """Groups of 300-500 rows: two or three 128-row m-tiles per pair tile, so
+    some pairs have a peer CTA with no rows; every row against the oracle."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    tensors, x = _small_case(shape, m, seed=141, device=cuda)
+    host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
+    ref = oracle_mod.reference(shape, host, x.cpu())
+    layer = binding.MoeLayer(shape, tensors)
+    out, ids, w = layer.moe_forward(x, tensors["router_w"], arm="gemm", return_routing=True)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    swapped, bad = check_ids(to_np(ids), ref["ids"], ref["logits"])
+    assert not bad, bad[:5]
+    assert len(swapped) <= max_swapped(m)
+    f_ids, f_w = forced_routing(oracle_mod, shape, ref["logits"], ref["ids"], ref["w"], to_np(ids), swapped)
+    want = oracle_mod.moe_forward(shape, host, x.cpu(), f_ids, f_w)
+    assert rel_l2(to_np(out), want) < TOL[False]
+
+
 SHARED_BF16 = I.LayerShape(hidden=512, num_experts=16, top_k=4, inter=256, shared_inter=256)
 TOP1 = I.LayerShape(hidden=256, num_experts=12, top_k=1, inter=128)
 
