@@ -361,25 +361,52 @@ def kernel_profile(reps, n, wl, m):
 
 
 def e2e_steps(reps, n, device, dist, m, shape):
-    """The same forward with the host<->device copies of x and out inside the
-    timed region (pinned host buffers)."""
-    stream = torch.cuda.current_stream(device)
+    """The same forward through the C-ABI with every step's input copied in
+    from pinned host memory and its output copied back, all inside the timed
+    region.  The copies run on a second stream and are pipelined with the
+    forwards (two device slots): step i+1's input uploads while step i
+    computes, and step i's output downloads while step i+1 computes, as a
+    serving loop would overlap them."""
+    compute = torch.cuda.current_stream(device)
+    copy = torch.cuda.Stream(device)
+    R = len(reps)
     xh = [r["x"].cpu().pin_memory() for r in reps]
-    oh = [torch.empty(m, shape.hidden, dtype=torch.bfloat16).pin_memory() for _ in reps]
-    xd = [torch.empty_like(r["x"]) for r in reps]
+    oh = [torch.empty(m, shape.hidden, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+    xd = [torch.empty_like(reps[0]["x"]) for _ in range(2)]
+    od = [torch.empty(m, shape.hidden, dtype=torch.bfloat16, device=device) for _ in range(2)]
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    h2d = [ev() for _ in range(n)]
+    fwd = [ev() for _ in range(n)]
+    d2h = [ev() for _ in range(n)]
     barrier(dist, device)
     torch.cuda.synchronize(device)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a.record(compute)
+    copy.wait_stream(compute)
+    with torch.cuda.stream(copy):
+        xd[0].copy_(xh[0], non_blocking=True)
+        h2d[0].record(copy)
     for i in range(n):
-        j = i % len(reps)
-        r = reps[j]
+        s = i % 2
+        r = reps[i % R]
         t = r["tensors"]
-        xd[j].copy_(xh[j], non_blocking=True)
-        out = r["layer"].moe_forward(xd[j], t["router_w"], t["router_bias"], out=r["out"])
-        oh[j].copy_(out, non_blocking=True)
-    b.record(stream)
+        compute.wait_event(h2d[i])
+        if i >= 2:
+            compute.wait_event(d2h[i - 2])  # this slot's previous output has been read back
+        r["layer"].moe_forward(xd[s], t["router_w"], t["router_bias"], out=od[s], stream=compute)
+        fwd[i].record(compute)
+        with torch.cuda.stream(copy):
+            if i + 1 < n:
+                if i >= 1:
+                    copy.wait_event(fwd[i - 1])  # the other slot's input is no longer read
+                xd[1 - s].copy_(xh[(i + 1) % R], non_blocking=True)
+                h2d[i + 1].record(copy)
+            copy.wait_event(fwd[i])
+            oh[i % R].copy_(od[s], non_blocking=True)
+            d2h[i].record(copy)
+    compute.wait_stream(copy)
+    b.record(compute)
     torch.cuda.synchronize(device)
     barrier(dist, device)
     bytes_in = m * shape.hidden * 2
