@@ -305,6 +305,7 @@ def build_replicas(wl, m, device, seed_base, max_bytes=48e9, replicas=0):
     for r in range(R):
         tensors = I.make_layer(wl, seed=seed_base + r, device=device)
         layer = binding.MoeLayer(shape, tensors)
+        layer.prepare_router(tensors["router_w"])  # load-time split of the router weight
         if ws is None:
             ws = layer.workspace(m)
         layer._ws = ws

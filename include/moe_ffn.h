@@ -285,6 +285,22 @@ MOE_API int moe_act_quant_nvfp4(const void* x, int64_t rows, int64_t n, uint8_t*
  * set, or MOE_ERR_CUDA.                                                     */
 MOE_API int moe_device_status(const void* workspace, void* stream, int32_t* device_code);
 
+/* Router weight preparation (optional).  For m > 64 tokens (and E <= 256)
+ * the router runs on the tensor cores over three bf16 planes whose sum
+ * represents the fp32 router weight (hi, mid, lo); each call splits router_w
+ * into its workspace first.  moe_router_prepare does that split once, into
+ * `planes` (caller-owned device memory of moe_router_planes_size bytes,
+ * 256-byte aligned, alive while prepared), on `stream`; later calls on this
+ * layer that pass the same router_w pointer use those planes and skip the
+ * split.  Only the pointer is compared: after rewriting the weight in place,
+ * call moe_router_prepare again (or with router_w or planes NULL, which
+ * forgets the prepared weight).  Results are identical either way.
+ * (forward_prefill.rs's gate GEMM reads its router weight every call; this
+ * is the load-time step an engine would run once per layer.)               */
+MOE_API int moe_router_planes_size(const moe_layer* layer, size_t* bytes);
+MOE_API int moe_router_prepare(moe_layer* layer, const float* router_w, void* planes, size_t planes_bytes,
+                               void* stream);
+
 /* Limit, in nanoseconds of GPU wall time, of every bounded wait inside the
  * grouped-GEMM kernels (the mbarrier waits between their TMA producer,
  * tensor-core issuer and epilogue warps); 0 restores the default of 2 s.

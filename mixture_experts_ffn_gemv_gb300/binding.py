@@ -25,7 +25,8 @@ EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_workspace_size", "moe_select_arm", "moe_route",
     "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_shared_expert_add", "moe_forward",
     "moe_forward_residual_rmsnorm",
-    "moe_act_quant_fp8", "moe_act_quant_nvfp4", "moe_device_status", "moe_layer_set_wait_limit",
+    "moe_act_quant_fp8", "moe_act_quant_nvfp4", "moe_device_status", "moe_router_planes_size",
+    "moe_router_prepare", "moe_layer_set_wait_limit",
     "moe_layer_stall_test",
     "moe_last_launch_count", "moe_kernel_timing_enable", "moe_kernel_timing_read", "moe_kernel_count",
     "moe_kernel_name", "moe_status_string",
@@ -84,6 +85,8 @@ def load_library(path: str | None = None, build: bool = True):
         lib.moe_act_quant_nvfp4.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp]
         lib.moe_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
         lib.moe_last_launch_count.argtypes = [_vp]
+        lib.moe_router_planes_size.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.moe_router_prepare.argtypes = [_vp, _vp, _vp, ctypes.c_size_t, _vp]
         lib.moe_layer_set_wait_limit.argtypes = [_vp, ctypes.c_uint64]
         lib.moe_layer_stall_test.argtypes = [_vp, ctypes.c_int]
         lib.moe_kernel_timing_enable.argtypes = [_vp, ctypes.c_int]
@@ -208,6 +211,19 @@ class MoeLayer:
 
     def select_arm(self, m: int) -> int:
         return self.lib.moe_select_arm(self.handle, int(m))
+
+    def prepare_router(self, router_w, stream=None):
+        """Split router_w once into planes this handle keeps (moe_router_prepare);
+        router_w=None forgets them."""
+        if router_w is None:
+            _check(self.lib.moe_router_prepare(self.handle, None, None, 0, _stream(stream)), "moe_router_prepare")
+            self._planes = None
+            return
+        n = ctypes.c_size_t()
+        _check(self.lib.moe_router_planes_size(self.handle, ctypes.byref(n)), "moe_router_planes_size")
+        self._planes = torch.empty(max(n.value, 256), dtype=torch.uint8, device=router_w.device)
+        _check(self.lib.moe_router_prepare(self.handle, _p(router_w), _p(self._planes), self._planes.numel(),
+                                           _stream(stream)), "moe_router_prepare")
 
     def set_wait_limit(self, ns: int):
         """Limit (ns) of the grouped GEMMs' bounded waits; 0 restores 2 s."""

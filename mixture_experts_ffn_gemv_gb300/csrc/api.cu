@@ -98,6 +98,10 @@ struct moe_layer {
     // expert out of moe_forward (moe_shared_expert_add adds it)
     int e_lo, E_local;
     bool shard;
+    // router weight split once by moe_router_prepare: the tensor-core router
+    // uses these planes (and skips its split) when a call passes prep_w
+    const float* prep_w;
+    const uint16_t* prep_planes;
 };
 
 namespace {
@@ -243,9 +247,13 @@ int run_route(const moe_layer* L, const Layout& lo, const void* x, int m, const 
     float* part = at<float>(ws, lo.part);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     if (lo.router_tc) {
-        uint16_t* planes = at<uint16_t>(ws, lo.planes);
         WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
-        MOE_LAUNCH(K_ROUTER_SPLIT, launch_router_split(wr, c.num_experts, c.hidden, planes, st));
+        const uint16_t* planes = L->prep_planes;
+        if (!planes || L->prep_w != wr) {  // not prepared for this weight: split it into the workspace
+            uint16_t* own = at<uint16_t>(ws, lo.planes);
+            MOE_LAUNCH(K_ROUTER_SPLIT, launch_router_split(wr, c.num_experts, c.hidden, own, st));
+            planes = own;
+        }
         MOE_LAUNCH(K_ROUTER, launch_router_tc(xb, m, c.hidden, planes, c.num_experts, part, lo.S, hdr, st));
     } else {
         MOE_LAUNCH(K_ROUTER, launch_router(xb, m, c.hidden, wr, c.num_experts, part, lo.S, st));
@@ -521,6 +529,8 @@ int moe_layer_create(const moe_config* cfg, const moe_expert_weights* routed, co
     L->last_launches = 0;
     L->wait_ns = kDefaultWaitNs;
     L->stall_test = 0;
+    L->prep_w = nullptr;
+    L->prep_planes = nullptr;
     L->e_lo = c.expert_end ? c.expert_begin : 0;
     L->E_local = c.expert_end ? c.expert_end - c.expert_begin : c.num_experts;
     L->shard = L->E_local < c.num_experts;
@@ -689,6 +699,32 @@ int moe_device_status(const void* workspace, void* stream, int32_t* device_code)
 }
 
 int moe_last_launch_count(const moe_layer* layer) { return layer ? layer->last_launches : -1; }
+
+int moe_router_planes_size(const moe_layer* layer, size_t* bytes) {
+    if (!layer || !bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = router_tc_split_bytes(layer->cfg.num_experts, layer->cfg.hidden);
+    return MOE_OK;
+}
+
+int moe_router_prepare(moe_layer* layer, const float* router_w, void* planes, size_t planes_bytes, void* stream) {
+    if (!layer) return MOE_ERR_INVALID_ARG;
+    if (!router_w || !planes) {  // forget the prepared weight
+        layer->prep_w = nullptr;
+        layer->prep_planes = nullptr;
+        return MOE_OK;
+    }
+    if (!aligned(router_w, 16) || !aligned(planes, 256)) return MOE_ERR_INVALID_ARG;
+    if (planes_bytes < router_tc_split_bytes(layer->cfg.num_experts, layer->cfg.hidden)) return MOE_ERR_WORKSPACE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev != layer->device) return MOE_ERR_INVALID_ARG;
+    if (launch_router_split(router_w, layer->cfg.num_experts, layer->cfg.hidden, static_cast<uint16_t*>(planes),
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    layer->prep_w = router_w;
+    layer->prep_planes = static_cast<const uint16_t*>(planes);
+    return MOE_OK;
+}
 
 int moe_layer_set_wait_limit(moe_layer* layer, uint64_t ns) {
     if (!layer) return MOE_ERR_INVALID_ARG;

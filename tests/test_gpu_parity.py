@@ -380,6 +380,34 @@ def test_route_and_permute_at_the_largest_expert_count(cuda, oracle_mod, m):
     assert np.abs(to_np(w).astype(np.float64).sum(1) - 1).max() < 1e-5
 
 
+def test_prepared_router_weight(cuda):
+    """moe_router_prepare splits the router weight once; calls passing that
+    pointer skip the split and give identical results, a weight rewritten in
+    place needs (and gets) a new preparation, and forgetting it restores the
+    per-call split."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    shape = MEDIUM_BF16
+    tensors, x = _small_case(shape, 300, seed=151, device=cuda)  # m > 64: the tensor-core router
+    layer = binding.MoeLayer(shape, tensors)
+    wr = tensors["router_w"]
+    out0, ids0, w0 = layer.moe_forward(x, wr, return_routing=True)
+    n0 = layer.last_launch_count()
+    layer.prepare_router(wr)
+    out1, ids1, w1 = layer.moe_forward(x, wr, return_routing=True)
+    assert layer.last_launch_count() == n0 - 1  # no split
+    assert torch.equal(out0, out1) and torch.equal(ids0, ids1) and torch.equal(w0, w1)
+    wr.mul_(1.5)  # rewritten in place: prepare again
+    layer.prepare_router(wr)
+    out2 = layer.moe_forward(x, wr)
+    fresh = binding.MoeLayer(shape, tensors).moe_forward(x, wr)
+    assert torch.equal(out2, fresh)
+    other = wr.clone()  # another pointer: split per call
+    assert torch.equal(layer.moe_forward(x, other), fresh)
+    layer.prepare_router(None)
+    assert torch.equal(layer.moe_forward(x, wr), fresh)
+    assert layer.device_status() == 0
+
+
 # ------------------------------------------------------------------ whole layer, full sizes
 
 FULL_CASES = [("tiny", 16)] + [("qwen3_decode", m) for m in (1, 2, 4, 16, 64)] + \
