@@ -228,7 +228,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool ok = r < valid;
             uint16_t* orow = p.out + (size_t)(p.grp_off[g] + j * BM + r) * p.ldo;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            if (GATEUP) {
+            if (q * 32 >= valid) {
+                // a lane quarter with no valid row (the ragged last m-tile of a group)
+            } else if (GATEUP) {
 #pragma unroll 1
                 for (int c = 2 * half; c < 2 * half + 2; ++c) {
                     uint32_t gv[32], uv[32];
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool ok = r < valid;
             uint16_t* orow = p.out + (size_t)(p.grp_off[g] + j * BM + r) * p.ldo;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            {
+            if (q * 32 < valid) {  // a lane quarter with no valid row skips the epilogue
 #pragma unroll 1
                 for (int c = 2 * half; c < 2 * half + 2; ++c) {
                     uint32_t gv[32], uv[32];

@@ -239,14 +239,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t base = tmem_base + lane_off + b * BN;
                 constexpr int NCH = NC / 16;  // 16-column loads per thread
+                // a lane quarter with no valid row (the ragged last m-tile of a
+                // group) skips the loads and FMAs, but still waits and releases
+                // the partial in step with the others (warp-uniform branch)
+                if (q * 32 < valid) {
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    uint32_t v[16];
-                    tmem_ld16(base + (c < NCH / 2 ? c_lo + 16 * c : c_hi + 16 * (c - NCH / 2)), v);
-                    tmem_wait_ld();
-                    const float f = c < NCH / 2 ? f_lo : f_hi;
+                    for (int c = 0; c < NCH; ++c) {
+                        uint32_t v[16];
+                        tmem_ld16(base + (c < NCH / 2 ? c_lo + 16 * c : c_hi + 16 * (c - NCH / 2)), v);
+                        tmem_wait_ld();
+                        const float f = c < NCH / 2 ? f_lo : f_hi;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(__uint_as_float(v[i]), f, acc[16 * c + i]);
+                        for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(__uint_as_float(v[i]), f, acc[16 * c + i]);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
