@@ -64,13 +64,21 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
     if (!is_last) return;
     __threadfence();
 
-    // per-expert totals; chunk bases relative to the expert's first row
+    // per-expert totals; chunk bases relative to the expert's first row (the
+    // scatter adds the expert's offset).  Eight chunks' counts are loaded
+    // before any is used: one L2 round trip per eight chunks.
     for (int e = tid; e < E; e += 256) {
         int run = 0;
-        for (int cc = 0; cc < nchunk; ++cc) {
-            const int v = __ldcg(&o.chunk_base[(size_t)cc * E + e]);
-            o.chunk_base[(size_t)cc * E + e] = run;
-            run += v;
+        for (int c0 = 0; c0 < nchunk; c0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = c0 + u < nchunk ? __ldcg(&o.chunk_base[(size_t)(c0 + u) * E + e]) : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c0 + u < nchunk) {
+                    o.chunk_base[(size_t)(c0 + u) * E + e] = run;
+                    run += v[u];
+                }
         }
         hist[e] = run;
         off[e] = run;
@@ -82,7 +90,6 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
         o.grp_off[e] = off[e];
         o.grp_cnt[e] = hist[e];
         if (o.expert_offsets) o.expert_offsets[e] = off[e];
-        for (int cc = 0; cc < nchunk; ++cc) o.chunk_base[(size_t)cc * E + e] += off[e];
     }
     if (tid == 0) {
         o.grp_off[E] = P;
@@ -142,7 +149,7 @@ __global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict
     }
     __syncthreads();
     for (int e = tid; e < E; e += 256) {
-        int run = o.chunk_base[(size_t)c * E + e];
+        int run = o.chunk_base[(size_t)c * E + e] + o.grp_off[e];  // chunk base relative to the expert, + its offset
         for (int w = 0; w < 8; ++w) {
             const int v = wbase[w * E + e];
             wbase[w * E + e] = run;
@@ -211,7 +218,16 @@ __global__ __launch_bounds__(256) void gather_bf16(const uint16_t* __restrict__ 
     if (t < 0) return;  // an unused slot: no tile reads a valid row from it
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
-    for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+    // four 16-byte chunks per lane loaded before any is stored
+    for (int c0 = lane; c0 < H / 8; c0 += 128) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + 32 * u < H / 8) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + 32 * u < H / 8) dst[c0 + 32 * u] = v[u];
+    }
 }
 
 __global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq, const float* __restrict__ xsc,

@@ -101,18 +101,35 @@ __device__ __forceinline__ void warp_topk(const float* part, int S, int m, int E
                                           RouteMode rm, float* logits_out, int t, int lane, int* id, float* wt) {
     uint32_t key[VPL];  // 0 = not a candidate (outside [0, E), or already picked)
     float val[VPL];     // softmax: the logit; sigmoid: the pre-bias score
+    // the logits: the S slices added in slice order, four slices at a time
+    // with all their loads issued before the adds (one L2 round trip per four
+    // slices, not one per slice)
+    float sum[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) sum[i] = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 4) {
+        float v[4][VPL];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int e = lane + 32 * i;
+                const float* src = part + ((size_t)(s0 + u) * m + t) * E + e;
+                v[u][i] = (s0 + u < S && e < E) ? (LDCG ? __ldcg(src) : *src) : 0.f;
+            }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < VPL; ++i)
+                if (s0 + u < S) sum[i] += v[u][i];
+    }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
         key[i] = 0u;
         val[i] = 0.f;
         if (e < E) {
-            float a = 0.f;
-#pragma unroll 8
-            for (int s = 0; s < S; ++s) {
-                const float* src = part + ((size_t)s * m + t) * E + e;
-                a += LDCG ? __ldcg(src) : *src;
-            }
+            float a = sum[i];
             if (!rm.sigmoid) {
                 if (bias) a += bias[e];
                 val[i] = a;
