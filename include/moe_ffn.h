@@ -25,8 +25,13 @@
  *     launch_n: early return at n == 0; forward_prefill: no grid.x = 0).
  *   - Results are deterministic: fixed reduction orders, no float atomics.
  *   - The workspace must be at least moe_workspace_size(layer, m) bytes and
- *     256-byte aligned; it carries no state between calls except the device
- *     error word read by moe_device_status.  Calls that share a workspace
+ *     256-byte aligned.  Its first 256 bytes (the header) carry state between
+ *     calls: counters that every call leaves at zero, and the device error
+ *     word read (and cleared) by moe_device_status.  A layer zeroes the
+ *     header itself when a call passes a workspace other than the one its
+ *     previous call used; a caller that writes into those 256 bytes between
+ *     two calls of one layer on the same workspace must zero them itself
+ *     (cudaMemsetAsync on the call's stream).  Calls that share a workspace
  *     must be ordered on one stream.
  */
 #ifndef MOE_FFN_GB300_H
@@ -280,10 +285,11 @@ MOE_API int moe_act_quant_fp8(const void* x, int64_t rows, int64_t n, uint8_t* c
 MOE_API int moe_act_quant_nvfp4(const void* x, int64_t rows, int64_t n, uint8_t* codes, uint8_t* block_scales,
                                 float* row_scales, void* stream);
 
-/* Synchronises `stream` and reads the device error word a previous call left
- * in `workspace` (0 = none).  Returns MOE_OK, MOE_ERR_DEVICE when the word is
- * set, or MOE_ERR_CUDA.                                                     */
-MOE_API int moe_device_status(const void* workspace, void* stream, int32_t* device_code);
+/* Synchronises `stream` and reads the device error word of `workspace`: the
+ * first device error of the calls made on it since the word was last read
+ * (0 = none).  A set word is cleared (on `stream`) after it is read.
+ * Returns MOE_OK, MOE_ERR_DEVICE when the word was set, or MOE_ERR_CUDA.    */
+MOE_API int moe_device_status(void* workspace, void* stream, int32_t* device_code);
 
 /* Router weight preparation (optional).  For m > 64 tokens (and E <= 256)
  * the router runs on the tensor cores over three bf16 planes whose sum
@@ -308,7 +314,7 @@ MOE_API int moe_router_prepare(moe_layer* layer, const float* router_w, void* pl
  * workspace's device error word, stop issuing work, wait (2 s at most) for
  * the copies and MMAs it already issued, free its tensor memory and return;
  * that call's outputs are then unspecified and moe_device_status reports
- * MOE_ERR_DEVICE.  The next call clears the word.  For tests of this
+ * MOE_ERR_DEVICE, which also clears the word.  For tests of this
  * failure path (with moe_layer_stall_test) and for callers that want a hung
  * pipeline reported sooner; it takes effect from the next call on `layer`.
  * (The failure handling of forward_prefill.rs is Rust's Result/ensure!; this

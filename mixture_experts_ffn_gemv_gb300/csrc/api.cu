@@ -88,6 +88,10 @@ struct moe_layer {
     bool nvfp4;  // NVFP4 weights and activations (GEMV arm only)
     int device;
     mutable int last_launches;
+    // the workspace this layer's last call used: its header is known to be
+    // clean (every call leaves the counters at zero), so the next call on it
+    // needs no zeroing launch
+    mutable const void* last_ws;
     mutable KernelTimer timer;
     GemmWeights gemm;  // host-side TMA descriptors of the weights
     RouteMode rm;      // router scoring
@@ -112,7 +116,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-    size_t hdr, zero_bytes, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile,
+    size_t hdr, part, planes, ids, w, chunk_base, grp_off, grp_cnt, act_group, act_tile,
         sorted_pair, slot_of_pair;
     size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, sgate, total;
     size_t xsb, xg, hsb, hg;  // nvfp4: block scales and row scales of x and h
@@ -142,8 +146,7 @@ Layout layout(const moe_layer* L, int64_t m, bool shared_only = false) {
         return at;
     };
     const size_t ab = L->fp8 ? 1 : 2;  // activation element bytes
-    o.hdr = take(sizeof(WsHeader));
-    o.zero_bytes = off;  // the header is zeroed at the start of every call
+    o.hdr = take(sizeof(WsHeader));  // state kept between calls: see prepare_header
     o.part = take((size_t)o.S * m * Er * 4);
     o.planes = o.router_tc ? take(router_tc_split_bytes(Er, H)) : 0;
     o.ids = take((size_t)o.P * 4);
@@ -277,6 +280,19 @@ PermuteOut permute_out(const Layout& lo, void* ws, int32_t* sorted_pair, int32_t
 }
 
 // The GEMV kernels' view of a call: group tables in the workspace, weights.
+// The workspace header (its first 256 bytes) carries state between calls:
+// the ticket counters, which every kernel that counts on them resets once it
+// is done, so each call leaves them at zero; and the device error word, which
+// moe_device_status clears when it reads it.  A workspace this layer's last
+// call used therefore needs no zeroing; any other gets its header zeroed
+// first (one memset, which would otherwise open every call's launch chain).
+int prepare_header(const moe_layer* L, void* ws, cudaStream_t st) {
+    if (L->last_ws == ws) return MOE_OK;
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
+    L->last_ws = ws;
+    return MOE_OK;
+}
+
 GemvArgs gemv_args(const moe_layer* L, const Layout& lo, void* ws) {
     const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
     const int E = L->E_local;
@@ -444,7 +460,7 @@ int forward_impl(const moe_layer* layer, const void* x, int64_t m, const float* 
     int32_t* ids = topk_ids_out ? topk_ids_out : at<int32_t>(workspace, lo.ids);
     float* w = topk_w_out ? topk_w_out : at<float>(workspace, lo.w);
     Launcher ln{layer, st};
-    if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prepare_header(layer, workspace, st) != MOE_OK) return MOE_ERR_CUDA;
     const moe_config& c = layer->cfg;
     if (!lo.router_tc && !layer->shard && route_permute_fusable((int)m, c.top_k, c.num_experts)) {
         // decode: router, top-k and the permute in one launch.  For fp8 layers
@@ -580,7 +596,7 @@ int moe_route(const moe_layer* layer, const void* x, int64_t m, const float* rou
     if (!x || !router_w || !topk_ids || !topk_w || !aligned(x, 16) || !aligned(router_w, 16))
         return MOE_ERR_INVALID_ARG;
     Launcher ln{layer, static_cast<cudaStream_t>(stream)};
-    if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, ln.st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prepare_header(layer, workspace, ln.st) != MOE_OK) return MOE_ERR_CUDA;
     rc = run_route(layer, lo, x, (int)m, router_w, router_bias, logits_out, topk_ids, topk_w, workspace, ln);
     layer->last_launches = ln.n;
     return rc;
@@ -594,7 +610,7 @@ int moe_permute(const moe_layer* layer, const int32_t* topk_ids, int64_t m, int3
     if (!topk_ids || !expert_offsets || !sorted_pair || !slot_of_pair) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     WsHeader* hdr = at<WsHeader>(workspace, lo.hdr);
-    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prepare_header(layer, workspace, st) != MOE_OK) return MOE_ERR_CUDA;
     Launcher ln{layer, st};
     const PermuteOut po = permute_out(lo, workspace, sorted_pair, slot_of_pair, expert_offsets);
     const int k = layer->cfg.top_k, E = layer->E_local, Et = layer->cfg.num_experts;
@@ -612,7 +628,7 @@ int moe_experts(const moe_layer* layer, const void* x, int64_t m, const int32_t*
     if (!x || !topk_ids || !topk_w || !out || !aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
     if (arm < MOE_ARM_AUTO || arm > MOE_ARM_GEMM) return MOE_ERR_INVALID_ARG;
     Launcher ln{layer, static_cast<cudaStream_t>(stream)};
-    if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, ln.st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prepare_header(layer, workspace, ln.st) != MOE_OK) return MOE_ERR_CUDA;
     rc = run_experts(layer, lo, x, (int)m, topk_ids, topk_w, out, arm, workspace, ln);
     layer->last_launches = ln.n;
     return rc;
@@ -634,7 +650,7 @@ int moe_shared_expert_add(const moe_layer* layer, const void* x, int64_t m, void
     if (!workspace || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
     if (workspace_bytes < lo.total) return MOE_ERR_WORKSPACE;
     Launcher ln{layer, static_cast<cudaStream_t>(stream)};
-    if (cudaMemsetAsync(workspace, 0, lo.zero_bytes, ln.st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (prepare_header(layer, workspace, ln.st) != MOE_OK) return MOE_ERR_CUDA;
     // no routed pairs (P = 0): the id and weight arrays are never read
     const int rc = run_experts(layer, lo, x, (int)m, at<int32_t>(workspace, lo.ids), at<float>(workspace, lo.w), out,
                                arm, workspace, ln);
@@ -688,14 +704,17 @@ int moe_act_quant_nvfp4(const void* x, int64_t rows, int64_t n, uint8_t* codes, 
     return MOE_OK;
 }
 
-int moe_device_status(const void* workspace, void* stream, int32_t* device_code) {
+int moe_device_status(void* workspace, void* stream, int32_t* device_code) {
     if (!workspace || !device_code) return MOE_ERR_INVALID_ARG;
     WsHeader h;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
     *device_code = h.err;
-    return h.err ? MOE_ERR_DEVICE : MOE_OK;
+    if (!h.err) return MOE_OK;
+    // read and cleared: the word holds the first error since the last read
+    if (cudaMemsetAsync(workspace, 0, 2 * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_ERR_DEVICE;
 }
 
 int moe_last_launch_count(const moe_layer* layer) { return layer ? layer->last_launches : -1; }

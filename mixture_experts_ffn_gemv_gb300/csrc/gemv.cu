@@ -100,11 +100,16 @@ struct Group {
     int g, off, cnt;
 };
 
+// The active-group count and this block's list entry are read together (one
+// round trip, not two): the entry exists for every ga < max_groups and is
+// only used once ga is known to be active.
 __device__ __forceinline__ bool load_group(const GemvArgs& a, int ga, Group& gr) {
-    if (ga >= a.hdr->n_active) return false;
-    gr.g = a.act_group[ga];
-    gr.off = a.grp_off[gr.g];
-    gr.cnt = a.grp_cnt[gr.g];
+    const int n_active = __ldcg(&a.hdr->n_active);
+    const int g = __ldcg(a.act_group + ga);
+    if (ga >= n_active) return false;
+    gr.g = g;
+    gr.off = __ldcg(a.grp_off + g);
+    gr.cnt = __ldcg(a.grp_cnt + g);
     return true;
 }
 
@@ -120,7 +125,7 @@ __device__ __forceinline__ int row_token(const GemvArgs& a, int s) {
 // h = silu(g) * u is stored as bf16 [rows, I].
 // The body of one CTA's work item bid = (active group bid / n_slices, row
 // slice bid % n_slices).
-template <int NT, int RT>
+template <int NT, int RT, int U>
 __device__ __forceinline__ void gateup_bf16_item(const GemvArgs& a, const uint16_t* __restrict__ x,
                                                  uint16_t* __restrict__ h, int bid, int n_slices) {
     constexpr int KS = 8 / RT;
@@ -153,8 +158,28 @@ __device__ __forceinline__ void gateup_bf16_item(const GemvArgs& a, const uint16
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) c1[nt][i] = c3[nt][i] = 0.f;
-#pragma unroll 2
-        for (int kc = kc0 + tig; kc < kc1; kc += 4) {
+        // U steps' weight loads are issued before their MMAs: the loads are
+        // volatile asm, so this order is what keeps U steps in flight
+        int kc = kc0 + tig;
+        for (; kc + 4 * (U - 1) < kc1; kc += 4 * U) {
+            uint4 a1[U], a18[U], a3[U], a38[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                a1[u] = ldw<RT>(w1g + kc + 4 * u);
+                a18[u] = ldw<RT>(w1g8 + kc + 4 * u);
+                a3[u] = ldw<RT>(w3g + kc + 4 * u);
+                a38[u] = ldw<RT>(w3g8 + kc + 4 * u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint4 xb = __ldg(xr[nt] + kc + 4 * u);
+                    mma2_bf16(c1[nt], a1[u], a18[u], xb);
+                    mma2_bf16(c3[nt], a3[u], a38[u], xb);
+                }
+        }
+        for (; kc < kc1; kc += 4) {  // the steps left over by whole batches
             const uint4 a1 = ldw<RT>(w1g + kc), a18 = ldw<RT>(w1g8 + kc);
             const uint4 a3 = ldw<RT>(w3g + kc), a38 = ldw<RT>(w3g8 + kc);
 #pragma unroll
@@ -201,17 +226,17 @@ __device__ __forceinline__ void gateup_bf16_item(const GemvArgs& a, const uint16
     }
 }
 
-template <int NT, int RT>
-__global__ __launch_bounds__(256, (NT == 1 ? 4 : 2)) void gemv_gateup_bf16(const GemvArgs a, const uint16_t* __restrict__ x,
-                                                        uint16_t* __restrict__ h, int n_slices) {
+template <int NT, int RT, int U>
+__global__ __launch_bounds__(256, (NT == 1 ? (U <= 2 ? 4 : (U <= 4 ? 3 : 2)) : 2)) void gemv_gateup_bf16(
+    const GemvArgs a, const uint16_t* __restrict__ x, uint16_t* __restrict__ h, int n_slices) {
     pdl_wait();
     pdl_trigger();
-    gateup_bf16_item<NT, RT>(a, x, h, blockIdx.x, n_slices);
+    gateup_bf16_item<NT, RT, U>(a, x, h, blockIdx.x, n_slices);
 }
 
 // ============================================================ down, bf16
 // CTA: RT row tiles (16 rows of H) x 8/RT K-slices of I; y fp32 [rows, H].
-template <int NT, int RT>
+template <int NT, int RT, int U>
 __device__ __forceinline__ void down_bf16_item(const GemvArgs& a, const uint16_t* __restrict__ h,
                                                float* __restrict__ y, int bid, int n_slices) {
     constexpr int KS = 8 / RT;
@@ -240,8 +265,20 @@ __device__ __forceinline__ void down_bf16_item(const GemvArgs& a, const uint16_t
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) c[nt][i] = 0.f;
-#pragma unroll 2
-        for (int kc = kc0 + tig; kc < kc1; kc += 4) {
+        int kc = kc0 + tig;
+        for (; kc + 4 * (U - 1) < kc1; kc += 4 * U) {
+            uint4 w0[U], w8[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                w0[u] = ldw<RT>(wg + kc + 4 * u);
+                w8[u] = ldw<RT>(wg8 + kc + 4 * u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma2_bf16(c[nt], w0[u], w8[u], __ldg(hr[nt] + kc + 4 * u));
+        }
+        for (; kc < kc1; kc += 4) {
             const uint4 w0 = ldw<RT>(wg + kc), w8 = ldw<RT>(wg8 + kc);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma2_bf16(c[nt], w0, w8, __ldg(hr[nt] + kc));
@@ -268,12 +305,12 @@ __device__ __forceinline__ void down_bf16_item(const GemvArgs& a, const uint16_t
     }
 }
 
-template <int NT, int RT>
-__global__ __launch_bounds__(256, 4) void gemv_down_bf16(const GemvArgs a, const uint16_t* __restrict__ h,
+template <int NT, int RT, int U>
+__global__ __launch_bounds__(256, (U <= 2 ? 4 : (U <= 4 ? 3 : 2))) void gemv_down_bf16(const GemvArgs a, const uint16_t* __restrict__ h,
                                                       float* __restrict__ y, int n_slices) {
     pdl_wait();
     pdl_trigger();
-    down_bf16_item<NT, RT>(a, h, y, blockIdx.x, n_slices);
+    down_bf16_item<NT, RT, U>(a, h, y, blockIdx.x, n_slices);
 }
 
 // ============================================================ gate/up, fp8
@@ -732,13 +769,41 @@ static bool narrow(const GemvArgs& a, int n_out, int k, int kslice_align, bool g
         }                                                                                                 \
     } while (0)
 
+template <int NT, int RT, int U>
+static void gu_launch(const GemvArgs& a, dim3 grid, const uint16_t* x, uint16_t* h, int n_slices, cudaStream_t st) {
+    launch_pdl(gemv_gateup_bf16<NT, RT, U>, grid, dim3(256), 0, st, a, x, h, n_slices);
+}
+template <int NT, int RT, int U>
+static void dn_launch(const GemvArgs& a, dim3 grid, const uint16_t* h, float* y, int n_slices, cudaStream_t st) {
+    launch_pdl(gemv_down_bf16<NT, RT, U>, grid, dim3(256), 0, st, a, h, y, n_slices);
+}
+
 cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st) {
-    MOE_GEMV_LAUNCH(gemv_gateup_bf16, true, a.I, a.H, 32, x, h);
+    const bool nw = narrow(a, a.I, a.H, 32, true);
+    const int n_slices = a.I / (nw ? 16 : 32);
+    const dim3 grid(n_slices * a.max_groups);
+    // steps in flight per thread (U): all eight of a narrow block's steps at
+    // H = 2048, four for two-tile blocks; eight-column blocks keep two, the
+    // most their registers allow (measured per shape at the Qwen3 decode
+    // sizes)
+    if (wide(a)) {
+        if (nw) gu_launch<2, 1, 2>(a, grid, x, h, n_slices, st);
+        else gu_launch<2, 2, 2>(a, grid, x, h, n_slices, st);
+    } else if (nw) {
+        gu_launch<1, 1, 8>(a, grid, x, h, n_slices, st);
+    } else {
+        gu_launch<1, 2, 4>(a, grid, x, h, n_slices, st);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_down_bf16(const GemvArgs& a, const uint16_t* h, float* y, cudaStream_t st) {
-    MOE_GEMV_LAUNCH(gemv_down_bf16, false, a.H, a.I, 32, h, y);
+    const int n_slices = a.H / 32;
+    const dim3 grid(n_slices * a.max_groups);
+    // two steps in flight: more registers per thread cost resident blocks,
+    // which measured slower for this short-K projection
+    if (wide(a)) dn_launch<2, 2, 2>(a, grid, h, y, n_slices, st);
+    else dn_launch<1, 2, 2>(a, grid, h, y, n_slices, st);
     return cudaGetLastError();
 }
 

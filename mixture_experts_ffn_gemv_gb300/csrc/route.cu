@@ -247,6 +247,7 @@ __global__ __launch_bounds__(256) void route_permute_sliced(const uint16_t* __re
     if (threadIdx.x == 0) is_last = atomicAdd(&hdr->group_done[blockIdx.x], 1) == (int)gridDim.y - 1;
     __syncthreads();
     if (!is_last) return;
+    if (threadIdx.x == 0) hdr->group_done[blockIdx.x] = 0;  // ready for the next call
     __threadfence();
     const int ne = min(8, E - (int)blockIdx.x * 8);
     for (int i = threadIdx.x; i < m * ne; i += 256) {
