@@ -314,6 +314,7 @@ GemvArgs gemv_args(const moe_layer* L, const Layout& lo, void* ws) {
     a.ss1 = L->shared.s1; a.ss3 = L->shared.s3; a.ss2 = L->shared.s2;
     a.sb1 = L->routed.sb1; a.sb3 = L->routed.sb3; a.sb2 = L->routed.sb2;
     a.ssb1 = L->shared.sb1; a.ssb3 = L->shared.sb3; a.ssb2 = L->shared.sb2;
+    a.early = 0;
     return a;
 }
 

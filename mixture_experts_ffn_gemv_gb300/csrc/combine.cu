@@ -18,19 +18,24 @@ namespace moe {
 // grid (ceil(H / 1024), m), 128 threads x 8 columns
 // accumulate = 1: out += the sum (out read as bf16, the sum added in fp32,
 // rounded once) -- the shared expert added after an expert-parallel
-// all-reduce of the routed partial outputs.
+// all-reduce of the routed partial outputs.  The pairs' slots and weights are
+// read before the wait (see PairHead); early = 1 (the grid is one wave) lets
+// the next kernel be scheduled right away.
 template <typename YT>
-__global__ __launch_bounds__(128) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
+__global__ __launch_bounds__(128, 8) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
                                                const float* __restrict__ w, int k, int H, int P, int has_shared,
                                                const float* __restrict__ shared_g, uint16_t* __restrict__ out,
-                                               int accumulate) {
-    pdl_wait();
-    pdl_trigger();
+                                               int accumulate, int early) {
+    if (early) pdl_trigger();
     const int t = blockIdx.y;
     const int h0 = (blockIdx.x * 128 + threadIdx.x) * 8;
     if (h0 >= H) return;
+    PairHead ph;
+    pair_head(slot, w, k, t, ph);
+    pdl_wait();
+    if (!early) pdl_trigger();
     float acc[8];
-    pair_sum(y, slot, w, k, H, P, has_shared, shared_g, t, h0, acc);
+    pair_sum(y, ph, slot, w, k, H, P, has_shared, shared_g, t, h0, acc);
     if (accumulate) {
         float prev[8];
         load8(out + (size_t)t * H + h0, prev);
@@ -49,8 +54,9 @@ cudaError_t launch_combine_f32(const float* y, const int32_t* slot_of_pair, cons
                                int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st,
                                int accumulate) {
     const dim3 grid(ceil_div(H, 1024), m);
+    const int early = one_wave((const void*)combine<float>, grid.x * grid.y, 128, 0);
     launch_pdl(combine<float>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out,
-               accumulate);
+               accumulate, early);
     return cudaGetLastError();
 }
 
@@ -58,8 +64,9 @@ cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, 
                                 int H, int P, int has_shared, const float* shared_g, uint16_t* out, cudaStream_t st,
                                 int accumulate) {
     const dim3 grid(ceil_div(H, 1024), m);
+    const int early = one_wave((const void*)combine<uint16_t>, grid.x * grid.y, 128, 0);
     launch_pdl(combine<uint16_t>, dim3(grid), dim3(128), 0, st, y, slot_of_pair, w, k, H, P, has_shared, shared_g, out,
-               accumulate);
+               accumulate, early);
     return cudaGetLastError();
 }
 
@@ -72,17 +79,20 @@ cudaError_t launch_combine_bf16(const uint16_t* y, const int32_t* slot_of_pair, 
 template <typename YT>
 __global__ __launch_bounds__(256) void combine_tail(const YT* __restrict__ y, const int32_t* __restrict__ slot,
                                                     const float* __restrict__ w, int k, int H, int P, int has_shared,
-                                                    const float* __restrict__ shared_g, TailArgs tail) {
-    pdl_wait();
-    pdl_trigger();
+                                                    const float* __restrict__ shared_g, TailArgs tail, int early) {
+    if (early) pdl_trigger();
     extern __shared__ float rs[];  // [H]: the new residual's values
     __shared__ float wsum[8];
     const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    PairHead ph;
+    pair_head(slot, w, k, t, ph);
+    pdl_wait();
+    if (!early) pdl_trigger();
     uint16_t* res = tail.residual + (size_t)t * H;
     float ss = 0.f;
     for (int h0 = threadIdx.x * 8; h0 < H; h0 += 256 * 8) {
         float acc[8];
-        pair_sum(y, slot, w, k, H, P, has_shared, shared_g, t, h0, acc);
+        pair_sum(y, ph, slot, w, k, H, P, has_shared, shared_g, t, h0, acc);
         float rv[8];
         load8(res + h0, rv);
         uint32_t o[4];
@@ -124,8 +134,9 @@ static cudaError_t launch_tail(const YT* y, const int32_t* slot_of_pair, const f
     static cudaError_t attr = cudaFuncSetAttribute(combine_tail<YT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    kTailMaxH * 4);
     if (attr != cudaSuccess) return attr;
+    const int early = one_wave((const void*)combine_tail<YT>, m, 256, (size_t)H * 4);
     launch_pdl(combine_tail<YT>, dim3(m), dim3(256), (size_t)H * 4, st, y, slot_of_pair, w, k, H, P, has_shared,
-               shared_g, tail);
+               shared_g, tail, early);
     return cudaGetLastError();
 }
 

@@ -236,6 +236,10 @@ __global__ __launch_bounds__(256, (NT == 1 ? (U <= 2 ? 4 : (U <= 4 ? 3 : 2)) : 2
 
 // ============================================================ down, bf16
 // CTA: RT row tiles (16 rows of H) x 8/RT K-slices of I; y fp32 [rows, H].
+// The block reads its group before the wait on the gate/up kernel: the
+// routing tables come from the permute, two or more launches back, which had
+// completed before the gate/up kernel let this one be scheduled.  (Loading
+// the first weight steps there too measured slower from m = 16 up.)
 template <int NT, int RT, int U>
 __device__ __forceinline__ void down_bf16_item(const GemvArgs& a, const uint16_t* __restrict__ h,
                                                float* __restrict__ y, int bid, int n_slices) {
@@ -246,6 +250,8 @@ __device__ __forceinline__ void down_bf16_item(const GemvArgs& a, const uint16_t
     const int rt = warp % RT, kq = warp / RT;
     Group gr;
     if (!load_group(a, bid / n_slices, gr)) return;
+    pdl_wait();
+    if (!a.early) pdl_trigger();
     const int H = a.H, I = a.I;
     const int row0 = (bid % n_slices) * (16 * RT) + rt * 16;
     const uint16_t* W2 = gr.g < a.E ? (const uint16_t*)a.w2 + (size_t)gr.g * H * I : (const uint16_t*)a.sw2;
@@ -308,9 +314,8 @@ __device__ __forceinline__ void down_bf16_item(const GemvArgs& a, const uint16_t
 template <int NT, int RT, int U>
 __global__ __launch_bounds__(256, (U <= 2 ? 4 : (U <= 4 ? 3 : 2))) void gemv_down_bf16(const GemvArgs a, const uint16_t* __restrict__ h,
                                                       float* __restrict__ y, int n_slices) {
-    pdl_wait();
-    pdl_trigger();
-    down_bf16_item<NT, RT, U>(a, h, y, blockIdx.x, n_slices);
+    if (a.early) pdl_trigger();
+    down_bf16_item<NT, RT, U>(a, h, y, blockIdx.x, n_slices);  // waits inside
 }
 
 // ============================================================ gate/up, fp8
@@ -430,15 +435,16 @@ template <int NT, int RT>
 __global__ __launch_bounds__(256) void gemv_down_fp8(const GemvArgs a, const uint8_t* __restrict__ hq,
                                                      const float* __restrict__ hsc, float* __restrict__ y,
                                                      int n_slices) {
-    pdl_wait();
-    pdl_trigger();
+    if (a.early) pdl_trigger();
     constexpr int KS = 8 / RT;
     __shared__ float red[KS][RT][32][NT * 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, tig = lane & 3;
     const int rt = warp % RT, kq = warp / RT;
     Group gr;
-    if (!load_group(a, blockIdx.x / n_slices, gr)) return;
+    if (!load_group(a, blockIdx.x / n_slices, gr)) return;  // the routing tables: see down_bf16_item
+    pdl_wait();
+    if (!a.early) pdl_trigger();
     const int H = a.H, I = a.I, ib = I / 128;
     const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
     const bool routed = gr.g < a.E;
@@ -637,15 +643,16 @@ __global__ __launch_bounds__(256, (NT == 1 ? 4 : 3)) void gemv_down_nvfp4(const 
                                                        const uint8_t* __restrict__ hsb,
                                                        const float* __restrict__ hg, float* __restrict__ y,
                                                        int n_slices) {
-    pdl_wait();
-    pdl_trigger();
+    if (a.early) pdl_trigger();
     constexpr int KS = 8 / RT;
     __shared__ float red[KS][RT][32][NT * 4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g8 = lane >> 2, tig = lane & 3;
     const int rt = warp % RT, kq = warp / RT;
     Group gr;
-    if (!load_group(a, blockIdx.x / n_slices, gr)) return;
+    if (!load_group(a, blockIdx.x / n_slices, gr)) return;  // the routing tables: see down_bf16_item
+    pdl_wait();
+    if (!a.early) pdl_trigger();
     const int H = a.H, I = a.I, iq = I / 2, is = I / 16;
     const int row0 = (blockIdx.x % n_slices) * (16 * RT) + rt * 16;
     const bool routed = gr.g < a.E;
@@ -775,7 +782,21 @@ static void gu_launch(const GemvArgs& a, dim3 grid, const uint16_t* x, uint16_t*
 }
 template <int NT, int RT, int U>
 static void dn_launch(const GemvArgs& a, dim3 grid, const uint16_t* h, float* y, int n_slices, cudaStream_t st) {
-    launch_pdl(gemv_down_bf16<NT, RT, U>, grid, dim3(256), 0, st, a, h, y, n_slices);
+    GemvArgs b = a;
+    b.early = one_wave((const void*)gemv_down_bf16<NT, RT, U>, (int)grid.x, 256, 0);
+    launch_pdl(gemv_down_bf16<NT, RT, U>, grid, dim3(256), 0, st, b, h, y, n_slices);
+}
+// The fp8 / NVFP4 down projections: two-tile blocks (32 rows of H), eight
+// token columns per pass, or sixteen for many rows per group.
+template <typename... KArgs, typename... Args>
+static void down_launch(void (*k1)(KArgs...), void (*k2)(KArgs...), const GemvArgs& a, cudaStream_t st,
+                        Args... args) {
+    const int n_slices = a.H / 32;
+    const dim3 grid(n_slices * a.max_groups);
+    auto* k = wide(a) ? k2 : k1;
+    GemvArgs b = a;
+    b.early = one_wave((const void*)k, (int)grid.x, 256, 0);
+    launch_pdl(k, grid, dim3(256), 0, st, b, args..., n_slices);
 }
 
 cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st) {
@@ -815,7 +836,7 @@ cudaError_t launch_gemv_gateup_fp8(const GemvArgs& a, const uint8_t* xq, const f
 
 cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const float* hsc, float* y,
                                  cudaStream_t st) {
-    MOE_GEMV_LAUNCH(gemv_down_fp8, false, a.H, a.I, 128, hq, hsc, y);
+    down_launch(gemv_down_fp8<1, 2>, gemv_down_fp8<2, 2>, a, st, hq, hsc, y);
     return cudaGetLastError();
 }
 
@@ -827,7 +848,7 @@ cudaError_t launch_gemv_gateup_nvfp4(const GemvArgs& a, const uint8_t* xq, const
 
 cudaError_t launch_gemv_down_nvfp4(const GemvArgs& a, const uint8_t* hq, const uint8_t* hsb, const float* hg,
                                    float* y, cudaStream_t st) {
-    MOE_GEMV_LAUNCH(gemv_down_nvfp4, false, a.H, a.I, 128, hq, hsb, hg, y);
+    down_launch(gemv_down_nvfp4<1, 2>, gemv_down_nvfp4<2, 2>, a, st, hq, hsb, hg, y);
     return cudaGetLastError();
 }
 

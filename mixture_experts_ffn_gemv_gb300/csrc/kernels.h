@@ -94,6 +94,9 @@ struct GemvArgs {
     const float *s1, *s3, *s2, *ss1, *ss3, *ss2;
     // nvfp4: e4m3 block-scale codes, one per 16 inputs
     const uint8_t *sb1, *sb3, *sb2, *ssb1, *ssb3, *ssb2;
+    // set by the launchers: the down grid is one wave, so it may let the next
+    // kernel be scheduled before its own wait
+    int early;
 };
 cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st);
 cudaError_t launch_gemv_down_bf16(const GemvArgs& a, const uint16_t* h, float* y, cudaStream_t st);

@@ -190,7 +190,7 @@ __global__ __launch_bounds__(256) void route_permute_whole(const uint16_t* __res
     __shared__ int is_last;
     whole_logits<MT>(x, m, H, wr, E, logits, blockIdx.x * kWholeEB, red);
     if (!last_block(hdr, &is_last)) return;
-    route_tail<VPL>(logits, 1, m, E, k, bias, rm, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
+    route_tail<VPL, true>(logits, 1, m, E, k, bias, rm, ids, wts, has_shared, o, hdr, ids_s, tail_buf, wsum);
 }
 
 template <int VPL>
@@ -300,10 +300,13 @@ static void launch_rps(const uint16_t* x, int m, int H, const float* wr, int E, 
                        const float* bias, RouteMode rm, int32_t* ids, float* w, int has_shared, const PermuteOut& o,
                        WsHeader* hdr, uint8_t* xq, float* xsc, cudaStream_t st) {
     const dim3 whole(ceil_div(E, kWholeEB));
-    if (m <= 1)
-        launch_pdl(route_permute_whole<VPL, 1>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc);
-    else if (m <= 4)
-        launch_pdl(route_permute_whole<VPL, 4>, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc);
+    if (m <= 4) {
+        // (letting the expert kernel be scheduled before this one's wait
+        // measured no faster)
+        auto* kern = m <= 1 ? route_permute_whole<VPL, 1> : route_permute_whole<VPL, 4>;
+        launch_pdl(kern, whole, dim3(256), 0, st, x, m, H, wr, E, part, k, bias, rm, ids, w, has_shared, o, hdr, xq,
+                   xsc);
+    }
     else
         launch_pdl(route_permute_sliced<VPL>, dim3(ceil_div(E, 8), S), dim3(256), 0, st, x, m, H, wr, E, H / S, part, k, bias, rm, ids, w, has_shared, o, hdr, xq, xsc);
 }

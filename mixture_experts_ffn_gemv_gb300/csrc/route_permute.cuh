@@ -355,6 +355,82 @@ __device__ __forceinline__ void block_permute_tiny(const int* ids_s, int P, int 
     }
 }
 
+// The permute of P <= 32 pairs (ids in shared memory) by one warp, writing
+// what block_permute_tiny writes.  The keys expert * 32 + pair are sorted
+// across the lanes (bitonic), which is the stable order by expert; lane j
+// then holds slot j.  Each group has at most 32 rows, so each active group is
+// one m-tile.  An id outside [0, E) (which the top-k never picks) is dropped
+// like the general permute drops it: slot -1 and the device error word.
+__device__ __forceinline__ void warp_permute_small(const int* ids_s, int P, int m, int E, int has_shared,
+                                                   const PermuteOut& o, WsHeader* hdr, int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    const int id = lane < P ? ids_s[lane] : -1;
+    const bool ok = lane < P && (unsigned)id < (unsigned)E;
+    if (lane < P && !ok) {
+        o.slot_of_pair[lane] = -1;
+        set_error(hdr, DEV_ERR_BAD_ID, id);
+    }
+    const int Pv = __popc(__ballot_sync(FULL, ok));  // valid pairs: sorted lanes [0, Pv)
+    uint32_t key = ok ? ((uint32_t)id << 5) | (uint32_t)lane : 0xffffffffu;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t other = __shfl_xor_sync(FULL, key, stride);
+            const bool asc = (lane & size) == 0, lower = (lane & stride) == 0;
+            key = (asc == lower) ? min(key, other) : max(key, other);
+        }
+    const bool valid = lane < Pv;
+    const int e = valid ? (int)(key >> 5) : E;
+    if (valid) {
+        const int p = (int)(key & 31u);
+        o.sorted_pair[lane] = p;
+        o.slot_of_pair[p] = lane;
+    } else if (lane < P) {
+        o.sorted_pair[lane] = -1;
+    }
+    const int e_prev = __shfl_up_sync(FULL, e, 1);
+    const bool first = valid && (lane == 0 || e_prev != e);
+    const unsigned firsts = __ballot_sync(FULL, first);
+    const int n_routed = __popc(firsts);
+    if (first) {
+        const unsigned above = firsts & ~((2u << lane) - 1u);  // group starts after this lane
+        const int rank = __popc(firsts & ((1u << lane) - 1u));
+        o.grp_cnt[e] = (above ? __ffs(above) - 1 : Pv) - lane;
+        o.act_group[rank] = e;
+        o.act_tile[rank] = rank;
+    }
+    // groups (e_prev, e]: the empty ones, then this lane's own first row
+    if (valid) {
+        for (int g = (lane == 0 ? 0 : e_prev + 1); g <= e; ++g) {
+            if (g < e) o.grp_cnt[g] = 0;
+            o.grp_off[g] = lane;
+            if (o.expert_offsets) o.expert_offsets[g] = lane;
+        }
+    }
+    // groups after the last routed one; then the shared expert's group E,
+    // whose rows are P + t
+    const int e_last = Pv > 0 ? __shfl_sync(FULL, e, Pv - 1) : -1;
+    for (int g = e_last + 1 + lane; g < E; g += 32) {
+        o.grp_off[g] = Pv;
+        o.grp_cnt[g] = 0;
+        if (o.expert_offsets) o.expert_offsets[g] = Pv;
+    }
+    if (lane == 0) {
+        o.grp_off[E] = P;
+        o.grp_cnt[E] = has_shared ? m : 0;
+        if (o.expert_offsets) o.expert_offsets[E] = Pv;
+        const int n_active = n_routed + (has_shared && m > 0 ? 1 : 0);
+        if (n_active > n_routed) {
+            o.act_group[n_routed] = E;
+            o.act_tile[n_routed] = n_routed;
+        }
+        o.act_tile[n_active] = n_active;
+        hdr->n_active = n_active;
+        hdr->total_tiles = n_active;
+    }
+}
+
 // Recursive-halving sum over the 32 lanes of the C live values v[0, C) (C a
 // power of two), using xor offsets O, O/2, ..., 1: at each level a lane keeps
 // one half of its live values and adds the partner's copy of that half.  On
@@ -442,7 +518,9 @@ __device__ __forceinline__ void whole_logits(const uint16_t* __restrict__ x, int
 // permute.  Shared scratch: ids_s [kPermChunk], tail_buf [kRouteFuseLogits]
 // (the logits, then the permute's tables), wsum [9].
 // CAP: ints in tail_buf (it must also hold the m*E logits).
-template <int VPL, int CAP = kRouteFuseLogits>
+// FEW: the launch serves m <= 4 tokens, and m * k <= 32 takes the one-warp
+// permute (kept out of the other kernels' code, where it cost registers).
+template <int VPL, bool FEW = false, int CAP = kRouteFuseLogits>
 __device__ __forceinline__ void route_tail(const float* part, int S, int m, int E, int k, const float* bias, RouteMode rm,
                                            int32_t* ids, float* wts, int has_shared, const PermuteOut& o,
                                            WsHeader* hdr, int* ids_s, int* tail_buf, int* wsum) {
@@ -452,6 +530,24 @@ __device__ __forceinline__ void route_tail(const float* part, int S, int m, int 
     int* hist = tail_buf + 8 * 256;
     int* off = hist + 256 + 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (FEW && S == 1 && m * k <= 32) {
+        // a few tokens: each warp picks its token's experts straight from the
+        // logits in L2, and one warp sorts the pairs
+        for (int t = warp; t < m; t += 8) {
+            int id;
+            float wt;
+            warp_topk<VPL, true>(part, 1, m, E, k, bias, rm, nullptr, t, lane, &id, &wt);
+            if (lane < k) {
+                ids[(size_t)t * k + lane] = id;
+                wts[(size_t)t * k + lane] = wt;
+                ids_s[t * k + lane] = id;
+            }
+        }
+        __syncthreads();
+        if (warp == 0) warp_permute_small(ids_s, m * k, m, E, has_shared, o, hdr, lane);
+        if (threadIdx.x == 0) hdr->done = 0;
+        return;
+    }
     // all 256 threads reduce the slices (coalesced over e, many loads in
     // flight); the warps then pick from shared memory
     const int n = m * E;
