@@ -241,6 +241,16 @@ def layer_alg(shape, m, U):
     return byt, flops
 
 
+def tensor_ratio(shape):
+    """Dense tensor-core rate of the layer's MMA type over bf16's, the nominal
+    ratio (fp8 4.5 / 2.25, NVFP4 13.5 / 2.25 PFLOP/s), applied to the measured
+    bf16 peak.  (The block-scaled NVFP4 MMA measured 4x the bf16 MMA rate on
+    GB300, so against the nominal ratio an NVFP4 GEMM reads at most 0.67.)"""
+    if getattr(shape, "nvfp4", False):
+        return 6.0
+    return 2.0 if shape.fp8 else 1.0
+
+
 def kernel_flops(kernel, shape, m):
     H, I_, k = shape.hidden, shape.inter, shape.top_k
     rows = m * k + (m if shape.shared_inter else 0)
@@ -470,7 +480,7 @@ def sweep(device, steps, warmup, emit):
                 U = float(np.mean(active_groups(routing, wl.shape)))
                 byt, flops = layer_alg(wl.shape, m, U)
                 per = ms / n / 1e3
-                tc_peak = tc * (2.0 if wl.shape.fp8 else 1.0)
+                tc_peak = tc * tensor_ratio(wl.shape)
                 t_roof = max(byt / bw, flops / tc_peak)
                 arm = reps[0]["layer"].select_arm(m)
                 totals, _ = kernel_profile(reps, n, wl, m)
@@ -615,7 +625,7 @@ def run_ours(args):
     # a kernel timed inside a step that lasts over a second is held to the
     # sustained tensor peak, a shorter one to the burst peak
     tc_key = "bf16_tflops_sustained" if ms_max > 1000 else "bf16_tflops"
-    tc = pk.get(tc_key, FALLBACK_PEAKS["bf16_tflops"]) * (2.0 if shape.fp8 else 1.0)
+    tc = pk.get(tc_key, FALLBACK_PEAKS["bf16_tflops"]) * tensor_ratio(shape)
     if flops and alg and flops / (tc * 1e12) > alg / (bw * 1e9):
         roof = {"bound": "tensor", "achieved": flops / avg_s / 1e12, "peak": tc, "unit": "TFLOP/s"}
     else:

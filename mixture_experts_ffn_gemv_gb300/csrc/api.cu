@@ -120,7 +120,7 @@ struct Layout {
         sorted_pair, slot_of_pair;
     size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, sgate, total;
     size_t xsb, xg, hsb, hg;  // nvfp4: block scales and row scales of x and h
-    size_t xs_g, h16;         // nvfp4 GEMM arm: gathered rows' scales, f16 h
+    size_t xs_sb, xs_g;       // nvfp4 GEMM arm: the gathered rows' block scales and row scales
     int S, P, rows, nchunk;
     int k;        // pairs per token in this call (top_k; 0 for the shared expert alone)
     int shared;   // 1: group E (the shared expert, rows P .. P+m-1) runs in this call
@@ -169,10 +169,10 @@ Layout layout(const moe_layer* L, int64_t m, bool shared_only = false) {
         o.hf = take((size_t)o.rows * I * 4);
         o.y = take((size_t)o.rows * H * 4);
         o.sgate = L->shared.gate ? take((size_t)m * 4) : 0;
-        // grouped-GEMM arm: the sorted rows widened to f16, their scales, f16 h
-        o.xs = take((size_t)o.rows * H * 2);
+        // grouped-GEMM arm: the sorted rows' codes, block scales and row scales
+        o.xs = take((size_t)o.rows * H / 2);
+        o.xs_sb = take((size_t)o.rows * H / 16);
         o.xs_g = take((size_t)o.rows * 4);
-        o.h16 = take((size_t)o.rows * I * 2);
         o.total = off;
         return o;
     }
@@ -356,7 +356,7 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
             MOE_LAUNCH(K_ACT_QUANT_NVFP4,
                        launch_act_quant_nvfp4_bf16(static_cast<const uint16_t*>(x), m, H, xq, xsb, xg, st));
             MOE_LAUNCH(K_GEMV_GATEUP, launch_gemv_gateup_nvfp4(a, xq, xsb, xg, hf, st));
-            MOE_LAUNCH(K_H_QUANT_NVFP4, launch_act_quant_nvfp4_f32(hf, lo.rows, I, hq, hsb, hg, nullptr, st));
+            MOE_LAUNCH(K_H_QUANT_NVFP4, launch_act_quant_nvfp4_f32(hf, lo.rows, I, hq, hsb, hg, st));
             MOE_LAUNCH(K_GEMV_DOWN, launch_gemv_down_nvfp4(a, hq, hsb, hg, y, st));
         } else if (L->fp8) {
             uint8_t* xq = at<uint8_t>(ws, lo.xq);
@@ -398,17 +398,20 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     g.stall_test = L->stall_test;
     uint16_t* ybf = at<uint16_t>(ws, lo.y);
     if (L->nvfp4) {
-        // x to NVFP4, then the sorted rows widened to f16 (the A operand)
+        // x to NVFP4, then the sorted rows' codes and scales (the A operand)
         uint8_t* xq = at<uint8_t>(ws, lo.xq);
         uint8_t* xsb = at<uint8_t>(ws, lo.xsb);
         float* xg = at<float>(ws, lo.xg);
         MOE_LAUNCH(K_ACT_QUANT_NVFP4,
                    launch_act_quant_nvfp4_bf16(static_cast<const uint16_t*>(x), m, H, xq, xsb, xg, st));
         MOE_LAUNCH(K_GATHER, launch_gather_nvfp4(xq, xsb, xg, po.sorted_pair, k, lo.P, lo.rows, H,
-                                                 at<uint32_t>(ws, lo.xs), at<float>(ws, lo.xs_g), st));
+                                                 at<uint8_t>(ws, lo.xs), at<uint8_t>(ws, lo.xs_sb),
+                                                 at<float>(ws, lo.xs_g), st));
         g.xs = at<void>(ws, lo.xs);
+        g.xs_sb = at<uint8_t>(ws, lo.xs_sb);
         g.xs_g = at<float>(ws, lo.xs_g);
-        g.h = at<void>(ws, lo.h16);
+        g.h = at<void>(ws, lo.h);
+        g.h_sb = at<uint8_t>(ws, lo.hsb);
         g.h_g = at<float>(ws, lo.hg);
         g.hf = at<float>(ws, lo.hf);
     } else if (L->fp8) {
@@ -433,10 +436,9 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     int rc = gemm_plan(L->gemm, g, &gl);
     if (rc != MOE_OK) return rc;
     MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(gl, st));
-    if (L->nvfp4)  // h (fp32, both scales applied) to NVFP4 and to the down GEMM's f16 A operand
+    if (L->nvfp4)  // h (fp32, both scales applied) to NVFP4: the down GEMM's A operand
         MOE_LAUNCH(K_H_QUANT_NVFP4, launch_act_quant_nvfp4_f32(at<float>(ws, lo.hf), lo.rows, I, at<uint8_t>(ws, lo.h),
-                                                               at<uint8_t>(ws, lo.hsb), at<float>(ws, lo.hg),
-                                                               at<uint32_t>(ws, lo.h16), st));
+                                                               at<uint8_t>(ws, lo.hsb), at<float>(ws, lo.hg), st));
     MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(gl, st));
     if (tail)
         MOE_LAUNCH(K_COMBINE, launch_combine_tail_bf16(ybf, po.slot_of_pair, w, m, k, H, lo.P, has_shared, sg, *tail, st));

@@ -548,31 +548,9 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
     out->fp8 = c.weights == MOE_WEIGHTS_FP8_E4M3_B128;
     out->nvfp4 = c.weights == MOE_WEIGHTS_NVFP4;
     if (out->nvfp4) {
-        // packed codes, unswizzled 32-byte boxes (64 codes of K) of 128 (W1, W3)
-        // or 256 (W2) rows: the converter warps widen them in shared memory
-        const uint64_t H = c.hidden, I = c.inter, E = c.num_experts;
-        const uint64_t d13[3] = {H / 2, I, E}, d2[3] = {I / 2, H, E};
-        const uint64_t s13[3] = {H / 2, I, 1}, s2[3] = {I / 2, H, 1};
-        if (!tmap_encode(&out->w1, routed->w1, 3, d13, 1, 32, 128, false) ||
-            !tmap_encode(&out->w3, routed->w3, 3, d13, 1, 32, 128, false) ||
-            !tmap_encode(&out->w2, routed->w2, 3, d2, 1, 32, BN, false))
-            return MOE_ERR_CUDA;
-        out->s1 = routed->s1; out->s3 = routed->s3; out->s2 = routed->s2;
-        out->sb1 = routed->sb1; out->sb3 = routed->sb3; out->sb2 = routed->sb2;
-        if (shared) {
-            if (!tmap_encode(&out->sw1, shared->w1, 3, s13, 1, 32, 128, false) ||
-                !tmap_encode(&out->sw3, shared->w3, 3, s13, 1, 32, 128, false) ||
-                !tmap_encode(&out->sw2, shared->w2, 3, s2, 1, 32, BN, false))
-                return MOE_ERR_CUDA;
-            out->ss1 = shared->s1; out->ss3 = shared->s3; out->ss2 = shared->s2;
-            out->ssb1 = shared->sb1; out->ssb3 = shared->sb3; out->ssb2 = shared->sb2;
-        } else {
-            out->sw1 = out->w1; out->sw3 = out->w3; out->sw2 = out->w2;
-            out->ss1 = out->s1; out->ss3 = out->s3; out->ss2 = out->s2;
-            out->ssb1 = out->sb1; out->ssb3 = out->sb3; out->ssb2 = out->sb2;
-        }
-        out->ready = true;
-        return MOE_OK;
+        const int rc = gemm_nvfp4_weight_maps(c, routed, shared, out);
+        out->ready = rc == MOE_OK;
+        return rc;
     }
     const int es = out->fp8 ? 1 : 2;
     const uint32_t bc = 128 / es;  // one 128-byte swizzle row of K per box
@@ -610,6 +588,13 @@ int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out) {
     if (!w.ready) return MOE_ERR_UNSUPPORTED;
     out->w = &w;
     out->call = g;
+    if (w.nvfp4) {
+        if (!gemm_nvfp4_act_maps(g.xs, g.xs_sb, g.rows, g.H, &out->a_xs, &out->a_xs_sb) ||
+            !gemm_nvfp4_act_maps(g.h, g.h_sb, g.rows, g.I, &out->a_h, &out->a_h_sb))
+            return MOE_ERR_CUDA;
+        out->grid = std::max(1, std::min(num_sms(), g.max_tiles * std::max(g.I / 128, g.H / BN)));
+        return MOE_OK;
+    }
     const int es = w.fp8 ? 1 : 2;
     const uint64_t da[2] = {(uint64_t)g.H, (uint64_t)g.rows}, dh[2] = {(uint64_t)g.I, (uint64_t)g.rows};
     if (!tmap_encode(&out->a_xs, g.xs, 2, da, es, 128 / es, BM) || !tmap_encode(&out->a_h, g.h, 2, dh, es, 128 / es, BM))

@@ -337,12 +337,10 @@ __device__ __forceinline__ void load16<float>(const float* p, float (&f)[16]) {
 //   per 16-block: sb = e4m3(RNE, satfinite)(amax(block) / (6 g));
 //   code = e2m1(v / (decode(sb) * g)), 0 when that scale is 0.
 // Codes are packed two per byte, element 2j in the low nibble of byte j.
-// deq (optional): the f16 values decode(code) * decode(sb) (without g), as
-// nvfp4_word widens them -- the grouped GEMM's A operand.
 template <typename T, int WPR>
 __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, int rows, int n,
                                                        uint8_t* __restrict__ q, uint8_t* __restrict__ sb,
-                                                       float* __restrict__ g, uint32_t* __restrict__ deq) {
+                                                       float* __restrict__ g) {
     pdl_wait();
     pdl_trigger();
     constexpr int TPR = 32 * WPR;  // threads per row
@@ -390,15 +388,6 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
         }
         *reinterpret_cast<uint2*>(q + (size_t)r * (n / 2) + (size_t)b * 8) = make_uint2(lo, hi);
         sb[(size_t)r * nb + b] = (uint8_t)sc;
-        if (deq) {
-            const uint32_t s2 = nvfp4_scale1(sc);
-            uint32_t a[4], c[4];
-            nvfp4_word(lo, s2, a);
-            nvfp4_word(hi, s2, c);
-            uint4* d = reinterpret_cast<uint4*>(deq + ((size_t)r * n + (size_t)b * 16) / 2);
-            d[0] = make_uint4(a[0], a[1], a[2], a[3]);
-            d[1] = make_uint4(c[0], c[1], c[2], c[3]);
-        }
     }
 }
 
@@ -406,21 +395,20 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
 constexpr int kQuantFewRows = 1024;
 
 template <typename T>
-static void launch_act_quant_nvfp4(const T* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g, uint32_t* deq,
-                                   cudaStream_t st) {
+static void launch_act_quant_nvfp4(const T* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g, cudaStream_t st) {
     if (rows <= kQuantFewRows)
-        launch_pdl(act_quant_nvfp4<T, 4>, dim3(ceil_div(rows, 2)), dim3(256), 0, st, v, rows, n, q, sb, g, deq);
+        launch_pdl(act_quant_nvfp4<T, 4>, dim3(ceil_div(rows, 2)), dim3(256), 0, st, v, rows, n, q, sb, g);
     else
-        launch_pdl(act_quant_nvfp4<T, 1>, dim3(ceil_div(rows, 8)), dim3(256), 0, st, v, rows, n, q, sb, g, deq);
+        launch_pdl(act_quant_nvfp4<T, 1>, dim3(ceil_div(rows, 8)), dim3(256), 0, st, v, rows, n, q, sb, g);
 }
 
 // Grouped-GEMM A operand of an NVFP4 layer: row s of the sorted order gets
-// token t's codes widened to f16 (decode(code) * decode(sb), nvfp4_word) and
-// its row scale; one warp per row, 32 codes per lane step.
+// token t's packed codes, block scales and row scale; one warp per row.
 __global__ __launch_bounds__(256) void gather_nvfp4(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xsb,
                                                     const float* __restrict__ xg,
                                                     const int32_t* __restrict__ sorted_pair, int k, int P, int rows,
-                                                    int H, uint32_t* __restrict__ xs, float* __restrict__ xs_g) {
+                                                    int H, uint8_t* __restrict__ xs, uint8_t* __restrict__ xs_sb,
+                                                    float* __restrict__ xs_g) {
     pdl_wait();
     pdl_trigger();
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -428,39 +416,31 @@ __global__ __launch_bounds__(256) void gather_nvfp4(const uint8_t* __restrict__ 
     const int t = gather_token(sorted_pair, s, k, P);
     if (t < 0) return;  // an unused slot: no tile reads a valid row from it
     const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * (H / 2));
-    const uint16_t* ssrc = reinterpret_cast<const uint16_t*>(xsb + (size_t)t * (H / 16));
     uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * (H / 2));
-    for (int c = lane; c < H / 32; c += 32) {
-        const uint4 qv = __ldg(src + c);
-        uint32_t s0, s1;
-        nvfp4_scales(__ldg(ssrc + c), s0, s1);
-        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t v[4];
-            nvfp4_word(w[i], i < 2 ? s0 : s1, v);
-            dst[4 * c + i] = make_uint4(v[0], v[1], v[2], v[3]);
-        }
-    }
+    for (int c = lane; c < H / 32; c += 32) dst[c] = __ldg(src + c);
+    const uint4* ssrc = reinterpret_cast<const uint4*>(xsb + (size_t)t * (H / 16));
+    uint4* sdst = reinterpret_cast<uint4*>(xs_sb + (size_t)s * (H / 16));
+    for (int c = lane; c < H / 256; c += 32) sdst[c] = __ldg(ssrc + c);
     if (lane == 0) xs_g[s] = __ldg(xg + t);
 }
 
 cudaError_t launch_gather_nvfp4(const uint8_t* xq, const uint8_t* xsb, const float* xg, const int32_t* sorted_pair,
-                                int k, int P, int rows, int H, uint32_t* xs, float* xs_g, cudaStream_t st) {
+                                int k, int P, int rows, int H, uint8_t* xs, uint8_t* xs_sb, float* xs_g,
+                                cudaStream_t st) {
     launch_pdl(gather_nvfp4, dim3(ceil_div(rows, 8)), dim3(256), 0, st, xq, xsb, xg, sorted_pair, k, P, rows, H, xs,
-               xs_g);
+               xs_sb, xs_g);
     return cudaGetLastError();
 }
 
 cudaError_t launch_act_quant_nvfp4_bf16(const uint16_t* x, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                         cudaStream_t st) {
-    launch_act_quant_nvfp4<uint16_t>(x, rows, n, q, sb, g, nullptr, st);
+    launch_act_quant_nvfp4<uint16_t>(x, rows, n, q, sb, g, st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_act_quant_nvfp4_f32(const float* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
-                                       uint32_t* deq, cudaStream_t st) {
-    launch_act_quant_nvfp4<float>(v, rows, n, q, sb, g, deq, st);
+                                       cudaStream_t st) {
+    launch_act_quant_nvfp4<float>(v, rows, n, q, sb, g, st);
     return cudaGetLastError();
 }
 
