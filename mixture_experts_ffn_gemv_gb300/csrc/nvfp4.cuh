@@ -1,10 +1,10 @@
-// NVFP4 device helpers shared by the GEMV arm, the row quantiser and the
-// grouped GEMM: e2m1 code pairs widened to f16x2 and multiplied by their e4m3
-// block scale.  e2m1 times e4m3 has at most 6 significant bits and lies in
-// [2^-10, 2688], so the f16 product is exact.  Every widening in this library
-// goes through nvfp4_word, so however the conversion orders a pair's halves,
-// weights and activations come out in the same order and dot products over
-// them are unchanged.
+// NVFP4 device helpers of the GEMV arm: e2m1 code pairs widened to f16x2 and
+// multiplied by their e4m3 block scale.  e2m1 times e4m3 has at most 6
+// significant bits and lies in [2^-10, 2688], so the f16 product is exact.
+// Weights and tokens are both widened by nvfp4_word, so however the
+// conversion orders a pair's halves, they come out in the same order and dot
+// products over them are unchanged.  (The grouped GEMM feeds packed codes to
+// the tensor core's block-scaled MMA and widens nothing.)
 #pragma once
 
 #include <stdint.h>

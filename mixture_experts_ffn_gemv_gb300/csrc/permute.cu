@@ -19,7 +19,6 @@
 #include "kernels.h"
 #include "launch.cuh"
 #include "route_permute.cuh"
-#include "nvfp4.cuh"
 
 namespace moe {
 
