@@ -758,8 +758,11 @@ static int sm_count() {
 // the gate/up projection: its K (= hidden) is long enough that eight slices
 // still stream for a while; the K-slices must hold whole 4-chunk steps
 // (kslice_align elements).
-static bool narrow(const GemvArgs& a, int n_out, int k, int kslice_align, bool gateup) {
-    return gateup && (n_out / 32) * a.max_groups < 8 * sm_count() && k % (8 * kslice_align) == 0;
+// blocks_per_sm: below this many two-tile blocks per SM the narrow shape is
+// taken (bf16: 3, where the two-tile blocks keep four steps in flight; fp8
+// and NVFP4: 8).
+static bool narrow(const GemvArgs& a, int n_out, int k, int kslice_align, bool gateup, int blocks_per_sm = 8) {
+    return gateup && (n_out / 32) * a.max_groups < blocks_per_sm * sm_count() && k % (8 * kslice_align) == 0;
 }
 
 #define MOE_GEMV_LAUNCH(KERNEL, GATEUP, N_OUT, K, ALIGN, ...)                                                      \
@@ -800,7 +803,7 @@ static void down_launch(void (*k1)(KArgs...), void (*k2)(KArgs...), const GemvAr
 }
 
 cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16_t* h, cudaStream_t st) {
-    const bool nw = narrow(a, a.I, a.H, 32, true);
+    const bool nw = narrow(a, a.I, a.H, 32, true, 3);
     const int n_slices = a.I / (nw ? 16 : 32);
     const dim3 grid(n_slices * a.max_groups);
     // steps in flight per thread (U): all eight of a narrow block's steps at
