@@ -81,9 +81,11 @@ def test_act_quant_fp8_bitwise(cuda, oracle_mod):
         assert np.array_equal(scales[r].cpu().numpy(), s), f"row {r}"
 
 
-@pytest.mark.parametrize("n,rows", [(768, 23), (2048, 23), (7168, 23), (768, 1100)])
+@pytest.mark.parametrize("n,rows", [(768, 23), (2048, 23), (7168, 23), (768, 1100), (2048, 1100), (256, 1100),
+                                    (512, 1100), (1536, 1100), (7168, 1100)])
 def test_act_quant_nvfp4_bitwise(cuda, oracle_mod, n, rows):
-    """Both launch shapes: four warps per row (few rows), one warp per row (many)."""
+    """Both launch shapes: four warps per row (few rows), one warp per row
+    (many), over row lengths of 16 to 448 blocks."""
     from mixture_experts_ffn_gemv_gb300 import binding
     shape = I.LayerShape(hidden=n, num_experts=1, top_k=1, inter=256)
     x = I.make_x(shape, rows, seed=22, device=cuda)
