@@ -285,6 +285,14 @@ MOE_API int moe_act_quant_fp8(const void* x, int64_t rows, int64_t n, uint8_t* c
 MOE_API int moe_act_quant_nvfp4(const void* x, int64_t rows, int64_t n, uint8_t* codes, uint8_t* block_scales,
                                 float* row_scales, void* stream);
 
+/* The same quantisation of fp32 rows: the kernel that quantises the down
+ * projection's input h inside moe_forward (the NVFP4 layers keep h in fp32
+ * between the gate/up product and its quantisation).
+ *   x fp32 [rows, n], 16-byte aligned; everything else as moe_act_quant_nvfp4.
+ * Finite inputs only.                                                       */
+MOE_API int moe_act_quant_nvfp4_f32(const float* x, int64_t rows, int64_t n, uint8_t* codes,
+                                    uint8_t* block_scales, float* row_scales, void* stream);
+
 /* Synchronises `stream` and reads the device error word of `workspace`: the
  * first device error of the calls made on it since the word was last read
  * (0 = none).  A set word is cleared (on `stream`) after it is read.

@@ -25,7 +25,7 @@ EXPORTED = (
     "moe_layer_create", "moe_layer_destroy", "moe_workspace_size", "moe_select_arm", "moe_route",
     "moe_permute", "moe_permute_noalloc", "moe_experts", "moe_shared_expert_add", "moe_forward",
     "moe_forward_residual_rmsnorm",
-    "moe_act_quant_fp8", "moe_act_quant_nvfp4", "moe_device_status", "moe_router_planes_size",
+    "moe_act_quant_fp8", "moe_act_quant_nvfp4", "moe_act_quant_nvfp4_f32", "moe_device_status", "moe_router_planes_size",
     "moe_router_prepare", "moe_layer_set_wait_limit",
     "moe_layer_stall_test",
     "moe_last_launch_count", "moe_kernel_timing_enable", "moe_kernel_timing_read", "moe_kernel_count",
@@ -83,6 +83,7 @@ def load_library(path: str | None = None, build: bool = True):
                                                      _vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         lib.moe_act_quant_fp8.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp]
         lib.moe_act_quant_nvfp4.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp]
+        lib.moe_act_quant_nvfp4_f32.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp]
         lib.moe_device_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
         lib.moe_last_launch_count.argtypes = [_vp]
         lib.moe_router_planes_size.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
@@ -133,15 +134,19 @@ def moe_act_quant_fp8(x, stream=None):
 
 
 def moe_act_quant_nvfp4(x, stream=None):
-    """x bf16 [rows, n] (device) -> (packed codes uint8 [rows, n/2], e4m3
-    block-scale codes uint8 [rows, n/16], row scales fp32 [rows])."""
+    """x bf16 or fp32 [rows, n] (device) -> (packed codes uint8 [rows, n/2],
+    e4m3 block-scale codes uint8 [rows, n/16], row scales fp32 [rows])."""
     lib = load_library()
     rows, n = x.shape
     codes = torch.empty(rows, n // 2, dtype=torch.uint8, device=x.device)
     sb = torch.empty(rows, n // 16, dtype=torch.uint8, device=x.device)
     g = torch.empty(rows, dtype=torch.float32, device=x.device)
-    _check(lib.moe_act_quant_nvfp4(_p(x), rows, n, _p(codes), _p(sb), _p(g), _stream(stream)),
-           "moe_act_quant_nvfp4")
+    if x.dtype == torch.float32:
+        fn, name = lib.moe_act_quant_nvfp4_f32, "moe_act_quant_nvfp4_f32"
+    else:
+        assert x.dtype == torch.bfloat16, x.dtype
+        fn, name = lib.moe_act_quant_nvfp4, "moe_act_quant_nvfp4"
+    _check(fn(_p(x), rows, n, _p(codes), _p(sb), _p(g), _stream(stream)), name)
     return codes, sb, g
 
 

@@ -707,6 +707,19 @@ int moe_act_quant_nvfp4(const void* x, int64_t rows, int64_t n, uint8_t* codes, 
     return MOE_OK;
 }
 
+int moe_act_quant_nvfp4_f32(const float* x, int64_t rows, int64_t n, uint8_t* codes, uint8_t* block_scales,
+                            float* row_scales, void* stream) {
+    if (rows < 0 || n <= 0 || n % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (rows > INT32_MAX / 2 || n > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (!x || !codes || !block_scales || !row_scales || !aligned(x, 16) || !aligned(codes, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (launch_act_quant_nvfp4_f32(x, (int)rows, (int)n, codes, block_scales, row_scales,
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
 int moe_device_status(void* workspace, void* stream, int32_t* device_code) {
     if (!workspace || !device_code) return MOE_ERR_INVALID_ARG;
     WsHeader h;

@@ -283,21 +283,43 @@ cudaError_t launch_quant_rows_fp8(const float* v, int rows, int n, uint8_t* q, f
 }
 
 // ---- NVFP4 activation rows
-// e2m1 code of a finite float: nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with
-// ties to the even code (<= at the midpoints toward an even code, < toward
-// an odd one), saturating at 6; the sign bit is kept, zero included.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-    const float a = fabsf(v);
-    uint32_t c;
-    if (a <= 0.25f) c = 0;
-    else if (a < 0.75f) c = 1;
-    else if (a <= 1.25f) c = 2;
-    else if (a < 1.75f) c = 3;
-    else if (a <= 2.5f) c = 4;
-    else if (a < 3.5f) c = 5;
-    else if (a <= 5.0f) c = 6;
-    else c = 7;
-    return c | ((__float_as_uint(v) >> 28) & 8u);
+// Eight floats -> eight e2m1 codes in one word, element i in nibble i: the
+// nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with ties to the even code,
+// saturating at 6, the sign kept (zero included).
+__device__ __forceinline__ uint32_t e2m1x8(const float (&f)[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+    return r;
+}
+
+// The codes of f[0..8) / scale, each quotient an IEEE fp32 divide.  Most
+// elements skip the divide (Ziv's rounding test): with r = 1/scale rounded,
+// f * r * (1 -+ 2^-20) (each product rounded) bracket the rounded quotient
+// for any finite f (three roundings of at most 2^-24 each stay inside the
+// 2^-20 margin), and e2m1 rounding is monotone, so where both brackets give
+// the same codes the quotient gives them too.  Otherwise (a quotient within
+// about 2^-20 of a rounding midpoint) the eight are divided.  rd = r * (1 -
+// 2^-20), ru = r * (1 + 2^-20); fast is false when r overflowed or is
+// subnormal.
+__device__ __forceinline__ uint32_t e2m1x8_div(const float* f, float scale, float rd, float ru, bool fast) {
+    float a[8], b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        a[i] = __fmul_rn(f[i], rd);
+        b[i] = __fmul_rn(f[i], ru);
+    }
+    const uint32_t c = e2m1x8(a);
+    if (fast && c == e2m1x8(b)) return c;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = __fdiv_rn(f[i], scale);
+    return e2m1x8(a);
 }
 
 template <typename T>
@@ -379,11 +401,11 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
         const float scale = __fmul_rn(e4m3x2_to_f32x2(sc).x, gs);
         uint32_t lo = 0, hi = 0;
         if (scale != 0.f) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                lo |= e2m1_code(__fdiv_rn(f[i], scale)) << (4 * i);
-                hi |= e2m1_code(__fdiv_rn(f[8 + i], scale)) << (4 * i);
-            }
+            const float r = __frcp_rn(scale);
+            const float rd = __fmul_rn(r, 1.0f - 0x1p-20f), ru = __fmul_rn(r, 1.0f + 0x1p-20f);
+            const bool fast = ru <= 3.0e38f && rd >= 0x1p-125f;
+            lo = e2m1x8_div(f, scale, rd, ru, fast);
+            hi = e2m1x8_div(f + 8, scale, rd, ru, fast);
         }
         *reinterpret_cast<uint2*>(q + (size_t)r * (n / 2) + (size_t)b * 8) = make_uint2(lo, hi);
         sb[(size_t)r * nb + b] = (uint8_t)sc;

@@ -142,3 +142,6 @@ def test_null_layer_calls_are_rejected(lib):
     assert lib.moe_act_quant_nvfp4(None, 4, 100, None, None, None, None) == 1  # n % 16 != 0
     assert lib.moe_act_quant_nvfp4(None, 0, 128, None, None, None, None) == 0
     assert lib.moe_act_quant_nvfp4(None, 4, 128, None, None, None, None) == 1  # null pointers
+    assert lib.moe_act_quant_nvfp4_f32(None, 4, 100, None, None, None, None) == 1
+    assert lib.moe_act_quant_nvfp4_f32(None, 0, 128, None, None, None, None) == 0
+    assert lib.moe_act_quant_nvfp4_f32(None, 4, 128, None, None, None, None) == 1

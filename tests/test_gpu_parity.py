@@ -103,6 +103,80 @@ def test_act_quant_nvfp4_bitwise(cuda, oracle_mod, n, rows):
     assert np.array_equal(codes.cpu().numpy(), q)
 
 
+def _midpoint_rows(n, rows, seed):
+    """fp32 rows whose quotients v / scale land on e2m1 rounding midpoints
+    (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) and one float either side of them,
+    for power-of-two scales (exact ties) and arbitrary ones (near ties).  The
+    scale a block gets is worked out with the quantisation's own fp32 steps
+    (round-to-nearest numpy float32 arithmetic) so that the constructed
+    values hit the intended quotients."""
+    rng = np.random.default_rng(seed)
+    f32 = np.float32
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], f32)
+    e4m3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    e4m3_pos = np.sort(np.unique(e4m3[np.isfinite(e4m3) & (e4m3 > 0)]))
+
+    def e4m3_round(x):  # nearest positive e4m3 value (ties are not hit here)
+        return e4m3_pos[np.argmin(np.abs(e4m3_pos.astype(np.float64) - float(x)))]
+
+    out = np.zeros((rows, n), f32)
+    for r in range(rows):
+        amax = f32(2688.0) if r % 2 == 0 else f32(rng.uniform(0.5, 4000.0))
+        gs = f32(amax / f32(2688.0))
+        out[r, 0] = amax
+        for b in range(1, n // 16):
+            bmax = f32(6.0 * 2.0 ** rng.integers(-3, 3)) if r % 2 == 0 else f32(rng.uniform(0.01, 1.0) * amax)
+            sc = e4m3_round(f32(bmax / f32(f32(6.0) * gs)))
+            scale = f32(f32(sc) * gs)
+            t = mids[rng.integers(0, len(mids), 15)] * rng.choice([f32(-1), f32(1)], 15)
+            v = (t * scale).astype(f32)
+            step = rng.integers(-1, 2, 15)
+            v = np.where(step < 0, np.nextafter(v, f32(-np.inf)), np.where(step > 0, np.nextafter(v, f32(np.inf)), v))
+            blk = np.concatenate([[bmax], v]).astype(f32)
+            out[r, 16 * b:16 * b + 16] = blk[rng.permutation(16)]
+    return out
+
+
+@pytest.mark.parametrize("n,rows", [(256, 40), (768, 1100)])
+def test_act_quant_nvfp4_f32_bitwise(cuda, oracle_mod, n, rows):
+    """The fp32 quantiser (the down projection's input) against the oracle,
+    bit for bit, on random rows and on rows built to put quotients on and
+    next to the e2m1 rounding midpoints."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((rows, n)).astype(np.float32) * rng.uniform(0.1, 10.0, (rows, 1)).astype(np.float32)
+    x[1] = 0
+    x[2, 16:32] = 0
+    x[3, :n // 2] *= 1e-5
+    x[5, 9] = -0.0
+    x[6] = 1.0
+    x[7] = 0                     # subnormal row scale; the second block's scale is subnormal
+    x[7, :16] = 1e-36            # too, so its reciprocal overflows and every quotient is divided
+    x[7, 16:32] = rng.uniform(-1, 1, 16).astype(np.float32) * np.float32(1e-36 / 256)
+    x[8:24] = _midpoint_rows(n, 16, seed=n)
+    xd = torch.from_numpy(x).to(cuda)
+    codes, sb, g = binding.moe_act_quant_nvfp4(xd)
+    torch.cuda.synchronize()
+    q, r_sb, r_g, _ = oracle_mod.nvfp4_quant(x)
+    assert np.array_equal(g.cpu().numpy(), r_g)
+    assert np.array_equal(sb.cpu().numpy(), r_sb)
+    bad = np.nonzero(codes.cpu().numpy() != q)
+    assert bad[0].size == 0, f"{bad[0].size} code bytes differ, first at row {bad[0][0]} byte {bad[1][0]}"
+
+
+def test_act_quant_nvfp4_bf16_midpoints(cuda, oracle_mod):
+    """bf16 rows on exact e2m1 rounding midpoints (power-of-two scales)."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    x = _midpoint_rows(512, 32, seed=5)[::2]          # the power-of-two rows: exact in bf16
+    xb = torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16)
+    codes, sb, g = binding.moe_act_quant_nvfp4(xb.to(cuda))
+    torch.cuda.synchronize()
+    q, r_sb, r_g, _ = oracle_mod.nvfp4_quant(xb.float().numpy())
+    assert np.array_equal(g.cpu().numpy(), r_g)
+    assert np.array_equal(sb.cpu().numpy(), r_sb)
+    assert np.array_equal(codes.cpu().numpy(), q)
+
+
 # ------------------------------------------------------------------ permute
 
 @pytest.mark.parametrize("m,k,E,kind", [
