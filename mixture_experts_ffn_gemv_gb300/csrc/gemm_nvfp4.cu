@@ -347,6 +347,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            // the accumulator is free for the next tile's MMAs once it is read:
+            // released before this tile's stores (Qwen3 NVFP4 m = 4096: down
+            // 106.8 -> 102.9 us)
+            auto release_acc = [&] {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            };
             if (GATEUP) {
                 // columns [0, 64): W1 rows (gate), [64, 128): the same W3 rows (up);
                 // this warp: 32 of each
@@ -357,6 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld32(taddr + half * 32, gv);
                 tmem_ld32(taddr + BN / 2 + half * 32, uv);
                 tmem_wait_ld();
+                release_acc();
                 if (ok) {  // 32 fp32 columns = four 32-byte stores
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -375,6 +384,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld32(taddr + half * 64, dv[0]);
                 tmem_ld32(taddr + half * 64 + 32, dv[1]);
                 tmem_wait_ld();
+                release_acc();
                 if (ok) {  // 64 bf16 columns = four 32-byte stores
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
@@ -389,9 +399,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
         }
     }
     tc_fence_before();
