@@ -270,17 +270,6 @@ __global__ __launch_bounds__(256) void act_quant_fp8(const T* __restrict__ x, in
     quant_block_fp8(x, H, blk, xq, xsc, threadIdx.x & 31);
 }
 
-cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st) {
-    const int blocks = m * (H / 128);
-    launch_pdl(act_quant_fp8<uint16_t>, dim3(ceil_div(blocks, 8)), dim3(256), 0, st, x, m, H, xq, xs);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_quant_rows_fp8(const float* v, int rows, int n, uint8_t* q, float* s, cudaStream_t st) {
-    const int blocks = rows * (n / 128);
-    launch_pdl(act_quant_fp8<float>, dim3(ceil_div(blocks, 8)), dim3(256), 0, st, v, rows, n, q, s);
-    return cudaGetLastError();
-}
 
 // ---- NVFP4 activation rows
 // Eight floats -> eight e2m1 codes in one word, element i in nibble i: the
@@ -349,6 +338,78 @@ __device__ __forceinline__ void load16<float>(const float* p, float (&f)[16]) {
         f[4 * i + 2] = u.z;
         f[4 * i + 3] = u.w;
     }
+}
+
+// ---- fp8 activations, four 128-blocks per warp (rows of a multiple of 512)
+// Lane l holds elements [16 (l % 8), +16) of block l / 8 of the warp's four:
+// one or two pairs of 16-byte loads per lane, the block's amax over its eight
+// lanes, codes as in quant_block_fp8 (the bracketed e4m3 rounding of each
+// quotient, the divide where a bracket straddles a rounding midpoint).
+template <typename T>
+__global__ __launch_bounds__(256) void act_quant_fp8_x4(const T* __restrict__ x, int m, int H,
+                                                        uint8_t* __restrict__ xq, float* __restrict__ xsc) {
+    pdl_wait();
+    pdl_trigger();
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    const int nb = H / 128, nq = nb / 4;
+    if (w >= m * nq) return;
+    const int t = w / nq, b = (w % nq) * 4 + (lane >> 3);
+    const size_t base = (size_t)t * H + (size_t)b * 128 + (lane & 7) * 16;
+    float f[16];
+    load16(x + base, f);
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(f[i]));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    uint32_t c[4] = {0u, 0u, 0u, 0u};
+    float s = 1.0f;
+    if (a > 0.f) {
+        s = __fdiv_rn(a, 448.0f);
+        const float r = __frcp_rn(s);
+        const float rd = __fmul_rn(r, 1.0f - 0x1p-20f), ru = __fmul_rn(r, 1.0f + 0x1p-20f);
+        bool same = ru <= 3.0e38f && rd >= 0x1p-125f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float* g = f + 4 * j;
+            c[j] = f32x2_to_e4m3x2(__fmul_rn(g[0], rd), __fmul_rn(g[1], rd)) |
+                   (f32x2_to_e4m3x2(__fmul_rn(g[2], rd), __fmul_rn(g[3], rd)) << 16);
+            const uint32_t up = f32x2_to_e4m3x2(__fmul_rn(g[0], ru), __fmul_rn(g[1], ru)) |
+                                (f32x2_to_e4m3x2(__fmul_rn(g[2], ru), __fmul_rn(g[3], ru)) << 16);
+            same = same && c[j] == up;
+        }
+        if (!same) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float* g = f + 4 * j;
+                c[j] = f32x2_to_e4m3x2(__fdiv_rn(g[0], s), __fdiv_rn(g[1], s)) |
+                       (f32x2_to_e4m3x2(__fdiv_rn(g[2], s), __fdiv_rn(g[3], s)) << 16);
+            }
+        }
+    }
+    *reinterpret_cast<uint4*>(xq + base) = make_uint4(c[0], c[1], c[2], c[3]);
+    if ((lane & 7) == 0) xsc[(size_t)t * nb + b] = s;
+}
+
+template <typename T>
+static void launch_act_quant_fp8_rows(const T* v, int rows, int n, uint8_t* q, float* s, cudaStream_t st) {
+    if ((n / 128) % 4 == 0) {
+        const int warps = rows * (n / 512);
+        launch_pdl(act_quant_fp8_x4<T>, dim3(ceil_div(warps, 8)), dim3(256), 0, st, v, rows, n, q, s);
+    } else {
+        const int blocks = rows * (n / 128);
+        launch_pdl(act_quant_fp8<T>, dim3(ceil_div(blocks, 8)), dim3(256), 0, st, v, rows, n, q, s);
+    }
+}
+
+cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st) {
+    launch_act_quant_fp8_rows<uint16_t>(x, m, H, xq, xs, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows_fp8(const float* v, int rows, int n, uint8_t* q, float* s, cudaStream_t st) {
+    launch_act_quant_fp8_rows<float>(v, rows, n, q, s, st);
+    return cudaGetLastError();
 }
 
 // WPR warps per row of n (a multiple of 16) values, 8 / WPR rows per block

@@ -65,9 +65,11 @@ ODD_E = I.LayerShape(hidden=256, num_experts=40, top_k=3, inter=128)
 
 # ------------------------------------------------------------------ activations
 
-def test_act_quant_fp8_bitwise(cuda, oracle_mod):
+@pytest.mark.parametrize("H", [384, 512, 7168])
+def test_act_quant_fp8_bitwise(cuda, oracle_mod, H):
+    """Rows of 3 blocks (one warp per block) and of 4 and 56 (four blocks per warp)."""
     from mixture_experts_ffn_gemv_gb300 import binding
-    x = I.make_x(SMALL_FP8, 37, seed=21, device=cuda)
+    x = I.make_x(dataclasses.replace(SMALL_FP8, hidden=H), 37, seed=21, device=cuda)
     x[3, 128:256] = 0            # an all-zero block
     x[5, :128] *= 1e-3           # small magnitudes (subnormal codes)
     x[6, 7] = -0.0
@@ -79,6 +81,34 @@ def test_act_quant_fp8_bitwise(cuda, oracle_mod):
         q, s, _ = oracle_mod.act_quant(xc[r].float().numpy())
         assert np.array_equal(codes[r].cpu().numpy(), q), f"row {r}"
         assert np.array_equal(scales[r].cpu().numpy(), s), f"row {r}"
+
+
+def test_act_quant_fp8_midpoints(cuda, oracle_mod):
+    """Blocks whose amax is 448 * 2^j (a power-of-two scale), so every
+    quotient is exact: values on e4m3 rounding midpoints (ties to even,
+    normal and subnormal codes) and next to them, bit for bit."""
+    from mixture_experts_ffn_gemv_gb300 import binding
+    rng = np.random.default_rng(31)
+    e4 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    pos = np.sort(np.unique(e4[np.isfinite(e4) & (e4 > 0)]))
+    vals = np.concatenate([[0.0], pos])
+    mids = (vals[:-1] + vals[1:]) / 2                       # every midpoint below 448
+    rows, H = 16, 1024
+    x = np.zeros((rows, H), np.float32)
+    for r in range(rows):
+        for b in range(H // 128):
+            j = int(rng.integers(-4, 4))
+            blk = rng.choice(mids, 128) * rng.choice([-1.0, 1.0], 128)
+            blk[rng.integers(0, 128)] = 448.0                  # the block's amax
+            x[r, 128 * b:128 * b + 128] = blk * 2.0 ** j
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    assert np.array_equal(xb.float().numpy(), x)           # the midpoints are exact in bf16
+    codes, scales = binding.moe_act_quant_fp8(xb.to(cuda))
+    torch.cuda.synchronize()
+    for r in range(rows):
+        q, sc, _ = oracle_mod.act_quant(x[r])
+        assert np.array_equal(codes[r].cpu().numpy(), q), f"row {r}"
+        assert np.array_equal(scales[r].cpu().numpy(), sc), f"row {r}"
 
 
 @pytest.mark.parametrize("n,rows", [(768, 23), (2048, 23), (7168, 23), (768, 1100), (2048, 1100), (256, 1100),
