@@ -386,7 +386,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int pt = t / p.n_tiles, nt = t % p.n_tiles;
                 const int a = find_group(s_pair, n_active, pt);
                 const int g = s_group[a];
-                const int row0 = p.grp_off[g] + (2 * (pt - s_pair[a]) + (int)rank) * BM;
+                const int jm = 2 * (pt - s_pair[a]) + (int)rank;  // this CTA's m-tile of the group
+                // a CTA with no row of the group (the peer of a group's last,
+                // short pair tile) loads its A tile from past the end of the
+                // tensor: zeros, with no memory traffic
+                const int row0 = p.grp_cnt[g] > jm * BM ? p.grp_off[g] + jm * BM : (1 << 30);
                 const bool routed = g < p.E;
                 const CUtensorMap* b0 = routed ? &tmB0 : &tmS0;
                 const CUtensorMap* b1 = routed ? &tmB1 : &tmS1;
