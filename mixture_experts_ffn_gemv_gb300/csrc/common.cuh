@@ -117,4 +117,36 @@ __device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g,
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// ---- fp8 / fp4 codes of quotients without a divide per element.
+// Each code is the rounding (nearest even, saturating) of the IEEE fp32
+// quotient f / s.  With r = 1/s rounded, the products f * r * (1 - 2^-20) and
+// f * r * (1 + 2^-20) (each rounded) lie on either side of the rounded
+// quotient: three roundings of at most 2^-24 each stay inside the 2^-20
+// margin.  Rounding to e4m3 or e2m1 is monotone, so where both brackets give
+// the same code, so does the quotient; elsewhere (a quotient within about
+// 2^-20 of a rounding midpoint) the code is taken from the divide.  This is
+// Ziv's rounding test.  `fast` is false when 1/s overflowed or is subnormal.
+struct QuotientBracket {
+    float rd, ru;
+    bool fast;
+};
+__device__ __forceinline__ QuotientBracket quotient_bracket(float s) {
+    const float r = __frcp_rn(s);
+    QuotientBracket b;
+    b.rd = __fmul_rn(r, 1.0f - 0x1p-20f);
+    b.ru = __fmul_rn(r, 1.0f + 0x1p-20f);
+    b.fast = b.ru <= 3.0e38f && b.rd >= 0x1p-125f;
+    return b;
+}
+// Four e4m3 codes of f[0..4) / s, element 0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3x4_quotient(const float* f, float s, const QuotientBracket& b) {
+    const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(f[0], b.rd), __fmul_rn(f[1], b.rd)) |
+                        (f32x2_to_e4m3x2(__fmul_rn(f[2], b.rd), __fmul_rn(f[3], b.rd)) << 16);
+    const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(f[0], b.ru), __fmul_rn(f[1], b.ru)) |
+                        (f32x2_to_e4m3x2(__fmul_rn(f[2], b.ru), __fmul_rn(f[3], b.ru)) << 16);
+    if (b.fast && lo == hi) return lo;
+    return f32x2_to_e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
+           (f32x2_to_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
+}
+
 }  // namespace moe

@@ -282,10 +282,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t w[NH / 4];
                     if (amax > 0.f) {
                         s = __fdiv_rn(amax, 448.0f);
+                        const QuotientBracket br = quotient_bracket(s);
 #pragma unroll
-                        for (int i = 0; i < NH / 4; ++i)
-                            w[i] = f32x2_to_e4m3x2(__fdiv_rn(acc[4 * i], s), __fdiv_rn(acc[4 * i + 1], s)) |
-                                   (f32x2_to_e4m3x2(__fdiv_rn(acc[4 * i + 2], s), __fdiv_rn(acc[4 * i + 3], s)) << 16);
+                        for (int i = 0; i < NH / 4; ++i) w[i] = e4m3x4_quotient(acc + 4 * i, s, br);
                     } else {
 #pragma unroll
                         for (int i = 0; i < NH / 4; ++i) w[i] = 0;

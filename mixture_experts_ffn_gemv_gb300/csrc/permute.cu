@@ -288,24 +288,17 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&f)[8]) {
     return r;
 }
 
-// The codes of f[0..8) / scale, each quotient an IEEE fp32 divide.  Most
-// elements skip the divide (Ziv's rounding test): with r = 1/scale rounded,
-// f * r * (1 -+ 2^-20) (each product rounded) bracket the rounded quotient
-// for any finite f (three roundings of at most 2^-24 each stay inside the
-// 2^-20 margin), and e2m1 rounding is monotone, so where both brackets give
-// the same codes the quotient gives them too.  Otherwise (a quotient within
-// about 2^-20 of a rounding midpoint) the eight are divided.  rd = r * (1 -
-// 2^-20), ru = r * (1 + 2^-20); fast is false when r overflowed or is
-// subnormal.
-__device__ __forceinline__ uint32_t e2m1x8_div(const float* f, float scale, float rd, float ru, bool fast) {
-    float a[8], b[8];
+// The e2m1 codes of f[0..8) / scale (element i in nibble i), by the
+// quotient bracket of common.cuh.
+__device__ __forceinline__ uint32_t e2m1x8_quotient(const float* f, float scale, const QuotientBracket& b) {
+    float a[8], c[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        a[i] = __fmul_rn(f[i], rd);
-        b[i] = __fmul_rn(f[i], ru);
+        a[i] = __fmul_rn(f[i], b.rd);
+        c[i] = __fmul_rn(f[i], b.ru);
     }
-    const uint32_t c = e2m1x8(a);
-    if (fast && c == e2m1x8(b)) return c;
+    const uint32_t lo = e2m1x8(a);
+    if (b.fast && lo == e2m1x8(c)) return lo;
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = __fdiv_rn(f[i], scale);
     return e2m1x8(a);
@@ -343,8 +336,7 @@ __device__ __forceinline__ void load16<float>(const float* p, float (&f)[16]) {
 // ---- fp8 activations, four 128-blocks per warp (rows of a multiple of 512)
 // Lane l holds elements [16 (l % 8), +16) of block l / 8 of the warp's four:
 // one or two pairs of 16-byte loads per lane, the block's amax over its eight
-// lanes, codes as in quant_block_fp8 (the bracketed e4m3 rounding of each
-// quotient, the divide where a bracket straddles a rounding midpoint).
+// lanes, codes as in quant_block_fp8 (e4m3x4_quotient).
 template <typename T>
 __global__ __launch_bounds__(256) void act_quant_fp8_x4(const T* __restrict__ x, int m, int H,
                                                         uint8_t* __restrict__ xq, float* __restrict__ xsc) {
@@ -366,26 +358,9 @@ __global__ __launch_bounds__(256) void act_quant_fp8_x4(const T* __restrict__ x,
     float s = 1.0f;
     if (a > 0.f) {
         s = __fdiv_rn(a, 448.0f);
-        const float r = __frcp_rn(s);
-        const float rd = __fmul_rn(r, 1.0f - 0x1p-20f), ru = __fmul_rn(r, 1.0f + 0x1p-20f);
-        bool same = ru <= 3.0e38f && rd >= 0x1p-125f;
+        const QuotientBracket br = quotient_bracket(s);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float* g = f + 4 * j;
-            c[j] = f32x2_to_e4m3x2(__fmul_rn(g[0], rd), __fmul_rn(g[1], rd)) |
-                   (f32x2_to_e4m3x2(__fmul_rn(g[2], rd), __fmul_rn(g[3], rd)) << 16);
-            const uint32_t up = f32x2_to_e4m3x2(__fmul_rn(g[0], ru), __fmul_rn(g[1], ru)) |
-                                (f32x2_to_e4m3x2(__fmul_rn(g[2], ru), __fmul_rn(g[3], ru)) << 16);
-            same = same && c[j] == up;
-        }
-        if (!same) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float* g = f + 4 * j;
-                c[j] = f32x2_to_e4m3x2(__fdiv_rn(g[0], s), __fdiv_rn(g[1], s)) |
-                       (f32x2_to_e4m3x2(__fdiv_rn(g[2], s), __fdiv_rn(g[3], s)) << 16);
-            }
-        }
+        for (int j = 0; j < 4; ++j) c[j] = e4m3x4_quotient(f + 4 * j, s, br);
     }
     *reinterpret_cast<uint4*>(xq + base) = make_uint4(c[0], c[1], c[2], c[3]);
     if ((lane & 7) == 0) xsc[(size_t)t * nb + b] = s;
@@ -462,11 +437,9 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
         const float scale = __fmul_rn(e4m3x2_to_f32x2(sc).x, gs);
         uint32_t lo = 0, hi = 0;
         if (scale != 0.f) {
-            const float r = __frcp_rn(scale);
-            const float rd = __fmul_rn(r, 1.0f - 0x1p-20f), ru = __fmul_rn(r, 1.0f + 0x1p-20f);
-            const bool fast = ru <= 3.0e38f && rd >= 0x1p-125f;
-            lo = e2m1x8_div(f, scale, rd, ru, fast);
-            hi = e2m1x8_div(f + 8, scale, rd, ru, fast);
+            const QuotientBracket br = quotient_bracket(scale);
+            lo = e2m1x8_quotient(f, scale, br);
+            hi = e2m1x8_quotient(f + 8, scale, br);
         }
         *reinterpret_cast<uint2*>(q + (size_t)r * (n / 2) + (size_t)b * 8) = make_uint2(lo, hi);
         sb[(size_t)r * nb + b] = (uint8_t)sc;

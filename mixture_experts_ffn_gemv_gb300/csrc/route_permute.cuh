@@ -68,20 +68,7 @@ __device__ __forceinline__ void quant_block_fp8(const T* x, int H, int blk, uint
     float s = 1.0f;
     if (amax > 0.f) {
         s = __fdiv_rn(amax, 448.0f);
-        // Each code is the e4m3 rounding of the IEEE quotient f / s.  The
-        // divides are taken only where needed (Ziv's rounding test): with
-        // r = 1/s rounded, f * r * (1 -+ 2^-20) (each product rounded) bracket
-        // the rounded quotient, and e4m3 rounding is monotone, so when both
-        // brackets give the same four codes those are the quotients' codes.
-        const float r = __frcp_rn(s);
-        const float rd = __fmul_rn(r, 1.0f - 0x1p-20f), ru = __fmul_rn(r, 1.0f + 0x1p-20f);
-        codes = f32x2_to_e4m3x2(__fmul_rn(f[0], rd), __fmul_rn(f[1], rd)) |
-                (f32x2_to_e4m3x2(__fmul_rn(f[2], rd), __fmul_rn(f[3], rd)) << 16);
-        const uint32_t up = f32x2_to_e4m3x2(__fmul_rn(f[0], ru), __fmul_rn(f[1], ru)) |
-                            (f32x2_to_e4m3x2(__fmul_rn(f[2], ru), __fmul_rn(f[3], ru)) << 16);
-        if (codes != up || !(ru <= 3.0e38f) || rd < 0x1p-125f)  // near a rounding midpoint, or r out of range
-            codes = f32x2_to_e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s)) |
-                    (f32x2_to_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
+        codes = e4m3x4_quotient(f, s, quotient_bracket(s));
     }
     *reinterpret_cast<uint32_t*>(xq + base) = codes;
     if (lane == 0) xsc[(size_t)t * nb + b] = s;
