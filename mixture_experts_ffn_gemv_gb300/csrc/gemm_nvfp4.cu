@@ -62,8 +62,11 @@ constexpr int EPI_WARPS = 8;     // two per TMEM lane quarter
 constexpr int SCALE0 = 2 + EPI_WARPS, SCALE_WARPS = 4;
 constexpr int THREADS = 32 * (SCALE0 + SCALE_WARPS);
 constexpr uint64_t DRAIN_NS = 2000000000ull;  // 2 s: drains of in-flight copies / MMAs
-constexpr int TABLE_INTS = 4 * kMaxExperts + 8;  // first m-tile, group, first row and row count of each active group
-constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256 + TABLE_INTS * 4;
+constexpr int TABLE_INTS = 3 * (kMaxExperts + 2);  // first m-tile, group and first row of each active group
+// Output staging: 256 bytes per tile row.  An epilogue warp owns 128 bytes of
+// 32 rows (its lane quarter, its half of the columns) and nothing else.
+constexpr int STG_OFF = ((BAR_OFF + 256 + TABLE_INTS * 4) + 127) & ~127;
+constexpr int SMEM_BYTES = 1024 + STG_OFF + BM * 256;
 static_assert(A_BYTES % 1024 == 0 && B_OFF % 1024 == 0 && SA_OFF % 1024 == 0, "swizzled tiles keep 1024-byte alignment");
 static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "accumulators and scale columns fit tensor memory");
 static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM's shared memory");
@@ -97,6 +100,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ uint4 lds128_u(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int i) {
     return i == 0 ? q.x : (i == 1 ? q.y : (i == 2 ? q.z : q.w));
 }
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int* s_tile = reinterpret_cast<int*>(smem + BAR_OFF + 256);
     int* s_group = s_tile + kMaxExperts + 2;
     int* s_off = s_group + kMaxExperts + 2;
-    int* s_cnt = s_off + kMaxExperts + 2;
+    const uint32_t stg = sbase + STG_OFF;  // output staging (epilogue)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_active = p.hdr->n_active;
@@ -165,7 +176,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int g = p.act_group[i];
         s_group[i] = g;
         s_off[i] = p.grp_off[g];
-        s_cnt[i] = p.grp_cnt[g];
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -332,11 +342,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int a = find_group(s_tile, n_active, mt);
             const int g = s_group[a];
             const int j = mt - s_tile[a];
-            const int valid = s_cnt[a] - j * BM;
+            const int valid = __ldg(p.grp_cnt + g) - j * BM;
             const bool ok = r < valid;
             const bool routed = g < p.E;
-            const size_t srow = (size_t)(s_off[a] + j * BM + r);
-            const float ar = ok ? __ldg(p.arow + srow) : 0.f;
+            const size_t row0 = (size_t)(s_off[a] + j * BM);
+            const float ar = ok ? __ldg(p.arow + row0 + r) : 0.f;
             const float w0 = routed ? __ldg(p.g0 + g) : __ldg(p.sg0);
             const float w1 = routed ? __ldg(p.g1 + g) : __ldg(p.sg1);
             const uint32_t acc = tc & 1u, aph = (tc >> 1) & 1u;
@@ -347,58 +357,55 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            // the accumulator is free for the next tile's MMAs once it is read:
-            // released before this tile's stores (Qwen3 NVFP4 m = 4096: down
-            // 106.8 -> 102.9 us)
-            auto release_acc = [&] {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-            };
+            uint32_t o[32];  // this thread's 128 bytes of its output row
             if (GATEUP) {
                 // columns [0, 64): W1 rows (gate), [64, 128): the same W3 rows (up);
-                // this warp: 32 of each
+                // this warp: 32 of each, giving 32 fp32 h columns
                 const float sg = ar * w0;
                 const float su = ar * w1;
-                float* orow = static_cast<float*>(p.out) + srow * p.ldo + nt * (BN / 2) + half * 32;
                 uint32_t gv[32], uv[32];
                 tmem_ld32(taddr + half * 32, gv);
                 tmem_ld32(taddr + BN / 2 + half * 32, uv);
                 tmem_wait_ld();
-                release_acc();
-                if (ok) {  // 32 fp32 columns = four 32-byte stores
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint32_t o[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            o[i] = __float_as_uint(swiglu(__uint_as_float(gv[8 * v + i]) * sg,
-                                                          __uint_as_float(uv[8 * v + i]) * su));
-                        st_global_v8(orow + 8 * v, o);
-                    }
-                }
+                for (int i = 0; i < 32; ++i)
+                    o[i] = __float_as_uint(swiglu(__uint_as_float(gv[i]) * sg, __uint_as_float(uv[i]) * su));
             } else {
                 const float sy = ar * w0;
-                uint16_t* orow = static_cast<uint16_t*>(p.out) + srow * p.ldo + nt * BN + half * 64;
                 uint32_t dv[2][32];
                 tmem_ld32(taddr + half * 64, dv[0]);
                 tmem_ld32(taddr + half * 64 + 32, dv[1]);
                 tmem_wait_ld();
-                release_acc();
-                if (ok) {  // 64 bf16 columns = four 32-byte stores
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
-                        for (int v = 0; v < 2; ++v) {
-                            uint32_t o[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                o[i] = pack_bf16x2(__uint_as_float(dv[c][16 * v + 2 * i]) * sy,
-                                                   __uint_as_float(dv[c][16 * v + 2 * i + 1]) * sy);
-                            st_global_v8(orow + c * 32 + 16 * v, o);
-                        }
-                }
+                    for (int i = 0; i < 16; ++i)
+                        o[16 * c + i] = pack_bf16x2(__uint_as_float(dv[c][2 * i]) * sy,
+                                                    __uint_as_float(dv[c][2 * i + 1]) * sy);
             }
+            // the accumulator is free once read; the stores follow
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            // Row r's 128 bytes into this warp's staging (16-byte chunk v at
+            // position v ^ (r % 8) of the row's half), then the warp's 32
+            // half-rows out as whole 128-byte lines, four rows per store:
+            // 256 line writes per tile instead of 1024 32-byte ones.
+            const uint32_t mine = stg + (uint32_t)(r * 256 + half * 128);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                sts128(mine + ((v ^ (r & 7)) << 4), o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            __syncwarp();
+            const int v = lane & 7;
+            const size_t ldb = (size_t)p.ldo * (GATEUP ? 4 : 2);  // output row stride in bytes
+            uint8_t* gb = static_cast<uint8_t*>(p.out) + row0 * ldb + nt * 256 + half * 128 + v * 16;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int ra = q * 32 + 4 * i + (lane >> 3);
+                const uint4 val = lds128_u(stg + (uint32_t)(ra * 256 + half * 128) + ((v ^ (ra & 7)) << 4));
+                if (ra < valid) *reinterpret_cast<uint4*>(gb + (size_t)ra * ldb) = val;
+            }
+            __syncwarp();
         }
     }
     tc_fence_before();
