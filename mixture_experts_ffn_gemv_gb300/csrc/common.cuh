@@ -149,4 +149,44 @@ __device__ __forceinline__ uint32_t e4m3x4_quotient(const float* f, float s, con
            (f32x2_to_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s)) << 16);
 }
 
+// ---- warp-private staged row stores (GEMM epilogues)
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                 : "memory");
+    return v;
+}
+// Lane r of a warp holds W bytes (W = 64 or 128) of row r of a 32-row block of
+// a row-major output.  Stored straight from the lanes, every store
+// instruction would touch 32 rows.  Instead the rows go through the warp's
+// own 32 x W bytes of shared memory at `stg` and leave as whole W-byte row
+// segments, 512 / W rows per store instruction.  16-byte chunk c of row r sits
+// at position c ^ (r mod 8) for W = 128 and c ^ ((r / 2) mod 4) for W = 64, so
+// that the writes and the reads each take the minimum four wavefronts.  Rows
+// from `valid` on are not stored.  gdst: row 0's segment; ldb: the output's row
+// stride in bytes.
+template <int W>
+__device__ __forceinline__ void warp_store_rows(uint32_t stg, const uint32_t (&v)[W / 4], int lane, uint8_t* gdst,
+                                                size_t ldb, int valid) {
+    constexpr int NCH = W / 16;    // 16-byte chunks per row
+    constexpr int RPI = 32 / NCH;  // rows per store instruction
+    const int sw = W == 128 ? (lane & 7) : ((lane >> 1) & 3);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+        sts128(stg + lane * W + ((c ^ sw) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    __syncwarp();
+    const int c = lane % NCH;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int ra = i * RPI + lane / NCH;
+        const int swa = W == 128 ? (ra & 7) : ((ra >> 1) & 3);
+        const uint4 val = lds128(stg + ra * W + ((c ^ swa) << 4));
+        if (ra < valid) *reinterpret_cast<uint4*>(gdst + (size_t)ra * ldb + c * 16) = val;
+    }
+    __syncwarp();
+}
+
 }  // namespace moe

@@ -63,8 +63,8 @@ constexpr int SCALE0 = 2 + EPI_WARPS, SCALE_WARPS = 4;
 constexpr int THREADS = 32 * (SCALE0 + SCALE_WARPS);
 constexpr uint64_t DRAIN_NS = 2000000000ull;  // 2 s: drains of in-flight copies / MMAs
 constexpr int TABLE_INTS = 3 * (kMaxExperts + 2);  // first m-tile, group and first row of each active group
-// Output staging: 256 bytes per tile row.  An epilogue warp owns 128 bytes of
-// 32 rows (its lane quarter, its half of the columns) and nothing else.
+// Output staging: 4 KB per epilogue warp (its 32 rows x 128 bytes,
+// warp_store_rows).
 constexpr int STG_OFF = ((BAR_OFF + 256 + TABLE_INTS * 4) + 127) & ~127;
 constexpr int SMEM_BYTES = 1024 + STG_OFF + BM * 256;
 static_assert(A_BYTES % 1024 == 0 && B_OFF % 1024 == 0 && SA_OFF % 1024 == 0, "swizzled tiles keep 1024-byte alignment");
@@ -99,15 +99,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
-__device__ __forceinline__ uint4 lds128_u(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
+__device__ __forceinline__ uint4 ldsv(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ uint32_t word_of(const uint4& q, int i) {
     return i == 0 ? q.x : (i == 1 ? q.y : (i == 2 ? q.z : q.w));
 }
@@ -304,10 +296,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     ok = false;
                     break;
                 }
-                const uint4 av = lds128(smem + SA_OFF + s * SA_BYTES + (q * 32 + lane) * 16);
+                const uint4 av = ldsv(smem + SA_OFF + s * SA_BYTES + (q * 32 + lane) * 16);
                 uint4 bv[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) bv[c] = lds128(smem + SB_OFF + s * SB_BYTES + (c * 32 + lane) * 16);
+                for (int c = 0; c < 4; ++c) bv[c] = ldsv(smem + SB_OFF + s * SB_BYTES + (c * 32 + lane) * 16);
                 uint32_t va[16], vb[16];
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -387,25 +379,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-            // Row r's 128 bytes into this warp's staging (16-byte chunk v at
-            // position v ^ (r % 8) of the row's half), then the warp's 32
-            // half-rows out as whole 128-byte lines, four rows per store:
-            // 256 line writes per tile instead of 1024 32-byte ones.
-            const uint32_t mine = stg + (uint32_t)(r * 256 + half * 128);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-                sts128(mine + ((v ^ (r & 7)) << 4), o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-            __syncwarp();
-            const int v = lane & 7;
+            // this warp's 32 rows x 128 bytes leave as whole 128-byte lines
             const size_t ldb = (size_t)p.ldo * (GATEUP ? 4 : 2);  // output row stride in bytes
-            uint8_t* gb = static_cast<uint8_t*>(p.out) + row0 * ldb + nt * 256 + half * 128 + v * 16;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int ra = q * 32 + 4 * i + (lane >> 3);
-                const uint4 val = lds128_u(stg + (uint32_t)(ra * 256 + half * 128) + ((v ^ (ra & 7)) << 4));
-                if (ra < valid) *reinterpret_cast<uint4*>(gb + (size_t)ra * ldb) = val;
-            }
-            __syncwarp();
+            warp_store_rows<128>(stg + (warp - 2) * 4096, o, lane,
+                                 static_cast<uint8_t*>(p.out) + (row0 + q * 32) * ldb + nt * 256 + half * 128, ldb,
+                                 valid - q * 32);
         }
     }
     tc_fence_before();
