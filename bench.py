@@ -179,10 +179,12 @@ def expert_bytes(shape):
     return b
 
 
-def kernel_alg_bytes(kernel, shape, m, U):
+def kernel_alg_bytes(kernel, shape, m, U, gemm_arm=None):
     """Algorithmic bytes one launch of `kernel` must move: each weight and
     activation it needs read once, each output written once.  U = active
-    expert groups (distinct routed experts + the shared expert)."""
+    expert groups (distinct routed experts + the shared expert).  gemm_arm:
+    whether the expert kernels were the grouped GEMMs (their y rows are bf16;
+    the GEMV arm's are fp32)."""
     H, I_, E, k = shape.hidden, shape.inter, shape.num_experts, shape.top_k
     P = m * k
     rows = P + (m if shape.shared_inter else 0)
@@ -218,7 +220,7 @@ def kernel_alg_bytes(kernel, shape, m, U):
     if kernel == "router":
         return E * H * 4 + m * H * 2 + m * E * 4
     if kernel == "combine":
-        return rows * H * (4 if m * k <= 8 * E else 2) + m * H * 2 + P * 8
+        return rows * H * (2 if gemm_arm else 4) + m * H * 2 + P * 8
     if kernel == "gather_rows":
         return m * H * ab + rows * H * ab
     if kernel == "router_split":
@@ -488,7 +490,7 @@ def sweep(device, steps, warmup, emit):
                 for kname, (kms, kcnt) in sorted(totals.items(), key=lambda kv: -kv[1][0]):
                     avg = kms / kcnt / 1e3
                     ent = {"avg_us": avg * 1e6}
-                    kb = kernel_alg_bytes(kname, wl.shape, m, U)
+                    kb = kernel_alg_bytes(kname, wl.shape, m, U, gemm_arm=arm == 2)
                     kf = kernel_flops(kname, wl.shape, m)
                     if kb:
                         ent["hbm_frac"] = kb / avg / bw
@@ -620,7 +622,7 @@ def run_ours(args):
     dname, (dms, dcnt) = dom
     avg_s = dms / dcnt / 1e3
     flops = kernel_flops(dname, shape, m)
-    alg = kernel_alg_bytes(dname, shape, m, Umean)
+    alg = kernel_alg_bytes(dname, shape, m, Umean, gemm_arm=any(k.startswith("gemm") for k in totals))
     bw = pk["hbm_gbs"]
     # a kernel timed inside a step that lasts over a second is held to the
     # sustained tensor peak, a shorter one to the burst peak

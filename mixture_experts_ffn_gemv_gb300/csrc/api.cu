@@ -582,12 +582,21 @@ int moe_workspace_size(const moe_layer* layer, int64_t m, size_t* bytes) {
 
 int moe_select_arm(const moe_layer* layer, int64_t m) {
     if (!layer) return MOE_ERR_INVALID_ARG;
-    // rows per selected expert: the GEMV arm while they stay few (span-02
+    // Rows per selected expert: the GEMV arm while they stay few (span-02
     // forward_rows takes its GEMV path for r <= 16 rows; metrale moe_v41 for
-    // groups of at most eight rows)
-    const int64_t P = m * layer->cfg.top_k;
+    // groups of at most eight rows).  The crossover depends on the weight
+    // format; each threshold is where the two arms measured equal on GB300,
+    // in routed pairs P = m * k against E:
+    //   bf16  P > 4 E   (Qwen3 shape: m = 48 GEMV 207 / GEMM 210 us, m = 80 242 / 229)
+    //   NVFP4 P > 2 E   (m = 32: 123 / 128 us, m = 40: 121 / 119)
+    //   fp8   P > E / 4 (DeepSeek-V3 shape: m = 8 431 / 452 us, m = 12 612 / 603)
+    // The fp8 GEMV's per-block scale promotion costs more as rows grow, and
+    // the NVFP4 GEMV widens every weight code on the ALUs.
+    const int64_t P = m * layer->cfg.top_k, E = layer->cfg.num_experts;
     if (!gemm_supported(layer->cfg)) return MOE_ARM_GEMV;
-    return P <= (int64_t)8 * layer->cfg.num_experts ? MOE_ARM_GEMV : MOE_ARM_GEMM;
+    const int w = layer->cfg.weights;
+    const bool gemv = w == MOE_WEIGHTS_FP8_E4M3_B128 ? 4 * P <= E : (w == MOE_WEIGHTS_NVFP4 ? P <= 2 * E : P <= 4 * E);
+    return gemv ? MOE_ARM_GEMV : MOE_ARM_GEMM;
 }
 
 int moe_route(const moe_layer* layer, const void* x, int64_t m, const float* router_w, const float* router_bias,
