@@ -120,7 +120,7 @@ struct Layout {
         sorted_pair, slot_of_pair;
     size_t xq, xsc, xs, xs_sc, h, hsc, hf, y, sgate, total;
     size_t xsb, xg, hsb, hg;  // nvfp4: block scales and row scales of x and h
-    size_t xs_sb, xs_g;       // nvfp4 GEMM arm: the gathered rows' block scales and row scales
+    size_t xs_sb, xs_g;       // nvfp4 GEMM arm: the sorted rows' block scales and row scales
     int S, P, rows, nchunk;
     int k;        // pairs per token in this call (top_k; 0 for the shared expert alone)
     int shared;   // 1: group E (the shared expert, rows P .. P+m-1) runs in this call
@@ -398,15 +398,12 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     g.stall_test = L->stall_test;
     uint16_t* ybf = at<uint16_t>(ws, lo.y);
     if (L->nvfp4) {
-        // x to NVFP4, then the sorted rows' codes and scales (the A operand)
-        uint8_t* xq = at<uint8_t>(ws, lo.xq);
-        uint8_t* xsb = at<uint8_t>(ws, lo.xsb);
-        float* xg = at<float>(ws, lo.xg);
+        // x to NVFP4, straight into the sorted rows (the A operand): each
+        // token's codes, scales and row scale go to its pairs' slots
         MOE_LAUNCH(K_ACT_QUANT_NVFP4,
-                   launch_act_quant_nvfp4_bf16(static_cast<const uint16_t*>(x), m, H, xq, xsb, xg, st));
-        MOE_LAUNCH(K_GATHER, launch_gather_nvfp4(xq, xsb, xg, po.sorted_pair, k, lo.P, lo.rows, H,
-                                                 at<uint8_t>(ws, lo.xs), at<uint8_t>(ws, lo.xs_sb),
-                                                 at<float>(ws, lo.xs_g), st));
+                   launch_act_quant_nvfp4_sorted(static_cast<const uint16_t*>(x), m, H, po.slot_of_pair, k,
+                                                 has_shared ? lo.P : -1, at<uint8_t>(ws, lo.xs),
+                                                 at<uint8_t>(ws, lo.xs_sb), at<float>(ws, lo.xs_g), st));
         g.xs = at<void>(ws, lo.xs);
         g.xs_sb = at<uint8_t>(ws, lo.xs_sb);
         g.xs_g = at<float>(ws, lo.xs_g);

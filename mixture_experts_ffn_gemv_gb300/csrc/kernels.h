@@ -110,14 +110,14 @@ cudaError_t launch_gemv_down_fp8(const GemvArgs& a, const uint8_t* hq, const flo
 // take those and write fp32 h / y like the fp8 ones
 cudaError_t launch_act_quant_nvfp4_bf16(const uint16_t* x, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                         cudaStream_t st);
+// x quantised straight into the grouped GEMM's sorted rows: token t's codes,
+// scales and row scale go to rows slot_of_pair[t * k + j] (j < k, dropped
+// pairs skipped) and, when shared_row0 >= 0, to row shared_row0 + t.
+cudaError_t launch_act_quant_nvfp4_sorted(const uint16_t* x, int m, int n, const int32_t* slot_of_pair, int k,
+                                          int shared_row0, uint8_t* q, uint8_t* sb, float* g, cudaStream_t st);
 // the same for fp32 rows (h), which both arms' down projections take as A
 cudaError_t launch_act_quant_nvfp4_f32(const float* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                        cudaStream_t st);
-// sorted-row A operand of the NVFP4 grouped GEMM: the codes xs [rows, H/2],
-// block scales xs_sb [rows, H/16] and row scales xs_g [rows] of each slot's token
-cudaError_t launch_gather_nvfp4(const uint8_t* xq, const uint8_t* xsb, const float* xg, const int32_t* sorted_pair,
-                                int k, int P, int rows, int H, uint8_t* xs, uint8_t* xs_sb, float* xs_g,
-                                cudaStream_t st);
 cudaError_t launch_gemv_gateup_nvfp4(const GemvArgs& a, const uint8_t* xq, const uint8_t* xsb, const float* xg,
                                      float* hf, cudaStream_t st);
 cudaError_t launch_gemv_down_nvfp4(const GemvArgs& a, const uint8_t* hq, const uint8_t* hsb, const float* hg,

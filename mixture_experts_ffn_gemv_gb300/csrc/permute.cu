@@ -387,35 +387,79 @@ cudaError_t launch_quant_rows_fp8(const float* v, int rows, int n, uint8_t* q, f
     return cudaGetLastError();
 }
 
-// WPR warps per row of n (a multiple of 16) values, 8 / WPR rows per block
-// (four warps per row while rows are few, one warp per row when there are
-// many):
+// Where act_quant_nvfp4 puts a row's codes, block scales and row scale:
+// row r itself, or (dst_slot) the sorted rows of token r's pairs --
+// dst_slot[r * k + j] for j < k, skipping dropped pairs (-1) -- and, when
+// shared_row0 >= 0, the shared expert's row shared_row0 + r: the grouped
+// GEMM's A operand, written without a separate gather.
+struct QuantDest {
+    const int32_t* dst_slot;
+    int k;
+    int shared_row0;
+};
+
+// One row's NVFP4 codes of block b (two words) and its scale code, to every
+// destination row (SORTED: the pairs' sorted rows; else row r).
+template <bool SORTED>
+__device__ __forceinline__ void put_block(uint8_t* q, uint8_t* sb, int n, int r, int b, uint2 codes, uint8_t sc,
+                                          const QuantDest& d) {
+    const int nb = n / 16;
+    if (!SORTED) {
+        *reinterpret_cast<uint2*>(q + (size_t)r * (n / 2) + (size_t)b * 8) = codes;
+        sb[(size_t)r * nb + b] = sc;
+        return;
+    }
+    for (int j = 0; j <= d.k; ++j) {
+        const int s = j < d.k ? __ldg(d.dst_slot + (size_t)r * d.k + j) : (d.shared_row0 >= 0 ? d.shared_row0 + r : -1);
+        if (s < 0) continue;
+        *reinterpret_cast<uint2*>(q + (size_t)s * (n / 2) + (size_t)b * 8) = codes;
+        sb[(size_t)s * nb + b] = sc;
+    }
+}
+template <bool SORTED>
+__device__ __forceinline__ void put_row_scale(float* g, int r, float gs, const QuantDest& d) {
+    if (!SORTED) {
+        g[r] = gs;
+        return;
+    }
+    for (int j = 0; j <= d.k; ++j) {
+        const int s = j < d.k ? __ldg(d.dst_slot + (size_t)r * d.k + j) : (d.shared_row0 >= 0 ? d.shared_row0 + r : -1);
+        if (s >= 0) g[s] = gs;
+    }
+}
+
+// LPR lanes per row of n (a multiple of 16) values, 256 / LPR rows per block:
+// four warps per row while rows are few, else one warp per row (half a warp
+// per row, which balances I = 768's 48 blocks at three per lane, measured
+// slower: 32.5 -> 36.3 us for h at Qwen3 NVFP4 m = 4096):
 //   g = amax(row) / 2688 (1 for an all-zero row), 2688 = 6 * 448;
 //   per 16-block: sb = e4m3(RNE, satfinite)(amax(block) / (6 g));
 //   code = e2m1(v / (decode(sb) * g)), 0 when that scale is 0.
 // Codes are packed two per byte, element 2j in the low nibble of byte j.
-template <typename T, int WPR>
+// d: where the results go (QuantDest).
+template <typename T, int LPR, bool SORTED>
 __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, int rows, int n,
                                                        uint8_t* __restrict__ q, uint8_t* __restrict__ sb,
-                                                       float* __restrict__ g) {
+                                                       float* __restrict__ g, QuantDest d) {
     pdl_wait();
     pdl_trigger();
-    constexpr int TPR = 32 * WPR;  // threads per row
+    constexpr int WPR = LPR >= 32 ? LPR / 32 : 1;  // warps per row
     __shared__ float wmax[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * (8 / WPR) + warp / WPR;
-    const int tr = (warp % WPR) * 32 + lane;  // thread index within the row
-    const bool live = r < rows;                // rows past the end still meet the barrier
+    const int r = blockIdx.x * (256 / LPR) + (LPR >= 32 ? warp / WPR : warp * (32 / LPR) + lane / LPR);
+    const int tr = LPR >= 32 ? (warp % WPR) * 32 + lane : lane % LPR;  // thread index within the row
+    const bool live = r < rows;  // rows past the end still take part in the reductions
     const int nb = n / 16;
     const T* row = v + (size_t)(live ? r : 0) * n;
     float am = 0.f;
-    for (int b = tr; live && b < nb; b += TPR) {
+    for (int b = tr; live && b < nb; b += LPR) {
         float f[16];
         load16(row + (size_t)b * 16, f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(f[i]));
     }
-    am = warp_max(am);
+#pragma unroll
+    for (int o = (LPR >= 32 ? 16 : LPR / 2); o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     if (WPR > 1) {
         if (lane == 0) wmax[warp] = am;
         __syncthreads();
@@ -425,9 +469,9 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
     }
     if (!live) return;
     const float gs = am > 0.f ? __fdiv_rn(am, 2688.0f) : 1.0f;
-    if (tr == 0) g[r] = gs;
+    if (tr == 0) put_row_scale<SORTED>(g, r, gs, d);
     const float six_g = __fmul_rn(6.0f, gs);
-    for (int b = tr; b < nb; b += TPR) {
+    for (int b = tr; b < nb; b += LPR) {
         float f[16];
         load16(row + (size_t)b * 16, f);
         float bm = 0.f;
@@ -441,61 +485,37 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
             lo = e2m1x8_quotient(f, scale, br);
             hi = e2m1x8_quotient(f + 8, scale, br);
         }
-        *reinterpret_cast<uint2*>(q + (size_t)r * (n / 2) + (size_t)b * 8) = make_uint2(lo, hi);
-        sb[(size_t)r * nb + b] = (uint8_t)sc;
+        put_block<SORTED>(q, sb, n, r, b, make_uint2(lo, hi), (uint8_t)sc, d);
     }
 }
 
 // rows up to this take four warps per row
 constexpr int kQuantFewRows = 1024;
 
-template <typename T>
-static void launch_act_quant_nvfp4(const T* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g, cudaStream_t st) {
+template <typename T, bool SORTED = false>
+static void launch_act_quant_nvfp4(const T* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g, QuantDest d,
+                                   cudaStream_t st) {
     if (rows <= kQuantFewRows)
-        launch_pdl(act_quant_nvfp4<T, 4>, dim3(ceil_div(rows, 2)), dim3(256), 0, st, v, rows, n, q, sb, g);
+        launch_pdl(act_quant_nvfp4<T, 128, SORTED>, dim3(ceil_div(rows, 2)), dim3(256), 0, st, v, rows, n, q, sb, g, d);
     else
-        launch_pdl(act_quant_nvfp4<T, 1>, dim3(ceil_div(rows, 8)), dim3(256), 0, st, v, rows, n, q, sb, g);
-}
-
-// Grouped-GEMM A operand of an NVFP4 layer: row s of the sorted order gets
-// token t's packed codes, block scales and row scale; one warp per row.
-__global__ __launch_bounds__(256) void gather_nvfp4(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xsb,
-                                                    const float* __restrict__ xg,
-                                                    const int32_t* __restrict__ sorted_pair, int k, int P, int rows,
-                                                    int H, uint8_t* __restrict__ xs, uint8_t* __restrict__ xs_sb,
-                                                    float* __restrict__ xs_g) {
-    pdl_wait();
-    pdl_trigger();
-    const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (s >= rows) return;
-    const int t = gather_token(sorted_pair, s, k, P);
-    if (t < 0) return;  // an unused slot: no tile reads a valid row from it
-    const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * (H / 2));
-    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * (H / 2));
-    for (int c = lane; c < H / 32; c += 32) dst[c] = __ldg(src + c);
-    const uint4* ssrc = reinterpret_cast<const uint4*>(xsb + (size_t)t * (H / 16));
-    uint4* sdst = reinterpret_cast<uint4*>(xs_sb + (size_t)s * (H / 16));
-    for (int c = lane; c < H / 256; c += 32) sdst[c] = __ldg(ssrc + c);
-    if (lane == 0) xs_g[s] = __ldg(xg + t);
-}
-
-cudaError_t launch_gather_nvfp4(const uint8_t* xq, const uint8_t* xsb, const float* xg, const int32_t* sorted_pair,
-                                int k, int P, int rows, int H, uint8_t* xs, uint8_t* xs_sb, float* xs_g,
-                                cudaStream_t st) {
-    launch_pdl(gather_nvfp4, dim3(ceil_div(rows, 8)), dim3(256), 0, st, xq, xsb, xg, sorted_pair, k, P, rows, H, xs,
-               xs_sb, xs_g);
-    return cudaGetLastError();
+        launch_pdl(act_quant_nvfp4<T, 32, SORTED>, dim3(ceil_div(rows, 8)), dim3(256), 0, st, v, rows, n, q, sb, g, d);
 }
 
 cudaError_t launch_act_quant_nvfp4_bf16(const uint16_t* x, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                         cudaStream_t st) {
-    launch_act_quant_nvfp4<uint16_t>(x, rows, n, q, sb, g, st);
+    launch_act_quant_nvfp4<uint16_t>(x, rows, n, q, sb, g, QuantDest{nullptr, 0, -1}, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant_nvfp4_sorted(const uint16_t* x, int m, int n, const int32_t* slot_of_pair, int k,
+                                          int shared_row0, uint8_t* q, uint8_t* sb, float* g, cudaStream_t st) {
+    launch_act_quant_nvfp4<uint16_t, true>(x, m, n, q, sb, g, QuantDest{slot_of_pair, k, shared_row0}, st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_act_quant_nvfp4_f32(const float* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                        cudaStream_t st) {
-    launch_act_quant_nvfp4<float>(v, rows, n, q, sb, g, st);
+    launch_act_quant_nvfp4<float>(v, rows, n, q, sb, g, QuantDest{nullptr, 0, -1}, st);
     return cudaGetLastError();
 }
 
