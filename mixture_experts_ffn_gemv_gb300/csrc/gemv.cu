@@ -806,15 +806,20 @@ cudaError_t launch_gemv_gateup_bf16(const GemvArgs& a, const uint16_t* x, uint16
     const bool nw = narrow(a, a.I, a.H, 32, true, 3);
     const int n_slices = a.I / (nw ? 16 : 32);
     const dim3 grid(n_slices * a.max_groups);
-    // steps in flight per thread (U): all eight of a narrow block's steps at
-    // H = 2048, four for two-tile blocks; eight-column blocks keep two, the
-    // most their registers allow (measured per shape at the Qwen3 decode
-    // sizes)
+    // steps in flight per thread (U): four (three blocks per SM) while the
+    // grid is a few waves, so that its last wave is not a short tail; eight
+    // (two blocks per SM) for two-tile grids of more than six blocks per SM.
+    // Sixteen-column blocks keep two, the most their registers allow.
+    // Measured at the Qwen3 decode sizes: m = 1 narrow U = 4 31.9 us against
+    // U = 8 32.8; m = 4 two-tile U = 4 57.8 against U = 8 59.2; m = 16
+    // two-tile U = 8 137.7 against U = 4 144.0.
     if (wide(a)) {
         if (nw) gu_launch<2, 1, 2>(a, grid, x, h, n_slices, st);
         else gu_launch<2, 2, 2>(a, grid, x, h, n_slices, st);
     } else if (nw) {
-        gu_launch<1, 1, 8>(a, grid, x, h, n_slices, st);
+        gu_launch<1, 1, 4>(a, grid, x, h, n_slices, st);
+    } else if ((int)grid.x > 6 * sm_count()) {
+        gu_launch<1, 2, 8>(a, grid, x, h, n_slices, st);
     } else {
         gu_launch<1, 2, 4>(a, grid, x, h, n_slices, st);
     }
