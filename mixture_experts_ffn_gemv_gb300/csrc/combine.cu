@@ -20,9 +20,10 @@ namespace moe {
 // rounded once) -- the shared expert added after an expert-parallel
 // all-reduce of the routed partial outputs.  The pairs' slots and weights are
 // read before the wait (see PairHead); early = 1 (the grid is one wave) lets
-// the next kernel be scheduled right away.
+// the next kernel be scheduled right away.  bf16 rows stay packed until
+// their sums, so 32 registers do and the SM holds 16 blocks.
 template <typename YT>
-__global__ __launch_bounds__(128, 8) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
+__global__ __launch_bounds__(128, sizeof(YT) == 2 ? 16 : 8) void combine(const YT* __restrict__ y, const int32_t* __restrict__ slot,
                                                const float* __restrict__ w, int k, int H, int P, int has_shared,
                                                const float* __restrict__ shared_g, uint16_t* __restrict__ out,
                                                int accumulate, int early) {

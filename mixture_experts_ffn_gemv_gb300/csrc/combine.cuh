@@ -64,6 +64,29 @@ __device__ __forceinline__ void add_pairs8(const YT* __restrict__ y, const int (
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], v[u][i], acc[i]);
 }
+// bf16 rows: the eight rows stay packed (4 registers each) until their sums,
+// in the same order as above.
+template <>
+__device__ __forceinline__ void add_pairs8<uint16_t>(const uint16_t* __restrict__ y, const int (&sl)[8],
+                                                     const float (&w8)[8], int H, int P, int h0, float (&acc)[8]) {
+    float wj[8];
+    uint4 raw[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const bool in = sl[u] >= 0 && sl[u] < P;
+        wj[u] = in ? w8[u] : 0.f;
+        raw[u] = in ? __ldg(reinterpret_cast<const uint4*>(y + (size_t)sl[u] * H + h0)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(wj[u], bf16lo(w[i]), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wj[u], bf16hi(w[i]), acc[2 * i + 1]);
+        }
+    }
+}
 
 // acc[i] = out[t, h0 + i] in fp32 before rounding, i < 8: the k pairs' rows in
 // ascending j (the first 8 from ph, the rest 8 at a time), then the shared
