@@ -204,6 +204,22 @@ __device__ __forceinline__ int gather_token(const int32_t* sorted_pair, int s, i
     return (p >= 0 && p < P) ? p / k : -1;
 }
 
+// A warp copies n16 16-byte chunks from src to dst; each lane loads four
+// chunks (c, c + 32, ...) before it stores any.  (Eight made the bf16 gather
+// slower: 26.7 -> 32.7 us at Qwen3 m = 4096.)
+__device__ __forceinline__ void warp_copy16(uint4* __restrict__ dst, const uint4* __restrict__ src, int n16,
+                                            int lane) {
+    for (int c0 = lane; c0 < n16; c0 += 128) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + 32 * u < n16) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+    }
+}
+
 // Row s of the grouped-GEMM input: token sorted_pair[s] / k for s < P (routed
 // pairs), token s - P for the shared expert's rows.  One warp per row.
 __global__ __launch_bounds__(256) void gather_bf16(const uint16_t* __restrict__ x,
@@ -215,18 +231,8 @@ __global__ __launch_bounds__(256) void gather_bf16(const uint16_t* __restrict__ 
     if (s >= rows) return;
     const int t = gather_token(sorted_pair, s, k, P);
     if (t < 0) return;  // an unused slot: no tile reads a valid row from it
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
-    // four 16-byte chunks per lane loaded before any is stored
-    for (int c0 = lane; c0 < H / 8; c0 += 128) {
-        uint4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (c0 + 32 * u < H / 8) v[u] = __ldg(src + c0 + 32 * u);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (c0 + 32 * u < H / 8) dst[c0 + 32 * u] = v[u];
-    }
+    warp_copy16(reinterpret_cast<uint4*>(xs + (size_t)s * H), reinterpret_cast<const uint4*>(x + (size_t)t * H), H / 8,
+                lane);
 }
 
 __global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq, const float* __restrict__ xsc,
@@ -238,9 +244,8 @@ __global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq
     if (s >= rows) return;
     const int t = gather_token(sorted_pair, s, k, P);
     if (t < 0) return;  // an unused slot: no tile reads a valid row from it
-    const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * H);
-    uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)s * H);
-    for (int c = lane; c < H / 16; c += 32) dst[c] = __ldg(src + c);
+    warp_copy16(reinterpret_cast<uint4*>(xs + (size_t)s * H), reinterpret_cast<const uint4*>(xq + (size_t)t * H), H / 16,
+                lane);
     const int nb = H / 128;
     for (int b = lane; b < nb; b += 32) xs_sc[(size_t)s * nb + b] = xsc[(size_t)t * nb + b];
 }
