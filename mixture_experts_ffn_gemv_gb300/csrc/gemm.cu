@@ -296,14 +296,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 // copies signal it); the MMA commits are multicast to both CTAs' empty and
 // accumulator-full barriers; both CTAs' epilogue warps arrive on the
 // leader's accumulator-empty barrier.  Every wait is bounded as above.
-constexpr int P_STAGES = 6;
+// The ring takes 7 stages when the group tables (three of E + 2 ints) leave
+// room for them, else 6: the operand fetch rate per SM grows with the bytes in
+// flight.
 constexpr int P_A_BYTES = BM * BK * 2;   // this CTA's 128 token rows
 constexpr int P_B_BYTES = 128 * BK * 2;  // this CTA's half of the 256 weight rows
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_TABLE_INTS = 3 * (kMaxExperts + 2);
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + 256 + P_TABLE_INTS * 4;
-static_assert(P_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+constexpr int P_SMEM_MAX = 227 * 1024;
+__host__ __device__ constexpr int pair_smem_bytes(int stages, int E) {
+    return 1024 + stages * P_STAGE_BYTES + 256 + 3 * (E + 2) * 4;
+}
+static_assert(pair_smem_bytes(6, kMaxExperts) <= P_SMEM_MAX, "shared memory per CTA");
 
+template <int P_STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_bf16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
@@ -321,8 +326,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * P_STAGES + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_tile = reinterpret_cast<int*>(smem + P_STAGES * P_STAGE_BYTES + 256);
-    int* s_group = s_tile + (kMaxExperts + 2);
-    int* s_pair = s_group + (kMaxExperts + 2);  // pair counts, then their exclusive prefix
+    int* s_group = s_tile + (p.E + 2);
+    int* s_pair = s_group + (p.E + 2);  // pair counts, then their exclusive prefix
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -623,17 +628,21 @@ bool use_pairs(const GemmCall& g) {
 }
 
 cudaError_t launch_pair_gateup(const GemmLaunch& L, cudaStream_t st) {
-    static cudaError_t attr = cudaFuncSetAttribute(grouped_gemm_bf16_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   P_SMEM_BYTES);
-    if (attr != cudaSuccess) return attr;
+    static cudaError_t attr6 = cudaFuncSetAttribute(grouped_gemm_bf16_pair<6>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_MAX);
+    static cudaError_t attr7 = cudaFuncSetAttribute(grouped_gemm_bf16_pair<7>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_MAX);
+    if (attr6 != cudaSuccess) return attr6;
+    if (attr7 != cudaSuccess) return attr7;
     const GemmCall& g = L.call;
+    const bool seven = pair_smem_bytes(7, g.E) <= P_SMEM_MAX;
     GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.I / 128, g.H / BK, g.I, 128,
                  static_cast<uint16_t*>(g.h), g.wait_ns, g.stall_test};
     const int pairs = std::max(1, std::min(num_sms() / 2, g.max_tiles * p.n_tiles));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    cfg.dynamicSmemBytes = pair_smem_bytes(seven ? 7 : 6, g.E);
     cfg.stream = st;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -645,7 +654,8 @@ cudaError_t launch_pair_gateup(const GemmLaunch& L, cudaStream_t st) {
     cfg.attrs = at;
     cfg.numAttrs = 2;
     const GemmWeights& w = *L.w;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
+    return seven ? cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<7>, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p)
+                 : cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<6>, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
 }
 
 cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {

@@ -44,14 +44,24 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
     const int c = blockIdx.x;
     const int p0 = c * kPermChunk, p1 = min(P, p0 + kPermChunk);
     for (int e = tid; e < E; e += 256) hist[e] = 0;
+    // the thread's ids, all loaded before any is counted: one memory round
+    // trip instead of one per id
+    int idv[kPermChunk / 256];
+#pragma unroll
+    for (int u = 0; u < kPermChunk / 256; ++u) {
+        const int p = p0 + tid + 256 * u;
+        idv[u] = p < p1 ? ids[p] : 0;
+    }
     __syncthreads();
-    for (int p = p0 + tid; p < p1; p += 256) {
-        const int id = ids[p];
-        if (id < 0 || id >= E_total) {
+#pragma unroll
+    for (int u = 0; u < kPermChunk / 256; ++u) {
+        const int p = p0 + tid + 256 * u;
+        if (p >= p1) continue;
+        if (idv[u] < 0 || idv[u] >= E_total) {
             set_error(hdr, DEV_ERR_BAD_ID, p);
             continue;
         }
-        const int e = local_expert(id, e_lo, E, E_total);
+        const int e = local_expert(idv[u], e_lo, E, E_total);
         if (e >= 0) atomicAdd(&hist[e], 1);
     }
     __syncthreads();
@@ -133,15 +143,21 @@ __global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict
     const int p0 = c * kPermChunk + warp * (kPermChunk / 8);
     const int p1 = min(P, p0 + kPermChunk / 8);
     for (int i = tid; i < 8 * E; i += 256) wbase[i] = 0;
+    // the lane's experts for both passes, all loaded up front (one memory
+    // round trip instead of one per 32 pairs)
+    constexpr int PL = kPermChunk / 8 / 32;  // pairs per lane
+    int ev[PL];
+#pragma unroll
+    for (int u = 0; u < PL; ++u) {
+        const int p = p0 + 32 * u + lane;
+        ev[u] = p < p1 ? local_expert(ids[p], e_lo, E, E_total) : -1;
+    }
     __syncthreads();
     const unsigned lt = (1u << lane) - 1u;
     int* mine = wbase + warp * E;
-    for (int pb = p0; pb < p0 + kPermChunk / 8; pb += 32) {
-        const int p = pb + lane;
-        int e = -1;
-        if (p < p1) {
-            e = local_expert(ids[p], e_lo, E, E_total);
-        }
+#pragma unroll
+    for (int u = 0; u < PL; ++u) {
+        const int e = ev[u];
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
         __syncwarp();
@@ -156,12 +172,10 @@ __global__ __launch_bounds__(256) void permute_scatter(const int32_t* __restrict
         }
     }
     __syncthreads();
-    for (int pb = p0; pb < p0 + kPermChunk / 8; pb += 32) {
-        const int p = pb + lane;
-        int e = -1;
-        if (p < p1) {
-            e = local_expert(ids[p], e_lo, E, E_total);
-        }
+#pragma unroll
+    for (int u = 0; u < PL; ++u) {
+        const int p = p0 + 32 * u + lane;
+        const int e = ev[u];
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0) {
             const int slot = mine[e] + __popc(peers & lt);
