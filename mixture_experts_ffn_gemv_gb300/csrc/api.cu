@@ -328,12 +328,15 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     const int E = L->E_local, k = lo.k, H = c.hidden, I = c.inter;
     WsHeader* hdr = at<WsHeader>(ws, lo.hdr);
     const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
-    if (!permuted) {
-        MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->e_lo, c.num_experts, lo.shared, po, hdr, st));
-        MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(ids, m, k, E, L->e_lo, c.num_experts, po, st));
-    }
     if (arm == MOE_ARM_AUTO) arm = lo.k == 0 ? (m <= 64 || !gemm_supported(c) ? MOE_ARM_GEMV : MOE_ARM_GEMM)
                                              : moe_select_arm(L, m);
+    // the bf16 / fp8 grouped-GEMM arms place the pairs in their gather
+    const bool place_in_gather = !permuted && arm == MOE_ARM_GEMM && !L->nvfp4 && gemm_supported(c);
+    if (!permuted) {
+        MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->e_lo, c.num_experts, lo.shared, po, hdr, st));
+        if (!place_in_gather)
+            MOE_LAUNCH(K_PERMUTE_SCATTER, launch_permute_scatter(ids, m, k, E, L->e_lo, c.num_experts, po, st));
+    }
     const int has_shared = lo.shared;
     // the shared expert's sigmoid gate per token (forward_prefill step 8), or
     // null: weight 1
@@ -416,15 +419,24 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
         float* xsc = at<float>(ws, lo.xsc);
         if (!x_quantized)
             MOE_LAUNCH(K_ACT_QUANT, launch_act_quant_fp8(static_cast<const uint16_t*>(x), m, H, xq, xsc, st));
-        MOE_LAUNCH(K_GATHER, launch_gather_fp8(xq, xsc, po.sorted_pair, k, lo.P, lo.rows, H, at<uint8_t>(ws, lo.xs),
-                                     at<float>(ws, lo.xs_sc), st));
+        if (place_in_gather)
+            MOE_LAUNCH(K_GATHER, launch_gather_pairs_fp8(xq, xsc, ids, L->e_lo, E, c.num_experts, k, lo.P, lo.rows, H,
+                                                         po, at<uint8_t>(ws, lo.xs), at<float>(ws, lo.xs_sc), st));
+        else
+            MOE_LAUNCH(K_GATHER, launch_gather_fp8(xq, xsc, po.sorted_pair, k, lo.P, lo.rows, H,
+                                                   at<uint8_t>(ws, lo.xs), at<float>(ws, lo.xs_sc), st));
         g.xs = at<void>(ws, lo.xs);
         g.xs_sc = at<float>(ws, lo.xs_sc);
         g.h = at<void>(ws, lo.h);
         g.hsc = at<float>(ws, lo.hsc);
     } else {
-        MOE_LAUNCH(K_GATHER, launch_gather_bf16(static_cast<const uint16_t*>(x), po.sorted_pair, k, lo.P, lo.rows, H,
-                                      at<uint16_t>(ws, lo.xs), st));
+        if (place_in_gather)
+            MOE_LAUNCH(K_GATHER, launch_gather_pairs_bf16(static_cast<const uint16_t*>(x), ids, L->e_lo, E,
+                                                          c.num_experts, k, lo.P, lo.rows, H, po,
+                                                          at<uint16_t>(ws, lo.xs), st));
+        else
+            MOE_LAUNCH(K_GATHER, launch_gather_bf16(static_cast<const uint16_t*>(x), po.sorted_pair, k, lo.P, lo.rows,
+                                                    H, at<uint16_t>(ws, lo.xs), st));
         g.xs = at<void>(ws, lo.xs);
         g.h = at<void>(ws, lo.h);
     }

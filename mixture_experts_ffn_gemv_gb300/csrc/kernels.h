@@ -74,6 +74,13 @@ cudaError_t launch_route_permute_small(const uint16_t* x, int m, int H, const fl
 cudaError_t launch_act_quant_fp8(const uint16_t* x, int m, int H, uint8_t* xq, float* xs, cudaStream_t st);
 // the same 1x128 quantisation of fp32 rows (the GEMV arm's h)
 cudaError_t launch_quant_rows_fp8(const float* v, int rows, int n, uint8_t* q, float* s, cudaStream_t st);
+// gathers that also place each pair (the bf16 / fp8 grouped-GEMM arms, after
+// permute_count alone)
+cudaError_t launch_gather_pairs_bf16(const uint16_t* x, const int32_t* ids, int e_lo, int E, int E_total, int k,
+                                     int P, int rows, int H, const PermuteOut& o, uint16_t* xs, cudaStream_t st);
+cudaError_t launch_gather_pairs_fp8(const uint8_t* xq, const float* xsc, const int32_t* ids, int e_lo, int E,
+                                    int E_total, int k, int P, int rows, int H, const PermuteOut& o, uint8_t* xs,
+                                    float* xs_sc, cudaStream_t st);
 cudaError_t launch_gather_bf16(const uint16_t* x, const int32_t* sorted_pair, int k, int P, int rows, int H,
                                uint16_t* xs, cudaStream_t st);
 cudaError_t launch_gather_fp8(const uint8_t* xq, const float* xsc, const int32_t* sorted_pair, int k, int P,

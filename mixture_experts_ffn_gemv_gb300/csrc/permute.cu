@@ -11,6 +11,11 @@
 //                   the grouped GEMM's m-tile starts;
 //   permute_scatter per chunk, warp-level ranks (match_any) give each pair
 //                   its slot: pairs keep ascending order within an expert.
+// The bf16 and fp8 grouped-GEMM arms skip permute_scatter: their gather runs
+// one warp per pair and places it itself, at its expert's offset + its
+// chunk's base + its rank within the chunk, which permute_count leaves in
+// slot_of_pair (the order of a chunk's pairs within an expert then follows
+// the shared-memory atomics; every slot is still used once).
 // Plus the activation gathers for the grouped GEMM, the fp8 activation
 // quantiser (one e4m3 code + fp32 scale per 128 inputs) and the NVFP4 one.
 #include <algorithm>
@@ -59,10 +64,12 @@ __global__ __launch_bounds__(256) void permute_count(const int32_t* __restrict__
         if (p >= p1) continue;
         if (idv[u] < 0 || idv[u] >= E_total) {
             set_error(hdr, DEV_ERR_BAD_ID, p);
+            o.slot_of_pair[p] = -1;
             continue;
         }
         const int e = local_expert(idv[u], e_lo, E, E_total);
-        if (e >= 0) atomicAdd(&hist[e], 1);
+        // the pair's rank within the chunk's pairs of its expert (-1: dropped)
+        o.slot_of_pair[p] = e >= 0 ? atomicAdd(&hist[e], 1) : -1;
     }
     __syncthreads();
     for (int e = tid; e < E; e += 256) o.chunk_base[(size_t)c * E + e] = hist[e];
@@ -262,6 +269,79 @@ __global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq
                 lane);
     const int nb = H / 128;
     for (int b = lane; b < nb; b += 32) xs_sc[(size_t)s * nb + b] = xsc[(size_t)t * nb + b];
+}
+
+// The scatter and the gather in one pass (bf16 and fp8 grouped-GEMM arms):
+// warp w < P places pair w -- slot = its expert's first sorted row + its
+// chunk's base within the expert + its rank within the chunk, the rank from
+// permute_count's slot_of_pair -- records the slot both ways and copies its
+// token's row there; warps P.. copy the shared expert's rows (slot P + t).
+// Returns the slot and token, or -1 for a dropped pair.
+__device__ __forceinline__ int place_pair(const int32_t* __restrict__ ids, int e_lo, int E, int E_total, int k, int P,
+                                          const PermuteOut& o, int w, int lane, int* t) {
+    if (w >= P) {
+        *t = w - P;
+        return w;
+    }
+    int s = -1;
+    if (lane == 0) {
+        const int r = o.slot_of_pair[w];
+        if (r >= 0) {
+            const int e = local_expert(ids[w], e_lo, E, E_total);
+            s = o.grp_off[e] + o.chunk_base[(size_t)(w / kPermChunk) * E + e] + r;
+            o.sorted_pair[s] = w;
+            o.slot_of_pair[w] = s;
+        }
+    }
+    *t = w / k;
+    return __shfl_sync(0xffffffffu, s, 0);
+}
+
+__global__ __launch_bounds__(256) void gather_pairs_bf16(const uint16_t* __restrict__ x,
+                                                         const int32_t* __restrict__ ids, int e_lo, int E,
+                                                         int E_total, int k, int P, int rows, int H, PermuteOut o,
+                                                         uint16_t* __restrict__ xs) {
+    pdl_wait();
+    pdl_trigger();
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= rows) return;
+    int t;
+    const int s = place_pair(ids, e_lo, E, E_total, k, P, o, w, lane, &t);
+    if (s < 0) return;
+    warp_copy16(reinterpret_cast<uint4*>(xs + (size_t)s * H), reinterpret_cast<const uint4*>(x + (size_t)t * H), H / 8,
+                lane);
+}
+
+__global__ __launch_bounds__(256) void gather_pairs_fp8(const uint8_t* __restrict__ xq, const float* __restrict__ xsc,
+                                                        const int32_t* __restrict__ ids, int e_lo, int E,
+                                                        int E_total, int k, int P, int rows, int H, PermuteOut o,
+                                                        uint8_t* __restrict__ xs, float* __restrict__ xs_sc) {
+    pdl_wait();
+    pdl_trigger();
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= rows) return;
+    int t;
+    const int s = place_pair(ids, e_lo, E, E_total, k, P, o, w, lane, &t);
+    if (s < 0) return;
+    warp_copy16(reinterpret_cast<uint4*>(xs + (size_t)s * H), reinterpret_cast<const uint4*>(xq + (size_t)t * H), H / 16,
+                lane);
+    const int nb = H / 128;
+    for (int b = lane; b < nb; b += 32) xs_sc[(size_t)s * nb + b] = xsc[(size_t)t * nb + b];
+}
+
+cudaError_t launch_gather_pairs_bf16(const uint16_t* x, const int32_t* ids, int e_lo, int E, int E_total, int k,
+                                     int P, int rows, int H, const PermuteOut& o, uint16_t* xs, cudaStream_t st) {
+    launch_pdl(gather_pairs_bf16, dim3(ceil_div(rows, 8)), dim3(256), 0, st, x, ids, e_lo, E, E_total, k, P, rows, H,
+               o, xs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_pairs_fp8(const uint8_t* xq, const float* xsc, const int32_t* ids, int e_lo, int E,
+                                    int E_total, int k, int P, int rows, int H, const PermuteOut& o, uint8_t* xs,
+                                    float* xs_sc, cudaStream_t st) {
+    launch_pdl(gather_pairs_fp8, dim3(ceil_div(rows, 8)), dim3(256), 0, st, xq, xsc, ids, e_lo, E, E_total, k, P,
+               rows, H, o, xs, xs_sc);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gather_bf16(const uint16_t* x, const int32_t* sorted_pair, int k, int P, int rows, int H,

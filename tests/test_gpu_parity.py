@@ -675,8 +675,13 @@ def test_bad_expert_id_sets_device_flag(cuda, oracle_mod, arm):
     assert layer.device_status() == 0  # the next call starts clean
 
 
+# The grouped-GEMM arm's gather places a chunk's pairs of one expert in the
+# order of shared-memory atomics, so its sorted rows may differ from call to
+# call; the bf16 (qwen3_prefill) and fp8 (deepseek_v3_fp8 at m = 256) cases
+# check that the output does not.
 @pytest.mark.parametrize("wl_name,m", [("tiny", 16), ("qwen3_decode", 16), ("qwen3_decode", 1),
-                                       ("deepseek_v3_fp8", 1), ("qwen3_nvfp4", 16)])
+                                       ("deepseek_v3_fp8", 1), ("qwen3_nvfp4", 16), ("qwen3_prefill", 4096),
+                                       ("deepseek_v3_fp8", 256)])
 def test_deterministic_and_graph_capturable(cuda, wl_name, m):
     wl = I.WORKLOADS[wl_name]
     tensors, layer = layer_for(wl, cuda)
