@@ -330,8 +330,9 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     const PermuteOut po = permute_out(lo, ws, nullptr, nullptr, nullptr);
     if (arm == MOE_ARM_AUTO) arm = lo.k == 0 ? (m <= 64 || !gemm_supported(c) ? MOE_ARM_GEMV : MOE_ARM_GEMM)
                                              : moe_select_arm(L, m);
-    // the bf16 / fp8 grouped-GEMM arms place the pairs in their gather
-    const bool place_in_gather = !permuted && arm == MOE_ARM_GEMM && !L->nvfp4 && gemm_supported(c);
+    // the grouped-GEMM arms place the pairs in their gather (NVFP4: in the
+    // quantiser that writes the sorted rows)
+    const bool place_in_gather = !permuted && arm == MOE_ARM_GEMM && gemm_supported(c);
     if (!permuted) {
         MOE_LAUNCH(K_PERMUTE_COUNT, launch_permute_count(ids, m, k, E, L->e_lo, c.num_experts, lo.shared, po, hdr, st));
         if (!place_in_gather)
@@ -403,10 +404,17 @@ int run_experts(const moe_layer* L, const Layout& lo, const void* x, int m, cons
     if (L->nvfp4) {
         // x to NVFP4, straight into the sorted rows (the A operand): each
         // token's codes, scales and row scale go to its pairs' slots
-        MOE_LAUNCH(K_ACT_QUANT_NVFP4,
-                   launch_act_quant_nvfp4_sorted(static_cast<const uint16_t*>(x), m, H, po.slot_of_pair, k,
-                                                 has_shared ? lo.P : -1, at<uint8_t>(ws, lo.xs),
-                                                 at<uint8_t>(ws, lo.xs_sb), at<float>(ws, lo.xs_g), st));
+        if (place_in_gather)
+            MOE_LAUNCH(K_ACT_QUANT_NVFP4,
+                       launch_act_quant_nvfp4_place(static_cast<const uint16_t*>(x), m, H, ids, L->e_lo, E,
+                                                    c.num_experts, k, has_shared ? lo.P : -1, po,
+                                                    at<uint8_t>(ws, lo.xs), at<uint8_t>(ws, lo.xs_sb),
+                                                    at<float>(ws, lo.xs_g), st));
+        else
+            MOE_LAUNCH(K_ACT_QUANT_NVFP4,
+                       launch_act_quant_nvfp4_sorted(static_cast<const uint16_t*>(x), m, H, po.slot_of_pair, k,
+                                                     has_shared ? lo.P : -1, at<uint8_t>(ws, lo.xs),
+                                                     at<uint8_t>(ws, lo.xs_sb), at<float>(ws, lo.xs_g), st));
         g.xs = at<void>(ws, lo.xs);
         g.xs_sb = at<uint8_t>(ws, lo.xs_sb);
         g.xs_g = at<float>(ws, lo.xs_g);

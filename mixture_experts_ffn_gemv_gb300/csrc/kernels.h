@@ -122,6 +122,11 @@ cudaError_t launch_act_quant_nvfp4_bf16(const uint16_t* x, int rows, int n, uint
 // pairs skipped) and, when shared_row0 >= 0, to row shared_row0 + t.
 cudaError_t launch_act_quant_nvfp4_sorted(const uint16_t* x, int m, int n, const int32_t* slot_of_pair, int k,
                                           int shared_row0, uint8_t* q, uint8_t* sb, float* g, cudaStream_t st);
+// the same, placing each pair itself from permute_count's ranks (the NVFP4
+// grouped-GEMM arm, which then skips permute_scatter)
+cudaError_t launch_act_quant_nvfp4_place(const uint16_t* x, int m, int n, const int32_t* ids, int e_lo, int E,
+                                         int E_total, int k, int shared_row0, const PermuteOut& o, uint8_t* q,
+                                         uint8_t* sb, float* g, cudaStream_t st);
 // the same for fp32 rows (h), which both arms' down projections take as A
 cudaError_t launch_act_quant_nvfp4_f32(const float* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                        cudaStream_t st);

@@ -271,6 +271,20 @@ __global__ __launch_bounds__(256) void gather_fp8(const uint8_t* __restrict__ xq
     for (int b = lane; b < nb; b += 32) xs_sc[(size_t)s * nb + b] = xsc[(size_t)t * nb + b];
 }
 
+// Slot of pair p from permute_count's rank (in o.slot_of_pair): its expert's
+// first sorted row + its chunk's base within the expert + the rank; recorded
+// in o.sorted_pair and o.slot_of_pair.  -1 for a dropped pair.
+__device__ __forceinline__ int pair_slot(const int32_t* __restrict__ ids, int e_lo, int E, int E_total,
+                                         const PermuteOut& o, int p) {
+    const int r = o.slot_of_pair[p];
+    if (r < 0) return -1;
+    const int e = local_expert(ids[p], e_lo, E, E_total);
+    const int s = o.grp_off[e] + o.chunk_base[(size_t)(p / kPermChunk) * E + e] + r;
+    o.sorted_pair[s] = p;
+    o.slot_of_pair[p] = s;
+    return s;
+}
+
 // The scatter and the gather in one pass (bf16 and fp8 grouped-GEMM arms):
 // warp w < P places pair w -- slot = its expert's first sorted row + its
 // chunk's base within the expert + its rank within the chunk, the rank from
@@ -283,16 +297,7 @@ __device__ __forceinline__ int place_pair(const int32_t* __restrict__ ids, int e
         *t = w - P;
         return w;
     }
-    int s = -1;
-    if (lane == 0) {
-        const int r = o.slot_of_pair[w];
-        if (r >= 0) {
-            const int e = local_expert(ids[w], e_lo, E, E_total);
-            s = o.grp_off[e] + o.chunk_base[(size_t)(w / kPermChunk) * E + e] + r;
-            o.sorted_pair[s] = w;
-            o.slot_of_pair[w] = s;
-        }
-    }
+    const int s = lane == 0 ? pair_slot(ids, e_lo, E, E_total, o, w) : 0;
     *t = w / k;
     return __shfl_sync(0xffffffffu, s, 0);
 }
@@ -495,13 +500,25 @@ struct QuantDest {
     const int32_t* dst_slot;
     int k;
     int shared_row0;
+    // placing (ids non-null): dst_slot holds permute_count's ranks and the
+    // quantiser places each pair itself (pair_slot), recording the slot in
+    // o.sorted_pair / o.slot_of_pair
+    const int32_t* ids;
+    int e_lo, E, E_total;
+    PermuteOut o;
 };
 
 // One row's NVFP4 codes of block b (two words) and its scale code, to every
 // destination row (SORTED: the pairs' sorted rows; else row r).
+// Destination j <= k of row r: pair j's sorted row (from the row's placed
+// slots in shared memory, or dst_slot), then the shared expert's row.
+__device__ __forceinline__ int dest_row(const QuantDest& d, const int* placed, int r, int j) {
+    if (j == d.k) return d.shared_row0 >= 0 ? d.shared_row0 + r : -1;
+    return placed ? placed[j] : __ldg(d.dst_slot + (size_t)r * d.k + j);
+}
 template <bool SORTED>
 __device__ __forceinline__ void put_block(uint8_t* q, uint8_t* sb, int n, int r, int b, uint2 codes, uint8_t sc,
-                                          const QuantDest& d) {
+                                          const QuantDest& d, const int* placed) {
     const int nb = n / 16;
     if (!SORTED) {
         *reinterpret_cast<uint2*>(q + (size_t)r * (n / 2) + (size_t)b * 8) = codes;
@@ -509,20 +526,20 @@ __device__ __forceinline__ void put_block(uint8_t* q, uint8_t* sb, int n, int r,
         return;
     }
     for (int j = 0; j <= d.k; ++j) {
-        const int s = j < d.k ? __ldg(d.dst_slot + (size_t)r * d.k + j) : (d.shared_row0 >= 0 ? d.shared_row0 + r : -1);
+        const int s = dest_row(d, placed, r, j);
         if (s < 0) continue;
         *reinterpret_cast<uint2*>(q + (size_t)s * (n / 2) + (size_t)b * 8) = codes;
         sb[(size_t)s * nb + b] = sc;
     }
 }
 template <bool SORTED>
-__device__ __forceinline__ void put_row_scale(float* g, int r, float gs, const QuantDest& d) {
+__device__ __forceinline__ void put_row_scale(float* g, int r, float gs, const QuantDest& d, const int* placed) {
     if (!SORTED) {
         g[r] = gs;
         return;
     }
     for (int j = 0; j <= d.k; ++j) {
-        const int s = j < d.k ? __ldg(d.dst_slot + (size_t)r * d.k + j) : (d.shared_row0 >= 0 ? d.shared_row0 + r : -1);
+        const int s = dest_row(d, placed, r, j);
         if (s >= 0) g[s] = gs;
     }
 }
@@ -545,16 +562,25 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
     pdl_wait();
     pdl_trigger();
     constexpr int WPR = LPR >= 32 ? LPR / 32 : 1;  // warps per row
+    static_assert(LPR >= 32, "a row's threads are whole warps");
     __shared__ float wmax[8];
+    __shared__ int s_placed[256 / LPR][kMaxTopK];  // placing: the slots of each row's pairs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x * (256 / LPR) + (LPR >= 32 ? warp / WPR : warp * (32 / LPR) + lane / LPR);
-    const int tr = LPR >= 32 ? (warp % WPR) * 32 + lane : lane % LPR;  // thread index within the row
+    const int rb = warp / WPR;  // the row's index within the block
+    const int r = blockIdx.x * (256 / LPR) + rb;
+    const int tr = (warp % WPR) * 32 + lane;  // thread index within the row
     const bool live = r < rows;  // rows past the end still take part in the reductions
     const int nb = n / 16;
     const T* row = v + (size_t)(live ? r : 0) * n;
     constexpr int NR = RB > 0 ? RB : 1;
     float fr[NR][16];
     float am = 0.f;
+    // placing: the slots of the row's pairs (their loads overlap the row's;
+    // the barrier below publishes them to the row's other warps)
+    const bool placing = SORTED && d.ids;
+    auto place = [&]() {
+        if (placing && live && tr < d.k) s_placed[rb][tr] = pair_slot(d.ids, d.e_lo, d.E, d.E_total, d.o, r * d.k + tr);
+    };
     if (RB > 0) {
 #pragma unroll
         for (int k = 0; k < NR; ++k) {
@@ -566,11 +592,13 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
                 for (int i = 0; i < 16; ++i) fr[k][i] = 0.f;
             }
         }
+        place();
 #pragma unroll
         for (int k = 0; k < NR; ++k)
 #pragma unroll
             for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(fr[k][i]));
     } else {
+        place();
         for (int b = tr; live && b < nb; b += LPR) {
             float f[16];
             load16(row + (size_t)b * 16, f);
@@ -579,17 +607,20 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
         }
     }
 #pragma unroll
-    for (int o = (LPR >= 32 ? 16 : LPR / 2); o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     if (WPR > 1) {
         if (lane == 0) wmax[warp] = am;
         __syncthreads();
         const int w0 = (warp / WPR) * WPR;
 #pragma unroll
         for (int i = 0; i < WPR; ++i) am = fmaxf(am, wmax[w0 + i]);
+    } else if (placing) {
+        __syncwarp();
     }
     if (!live) return;
+    const int* placed = placing ? s_placed[rb] : nullptr;
     const float gs = am > 0.f ? __fdiv_rn(am, 2688.0f) : 1.0f;
-    if (tr == 0) put_row_scale<SORTED>(g, r, gs, d);
+    if (tr == 0) put_row_scale<SORTED>(g, r, gs, d, placed);
     const float six_g = __fmul_rn(6.0f, gs);
     auto block_codes = [&](int b, const float (&f)[16]) {
         float bm = 0.f;
@@ -603,7 +634,7 @@ __global__ __launch_bounds__(256) void act_quant_nvfp4(const T* __restrict__ v, 
             lo = e2m1x8_quotient(f, scale, br);
             hi = e2m1x8_quotient(f + 8, scale, br);
         }
-        put_block<SORTED>(q, sb, n, r, b, make_uint2(lo, hi), (uint8_t)sc, d);
+        put_block<SORTED>(q, sb, n, r, b, make_uint2(lo, hi), (uint8_t)sc, d, placed);
     };
     if (RB > 0) {
 #pragma unroll
@@ -647,19 +678,28 @@ static void launch_act_quant_nvfp4(const T* v, int rows, int n, uint8_t* q, uint
 
 cudaError_t launch_act_quant_nvfp4_bf16(const uint16_t* x, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                         cudaStream_t st) {
-    launch_act_quant_nvfp4<uint16_t>(x, rows, n, q, sb, g, QuantDest{nullptr, 0, -1}, st);
+    launch_act_quant_nvfp4<uint16_t>(x, rows, n, q, sb, g, QuantDest{nullptr, 0, -1, nullptr, 0, 0, 0, PermuteOut{}}, st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_act_quant_nvfp4_sorted(const uint16_t* x, int m, int n, const int32_t* slot_of_pair, int k,
                                           int shared_row0, uint8_t* q, uint8_t* sb, float* g, cudaStream_t st) {
-    launch_act_quant_nvfp4<uint16_t, true>(x, m, n, q, sb, g, QuantDest{slot_of_pair, k, shared_row0}, st);
+    launch_act_quant_nvfp4<uint16_t, true>(x, m, n, q, sb, g,
+                                           QuantDest{slot_of_pair, k, shared_row0, nullptr, 0, 0, 0, PermuteOut{}}, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant_nvfp4_place(const uint16_t* x, int m, int n, const int32_t* ids, int e_lo, int E,
+                                         int E_total, int k, int shared_row0, const PermuteOut& o, uint8_t* q,
+                                         uint8_t* sb, float* g, cudaStream_t st) {
+    launch_act_quant_nvfp4<uint16_t, true>(x, m, n, q, sb, g,
+                                           QuantDest{o.slot_of_pair, k, shared_row0, ids, e_lo, E, E_total, o}, st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_act_quant_nvfp4_f32(const float* v, int rows, int n, uint8_t* q, uint8_t* sb, float* g,
                                        cudaStream_t st) {
-    launch_act_quant_nvfp4<float>(v, rows, n, q, sb, g, QuantDest{nullptr, 0, -1}, st);
+    launch_act_quant_nvfp4<float>(v, rows, n, q, sb, g, QuantDest{nullptr, 0, -1, nullptr, 0, 0, 0, PermuteOut{}}, st);
     return cudaGetLastError();
 }
 
