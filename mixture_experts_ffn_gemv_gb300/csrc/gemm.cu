@@ -284,13 +284,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------- CTA pairs
-// The bf16 gate/up GEMM on pairs of CTAs (a cluster of two, tcgen05
-// cta_group::2): a work item is 256 sorted rows of one group (the two CTAs'
-// 128-row m-tiles 2j and 2j+1) times one n-tile.  Each CTA loads its own 128
-// token rows and half of the 256 weight rows (the leader the 128 rows of W1,
-// the peer the same rows of W3), the leader issues M = 256, N = 256 MMAs and
-// each CTA's TMEM receives its own rows of the result -- G and U side by side,
-// as in the one-CTA kernel, whose epilogue this is.  Per SM and K step that is 32 KB written to and read from
+// The bf16 GEMMs on pairs of CTAs (a cluster of two, tcgen05 cta_group::2): a
+// work item is 256 sorted rows of one group (the two CTAs' 128-row m-tiles 2j
+// and 2j+1) times one n-tile.  Each CTA loads its own 128 rows of A and half
+// of the 256 weight rows (gate/up: the leader the n-tile's 128 rows of W1,
+// the peer the same rows of W3; down: the leader the first 128 of the
+// n-tile's 256 rows of W2, the peer the other 128), the leader issues M = 256,
+// N = 256 MMAs and each CTA's TMEM receives its own rows of the result --
+// gate/up: G and U side by side, as in the one-CTA kernel, whose epilogues
+// these are.  Per SM and K step that is 32 KB written to and read from
 // shared memory for 128 x 256 x 64 MACs, against 48 KB for the one-CTA tile.
 // Barriers: the leader's full barrier counts both CTAs' TMA bytes (the peer's
 // copies signal it); the MMA commits are multicast to both CTAs' empty and
@@ -308,7 +310,7 @@ __host__ __device__ constexpr int pair_smem_bytes(int stages, int E) {
 }
 static_assert(pair_smem_bytes(6, kMaxExperts) <= P_SMEM_MAX, "shared memory per CTA");
 
-template <int P_STAGES>
+template <int P_STAGES, bool GATEUP>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_bf16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
@@ -409,7 +411,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sa = sbase + s * P_STAGE_BYTES, sb = sa + P_A_BYTES;
                     if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * P_STAGE_BYTES);
                     tma_load_2d_pair(sa, &tmA, kb * BK, row0, lead_full0 + 8 * s);
-                    tma_load_3d_pair(sb, rank ? b1 : b0, kb * BK, nt * 128, gz, lead_full0 + 8 * s);
+                    // gate/up: the n-tile's 128 rows of W1 (leader) or W3 (peer);
+                    // down: the leader's and the peer's 128 of its 256 rows of W2
+                    if (GATEUP) tma_load_3d_pair(sb, rank ? b1 : b0, kb * BK, nt * 128, gz, lead_full0 + 8 * s);
+                    else tma_load_3d_pair(sb, b0, kb * BK, nt * 256 + (int)rank * 128, gz, lead_full0 + 8 * s);
                 }
             }
             if (!ok) {
@@ -488,7 +493,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool ok = r < valid;
             uint16_t* orow = p.out + (size_t)(p.grp_off[g] + j * BM + r) * p.ldo;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            if (q * 32 < valid) {  // a lane quarter with no valid row skips the epilogue
+            if (q * 32 >= valid) {
+                // a lane quarter with no valid row skips the epilogue
+            } else if (GATEUP) {
 #pragma unroll 1
                 for (int c = 2 * half; c < 2 * half + 2; ++c) {
                     uint32_t gv[32], uv[32];
@@ -505,6 +512,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 o[i] = pack_bf16x2(swiglu(__uint_as_float(gv[16 * v + 2 * i]), __uint_as_float(uv[16 * v + 2 * i])),
                                                    swiglu(__uint_as_float(gv[16 * v + 2 * i + 1]),
                                                           __uint_as_float(uv[16 * v + 2 * i + 1])));
+                            st_global_v8(dst + 16 * v, o);
+                        }
+                    }
+                }
+            } else {
+                // down: y = D, the item's 256 output columns
+#pragma unroll 1
+                for (int c = 4 * half; c < 4 * half + 4; ++c) {
+                    uint32_t dv[32];
+                    tmem_ld32(taddr + c * 32, dv);
+                    tmem_wait_ld();
+                    if (ok) {
+                        uint16_t* dst = orow + nt * 256 + c * 32;
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            uint32_t o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                o[i] = pack_bf16x2(__uint_as_float(dv[16 * v + 2 * i]), __uint_as_float(dv[16 * v + 2 * i + 1]));
                             st_global_v8(dst + 16 * v, o);
                         }
                     }
@@ -568,7 +594,8 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
     const uint64_t s13[3] = {H, I, 1}, s2[3] = {I, H, 1};
     if (!tmap_encode(&out->w1, routed->w1, 3, d13, es, bc, 128) ||
         !tmap_encode(&out->w3, routed->w3, 3, d13, es, bc, 128) ||
-        !tmap_encode(&out->w2, routed->w2, 3, d2, es, bc, BN))
+        !tmap_encode(&out->w2, routed->w2, 3, d2, es, bc, BN) ||
+        !tmap_encode(&out->w2h, routed->w2, 3, d2, es, bc, 128))
         return MOE_ERR_CUDA;
     out->s1 = routed->s1;
     out->s3 = routed->s3;
@@ -576,7 +603,8 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
     if (shared) {
         if (!tmap_encode(&out->sw1, shared->w1, 3, s13, es, bc, 128) ||
             !tmap_encode(&out->sw3, shared->w3, 3, s13, es, bc, 128) ||
-            !tmap_encode(&out->sw2, shared->w2, 3, s2, es, bc, BN))
+            !tmap_encode(&out->sw2, shared->w2, 3, s2, es, bc, BN) ||
+            !tmap_encode(&out->sw2h, shared->w2, 3, s2, es, bc, 128))
             return MOE_ERR_CUDA;
         out->ss1 = shared->s1;
         out->ss3 = shared->s3;
@@ -585,6 +613,7 @@ int gemm_prepare_weights(const moe_config& c, const moe_expert_weights* routed, 
         out->sw1 = out->w1;
         out->sw3 = out->w3;
         out->sw2 = out->w2;
+        out->sw2h = out->w2h;
         out->ss1 = out->s1;
         out->ss3 = out->s3;
         out->ss2 = out->s2;
@@ -612,12 +641,13 @@ int gemm_plan(const GemmWeights& w, const GemmCall& g, GemmLaunch* out) {
     return MOE_OK;
 }
 
-// The bf16 gate/up GEMM runs on CTA pairs once the routed rows average 256
-// per active group (a pair's tile); below that the pairs' padding rows cost
-// more than the shared-memory traffic they save.  Measured on the Qwen3 shape:
-// gate/up 202 -> 196 us at m = 4096, 541 -> 520 us at m = 16384; slower at
-// m = 512, and the down GEMM (K = 768) was slower on pairs at every size.
-// MOE_GEMM_PAIR=0 keeps the one-CTA kernel everywhere.
+// The bf16 GEMMs run on CTA pairs once the routed rows average 256 per
+// active group (a pair's tile); below that the pairs' padding rows cost more
+// than the shared-memory traffic they save.  Measured on the Qwen3 shape:
+// gate/up 202 -> 196 us at m = 4096, 541 -> 520 us at m = 16384, slower at
+// m = 512; down (once a pair's missing rows were zero fills) 110 -> 110 us at
+// m = 4096, 332 -> 314 us at m = 16384.  MOE_GEMM_PAIR=0 keeps the one-CTA
+// kernel everywhere.
 bool use_pairs(const GemmCall& g) {
     static const bool allowed = [] {
         const char* v = getenv("MOE_GEMM_PAIR");
@@ -627,17 +657,22 @@ bool use_pairs(const GemmCall& g) {
     return allowed && g.rows / groups >= 2 * BM;
 }
 
-cudaError_t launch_pair_gateup(const GemmLaunch& L, cudaStream_t st) {
-    static cudaError_t attr6 = cudaFuncSetAttribute(grouped_gemm_bf16_pair<6>,
+// gate/up: A = the gathered rows, B = W1 / W3 (128-row boxes), out = h;
+// down: A = h, B = W2 in 128-row boxes, out = y
+template <bool GATEUP>
+cudaError_t launch_pair(const GemmLaunch& L, cudaStream_t st) {
+    static cudaError_t attr6 = cudaFuncSetAttribute(grouped_gemm_bf16_pair<6, GATEUP>,
                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_MAX);
-    static cudaError_t attr7 = cudaFuncSetAttribute(grouped_gemm_bf16_pair<7>,
+    static cudaError_t attr7 = cudaFuncSetAttribute(grouped_gemm_bf16_pair<7, GATEUP>,
                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_MAX);
     if (attr6 != cudaSuccess) return attr6;
     if (attr7 != cudaSuccess) return attr7;
     const GemmCall& g = L.call;
     const bool seven = pair_smem_bytes(7, g.E) <= P_SMEM_MAX;
-    GemmParams p{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.I / 128, g.H / BK, g.I, 128,
-                 static_cast<uint16_t*>(g.h), g.wait_ns, g.stall_test};
+    GemmParams p = GATEUP ? GemmParams{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.I / 128, g.H / BK,
+                                       g.I, 128, static_cast<uint16_t*>(g.h), g.wait_ns, g.stall_test}
+                          : GemmParams{g.hdr, g.grp_off, g.grp_cnt, g.act_group, g.act_tile, g.E, g.H / 256, g.I / BK,
+                                       g.H, 128, g.y, g.wait_ns, g.stall_test};
     const int pairs = std::max(1, std::min(num_sms() / 2, g.max_tiles * p.n_tiles));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
@@ -654,14 +689,19 @@ cudaError_t launch_pair_gateup(const GemmLaunch& L, cudaStream_t st) {
     cfg.attrs = at;
     cfg.numAttrs = 2;
     const GemmWeights& w = *L.w;
-    return seven ? cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<7>, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p)
-                 : cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<6>, L.a_xs, w.w1, w.w3, w.sw1, w.sw3, p);
+    const CUtensorMap& a = GATEUP ? L.a_xs : L.a_h;
+    const CUtensorMap& b0 = GATEUP ? w.w1 : w.w2h;
+    const CUtensorMap& b1 = GATEUP ? w.w3 : w.w2h;
+    const CUtensorMap& s0 = GATEUP ? w.sw1 : w.sw2h;
+    const CUtensorMap& s1 = GATEUP ? w.sw3 : w.sw2h;
+    return seven ? cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<7, GATEUP>, a, b0, b1, s0, s1, p)
+                 : cudaLaunchKernelEx(&cfg, grouped_gemm_bf16_pair<6, GATEUP>, a, b0, b1, s0, s1, p);
 }
 
 cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
     if (L.w->nvfp4) return launch_gemm_nvfp4_gateup(L, st);
     if (L.w->fp8) return launch_gemm_fp8_gateup(L, st);
-    if (use_pairs(L.call)) return launch_pair_gateup(L, st);
+    if (use_pairs(L.call)) return launch_pair<true>(L, st);
     cudaError_t e = set_smem_attr<true>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;
@@ -675,6 +715,7 @@ cudaError_t launch_gemm_gateup(const GemmLaunch& L, cudaStream_t st) {
 cudaError_t launch_gemm_down(const GemmLaunch& L, cudaStream_t st) {
     if (L.w->nvfp4) return launch_gemm_nvfp4_down(L, st);
     if (L.w->fp8) return launch_gemm_fp8_down(L, st);
+    if (use_pairs(L.call)) return launch_pair<false>(L, st);
     cudaError_t e = set_smem_attr<false>();
     if (e != cudaSuccess) return e;
     const GemmCall& g = L.call;

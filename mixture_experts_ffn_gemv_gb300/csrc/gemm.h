@@ -18,6 +18,7 @@ struct GemmWeights {
     bool nvfp4;  // packed e2m1 codes (256 codes of K per box) with e4m3 block scales
     CUtensorMap w1, w3, w2;
     CUtensorMap sw1, sw3, sw2;
+    CUtensorMap w2h, sw2h;  // bf16 W2 in 128-row boxes (the down GEMM on CTA pairs)
     CUtensorMap q1, q3, q2, sq1, sq3, sq2;        // nvfp4: block-scale maps (routed, shared)
     const float *s1, *s3, *s2, *ss1, *ss3, *ss2;  // fp8 block scales / nvfp4 matrix scales (routed, shared)
 };
