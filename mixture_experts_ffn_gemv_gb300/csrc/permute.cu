@@ -11,11 +11,12 @@
 //                   the grouped GEMM's m-tile starts;
 //   permute_scatter per chunk, warp-level ranks (match_any) give each pair
 //                   its slot: pairs keep ascending order within an expert.
-// The bf16 and fp8 grouped-GEMM arms skip permute_scatter: their gather runs
-// one warp per pair and places it itself, at its expert's offset + its
-// chunk's base + its rank within the chunk, which permute_count leaves in
-// slot_of_pair (the order of a chunk's pairs within an expert then follows
-// the shared-memory atomics; every slot is still used once).
+// The grouped-GEMM arms skip permute_scatter: the bf16 and fp8 gathers (one
+// warp per pair) and the NVFP4 x quantiser place each pair themselves, at its
+// expert's offset + its chunk's base + its rank within the chunk, which
+// permute_count leaves in slot_of_pair (the order of a chunk's pairs within
+// an expert then follows the shared-memory atomics; every slot is still used
+// once).
 // Plus the activation gathers for the grouped GEMM, the fp8 activation
 // quantiser (one e4m3 code + fp32 scale per 128 inputs) and the NVFP4 one.
 #include <algorithm>
