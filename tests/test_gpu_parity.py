@@ -443,31 +443,35 @@ def test_gateup_on_cta_pairs(cuda, oracle_mod, shape, m):
 # - 129: the peer has one row;
 # - 257 and 770: full pairs, then a tile with 1 or 2 rows;
 # - 384 and 385: a full pair, then a tile with 128 or 129 rows.
-# The shared expert's 2071 rows end in a 23-row tile, and I = 384 is an odd
-# count of 128-column n-tiles.
+# The shared expert's 2071 rows end in a 23-row tile.  bf16: I = 384 is an odd
+# count of 128-column n-tiles; NVFP4 (K in blocks of 256): I = 512.
 PAIR_EDGES = I.LayerShape(hidden=512, num_experts=8, top_k=1, inter=384, shared_inter=384)
+PAIR_EDGES_NVFP4 = I.LayerShape(hidden=512, num_experts=8, top_k=1, inter=512, shared_inter=512, nvfp4=True)
 PAIR_EDGES_COUNTS = (1, 17, 128, 129, 257, 384, 385, 770)
 
 
-def test_gateup_pair_group_edges(cuda, oracle_mod):
+@pytest.mark.parametrize("shape", [PAIR_EDGES, PAIR_EDGES_NVFP4], ids=["bf16", "nvfp4"])
+def test_gateup_pair_group_edges(cuda, oracle_mod, shape):
     """Every row of a layer whose groups end in each kind of pair tile, with
-    caller-given routing, against the oracle row by row."""
+    caller-given routing, against the oracle row by row (the bf16 GEMMs run on
+    CTA pairs at these row counts; the NVFP4 case covers the same ragged
+    groups on its one-CTA tiles)."""
     from mixture_experts_ffn_gemv_gb300 import binding
     m = sum(PAIR_EDGES_COUNTS)
-    tensors, x = _small_case(PAIR_EDGES, m, seed=143, device=cuda)
+    tensors, x = _small_case(shape, m, seed=143, device=cuda)
     gen = np.random.default_rng(143)
     ids = gen.permutation(np.repeat(np.arange(8, dtype=np.int32), PAIR_EDGES_COUNTS)).reshape(m, 1)
     w = gen.uniform(0.5, 1.0, (m, 1)).astype(np.float32)
-    layer = binding.MoeLayer(PAIR_EDGES, tensors)
+    layer = binding.MoeLayer(shape, tensors)
     out = layer.moe_experts(x, torch.from_numpy(ids).to(cuda), torch.from_numpy(w).to(cuda), arm="gemm")
     torch.cuda.synchronize()
     assert layer.device_status() == 0
     host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in tensors.items()}
-    want = oracle_mod.moe_forward(PAIR_EDGES, host, x.cpu(), ids, w)
+    want = oracle_mod.moe_forward(shape, host, x.cpu(), ids, w)
     got = to_np(out).astype(np.float64)
     row_err = np.linalg.norm(got - want, axis=1) / np.maximum(np.linalg.norm(want, axis=1), 1e-30)
-    assert rel_l2(got, want) < TOL[False]
-    assert row_err.max() < 3 * TOL[False], (int(row_err.argmax()), float(row_err.max()))
+    assert rel_l2(got, want) < tol(shape)
+    assert row_err.max() < 3 * tol(shape), (int(row_err.argmax()), float(row_err.max()))
 
 
 SHARED_BF16 = I.LayerShape(hidden=512, num_experts=16, top_k=4, inter=256, shared_inter=256)
